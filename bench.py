@@ -1,0 +1,463 @@
+"""Benchmark of the paged-attention hot path on GB300.
+
+Headline (one JSON line on rank 0): split-KV paged decode on the pages' decode
+microbench shape -- B=32, GQA 32/8, head_dim 128, seq_lens uniform in [200, 2000],
+page_size=1 random slot table, bf16 -- reported as K+V bytes read per second (GB/s),
+microseconds per call and the fraction of the measured HBM copy bandwidth.  A step is
+one decode call (split kernel + combine kernel) through the C ABI on inputs already in
+HBM.  L2 is defeated by rotating through several copies of the KV pools (working set
+well above the 126 MB L2), so every call reads its keys from DRAM.
+
+Also reported in the same line:
+  * roofline     -- the split kernel alone (the dominant kernel), timed with CUDA events
+                    on its stream: algorithmic K+V bytes per launch / mean duration.
+  * prefill      -- the ragged prefill entry point on the 16-request extend workload,
+                    FLOP/s against the measured dense bf16 tensor-core peak.
+  * e2e          -- the same decode metric with every input in pinned host memory, the
+                    host->device copies and the device->host read of `out` inside the
+                    timed region (and a variant where only q and the index arrays move).
+  * cpu_baseline -- the fp64 CPU oracle timed on this host on a bounded sample.
+
+--impl reference times the fp64 oracle (the only reference implementation this build
+has) on the same workload and prints the same line with "impl": "reference".
+Multi-GPU (torchrun): every rank runs its own replica (weak scaling); the elapsed time is
+the max over ranks and value sums all ranks' bytes.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workload  # noqa: E402
+
+METRIC = "paged decode KV GB/s (fraction of HBM peak) & us/call, B=32 GQA 32/8 d128"
+DECODE_CFG = 2
+PREFILL_CFG = 5
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+POOL_COPIES = 4          # rotate KV-pool copies so each call's working set is cold in L2
+MAX_SPLITS = 64
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"]))}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def prefill_flops(w) -> float:
+    """Causal-attended (query, key) pairs x 4 d Hq (QK^T and PV, 2 FLOP per MAC)."""
+    ql = w.q_lens.astype(np.int64)
+    c = w.seq_lens.astype(np.int64) - ql
+    pairs = int((ql * c + ql * (ql + 1) // 2).sum())
+    return 4.0 * w.head_dim * w.num_qo_heads * pairs
+
+
+def decode_bytes(w) -> dict:
+    kv = w.kv_bytes()
+    idx = 4 * int(w.seq_lens.sum()) + 8 * w.batch
+    qo = 2 * 2 * w.batch * w.num_qo_heads * w.head_dim
+    return {"kv": kv, "all": kv + idx + qo}
+
+
+# ------------------------------------------------------------------ traffic record
+
+
+def recorded_traffic(kernel: str, source: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on this source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(kernel)
+    if not rec:
+        return None
+    with open(os.path.join(ROOT, "prefill_attention_gb300", "csrc", source), "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    if rec.get("source_sha") != sha:
+        return None
+    return rec.get("bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out" if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else ".",
+                                 f".clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.dev), "-lms", "50"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ reference arm (oracle)
+
+
+def oracle_gbs(w, seconds: float, nthreads: int):
+    """Time the fp64 oracle on whole-batch decode calls for ~`seconds`; GB/s of K+V."""
+    import oracle
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.decode(w, nthreads=nthreads)  # one call also warms caches
+    one = time.perf_counter() - t0
+    reps = max(1, int(seconds / max(one, 1e-3)))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.decode(w, nthreads=nthreads)
+    dt = (time.perf_counter() - t0) / reps
+    return w.kv_bytes() / dt / 1e9, dt, reps
+
+
+def run_reference(args, rank: int, world: int):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    w = workload.config(DECODE_CFG)
+    cores = os.cpu_count() or 1
+    # each step: the whole B=32 batch (all 1024 (request, head) rows), fp64, all host cores
+    for _ in range(args.warmup):
+        oracle.decode(w, nthreads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.decode(w, nthreads=cores)
+    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    val = w.kv_bytes() / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "seed": w.seed, "sample": "whole batch per step"},
+        "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": "whole decode batch (32 requests x 32 heads) per step, fp64 C oracle"},
+        "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--num-splits", type=int, default=0, help="force the decode split count (0 = planned)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    import prefill_attention_gb300 as pa
+    from prefill_attention_gb300 import build as pbuild
+
+    pbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x: float) -> float:
+        if dist is None:
+            return x
+        t = torch.tensor([x], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum_over_ranks(x: float) -> float:
+        if dist is None:
+            return x
+        t = torch.tensor([x], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.SUM)
+        return float(t.item())
+
+    peaks, peaks_src = load_peaks()
+
+    # ---------------- decode inputs (replica per rank, same seed so every rank does equal work)
+    w = workload.config(DECODE_CFG)
+    nbytes = decode_bytes(w)
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    def i32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+
+    q = bf(w.q)
+    pools = [(bf(w.k_pool), bf(w.v_pool)) for _ in range(POOL_COPIES)]
+    r2t, seq, kvi = i32(w.req_to_token), i32(w.seq_lens), i32(w.kv_indptr)
+    dims = pa.make_dims(w.batch, w.num_qo_heads, w.num_kv_heads, w.head_dim, w.num_slots, w.r2t_stride,
+                        w.max_seq_len, max_splits=MAX_SPLITS, num_splits=args.num_splits)
+    S = pa.astr_attn_decode_num_splits(dims, local)
+    o_part, ml_part = pa.alloc_decode_workspace(dims, device=dev)
+    out = torch.empty_like(q)
+    stream = torch.cuda.Stream(device=dev)
+    sh = int(stream.cuda_stream)
+
+    def decode(i):
+        k, v = pools[i % POOL_COPIES]
+        pa.astr_attn_paged_decode(q, k, v, r2t, seq, kvi, o_part, ml_part, out, dims, w.sm_scale, stream=sh)
+
+    def split_only(i):
+        k, v = pools[i % POOL_COPIES]
+        pa.astr_attn_decode_split(q, k, v, r2t, seq, kvi, o_part, ml_part, dims, w.sm_scale, stream=sh)
+
+    def timed(fn, n):
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for i in range(n):
+                fn(i)
+            ev1.record(stream)
+        ev1.synchronize()
+        return ev0.elapsed_time(ev1) / 1e3  # seconds
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    # warm-up (also keeps the GPU loaded ~0.3 s so the clock samples reflect load)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            decode(i)
+    stream.synchronize()
+    t_end = time.perf_counter() + 0.3
+    while time.perf_counter() < t_end:
+        timed(decode, 200)
+
+    # ---------------- timed region: K decode steps
+    barrier()
+    elapsed = timed(decode, args.steps)
+    barrier()
+    clk = clocks.stop()
+    elapsed_max = max_over_ranks(elapsed)
+    total_kv = sum_over_ranks(float(nbytes["kv"]) * args.steps)
+    value = total_kv / elapsed_max / 1e9
+    us_per_call = elapsed_max / args.steps * 1e6
+
+    # ---------------- the split kernel alone (roofline of the dominant kernel)
+    n_split = max(200, min(args.steps, 2000))
+    timed(split_only, 20)
+    t_split = timed(split_only, n_split) / n_split
+    split_gbs = nbytes["kv"] / t_split / 1e9
+
+    # ---------------- CUDA-graph replay (launch overhead amortised)
+    graph_us = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        n_graph = 64
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n_graph):
+                decode(i)
+        g.replay()
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(10):
+                g.replay()
+            ev1.record(stream)
+        ev1.synchronize()
+        graph_us = ev0.elapsed_time(ev1) * 1e3 / (10 * n_graph)
+        del g
+    except Exception as e:  # capture problems are reported, not hidden
+        graph_us = f"capture failed: {e}"
+
+    # ---------------- e2e through the public API with host buffers
+    def pinned(t):
+        h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        h.copy_(t)
+        return h
+
+    hq, hk, hv = pinned(q), pinned(pools[0][0]), pinned(pools[0][1])
+    hr, hs, hi = pinned(r2t), pinned(seq), pinned(kvi)
+    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(pools[0][0]), torch.empty_like(pools[0][1])
+    dr, ds, di = torch.empty_like(r2t), torch.empty_like(seq), torch.empty_like(kvi)
+    n_e2e = max(5, min(args.steps // 20, 100))
+
+    def e2e_step(full: bool):
+        with torch.cuda.stream(stream):
+            dq.copy_(hq, non_blocking=True)
+            if full:
+                dk.copy_(hk, non_blocking=True)
+                dv.copy_(hv, non_blocking=True)
+            dr.copy_(hr, non_blocking=True)
+            ds.copy_(hs, non_blocking=True)
+            di.copy_(hi, non_blocking=True)
+            k, v = (dk, dv) if full else pools[0]
+            pa.astr_attn_paged_decode(dq, k, v, dr, ds, di, o_part, ml_part, out, dims, w.sm_scale, stream=sh)
+            hout.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    def e2e_time(full):
+        for _ in range(3):
+            e2e_step(full)
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            e2e_step(full)
+        barrier()
+        return max_over_ranks((time.perf_counter() - t0) / n_e2e)
+
+    t_e2e_full = e2e_time(True)
+    t_e2e_res = e2e_time(False)
+    h2d_full = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hr, hs, hi))
+    h2d_res = sum(t.numel() * t.element_size() for t in (hq, hr, hs, hi))
+    d2h = hout.numel() * hout.element_size()
+
+    # ---------------- prefill entry point on the extend workload
+    wp = workload.config(PREFILL_CFG)
+    pq, pk, pv = bf(wp.q), bf(wp.k_pool), bf(wp.v_pool)
+    pqo, pr, ps_, pki = i32(wp.qo_indptr), i32(wp.req_to_token), i32(wp.seq_lens), i32(wp.kv_indptr)
+    pdims = pa.make_dims(wp.batch, wp.num_qo_heads, wp.num_kv_heads, wp.head_dim, wp.num_slots, wp.r2t_stride,
+                         wp.max_seq_len, total_q=wp.total_q, max_q_len=wp.max_q_len)
+    pout = torch.empty_like(pq)
+
+    def prefill(i):
+        pa.astr_attn_prefill_ragged(pq, pqo, pk, pv, pr, ps_, pki, pout, pdims, wp.sm_scale, stream=sh)
+
+    timed(prefill, 5)
+    n_pf = max(20, min(args.steps // 10, 400))
+    t_pf = timed(prefill, n_pf) / n_pf
+    flops = prefill_flops(wp)
+    pf_tflops = flops / t_pf / 1e12
+
+    # ---------------- CPU baseline: the oracle on this host (rank 0 at N=1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cores = os.cpu_count() or 1
+        gbs, dt, reps = oracle_gbs(w, args.cpu_seconds, cores)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": f"whole B=32 decode batch, fp64 C oracle, {reps} calls of {dt:.3f} s"}
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    traffic = recorded_traffic("decode_split", "decode.cu")
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(elapsed_max / args.steps * 1e3, 6),
+        "us_per_call": round(us_per_call, 3),
+        "us_per_call_graph": round(graph_us, 3) if isinstance(graph_us, float) else graph_us,
+        "frac_of_hbm": round(value / world / peaks["hbm_gbs"], 4),
+        "frac_of_nominal_8tbs": round(value / world / 7900.0, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "seed": w.seed, "page_size": 1, "num_splits": S,
+                   "kv_bytes_per_call": nbytes["kv"], "total_keys": int(w.seq_lens.sum()),
+                   "l2": f"rotating {POOL_COPIES} KV-pool copies ({POOL_COPIES * nbytes['kv'] / 1e6:.0f} MB > L2)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": "decode_split_kernel<128,4>", "achieved": round(split_gbs, 2),
+                     "peak": peaks["hbm_gbs"], "peak_source": f"hbm_gbs ({peaks_src})", "unit": "GB/s",
+                     "frac": round(split_gbs / peaks["hbm_gbs"], 4), "us_per_launch": round(t_split * 1e6, 3),
+                     "traffic": traffic},
+        "prefill": {"workload": wp.name, "seed": wp.seed, "us_per_call": round(t_pf * 1e6, 3),
+                    "flops_per_call": flops,
+                    "roofline": {"bound": "tensor", "achieved": round(pf_tflops, 2), "peak": peaks["bf16_tflops"],
+                                 "peak_source": f"bf16_tflops burst ({peaks_src})", "unit": "TFLOP/s",
+                                 "frac": round(pf_tflops / peaks["bf16_tflops"], 4),
+                                 "traffic": recorded_traffic("prefill", "prefill.cu")}},
+        "e2e": {"value": round(sum_over_ranks(nbytes["kv"]) / t_e2e_full / 1e9, 3), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d_full, "d2h_bytes_per_step": d2h,
+                "resident_kv": {"value": round(sum_over_ranks(nbytes["kv"]) / t_e2e_res / 1e9, 3), "unit": "GB/s",
+                                "h2d_bytes_per_step": h2d_res, "d2h_bytes_per_step": d2h}},
+        "gpu_launches": 2 * args.steps,
+        "cpu_baseline": cpu,
+        "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
+                   "samples": clk["samples"]},
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

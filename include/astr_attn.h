@@ -1,0 +1,166 @@
+/*
+ * astr_attn.h -- C ABI of the GB300 (sm_103a) paged-attention library libastr_attn.so.
+ *
+ * One hot path of an LLM serving engine: batched bf16 attention with grouped KV heads
+ * over a KV-cache pool addressed through a req_to_token slot table at page_size = 1.
+ * Sources (AstrAI commit log pages; "P3" = page "astrai/extension @6f67ba8",
+ * "P1" = page "astrai/extension/backend/attention.py @c9ceca1",
+ * "P5" = page "astrai/extension/attention_backend.py @47b3ed4"):
+ *   - P3, CUDA-backend commit: decode goes through attn_paged_decode and prefill through
+ *     attn_prefill; req_to_token serves as the page table with one token per page.
+ *   - P3, kernel-rename commit: decode is split-KV only -- every split writes an
+ *     unnormalised partial (o_part) and its (m, l) pair (ml_part), and one combine kernel
+ *     merges them with a log-sum-exp rescale.
+ *   - P1, batched-SDPA commit: prefill/extend rows are packed flat by qo_indptr and use the
+ *     per-request causal offset seq_len - q_len; masked keys get exactly zero weight.
+ *   - P3, workspace and kv_indptr commits; P5, graph-workspace commit: the caller owns
+ *     o_part, ml_part and out, allocated once, so the decode loop allocates nothing and
+ *     can be captured into a CUDA graph; kv_indptr (exclusive prefix sum of seq_lens) is
+ *     built once per step by the caller.
+ *
+ * Conventions for every entry point below:
+ *   - Return value: ASTR_OK (0) or a negative astr_status.  Argument checks run on the
+ *     host from the arguments alone; no device memory is read on the host, nothing is
+ *     allocated, nothing synchronises, and no work goes to the legacy default stream
+ *     unless the caller passes stream 0.  The calls are therefore capturable in a CUDA
+ *     graph.  On an error status nothing has been launched.
+ *   - All array pointers are DEVICE pointers owned by the caller; the library keeps no
+ *     pointer after the call returns.  The dims struct is a HOST pointer read during the
+ *     call only.
+ *   - `stream` is a cudaStream_t passed as void*; all work is enqueued on it.
+ *   - bf16 arrays hold IEEE bfloat16 bit patterns (uint16_t storage).  bf16 and fp32
+ *     arrays must be 16-byte aligned; int32 arrays 4-byte aligned (ASTR_ERR_MISALIGNED).
+ *   - Layouts (row-major, innermost last):
+ *       q (decode)        [batch, num_qo_heads, head_dim]            bf16
+ *       q (prefill)       [total_q, num_qo_heads, head_dim]          bf16
+ *       k_pool, v_pool    [num_slots, num_kv_heads, head_dim]        bf16
+ *       req_to_token      [batch, r2t_stride]                        int32 slot ids
+ *       seq_lens          [batch]                                    int32
+ *       kv_indptr         [batch + 1]   kv_indptr[b] = sum_{b'<b} seq_lens[b']   int32
+ *       qo_indptr         [batch + 1]   flat query row range of request b        int32
+ *       out (decode)      [batch, num_qo_heads, head_dim]            bf16
+ *       out (prefill)     [total_q, num_qo_heads, head_dim]          bf16
+ *       o_part            [batch, num_qo_heads, max_splits, head_dim] fp32
+ *       ml_part           [batch, num_qo_heads, max_splits, 2]       fp32 (m, l)
+ *   - Query head h reads KV head h / (num_qo_heads / num_kv_heads) (consecutive groups).
+ *   - Caller preconditions (not checked, as that would need device reads): every slot id
+ *     in row b's first seq_lens[b] entries is in [0, num_slots); 0 <= seq_lens[b] <=
+ *     max_seq_len <= r2t_stride; kv_indptr is the exclusive prefix sum of seq_lens;
+ *     for prefill 0 <= qo_indptr[b+1] - qo_indptr[b] <= seq_lens[b], qo_indptr[0] = 0 and
+ *     qo_indptr[batch] = total_q.  Violations give undefined results.
+ */
+#ifndef ASTR_ATTN_H
+#define ASTR_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum astr_status {
+  ASTR_OK = 0,
+  ASTR_ERR_INVALID_ARG = -1,          /* null pointer, negative or inconsistent dims, non-finite sm_scale */
+  ASTR_ERR_UNSUPPORTED = -2,          /* head_dim not 64/128, Hq % Hkv != 0, group size not supported */
+  ASTR_ERR_MISALIGNED = -3,           /* a pointer breaks the alignment rule above */
+  ASTR_ERR_WORKSPACE_TOO_SMALL = -4,  /* max_splits below what the call needs */
+  ASTR_ERR_LAUNCH_FAILED = -5,        /* a CUDA launch or attribute call failed (cudaGetLastError) */
+  ASTR_ERR_DEVICE = -6                /* querying the current device failed */
+} astr_status;
+
+/* Shapes and capacities; host struct read during the call only. */
+typedef struct astr_attn_dims {
+  int32_t batch;         /* requests in the batch (0 = nothing to do) */
+  int32_t num_qo_heads;  /* Hq */
+  int32_t num_kv_heads;  /* Hkv; Hq % Hkv == 0; group size Hq/Hkv in {1,2,4,8,16} */
+  int32_t head_dim;      /* 64 or 128 */
+  int64_t num_slots;     /* rows of k_pool / v_pool */
+  int32_t r2t_stride;    /* elements between consecutive req_to_token rows */
+  int32_t max_seq_len;   /* host-known upper bound of seq_lens (plans the split count) */
+  int32_t total_q;       /* prefill: flat query rows (= qo_indptr[batch]); ignored by decode */
+  int32_t max_q_len;     /* prefill: upper bound of q_len (sizes the grid); ignored by decode */
+  int32_t max_splits;    /* decode: split capacity of o_part / ml_part (>= 1) */
+  int32_t num_splits;    /* decode: 0 = plan automatically, > 0 forces this split count */
+} astr_attn_dims;
+
+/*
+ * Split count the decode call will use for these dims on `device` (P3, shared-helpers
+ * commit: the split count is chosen per call).  Chosen so that batch * Hkv * splits
+ * CTAs fill the GPU's SMs, bounded by max_splits and by max_seq_len (at least a few
+ * dozen keys per split).  Depends only on host-known values, never on seq_lens contents.
+ * Errors: INVALID_ARG (null, bad dims), DEVICE (device query failed).
+ */
+int astr_attn_decode_num_splits(const astr_attn_dims* dims, int device, int* num_splits);
+
+/*
+ * Bytes the caller must provide for o_part and ml_part: batch * Hq * max_splits *
+ * head_dim * 4 and batch * Hq * max_splits * 2 * 4.  Errors: INVALID_ARG.
+ */
+int astr_attn_decode_workspace_bytes(const astr_attn_dims* dims, size_t* o_part_bytes, size_t* ml_part_bytes);
+
+/*
+ * Split-KV paged decode (one query row per request).
+ *   out[b, h, :] = sum_{j < seq_lens[b]} softmax_j(sm_scale * <q[b,h], K_j>) V_j,
+ *   K_j, V_j = pool[req_to_token[b * r2t_stride + j], h / G, :].
+ * Launches the split kernel (each split owns a contiguous range of one request's keys
+ * for one KV head and all G query heads sharing it, and writes o_part/ml_part for every
+ * split it owns, empty ones as m = -inf, l = 0, o = 0) and then the combine kernel.
+ * ml_part m is the max scaled logit in natural-log units; o_part is unnormalised.
+ * seq_lens[b] = 0 gives a zero output row.  Deterministic for fixed dims.
+ * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, WORKSPACE_TOO_SMALL (forced num_splits
+ * above max_splits), DEVICE, LAUNCH_FAILED.
+ */
+int astr_attn_paged_decode(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
+                           const int32_t* req_to_token, const int32_t* seq_lens, const int32_t* kv_indptr,
+                           float* o_part, float* ml_part, uint16_t* out, const astr_attn_dims* dims,
+                           float sm_scale, void* stream);
+
+/*
+ * The split step alone: the first of the two launches of astr_attn_paged_decode.  Writes
+ * o_part / ml_part for every split (num_splits as planned for `dims`) and nothing else;
+ * astr_attn_decode_combine then produces `out`.  Same arguments, rules and errors as
+ * astr_attn_paged_decode minus `out`.
+ */
+int astr_attn_decode_split(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
+                           const int32_t* req_to_token, const int32_t* seq_lens, const int32_t* kv_indptr,
+                           float* o_part, float* ml_part, const astr_attn_dims* dims, float sm_scale, void* stream);
+
+/*
+ * The combine step alone (P3, kernel-rename commit: the log-sum-exp merge shared by the
+ * split paths): for each (b, h) with S = num_splits as planned for `dims`,
+ *   M = max_s m_s,  w_s = exp(m_s - M),  out = (sum_s w_s o_s) / (sum_s w_s l_s)  -> bf16.
+ * A row whose splits are all empty (M = -inf) is written as zeros.  Reads only o_part,
+ * ml_part; seq_lens and kv_indptr may be NULL.  Errors as astr_attn_paged_decode.
+ */
+int astr_attn_decode_combine(const float* o_part, const float* ml_part, const int32_t* seq_lens,
+                             const int32_t* kv_indptr, uint16_t* out, const astr_attn_dims* dims, void* stream);
+
+/*
+ * Ragged packed prefill/extend over the same pool (P1, batched-SDPA commit; P3,
+ * CUDA-backend and unified-causal-offset commits).  For request b with q_len_b =
+ * qo_indptr[b+1] - qo_indptr[b] and causal offset c_b = seq_lens[b] - q_len_b, flat row
+ * r = qo_indptr[b] + i (0 <= i < q_len_b) and query head h:
+ *   out[r, h, :] = sum_{j <= c_b + i} softmax_j(sm_scale * <q[r,h], K_j>) V_j.
+ * The new tokens' K/V must already be in the pool (positions c_b .. seq_len_b - 1).
+ * Requests with q_len = 0 write nothing.  kv_indptr is accepted for interface symmetry
+ * with decode and is not read (may be NULL).  Tensor cores (tcgen05, accumulators in
+ * tensor memory) compute Q K^T and P V.
+ * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, DEVICE, LAUNCH_FAILED.
+ */
+int astr_attn_prefill_ragged(const uint16_t* q, const int32_t* qo_indptr, const uint16_t* k_pool,
+                             const uint16_t* v_pool, const int32_t* req_to_token, const int32_t* seq_lens,
+                             const int32_t* kv_indptr, uint16_t* out, const astr_attn_dims* dims, float sm_scale,
+                             void* stream);
+
+/* Static description of a status code (never NULL). */
+const char* astr_attn_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int astr_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ASTR_ATTN_H */

@@ -1,0 +1,184 @@
+"""Python binding of libastr_attn.so: GB300 paged decode and ragged prefill attention.
+
+This module only marshals arguments: it takes device tensors (PyTorch is used for device
+memory and streams), passes their pointers and shapes to the C ABI declared in
+``include/astr_attn.h`` and returns the status code.  Every step of the computation runs
+in the library's CUDA kernels; there is no CPU or PyTorch fallback.  If the library has
+not been built, importing succeeds but every call raises ``RuntimeError``.
+
+Function names mirror the C entry points.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+__all__ = [
+    "Dims", "AstrAttnError", "load", "lib_path", "make_dims",
+    "astr_attn_paged_decode", "astr_attn_decode_split", "astr_attn_decode_combine", "astr_attn_prefill_ragged",
+    "astr_attn_decode_num_splits", "astr_attn_decode_workspace_bytes", "astr_attn_status_string",
+    "astr_attn_version", "alloc_decode_workspace",
+    "ASTR_OK", "ASTR_ERR_INVALID_ARG", "ASTR_ERR_UNSUPPORTED", "ASTR_ERR_MISALIGNED",
+    "ASTR_ERR_WORKSPACE_TOO_SMALL", "ASTR_ERR_LAUNCH_FAILED", "ASTR_ERR_DEVICE", "EXPORTED_SYMBOLS",
+]
+
+ASTR_OK = 0
+ASTR_ERR_INVALID_ARG = -1
+ASTR_ERR_UNSUPPORTED = -2
+ASTR_ERR_MISALIGNED = -3
+ASTR_ERR_WORKSPACE_TOO_SMALL = -4
+ASTR_ERR_LAUNCH_FAILED = -5
+ASTR_ERR_DEVICE = -6
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libastr_attn.so")
+_lib = None
+
+EXPORTED_SYMBOLS = [
+    "astr_attn_decode_num_splits", "astr_attn_decode_workspace_bytes", "astr_attn_paged_decode",
+    "astr_attn_decode_combine", "astr_attn_prefill_ragged", "astr_attn_status_string", "astr_attn_version",
+    "astr_attn_decode_split",
+]
+
+
+class AstrAttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: status {status} ({astr_attn_status_string(status)})")
+        self.status = status
+
+
+class Dims(ctypes.Structure):
+    """Mirror of ``astr_attn_dims`` (see include/astr_attn.h for the meaning of each field)."""
+    _fields_ = [
+        ("batch", ctypes.c_int32), ("num_qo_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32), ("num_slots", ctypes.c_int64), ("r2t_stride", ctypes.c_int32),
+        ("max_seq_len", ctypes.c_int32), ("total_q", ctypes.c_int32), ("max_q_len", ctypes.c_int32),
+        ("max_splits", ctypes.c_int32), ("num_splits", ctypes.c_int32),
+    ]
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load libastr_attn.so (built by ``prefill_attention_gb300.build``); raise if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"{_LIB_PATH} is not built; run `python -m prefill_attention_gb300.build` "
+                           "(or __graft_entry__.build()) first")
+    lib = ctypes.CDLL(_LIB_PATH)
+    P, I32, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    D = ctypes.POINTER(Dims)
+    lib.astr_attn_decode_num_splits.argtypes = [D, I32, ctypes.POINTER(ctypes.c_int)]
+    lib.astr_attn_decode_workspace_bytes.argtypes = [D, ctypes.POINTER(ctypes.c_size_t),
+                                                     ctypes.POINTER(ctypes.c_size_t)]
+    lib.astr_attn_paged_decode.argtypes = [P, P, P, P, P, P, P, P, P, D, F, P]
+    lib.astr_attn_decode_split.argtypes = [P, P, P, P, P, P, P, P, D, F, P]
+    lib.astr_attn_decode_combine.argtypes = [P, P, P, P, P, D, P]
+    lib.astr_attn_prefill_ragged.argtypes = [P, P, P, P, P, P, P, P, D, F, P]
+    lib.astr_attn_status_string.argtypes = [I32]
+    lib.astr_attn_status_string.restype = ctypes.c_char_p
+    lib.astr_attn_version.argtypes = []
+    for f in ("astr_attn_decode_num_splits", "astr_attn_decode_workspace_bytes", "astr_attn_paged_decode",
+              "astr_attn_decode_split", "astr_attn_decode_combine", "astr_attn_prefill_ragged", "astr_attn_version"):
+        getattr(lib, f).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def make_dims(batch, num_qo_heads, num_kv_heads, head_dim, num_slots, r2t_stride, max_seq_len, total_q=0,
+              max_q_len=0, max_splits=1, num_splits=0) -> Dims:
+    return Dims(int(batch), int(num_qo_heads), int(num_kv_heads), int(head_dim), int(num_slots), int(r2t_stride),
+                int(max_seq_len), int(total_q), int(max_q_len), int(max_splits), int(num_splits))
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return int(t.data_ptr())
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def _check(status: int, where: str, check: bool) -> int:
+    if check and status != ASTR_OK:
+        raise AstrAttnError(status, where)
+    return status
+
+
+def astr_attn_status_string(status: int) -> str:
+    return load().astr_attn_status_string(int(status)).decode()
+
+
+def astr_attn_version() -> int:
+    return int(load().astr_attn_version())
+
+
+def astr_attn_decode_num_splits(dims: Dims, device: int = 0, check: bool = True) -> int:
+    n = ctypes.c_int(0)
+    st = load().astr_attn_decode_num_splits(ctypes.byref(dims), int(device), ctypes.byref(n))
+    _check(st, "astr_attn_decode_num_splits", check)
+    return n.value if st == ASTR_OK else st
+
+
+def astr_attn_decode_workspace_bytes(dims: Dims, check: bool = True):
+    a, b = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    st = load().astr_attn_decode_workspace_bytes(ctypes.byref(dims), ctypes.byref(a), ctypes.byref(b))
+    _check(st, "astr_attn_decode_workspace_bytes", check)
+    return (a.value, b.value) if st == ASTR_OK else st
+
+
+def astr_attn_paged_decode(q, k_pool, v_pool, req_to_token, seq_lens, kv_indptr, o_part, ml_part, out,
+                           dims: Dims, sm_scale: float, stream=None, check: bool = True) -> int:
+    """Split-KV paged decode; arrays are device tensors (or raw device pointers as ints)."""
+    st = load().astr_attn_paged_decode(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(req_to_token), _ptr(seq_lens),
+                                       _ptr(kv_indptr), _ptr(o_part), _ptr(ml_part), _ptr(out), ctypes.byref(dims),
+                                       float(sm_scale), _stream(stream))
+    return _check(st, "astr_attn_paged_decode", check)
+
+
+def astr_attn_decode_split(q, k_pool, v_pool, req_to_token, seq_lens, kv_indptr, o_part, ml_part, dims: Dims,
+                           sm_scale: float, stream=None, check: bool = True) -> int:
+    """The split kernel alone (writes o_part / ml_part)."""
+    st = load().astr_attn_decode_split(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(req_to_token), _ptr(seq_lens),
+                                       _ptr(kv_indptr), _ptr(o_part), _ptr(ml_part), ctypes.byref(dims),
+                                       float(sm_scale), _stream(stream))
+    return _check(st, "astr_attn_decode_split", check)
+
+
+def astr_attn_decode_combine(o_part, ml_part, seq_lens, kv_indptr, out, dims: Dims, stream=None,
+                             check: bool = True) -> int:
+    st = load().astr_attn_decode_combine(_ptr(o_part), _ptr(ml_part), _ptr(seq_lens), _ptr(kv_indptr), _ptr(out),
+                                         ctypes.byref(dims), _stream(stream))
+    return _check(st, "astr_attn_decode_combine", check)
+
+
+def astr_attn_prefill_ragged(q, qo_indptr, k_pool, v_pool, req_to_token, seq_lens, kv_indptr, out, dims: Dims,
+                             sm_scale: float, stream=None, check: bool = True) -> int:
+    st = load().astr_attn_prefill_ragged(_ptr(q), _ptr(qo_indptr), _ptr(k_pool), _ptr(v_pool), _ptr(req_to_token),
+                                         _ptr(seq_lens), _ptr(kv_indptr), _ptr(out), ctypes.byref(dims),
+                                         float(sm_scale), _stream(stream))
+    return _check(st, "astr_attn_prefill_ragged", check)
+
+
+def alloc_decode_workspace(dims: Dims, device="cuda"):
+    """Allocate (once, outside the hot loop) o_part and ml_part for ``dims`` with PyTorch."""
+    import torch
+    ob, mb = astr_attn_decode_workspace_bytes(dims)
+    o_part = torch.empty(ob // 4, dtype=torch.float32, device=device)
+    ml_part = torch.empty(mb // 4, dtype=torch.float32, device=device)
+    return o_part, ml_part

@@ -1,0 +1,240 @@
+// api.cu -- the C ABI declared in include/astr_attn.h: argument checks, split planning
+// and kernel launches on the caller's stream.  No allocation, no synchronisation, no
+// device-memory reads on the host, so every entry point can be captured in a CUDA graph.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "astr_attn.h"
+#include "astr_attn_internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kDecodeCtasPerSm = 3;     // resident split-kernel CTAs per SM (launch bounds)
+constexpr int kMinKeysPerSplit = 64;    // below this a split is mostly fixed cost
+
+std::mutex g_mu;
+int g_sm_count[kMaxDevices] = {0};
+
+int sm_count(int device, int* out) {
+  if (device < 0 || device >= kMaxDevices) return ASTR_ERR_DEVICE;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_sm_count[device] > 0) {
+      *out = g_sm_count[device];
+      return ASTR_OK;
+    }
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || n <= 0) {
+    cudaGetLastError();  // clear the sticky-free error so later launches are not blamed
+    return ASTR_ERR_DEVICE;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_sm_count[device] = n;
+  *out = n;
+  return ASTR_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Shape checks common to both paths.
+int check_common(const astr_attn_dims* d) {
+  if (d == nullptr) return ASTR_ERR_INVALID_ARG;
+  if (d->batch < 0 || d->num_qo_heads < 1 || d->num_kv_heads < 1 || d->head_dim < 1 || d->num_slots < 0 ||
+      d->r2t_stride < 0 || d->max_seq_len < 0)
+    return ASTR_ERR_INVALID_ARG;
+  if (d->num_qo_heads % d->num_kv_heads != 0) return ASTR_ERR_UNSUPPORTED;
+  if (d->head_dim != 64 && d->head_dim != 128) return ASTR_ERR_UNSUPPORTED;
+  if (d->r2t_stride < d->max_seq_len) return ASTR_ERR_INVALID_ARG;
+  if (d->batch > 0 && d->max_seq_len > 0 && d->num_slots < 1) return ASTR_ERR_INVALID_ARG;
+  if (d->num_kv_heads > 65535 || d->batch > 65535) return ASTR_ERR_INVALID_ARG;  // grid y / z limits
+  return ASTR_OK;
+}
+
+int plan_splits(const astr_attn_dims* d, int sms) {
+  if (d->num_splits > 0) return d->num_splits;
+  const int64_t units = (int64_t)d->batch * d->num_kv_heads;
+  if (units <= 0) return 1;
+  const int64_t target = (int64_t)sms * kDecodeCtasPerSm;
+  int64_t s = (target + units - 1) / units;
+  const int64_t by_len = ((int64_t)d->max_seq_len + kMinKeysPerSplit - 1) / kMinKeysPerSplit;
+  if (s > by_len) s = by_len;
+  if (s > d->max_splits) s = d->max_splits;
+  if (s < 1) s = 1;
+  return (int)s;
+}
+
+int current_device(int* dev) {
+  if (cudaGetDevice(dev) != cudaSuccess) {
+    cudaGetLastError();
+    return ASTR_ERR_DEVICE;
+  }
+  return ASTR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* astr_attn_status_string(int status) {
+  switch (status) {
+    case ASTR_OK: return "ok";
+    case ASTR_ERR_INVALID_ARG: return "invalid argument (null pointer, negative or inconsistent dims, non-finite scale)";
+    case ASTR_ERR_UNSUPPORTED: return "unsupported shape (head_dim must be 64 or 128; Hq % Hkv == 0; supported group size)";
+    case ASTR_ERR_MISALIGNED: return "misaligned pointer (bf16/fp32 arrays need 16-byte, int32 arrays 4-byte alignment)";
+    case ASTR_ERR_WORKSPACE_TOO_SMALL: return "workspace too small (num_splits above max_splits)";
+    case ASTR_ERR_LAUNCH_FAILED: return "CUDA launch failed";
+    case ASTR_ERR_DEVICE: return "CUDA device query failed";
+    default: return "unknown status";
+  }
+}
+
+int astr_attn_version(void) { return 100; }
+
+int astr_attn_decode_workspace_bytes(const astr_attn_dims* d, size_t* o_bytes, size_t* ml_bytes) {
+  if (d == nullptr || o_bytes == nullptr || ml_bytes == nullptr) return ASTR_ERR_INVALID_ARG;
+  if (d->batch < 0 || d->num_qo_heads < 1 || d->head_dim < 1 || d->max_splits < 1) return ASTR_ERR_INVALID_ARG;
+  const size_t rows = (size_t)d->batch * (size_t)d->num_qo_heads * (size_t)d->max_splits;
+  *o_bytes = rows * (size_t)d->head_dim * sizeof(float);
+  *ml_bytes = rows * 2 * sizeof(float);
+  return ASTR_OK;
+}
+
+int astr_attn_decode_num_splits(const astr_attn_dims* d, int device, int* num_splits) {
+  if (num_splits == nullptr) return ASTR_ERR_INVALID_ARG;
+  int st = check_common(d);
+  if (st != ASTR_OK) return st;
+  if (d->max_splits < 1 || d->num_splits < 0) return ASTR_ERR_INVALID_ARG;
+  if (d->num_splits > d->max_splits) return ASTR_ERR_WORKSPACE_TOO_SMALL;
+  int sms = 0;
+  st = sm_count(device, &sms);
+  if (st != ASTR_OK) return st;
+  *num_splits = plan_splits(d, sms);
+  return ASTR_OK;
+}
+
+static int decode_prepare(const astr_attn_dims* d, float sm_scale, astr::DecodeParams* p, bool* nothing) {
+  int st = check_common(d);
+  if (st != ASTR_OK) return st;
+  if (d->max_splits < 1 || d->num_splits < 0) return ASTR_ERR_INVALID_ARG;
+  if (d->num_splits > d->max_splits) return ASTR_ERR_WORKSPACE_TOO_SMALL;
+  if (!std::isfinite(sm_scale)) return ASTR_ERR_INVALID_ARG;
+  const int G = d->num_qo_heads / d->num_kv_heads;
+  if (!astr::decode_supported(d->head_dim, G)) return ASTR_ERR_UNSUPPORTED;
+  *nothing = (d->batch == 0);
+  int dev = 0, sms = 0;
+  if ((st = current_device(&dev)) != ASTR_OK) return st;
+  if ((st = sm_count(dev, &sms)) != ASTR_OK) return st;
+  p->r2t_stride = d->r2t_stride;
+  p->batch = d->batch;
+  p->num_qo_heads = d->num_qo_heads;
+  p->num_kv_heads = d->num_kv_heads;
+  p->head_dim = d->head_dim;
+  p->num_splits = plan_splits(d, sms);
+  p->part_pitch = d->max_splits;
+  p->scale_log2 = sm_scale * 1.4426950408889634f;
+  if (p->num_splits > d->max_splits) return ASTR_ERR_WORKSPACE_TOO_SMALL;
+  return ASTR_OK;
+}
+
+int astr_attn_paged_decode(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
+                           const int32_t* req_to_token, const int32_t* seq_lens, const int32_t* kv_indptr,
+                           float* o_part, float* ml_part, uint16_t* out, const astr_attn_dims* dims, float sm_scale,
+                           void* stream) {
+  if (!q || !k_pool || !v_pool || !req_to_token || !seq_lens || !kv_indptr || !o_part || !ml_part || !out)
+    return ASTR_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(o_part, 16) ||
+      !aligned(ml_part, 16) || !aligned(out, 16) || !aligned(req_to_token, 4) || !aligned(seq_lens, 4) ||
+      !aligned(kv_indptr, 4))
+    return ASTR_ERR_MISALIGNED;
+  astr::DecodeParams p{};
+  bool nothing = false;
+  int st = decode_prepare(dims, sm_scale, &p, &nothing);
+  if (st != ASTR_OK || nothing) return st;
+  p.q = q; p.k_pool = k_pool; p.v_pool = v_pool; p.req_to_token = req_to_token; p.seq_lens = seq_lens;
+  p.o_part = o_part; p.ml_part = ml_part; p.out = out;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (astr::launch_decode_split(p, s) != cudaSuccess) return ASTR_ERR_LAUNCH_FAILED;
+  if (astr::launch_decode_combine(p, s) != cudaSuccess) return ASTR_ERR_LAUNCH_FAILED;
+  return ASTR_OK;
+}
+
+int astr_attn_decode_split(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
+                           const int32_t* req_to_token, const int32_t* seq_lens, const int32_t* kv_indptr,
+                           float* o_part, float* ml_part, const astr_attn_dims* dims, float sm_scale, void* stream) {
+  if (!q || !k_pool || !v_pool || !req_to_token || !seq_lens || !kv_indptr || !o_part || !ml_part)
+    return ASTR_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(o_part, 16) ||
+      !aligned(ml_part, 16) || !aligned(req_to_token, 4) || !aligned(seq_lens, 4) || !aligned(kv_indptr, 4))
+    return ASTR_ERR_MISALIGNED;
+  astr::DecodeParams p{};
+  bool nothing = false;
+  int st = decode_prepare(dims, sm_scale, &p, &nothing);
+  if (st != ASTR_OK || nothing) return st;
+  p.q = q; p.k_pool = k_pool; p.v_pool = v_pool; p.req_to_token = req_to_token; p.seq_lens = seq_lens;
+  p.o_part = o_part; p.ml_part = ml_part;
+  if (astr::launch_decode_split(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ASTR_ERR_LAUNCH_FAILED;
+  return ASTR_OK;
+}
+
+int astr_attn_decode_combine(const float* o_part, const float* ml_part, const int32_t* seq_lens,
+                             const int32_t* kv_indptr, uint16_t* out, const astr_attn_dims* dims, void* stream) {
+  (void)seq_lens;
+  (void)kv_indptr;
+  if (!o_part || !ml_part || !out) return ASTR_ERR_INVALID_ARG;
+  if (!aligned(o_part, 16) || !aligned(ml_part, 16) || !aligned(out, 16)) return ASTR_ERR_MISALIGNED;
+  astr::DecodeParams p{};
+  bool nothing = false;
+  int st = decode_prepare(dims, 1.0f, &p, &nothing);
+  if (st != ASTR_OK || nothing) return st;
+  p.o_part = const_cast<float*>(o_part);
+  p.ml_part = const_cast<float*>(ml_part);
+  p.out = out;
+  if (astr::launch_decode_combine(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ASTR_ERR_LAUNCH_FAILED;
+  return ASTR_OK;
+}
+
+int astr_attn_prefill_ragged(const uint16_t* q, const int32_t* qo_indptr, const uint16_t* k_pool,
+                             const uint16_t* v_pool, const int32_t* req_to_token, const int32_t* seq_lens,
+                             const int32_t* kv_indptr, uint16_t* out, const astr_attn_dims* d, float sm_scale,
+                             void* stream) {
+  (void)kv_indptr;
+  if (!q || !qo_indptr || !k_pool || !v_pool || !req_to_token || !seq_lens || !out) return ASTR_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16) ||
+      !aligned(qo_indptr, 4) || !aligned(req_to_token, 4) || !aligned(seq_lens, 4) ||
+      (kv_indptr != nullptr && !aligned(kv_indptr, 4)))
+    return ASTR_ERR_MISALIGNED;
+  int st = check_common(d);
+  if (st != ASTR_OK) return st;
+  if (d->total_q < 0 || d->max_q_len < 0 || d->max_q_len > d->max_seq_len) return ASTR_ERR_INVALID_ARG;
+  if (!std::isfinite(sm_scale)) return ASTR_ERR_INVALID_ARG;
+  const int G = d->num_qo_heads / d->num_kv_heads;
+  if (!astr::prefill_supported(d->head_dim, G)) return ASTR_ERR_UNSUPPORTED;
+  if (d->batch == 0 || d->total_q == 0 || d->max_q_len == 0) return ASTR_OK;
+  int dev = 0;
+  if ((st = current_device(&dev)) != ASTR_OK) return st;
+  astr::PrefillParams p{};
+  p.q = q; p.qo_indptr = qo_indptr; p.k_pool = k_pool; p.v_pool = v_pool; p.req_to_token = req_to_token;
+  p.seq_lens = seq_lens; p.out = out;
+  p.r2t_stride = d->r2t_stride;
+  p.batch = d->batch;
+  p.num_qo_heads = d->num_qo_heads;
+  p.num_kv_heads = d->num_kv_heads;
+  p.head_dim = d->head_dim;
+  p.total_q = d->total_q;
+  const int bq = astr::prefill_rows_per_tile() / G;  // query positions per tile
+  const int64_t by_total = ((int64_t)d->total_q + bq - 1) / bq + d->batch;
+  const int64_t by_max = (int64_t)d->batch * (((int64_t)d->max_q_len + bq - 1) / bq);
+  const int64_t tiles = by_total < by_max ? by_total : by_max;
+  if (tiles > 0x7fffffffLL) return ASTR_ERR_INVALID_ARG;
+  p.num_q_tiles = (int)tiles;
+  p.scale_log2 = sm_scale * 1.4426950408889634f;
+  if (astr::launch_prefill(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ASTR_ERR_LAUNCH_FAILED;
+  return ASTR_OK;
+}
+
+}  // extern "C"

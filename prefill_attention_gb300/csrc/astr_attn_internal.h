@@ -1,0 +1,53 @@
+// astr_attn_internal.h -- parameter blocks and launcher declarations shared between the
+// C-ABI layer (api.cu) and the kernel translation units.  Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace astr {
+
+// Decode: one launch of the split kernel followed by one launch of the combine kernel.
+struct DecodeParams {
+  const uint16_t* q;             // [B, Hq, D]
+  const uint16_t* k_pool;        // [num_slots, Hkv, D]
+  const uint16_t* v_pool;
+  const int32_t* req_to_token;   // [B, r2t_stride]
+  const int32_t* seq_lens;       // [B]
+  float* o_part;                 // [B, Hq, part_pitch, D]
+  float* ml_part;                // [B, Hq, part_pitch, 2]
+  uint16_t* out;                 // [B, Hq, D]
+  int64_t r2t_stride;
+  int batch, num_qo_heads, num_kv_heads, head_dim;
+  int num_splits;                // S used by this call
+  int part_pitch;                // splits between consecutive (b, h) rows of o_part (= max_splits)
+  float scale_log2;              // sm_scale * log2(e): logits are kept in base-2 units on chip
+};
+
+// Prefill/extend: one launch of the tensor-core kernel.
+struct PrefillParams {
+  const uint16_t* q;             // [total_q, Hq, D]
+  const int32_t* qo_indptr;      // [B + 1]
+  const uint16_t* k_pool;        // [num_slots, Hkv, D]
+  const uint16_t* v_pool;
+  const int32_t* req_to_token;   // [B, r2t_stride]
+  const int32_t* seq_lens;       // [B]
+  uint16_t* out;                 // [total_q, Hq, D]
+  int64_t r2t_stride;
+  int batch, num_qo_heads, num_kv_heads, head_dim;
+  int total_q;
+  int num_q_tiles;               // grid upper bound on (request, query tile) pairs
+  float scale_log2;
+};
+
+// Launchers return cudaSuccess or the launch error; they never synchronise.
+cudaError_t launch_decode_split(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream);
+
+// Whether the kernels exist for this (head_dim, group size).
+bool decode_supported(int head_dim, int group);
+bool prefill_supported(int head_dim, int group);
+int prefill_rows_per_tile();  // query-head rows per tensor-core tile (M)
+
+}  // namespace astr

@@ -1,0 +1,142 @@
+"""Host-side checks of the C ABI: the library loads, exports what the header declares, and
+rejects bad arguments with the documented status codes before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import prefill_attention_gb300 as pa
+from prefill_attention_gb300 import build as pbuild
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "astr_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pbuild.build()
+    return pa.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(astr_attn_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_and_library_exports_every_entry_point(lib):
+    names = declared_functions()
+    assert set(names) == set(pa.EXPORTED_SYMBOLS), names
+    for n in names:
+        assert hasattr(lib, n), f"missing export {n}"
+
+
+def test_dims_struct_layout_matches_header():
+    # int32 x4, int64, int32 x6 -> 48 bytes (int64 at offset 16, tail padded to 8)
+    assert ctypes.sizeof(pa.Dims) == 48
+    assert pa.Dims.num_slots.offset == 16
+    assert pa.Dims.num_splits.offset == 44
+
+
+def test_status_strings(lib):
+    for st in (0, -1, -2, -3, -4, -5, -6, 17):
+        assert isinstance(pa.astr_attn_status_string(st), str)
+    assert pa.astr_attn_version() >= 100
+
+
+def _dims(**kw):
+    base = dict(batch=4, num_qo_heads=32, num_kv_heads=8, head_dim=128, num_slots=1000, r2t_stride=2000,
+                max_seq_len=2000, total_q=64, max_q_len=16, max_splits=8, num_splits=0)
+    base.update(kw)
+    return pa.make_dims(**base)
+
+
+A = 1 << 20  # fake, 16-byte aligned device addresses: validation fails before any dereference
+
+
+def _dec(d, **ptr):
+    p = dict(q=A, k=A, v=A, r2t=A, seq=A, kvi=A, o=A, ml=A, out=A)
+    p.update(ptr)
+    return pa.astr_attn_paged_decode(p["q"], p["k"], p["v"], p["r2t"], p["seq"], p["kvi"], p["o"], p["ml"],
+                                     p["out"], d, 0.1, stream=0, check=False)
+
+
+def _pf(d, scale=0.1, **ptr):
+    p = dict(q=A, qo=A, k=A, v=A, r2t=A, seq=A, kvi=A, out=A)
+    p.update(ptr)
+    return pa.astr_attn_prefill_ragged(p["q"], p["qo"], p["k"], p["v"], p["r2t"], p["seq"], p["kvi"], p["out"], d,
+                                       scale, stream=0, check=False)
+
+
+@pytest.mark.parametrize("name", ["q", "k", "v", "r2t", "seq", "kvi", "o", "ml", "out"])
+def test_decode_null_pointer(lib, name):
+    assert _dec(_dims(), **{name: 0}) == pa.ASTR_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("name,addr", [("q", A + 8), ("k", A + 2), ("out", A + 4), ("o", A + 4), ("ml", A + 8),
+                                       ("r2t", A + 2), ("seq", A + 1)])
+def test_decode_misaligned(lib, name, addr):
+    assert _dec(_dims(), **{name: addr}) == pa.ASTR_ERR_MISALIGNED
+
+
+def test_int_arrays_need_only_4_byte_alignment(lib):
+    # 4-byte aligned int32 arrays pass the alignment check and fail later on the bad head_dim
+    assert _dec(_dims(head_dim=96), r2t=A + 4, seq=A + 4, kvi=A + 12) == pa.ASTR_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(head_dim=96), pa.ASTR_ERR_UNSUPPORTED),
+    (dict(head_dim=256), pa.ASTR_ERR_UNSUPPORTED),
+    (dict(num_qo_heads=30, num_kv_heads=8), pa.ASTR_ERR_UNSUPPORTED),
+    (dict(num_qo_heads=128, num_kv_heads=4), pa.ASTR_ERR_UNSUPPORTED),   # decode group 32 not built
+    (dict(batch=-1), pa.ASTR_ERR_INVALID_ARG),
+    (dict(num_kv_heads=0), pa.ASTR_ERR_INVALID_ARG),
+    (dict(r2t_stride=100), pa.ASTR_ERR_INVALID_ARG),                      # stride below max_seq_len
+    (dict(max_splits=0), pa.ASTR_ERR_INVALID_ARG),
+    (dict(num_splits=9), pa.ASTR_ERR_WORKSPACE_TOO_SMALL),
+    (dict(num_splits=-1), pa.ASTR_ERR_INVALID_ARG),
+    (dict(num_slots=0), pa.ASTR_ERR_INVALID_ARG),
+])
+def test_decode_bad_dims(lib, kw, status):
+    assert _dec(_dims(**kw)) == status
+
+
+def test_decode_non_finite_scale(lib):
+    st = pa.astr_attn_paged_decode(A, A, A, A, A, A, A, A, A, _dims(), float("nan"), stream=0, check=False)
+    assert st == pa.ASTR_ERR_INVALID_ARG
+
+
+def test_decode_null_dims(lib):
+    st = lib.astr_attn_paged_decode(A, A, A, A, A, A, A, A, A, None, ctypes.c_float(0.1), None)
+    assert st == pa.ASTR_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("name", ["q", "qo", "k", "v", "r2t", "seq", "out"])
+def test_prefill_null_pointer(lib, name):
+    assert _pf(_dims(), **{name: 0}) == pa.ASTR_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(head_dim=80), pa.ASTR_ERR_UNSUPPORTED),
+    (dict(num_qo_heads=12, num_kv_heads=8), pa.ASTR_ERR_UNSUPPORTED),
+    (dict(num_qo_heads=96, num_kv_heads=3), pa.ASTR_ERR_UNSUPPORTED),    # group 32 not built
+    (dict(total_q=-1), pa.ASTR_ERR_INVALID_ARG),
+    (dict(max_q_len=3000), pa.ASTR_ERR_INVALID_ARG),                    # q_len bound above max_seq_len
+])
+def test_prefill_bad_dims(lib, kw, status):
+    assert _pf(_dims(**kw)) == status
+
+
+def test_prefill_misaligned(lib):
+    assert _pf(_dims(), q=A + 2) == pa.ASTR_ERR_MISALIGNED
+    assert _pf(_dims(), qo=A + 2) == pa.ASTR_ERR_MISALIGNED
+    assert _pf(_dims(), kvi=A + 1) == pa.ASTR_ERR_MISALIGNED
+
+
+def test_prefill_kv_indptr_may_be_null_and_empty_batch_is_noop(lib):
+    # batch 0 returns OK without launching (and without a GPU)
+    assert _pf(_dims(batch=0), kvi=0) == pa.ASTR_OK
+
+
+def test_workspace_bytes(lib):
+    ob, mb = pa.astr_attn_decode_workspace_bytes(_dims(batch=32, max_splits=5))
+    assert ob == 32 * 32 * 5 * 128 * 4 and mb == 32 * 32 * 5 * 2 * 4

@@ -1,0 +1,226 @@
+"""GPU parity of the split-KV paged decode (C ABI) against the fp64 oracle.
+
+Tolerance: max abs error <= 1e-2 on bf16 outputs; slot-table routing bit-exact.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workload
+from workload import bf16_bits_to_fp32, fp32_to_bf16_bits, make_from_lengths
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+import prefill_attention_gb300 as pa  # noqa: E402
+from gpu_util import TOL, run_decode, sample_rows, to_f64, upload, decode_dims  # noqa: E402
+
+
+def _err(got, ref):
+    return float(np.abs(got - ref).max())
+
+
+@pytest.mark.parametrize("cfg", [1, 2])
+def test_decode_config_full(cfg):
+    w = workload.config(cfg)
+    got = to_f64(run_decode(w))
+    assert _err(got, oracle.decode(w)) <= TOL
+
+
+@pytest.mark.parametrize("cfg", [3, 4])
+def test_decode_config_sampled(cfg):
+    w = workload.config(cfg)
+    out = to_f64(run_decode(w))
+    rows = sample_rows(np.random.default_rng(cfg), w.batch, w.num_qo_heads, 48)
+    ref = oracle.decode(w, rows=rows)
+    got = out[rows[:, 0], rows[:, 1]]
+    assert _err(got, ref) <= TOL
+    assert np.isfinite(out).all()
+
+
+@pytest.mark.parametrize("S", [1, 2, 3, 5, 16, 32])
+def test_forced_split_counts(S):
+    w = workload.config(1)
+    got = to_f64(run_decode(w, max_splits=32, num_splits=S))
+    assert _err(got, oracle.decode(w)) <= TOL
+
+
+@pytest.mark.parametrize("d,Hq,Hkv", [(128, 32, 8), (128, 8, 8), (128, 16, 8), (128, 64, 8),
+                                      (64, 8, 2), (64, 4, 4), (64, 8, 4), (64, 16, 2)])
+def test_head_shapes_and_ragged_tails(d, Hq, Hkv):
+    rng = np.random.default_rng(d * 1000 + Hq * 10 + Hkv)
+    seq = [1, 7, 8, 9, 31, 33, 64, 65, 200, 257]
+    w = make_from_lengths(rng, kind="decode", name="shapes", seq_lens=seq, q_lens=None, Hq=Hq, Hkv=Hkv, d=d)
+    for S in (0, 1, 4):
+        got = to_f64(run_decode(w, num_splits=S))
+        assert _err(got, oracle.decode(w)) <= TOL, f"S={S}"
+
+
+def test_partials_match_oracle_split():
+    w = workload.config(1)
+    S = 3
+    out, o, ml, S_used = run_decode(w, max_splits=8, num_splits=S, return_parts=True)
+    assert S_used == S
+    o_ref, ml_ref = oracle.decode_split_partials(w, S)
+    m, l = ml[..., 0], ml[..., 1]
+    assert np.array_equal(np.isneginf(m), np.isneginf(ml_ref[..., 0]))
+    fin = np.isfinite(ml_ref[..., 0])
+    assert np.abs(m[fin] - ml_ref[..., 0][fin]).max() <= 1e-3
+    assert np.abs(l[fin] / ml_ref[..., 1][fin] - 1).max() <= 1e-3
+    np.testing.assert_array_equal(l[~fin], 0)
+    norm = o[fin] / l[fin][:, None]
+    norm_ref = o_ref[fin] / ml_ref[..., 1][fin][:, None]
+    assert np.abs(norm - norm_ref).max() <= TOL
+
+
+def test_combine_alone_on_oracle_partials():
+    w = workload.config(1)
+    S = 4
+    o_ref, ml_ref = oracle.decode_split_partials(w, S)
+    dims = decode_dims(w, max_splits=S, num_splits=S)
+    o_part = torch.from_numpy(o_ref.astype(np.float32)).cuda().contiguous()
+    ml_part = torch.from_numpy(ml_ref.astype(np.float32)).cuda().contiguous()
+    out = torch.empty((w.batch, w.num_qo_heads, w.head_dim), dtype=torch.bfloat16, device="cuda")
+    pa.astr_attn_decode_combine(o_part, ml_part, None, None, out, dims)
+    torch.cuda.synchronize()
+    assert _err(to_f64(out), oracle.combine(o_ref, ml_ref)) <= TOL
+
+
+def test_deterministic_bits():
+    w = workload.config(2)
+    t = upload(w)
+    a = run_decode(w, t).view(torch.int16).cpu().numpy()
+    b = run_decode(w, t).view(torch.int16).cpu().numpy()
+    assert np.array_equal(a, b)
+
+
+def test_slot_permutation_bit_exact():
+    """Paged == contiguous: identity slot table vs a permuted one, same S, same bits."""
+    rng = np.random.default_rng(5)
+    w = make_from_lengths(rng, kind="decode", name="perm", seq_lens=[100, 37, 512, 1], q_lens=None, Hq=32, Hkv=8,
+                          d=128)
+    T = w.num_slots
+    # contiguous: token j of request b in slot kv_indptr[b] + j
+    k_c = np.empty_like(w.k_pool); v_c = np.empty_like(w.v_pool)
+    r2t_c = np.zeros_like(w.req_to_token)
+    for b in range(w.batch):
+        n = w.seq_lens[b]
+        src = w.req_to_token[b, :n]
+        dst = np.arange(w.kv_indptr[b], w.kv_indptr[b] + n)
+        k_c[dst] = w.k_pool[src]; v_c[dst] = w.v_pool[src]
+        r2t_c[b, :n] = dst
+    wc = workload.Workload(**{**w.__dict__, "k_pool": k_c, "v_pool": v_c, "req_to_token": r2t_c})
+    a = run_decode(w, num_splits=3).view(torch.int16).cpu().numpy()
+    b = run_decode(wc, num_splits=3).view(torch.int16).cpu().numpy()
+    assert np.array_equal(a, b)
+    assert T == int(w.seq_lens.sum())
+
+
+def test_per_request_marker_exact():
+    rng = np.random.default_rng(6)
+    seq = [5, 300, 64, 1000, 2, 129]
+    w = make_from_lengths(rng, kind="decode", name="marker", seq_lens=seq, q_lens=None, Hq=32, Hkv=8, d=128)
+    for b in range(w.batch):
+        sl = w.req_to_token[b, :seq[b]]
+        w.v_pool[sl] = fp32_to_bf16_bits(np.full((len(sl), 8, 128), b + 1, np.float32))
+    got = to_f64(run_decode(w))
+    ref = np.broadcast_to((np.arange(w.batch) + 1.0)[:, None, None], got.shape)
+    assert np.array_equal(got, ref)
+
+
+def test_single_key_returns_v_exactly():
+    rng = np.random.default_rng(8)
+    w = make_from_lengths(rng, kind="decode", name="one", seq_lens=[1] * 5, q_lens=None, Hq=32, Hkv=8, d=128)
+    got = to_f64(run_decode(w))
+    v = bf16_bits_to_fp32(w.v_pool).astype(np.float64)
+    for b in range(5):
+        for h in range(32):
+            assert np.array_equal(got[b, h], v[w.req_to_token[b, 0], h // 4])
+
+
+def test_poisoned_unreferenced_slots_are_never_read():
+    rng = np.random.default_rng(9)
+    seq = np.array([50, 3, 700, 129])
+    w = make_from_lengths(rng, kind="decode", name="poison", seq_lens=seq, q_lens=None, Hq=32, Hkv=8, d=128,
+                          extra_slots=64, stride=1024)
+    base = to_f64(run_decode(w, num_splits=5))
+    T = int(seq.sum())
+    w.k_pool[T:] = 0x7FC0
+    w.v_pool[T:] = 0x7FC0
+    for b in range(w.batch):
+        w.req_to_token[b, seq[b]:] = T + (b * 7) % 64
+    got = to_f64(run_decode(w, num_splits=5))
+    assert np.isfinite(got).all()
+    assert np.array_equal(base, got)
+
+
+def test_zero_length_request_gives_zeros():
+    rng = np.random.default_rng(10)
+    w = make_from_lengths(rng, kind="decode", name="empty", seq_lens=[0, 40, 0, 3], q_lens=None, Hq=8, Hkv=2, d=64,
+                          stride=64)
+    got = to_f64(run_decode(w, num_splits=4))
+    assert np.all(got[0] == 0) and np.all(got[2] == 0)
+    assert _err(got, oracle.decode(w)) <= TOL
+
+
+def test_q_zero_is_mean_of_v():
+    rng = np.random.default_rng(11)
+    w = make_from_lengths(rng, kind="decode", name="q0", seq_lens=[10, 999, 64], q_lens=None, Hq=32, Hkv=8, d=128)
+    w.q[:] = 0
+    got = to_f64(run_decode(w))
+    v = bf16_bits_to_fp32(w.v_pool).astype(np.float64)
+    for b in range(w.batch):
+        ref = v[w.req_to_token[b, :w.seq_lens[b]]].mean(axis=0)  # [Hkv, d]
+        assert np.abs(got[b] - np.repeat(ref, 4, axis=0)).max() <= TOL
+
+
+def test_runs_on_callers_stream():
+    w = workload.config(1)
+    t = upload(w)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        out = run_decode(w, t, stream=s)
+    assert _err(to_f64(out), oracle.decode(w)) <= TOL
+
+
+def test_cuda_graph_replay_bit_exact():
+    w = workload.config(2)
+    t = upload(w)
+    dims = decode_dims(w, max_splits=32)
+    o_part, ml_part = pa.alloc_decode_workspace(dims)
+    out = torch.empty_like(t["q"])
+    args = (t["q"], t["k"], t["v"], t["r2t"], t["seq"], t["kvi"], o_part, ml_part, out, dims, w.sm_scale)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        pa.astr_attn_paged_decode(*args, stream=s)   # eager run (also sets kernel attributes)
+    torch.cuda.synchronize()
+    eager = out.clone()
+    out.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        pa.astr_attn_paged_decode(*args, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+
+
+def test_guard_bands_untouched():
+    w = workload.config(1)
+    t = upload(w)
+    dims = decode_dims(w, max_splits=8)
+    ob, mb = pa.astr_attn_decode_workspace_bytes(dims)
+    pad = 256
+    o_buf = torch.full((ob // 4 + 2 * pad,), 12345.0, device="cuda")
+    m_buf = torch.full((mb // 4 + 2 * pad,), 12345.0, device="cuda")
+    n_out = w.batch * w.num_qo_heads * w.head_dim
+    out_buf = torch.full((n_out + 2 * pad,), 7.0, device="cuda", dtype=torch.bfloat16)
+    pa.astr_attn_paged_decode(t["q"], t["k"], t["v"], t["r2t"], t["seq"], t["kvi"], o_buf[pad:pad + ob // 4],
+                              m_buf[pad:pad + mb // 4], out_buf[pad:pad + n_out], dims, w.sm_scale)
+    torch.cuda.synchronize()
+    for buf, n, val in ((o_buf, ob // 4, 12345.0), (m_buf, mb // 4, 12345.0), (out_buf, n_out, 7.0)):
+        assert torch.all(buf[:pad] == val) and torch.all(buf[pad + n:] == val)
+    got = to_f64(out_buf[pad:pad + n_out].view(w.batch, w.num_qo_heads, w.head_dim))
+    assert _err(got, oracle.decode(w)) <= TOL
