@@ -95,6 +95,26 @@ def recorded_traffic(kernel: str, source: str):
     return rec.get("bytes_per_launch")
 
 
+# ------------------------------------------------------------------ multi-rank aggregation
+
+
+def rank_reduce(dist, x: float, op: str, device=None) -> float:
+    """Reduce one float over ranks ("max" or "sum"); identity without a process group."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def aggregate_weak(dist, elapsed_s: float, units: float, device=None):
+    """Weak scaling: job time = slowest rank, job work = every rank's units."""
+    t = rank_reduce(dist, elapsed_s, "max", device)
+    u = rank_reduce(dist, units, "sum", device)
+    return t, u, (u / t if t > 0 else 0.0)
+
+
 # ------------------------------------------------------------------ clocks
 
 
@@ -237,18 +257,10 @@ def main():
         torch.cuda.synchronize()
 
     def max_over_ranks(x: float) -> float:
-        if dist is None:
-            return x
-        t = torch.tensor([x], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return rank_reduce(dist, x, "max", dev)
 
     def sum_over_ranks(x: float) -> float:
-        if dist is None:
-            return x
-        t = torch.tensor([x], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.SUM)
-        return float(t.item())
+        return rank_reduce(dist, x, "sum", dev)
 
     peaks, peaks_src = load_peaks()
 
@@ -307,9 +319,8 @@ def main():
     elapsed = timed(decode, args.steps)
     barrier()
     clk = clocks.stop()
-    elapsed_max = max_over_ranks(elapsed)
-    total_kv = sum_over_ranks(float(nbytes["kv"]) * args.steps)
-    value = total_kv / elapsed_max / 1e9
+    elapsed_max, total_kv, bytes_per_s = aggregate_weak(dist, elapsed, float(nbytes["kv"]) * args.steps, dev)
+    value = bytes_per_s / 1e9
     us_per_call = elapsed_max / args.steps * 1e6
 
     # ---------------- the split kernel alone (roofline of the dominant kernel)
@@ -435,7 +446,7 @@ def main():
                    "kv_bytes_per_call": nbytes["kv"], "total_keys": int(w.seq_lens.sum()),
                    "l2": f"rotating {POOL_COPIES} KV-pool copies ({POOL_COPIES * nbytes['kv'] / 1e6:.0f} MB > L2)",
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "kernel": "decode_split_kernel<128,4>", "achieved": round(split_gbs, 2),
+        "roofline": {"bound": "hbm", "kernel": "decode_split_tc_kernel<128,4>", "achieved": round(split_gbs, 2),
                      "peak": peaks["hbm_gbs"], "peak_source": f"hbm_gbs ({peaks_src})", "unit": "GB/s",
                      "frac": round(split_gbs / peaks["hbm_gbs"], 4), "us_per_launch": round(t_split * 1e6, 3),
                      "traffic": traffic},

@@ -64,7 +64,7 @@ typedef enum astr_status {
   ASTR_ERR_INVALID_ARG = -1,          /* null pointer, negative or inconsistent dims, non-finite sm_scale */
   ASTR_ERR_UNSUPPORTED = -2,          /* head_dim not 64/128, Hq % Hkv != 0, group size not supported */
   ASTR_ERR_MISALIGNED = -3,           /* a pointer breaks the alignment rule above */
-  ASTR_ERR_WORKSPACE_TOO_SMALL = -4,  /* max_splits below what the call needs */
+  ASTR_ERR_WORKSPACE_TOO_SMALL = -4,  /* explicit combine layout: num_splits above max_splits */
   ASTR_ERR_LAUNCH_FAILED = -5,        /* a CUDA launch or attribute call failed (cudaGetLastError) */
   ASTR_ERR_DEVICE = -6                /* querying the current device failed */
 } astr_status;
@@ -77,18 +77,25 @@ typedef struct astr_attn_dims {
   int32_t head_dim;      /* 64 or 128 */
   int64_t num_slots;     /* rows of k_pool / v_pool */
   int32_t r2t_stride;    /* elements between consecutive req_to_token rows */
-  int32_t max_seq_len;   /* host-known upper bound of seq_lens (plans the split count) */
+  int32_t max_seq_len;   /* host-known upper bound of seq_lens (bounds the partials per request) */
   int32_t total_q;       /* prefill: flat query rows (= qo_indptr[batch]); ignored by decode */
   int32_t max_q_len;     /* prefill: upper bound of q_len (sizes the grid); ignored by decode */
-  int32_t max_splits;    /* decode: split capacity of o_part / ml_part (>= 1) */
-  int32_t num_splits;    /* decode: 0 = plan automatically, > 0 forces this split count */
+  int32_t max_splits;    /* decode: partial slots per (request, head) in o_part / ml_part (>= 1) */
+  int32_t num_splits;    /* decode: key chunks per KV head; 0 = plan automatically (one wave) */
 } astr_attn_dims;
 
 /*
- * Split count the decode call will use for these dims on `device` (P3, shared-helpers
- * commit: the split count is chosen per call).  Chosen so that batch * Hkv * splits
- * CTAs fill the GPU's SMs, bounded by max_splits and by max_seq_len (at least a few
- * dozen keys per split).  Depends only on host-known values, never on seq_lens contents.
+ * Decode split schedule (P3, shared-helpers commit: the split count is chosen per call;
+ * P3, kv_indptr commit: kv_indptr is built once per step and drives it here).
+ * The batch's keys are laid end to end in kv_indptr order, T = kv_indptr[batch], and for
+ * every KV head cut into `num_splits` chunks of C keys, one CTA per chunk:
+ *   C = max(round_up(ceil(T / num_splits), 16), F),  F = max(16, ceil(max_seq_len / (max_splits - 1)))
+ *   (C = T when max_splits == 1), so every CTA reads the same number of K/V bytes.
+ * Request b overlaps chunks kv_indptr[b] / C .. (kv_indptr[b+1] - 1) / C; the piece of it
+ * in chunk c becomes partial slot c - kv_indptr[b] / C of (b, h), and the floor F keeps
+ * that below max_splits.  This call returns num_splits as planned for `device`: the
+ * forced dims->num_splits if > 0, else ceil(#SMs / Hkv) (one persistent CTA per SM).
+ * Depends only on host-known values, never on the contents of seq_lens.
  * Errors: INVALID_ARG (null, bad dims), DEVICE (device query failed).
  */
 int astr_attn_decode_num_splits(const astr_attn_dims* dims, int device, int* num_splits);
@@ -103,13 +110,14 @@ int astr_attn_decode_workspace_bytes(const astr_attn_dims* dims, size_t* o_part_
  * Split-KV paged decode (one query row per request).
  *   out[b, h, :] = sum_{j < seq_lens[b]} softmax_j(sm_scale * <q[b,h], K_j>) V_j,
  *   K_j, V_j = pool[req_to_token[b * r2t_stride + j], h / G, :].
- * Launches the split kernel (each split owns a contiguous range of one request's keys
- * for one KV head and all G query heads sharing it, and writes o_part/ml_part for every
- * split it owns, empty ones as m = -inf, l = 0, o = 0) and then the combine kernel.
- * ml_part m is the max scaled logit in natural-log units; o_part is unnormalised.
- * seq_lens[b] = 0 gives a zero output row.  Deterministic for fixed dims.
- * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, WORKSPACE_TOO_SMALL (forced num_splits
- * above max_splits), DEVICE, LAUNCH_FAILED.
+ * Launches the split kernel (schedule as for astr_attn_decode_num_splits; each chunk serves
+ * all G query heads of its KV head from one K/V load; a request that lies entirely inside
+ * one chunk has its output written directly; every other request piece writes its partial
+ * slot: o_part unnormalised, ml_part = (max scaled logit in natural-log units, sum of
+ * exponentials)) and then the combine kernel for the requests that span several chunks.
+ * Slots that no piece maps to are left untouched.  seq_lens[b] = 0 gives a zero output
+ * row.  Deterministic for fixed dims (no atomics).
+ * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, DEVICE, LAUNCH_FAILED.
  */
 int astr_attn_paged_decode(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
                            const int32_t* req_to_token, const int32_t* seq_lens, const int32_t* kv_indptr,
@@ -117,10 +125,10 @@ int astr_attn_paged_decode(const uint16_t* q, const uint16_t* k_pool, const uint
                            float sm_scale, void* stream);
 
 /*
- * The split step alone: the first of the two launches of astr_attn_paged_decode.  Writes
- * o_part / ml_part for every split (num_splits as planned for `dims`) and nothing else;
- * astr_attn_decode_combine then produces `out`.  Same arguments, rules and errors as
- * astr_attn_paged_decode minus `out`.
+ * The split step alone: the first of the two launches of astr_attn_paged_decode, except that
+ * every request piece (also single-chunk requests) writes its partial slot; nothing else is
+ * written.  astr_attn_decode_combine with the same kv_indptr then produces `out`.  Same
+ * arguments, rules and errors as astr_attn_paged_decode minus `out`.
  */
 int astr_attn_decode_split(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
                            const int32_t* req_to_token, const int32_t* seq_lens, const int32_t* kv_indptr,
@@ -128,10 +136,13 @@ int astr_attn_decode_split(const uint16_t* q, const uint16_t* k_pool, const uint
 
 /*
  * The combine step alone (P3, kernel-rename commit: the log-sum-exp merge shared by the
- * split paths): for each (b, h) with S = num_splits as planned for `dims`,
+ * split paths): for each (b, h) over its S partial slots,
  *   M = max_s m_s,  w_s = exp(m_s - M),  out = (sum_s w_s o_s) / (sum_s w_s l_s)  -> bf16.
- * A row whose splits are all empty (M = -inf) is written as zeros.  Reads only o_part,
- * ml_part; seq_lens and kv_indptr may be NULL.  Errors as astr_attn_paged_decode.
+ * With kv_indptr given, S is the number of chunks request b overlaps under the schedule
+ * of astr_attn_decode_num_splits (the layout astr_attn_decode_split writes).  With
+ * kv_indptr NULL, every row holds S = dims->num_splits slots (1 <= S <= max_splits, else
+ * INVALID_ARG / WORKSPACE_TOO_SMALL).  A row with S = 0 or all m_s = -inf is written as
+ * zeros.  seq_lens is not read (may be NULL).  Errors as astr_attn_paged_decode.
  */
 int astr_attn_decode_combine(const float* o_part, const float* ml_part, const int32_t* seq_lens,
                              const int32_t* kv_indptr, uint16_t* out, const astr_attn_dims* dims, void* stream);

@@ -21,7 +21,8 @@ _SRC = os.path.join(_HERE, "attn_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lib = None
 
-__all__ = ["build", "lib_path", "decode", "prefill", "decode_split_partials", "combine", "load_variant"]
+__all__ = ["build", "lib_path", "decode", "prefill", "decode_split_partials", "decode_chunk_partials",
+           "chunk_split_counts", "combine", "load_variant"]
 
 
 def _compile(src: str, out: str, extra: Sequence[str] = ()) -> None:
@@ -53,7 +54,9 @@ def _declare(lib):
     lib.oracle_prefill_rows.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _P, _L, _P, _D, _L, _P, _P, _P, _I]
     lib.oracle_decode_split_partials.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _L, _P, _D, _I, _P, _P, _I]
     lib.oracle_combine.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P]
-    for f in ("oracle_decode_rows", "oracle_prefill_rows", "oracle_decode_split_partials", "oracle_combine"):
+    lib.oracle_decode_chunk_partials.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _L, _P, _P, _D, _L, _I, _P, _P]
+    for f in ("oracle_decode_rows", "oracle_prefill_rows", "oracle_decode_split_partials", "oracle_combine",
+              "oracle_decode_chunk_partials"):
         getattr(lib, f).restype = None
     return lib
 
@@ -139,6 +142,29 @@ def decode_split_partials(w, S: int, nthreads: Optional[int] = None, lib=None):
     lib.oracle_decode_split_partials(B, Hq, Hkv, D, _ptr(q), _ptr(kp), _ptr(vp), _ptr(r2t), r2t.shape[1],
                                      _ptr(sl), float(w.sm_scale), int(S), _ptr(o), _ptr(ml), _threads(nthreads))
     return o, ml
+
+
+def decode_chunk_partials(w, C: int, pitch: int, lib=None):
+    """Token-balanced chunk partials (chunks of C keys over the batch's flat key space).
+
+    Returns (o_part [B,Hq,pitch,d], ml_part [B,Hq,pitch,2], nsplit [B]); unused slots hold NaN.
+    """
+    lib = lib or _get()
+    B, Hq, Hkv, D = w.batch, w.num_qo_heads, w.num_kv_heads, w.head_dim
+    o = np.full((B, Hq, pitch, D), np.nan, dtype=np.float64)
+    ml = np.full((B, Hq, pitch, 2), np.nan, dtype=np.float64)
+    q, kp, vp = _c(w.q, np.uint16), _c(w.k_pool, np.uint16), _c(w.v_pool, np.uint16)
+    r2t, sl, ki = _c(w.req_to_token, np.int32), _c(w.seq_lens, np.int32), _c(w.kv_indptr, np.int32)
+    lib.oracle_decode_chunk_partials(B, Hq, Hkv, D, _ptr(q), _ptr(kp), _ptr(vp), _ptr(r2t), r2t.shape[1], _ptr(sl),
+                                     _ptr(ki), float(w.sm_scale), int(C), int(pitch), _ptr(o), _ptr(ml))
+    return o, ml, chunk_split_counts(w.kv_indptr, C)
+
+
+def chunk_split_counts(kv_indptr, C: int) -> np.ndarray:
+    """Number of C-key chunks that overlap each request."""
+    ind = np.asarray(kv_indptr, dtype=np.int64)
+    a, e = ind[:-1], ind[1:]
+    return np.where(e > a, (e - 1) // C - a // C + 1, 0).astype(np.int32)
 
 
 def combine(o_part: np.ndarray, ml_part: np.ndarray, nsplit: Optional[np.ndarray] = None, lib=None) -> np.ndarray:

@@ -13,8 +13,7 @@
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kDecodeCtasPerSm = 3;     // resident split-kernel CTAs per SM (launch bounds)
-constexpr int kMinKeysPerSplit = 64;    // below this a split is mostly fixed cost
+constexpr int kDecodeCtasPerSm = 1;     // the split kernel is persistent: one CTA per SM
 
 std::mutex g_mu;
 int g_sm_count[kMaxDevices] = {0};
@@ -55,17 +54,22 @@ int check_common(const astr_attn_dims* d) {
   return ASTR_OK;
 }
 
+// Key chunks per KV head: one wave of persistent CTAs, kv heads x chunks = SMs.
 int plan_splits(const astr_attn_dims* d, int sms) {
   if (d->num_splits > 0) return d->num_splits;
-  const int64_t units = (int64_t)d->batch * d->num_kv_heads;
-  if (units <= 0) return 1;
   const int64_t target = (int64_t)sms * kDecodeCtasPerSm;
-  int64_t s = (target + units - 1) / units;
-  const int64_t by_len = ((int64_t)d->max_seq_len + kMinKeysPerSplit - 1) / kMinKeysPerSplit;
-  if (s > by_len) s = by_len;
-  if (s > d->max_splits) s = d->max_splits;
+  int64_t s = (target + d->num_kv_heads - 1) / d->num_kv_heads;
   if (s < 1) s = 1;
   return (int)s;
+}
+
+// Floor on the chunk length: a request of max_seq_len keys overlaps at most
+// ceil(max_seq_len / C) + 1 chunks, which must fit in max_splits partial slots.
+int plan_min_chunk(const astr_attn_dims* d) {
+  if (d->max_splits <= 1) return 1;  // single chunk per KV head (the kernel uses C = T)
+  int64_t c = ((int64_t)d->max_seq_len + d->max_splits - 2) / (d->max_splits - 1);
+  if (c < 16) c = 16;
+  return (int)c;
 }
 
 int current_device(int* dev) {
@@ -109,7 +113,6 @@ int astr_attn_decode_num_splits(const astr_attn_dims* d, int device, int* num_sp
   int st = check_common(d);
   if (st != ASTR_OK) return st;
   if (d->max_splits < 1 || d->num_splits < 0) return ASTR_ERR_INVALID_ARG;
-  if (d->num_splits > d->max_splits) return ASTR_ERR_WORKSPACE_TOO_SMALL;
   int sms = 0;
   st = sm_count(device, &sms);
   if (st != ASTR_OK) return st;
@@ -121,7 +124,6 @@ static int decode_prepare(const astr_attn_dims* d, float sm_scale, astr::DecodeP
   int st = check_common(d);
   if (st != ASTR_OK) return st;
   if (d->max_splits < 1 || d->num_splits < 0) return ASTR_ERR_INVALID_ARG;
-  if (d->num_splits > d->max_splits) return ASTR_ERR_WORKSPACE_TOO_SMALL;
   if (!std::isfinite(sm_scale)) return ASTR_ERR_INVALID_ARG;
   const int G = d->num_qo_heads / d->num_kv_heads;
   if (!astr::decode_supported(d->head_dim, G)) return ASTR_ERR_UNSUPPORTED;
@@ -129,15 +131,18 @@ static int decode_prepare(const astr_attn_dims* d, float sm_scale, astr::DecodeP
   int dev = 0, sms = 0;
   if ((st = current_device(&dev)) != ASTR_OK) return st;
   if ((st = sm_count(dev, &sms)) != ASTR_OK) return st;
+  if (d->num_slots * (int64_t)d->num_kv_heads > 0x7fffffffLL) return ASTR_ERR_INVALID_ARG;  // TMA row index
   p->r2t_stride = d->r2t_stride;
+  p->num_slots = d->num_slots;
   p->batch = d->batch;
   p->num_qo_heads = d->num_qo_heads;
   p->num_kv_heads = d->num_kv_heads;
   p->head_dim = d->head_dim;
   p->num_splits = plan_splits(d, sms);
   p->part_pitch = d->max_splits;
+  p->min_chunk = plan_min_chunk(d);
   p->scale_log2 = sm_scale * 1.4426950408889634f;
-  if (p->num_splits > d->max_splits) return ASTR_ERR_WORKSPACE_TOO_SMALL;
+  if (p->num_splits > 0x7fffffff / 2) return ASTR_ERR_INVALID_ARG;
   return ASTR_OK;
 }
 
@@ -156,7 +161,7 @@ int astr_attn_paged_decode(const uint16_t* q, const uint16_t* k_pool, const uint
   int st = decode_prepare(dims, sm_scale, &p, &nothing);
   if (st != ASTR_OK || nothing) return st;
   p.q = q; p.k_pool = k_pool; p.v_pool = v_pool; p.req_to_token = req_to_token; p.seq_lens = seq_lens;
-  p.o_part = o_part; p.ml_part = ml_part; p.out = out;
+  p.kv_indptr = kv_indptr; p.o_part = o_part; p.ml_part = ml_part; p.out = out;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (astr::launch_decode_split(p, s) != cudaSuccess) return ASTR_ERR_LAUNCH_FAILED;
   if (astr::launch_decode_combine(p, s) != cudaSuccess) return ASTR_ERR_LAUNCH_FAILED;
@@ -176,7 +181,7 @@ int astr_attn_decode_split(const uint16_t* q, const uint16_t* k_pool, const uint
   int st = decode_prepare(dims, sm_scale, &p, &nothing);
   if (st != ASTR_OK || nothing) return st;
   p.q = q; p.k_pool = k_pool; p.v_pool = v_pool; p.req_to_token = req_to_token; p.seq_lens = seq_lens;
-  p.o_part = o_part; p.ml_part = ml_part;
+  p.kv_indptr = kv_indptr; p.o_part = o_part; p.ml_part = ml_part;
   if (astr::launch_decode_split(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ASTR_ERR_LAUNCH_FAILED;
   return ASTR_OK;
 }
@@ -184,13 +189,20 @@ int astr_attn_decode_split(const uint16_t* q, const uint16_t* k_pool, const uint
 int astr_attn_decode_combine(const float* o_part, const float* ml_part, const int32_t* seq_lens,
                              const int32_t* kv_indptr, uint16_t* out, const astr_attn_dims* dims, void* stream) {
   (void)seq_lens;
-  (void)kv_indptr;
   if (!o_part || !ml_part || !out) return ASTR_ERR_INVALID_ARG;
-  if (!aligned(o_part, 16) || !aligned(ml_part, 16) || !aligned(out, 16)) return ASTR_ERR_MISALIGNED;
+  if (!aligned(o_part, 16) || !aligned(ml_part, 16) || !aligned(out, 16) ||
+      (kv_indptr != nullptr && !aligned(kv_indptr, 4)))
+    return ASTR_ERR_MISALIGNED;
+  if (kv_indptr == nullptr && dims != nullptr) {  // explicit layout: num_splits partials per (b, h)
+    if (dims->num_splits < 1) return ASTR_ERR_INVALID_ARG;
+    if (dims->num_splits > dims->max_splits) return ASTR_ERR_WORKSPACE_TOO_SMALL;
+  }
   astr::DecodeParams p{};
   bool nothing = false;
   int st = decode_prepare(dims, 1.0f, &p, &nothing);
   if (st != ASTR_OK || nothing) return st;
+  p.kv_indptr = kv_indptr;
+  p.combine_all = 1;  // standalone combine: every request's partials come from the caller
   p.o_part = const_cast<float*>(o_part);
   p.ml_part = const_cast<float*>(ml_part);
   p.out = out;

@@ -14,14 +14,18 @@ struct DecodeParams {
   const uint16_t* v_pool;
   const int32_t* req_to_token;   // [B, r2t_stride]
   const int32_t* seq_lens;       // [B]
+  const int32_t* kv_indptr;      // [B + 1] exclusive prefix sum of seq_lens
   float* o_part;                 // [B, Hq, part_pitch, D]
   float* ml_part;                // [B, Hq, part_pitch, 2]
   uint16_t* out;                 // [B, Hq, D]
   int64_t r2t_stride;
+  int64_t num_slots;             // rows of k_pool / v_pool (sizes the gather tensor maps)
   int batch, num_qo_heads, num_kv_heads, head_dim;
-  int num_splits;                // S used by this call
-  int part_pitch;                // splits between consecutive (b, h) rows of o_part (= max_splits)
+  int num_splits;                // key chunks per KV head (grid x of the split kernel)
+  int part_pitch;                // partial slots per (b, h) row of o_part (= max_splits)
+  int min_chunk;                 // floor on the chunk length so no request needs > part_pitch slots
   float scale_log2;              // sm_scale * log2(e): logits are kept in base-2 units on chip
+  int combine_all;               // combine even single-chunk requests (partials supplied by the caller)
 };
 
 // Prefill/extend: one launch of the tensor-core kernel.

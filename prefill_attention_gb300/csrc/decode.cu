@@ -1,401 +1,530 @@
-// decode.cu -- split-KV paged decode for sm_103a: split kernel + log-sum-exp combine.
+// decode.cu -- split-KV paged decode for sm_103a on the 5th-generation tensor core.
 //
 // Method (AstrAI commit log, page "astrai/extension @6f67ba8"):
 //   * CUDA-backend commit: req_to_token is the page table with one token per page, so
 //     every key row is gathered through its own slot id.
 //   * kernel-rename commit: decode is split-KV only; each split writes an unnormalised
-//     partial plus its (max, sum) pair and a shared combine kernel merges them.
-//   * split-partials commit: the partial buffers are not cleared, because every split
-//     writes every slot it owns -- so empty splits here write (m=-inf, l=0, o=0).
+//     partial plus its (max, sum) pair and a shared combine kernel merges them with a
+//     log-sum-exp rescale.
+//   * split-partials commit: partial buffers are never cleared -- every partial slot the
+//     combine reads is written by exactly one split.
 //   * pipeline commit: several tile loads stay in flight while an older tile is used.
+//   * kv_indptr commit: kv_indptr (exclusive prefix sum of seq_lens) is built once per
+//     step; here it drives the split schedule.
 //
-// GB300 design (not the pages' sm_89 design):
-//   grid (split, kv_head, request); 4 warps per CTA, each warp streams a contiguous share
-//   of the split's keys through its own 4-stage cp.async ring (8 keys per stage, K and V
-//   rows of 16-byte chunks, zero-filled past the end), so no CTA-wide barrier sits in the
-//   key loop.  All G query heads of a KV head are served from each K/V row load.
-//   Scores: each lane multiplies its slice of the row with its slice of the G query rows
-//   (packed fp32x2 FMAs), then a transpose-reduction across the lanes of a row leaves one
-//   finished score per lane.  Online softmax in base 2 (the scale carries log2 e) with a
-//   warp vote that skips the accumulator rescale when no running max moved.
-//   Warps merge in shared memory at the end and write one partial per (head, split).
+// GB300 design:
+//   * Token-balanced split schedule.  For each KV head the flat key space [0, T) of the
+//     whole batch (T = kv_indptr[B]) is cut into equal chunks of C keys, one CTA per chunk,
+//     so every CTA moves the same number of bytes however skewed seq_lens is.  A chunk may
+//     hold the tail of one request and the head of the next; each such piece produces one
+//     partial, indexed by (chunk - first chunk of the request).  C depends only on T, the
+//     grid and a host-supplied floor, so the combine recomputes it identically.
+//   * One persistent CTA per SM, warp specialised:
+//       warps 4-9 (producers) -- three groups of two warps, group g owning ring stage g
+//               (tiles g, g+3, ...): a group gathers the K and V rows of its 128-key tile slot
+//               by slot with 16-byte cp.async into the 128-byte-swizzled layout the tensor
+//               core reads (XOR of the 16-byte chunk index with the row), waits for its own
+//               copies, fences them to the async proxy and arrives on the stage's full
+//               barrier.  Three tiles are in flight and each is published as soon as it
+//               lands.  (TMA tile::gather4 was measured first: at one
+//               128-byte row per gathered row it delivered ~12 GB/s per SM, well below the
+//               ~45 GB/s per SM the HBM roofline needs, so the gather stays on the LSU path.)
+//       warp 10 (MMA)     -- one thread issues S^T = K Q^T (M = 128 keys, N = 16 padded
+//               query heads) into a double-buffered TMEM accumulator, one tile ahead of the
+//               softmax, then O^T += V^T P^T (M = head_dim, V read MN-major from the same
+//               tile) and releases the stage with tcgen05.commit.
+//       warps 0-3 (softmax) -- thread t owns key t of the tile: it reads its S^T row from
+//               TMEM, the per-head max goes through warp shuffles and a 4-entry exchange,
+//               exp2 runs on the CUDA cores (the scale carries log2 e), and P^T is written
+//               as two bf16 planes, hi = bf16(p) and lo = bf16(p - hi), side by side in the
+//               N dimension, so O^T accumulates p to ~2^-17 relative precision.  At the end
+//               of a request piece the same warps read O^T (thread = head_dim row) and
+//               write the partial.
+//     All G query heads of a KV head are served by each K/V tile.
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
 #include "common.cuh"
+#include "tcgen05.cuh"
 
 namespace astr {
+
+// Chunk length (keys per CTA) for T keys over n_chunks CTAs; shared by split and combine.
+__device__ __forceinline__ int decode_chunk_len(int T, int n_chunks, int min_chunk, int max_splits) {
+  if (max_splits <= 1) return T > 0 ? T : 1;
+  int c = (T + n_chunks - 1) / n_chunks;
+  c = (c + 15) & ~15;
+  return c > min_chunk ? c : min_chunk;
+}
+
 namespace {
 
 template <int D, int G>
-struct DecodeCfg {
-  static constexpr int EPL = (D == 128 && G <= 4) ? 16 : 8;  // elements per lane per row
-  static constexpr int CPL = EPL / 8;                          // 16-byte chunks per lane per row
-  static constexpr int CPR = D / 8;                            // 16-byte chunks per row
-  static constexpr int LPR = D / EPL;                          // lanes sharing one row
-  static constexpr int RPI = 32 / LPR;                         // rows a warp covers per load
-  static constexpr int TPS = 8;                                // keys per warp stage
-  static constexpr int NT = TPS / RPI;                         // keys per lane per stage
-  static constexpr int NV = NT * G;                            // partial scores per lane
-  static constexpr int NF = NV >= LPR ? NV / LPR : 1;          // finished scores per lane
-  static constexpr int NW = 4;                                 // warps per CTA
-  static constexpr int STAGES = 4;
-  static constexpr int ROW_BYTES = D * 2;
-  static constexpr int KV_BYTES = TPS * ROW_BYTES;             // one K (or V) stage tile
-  static constexpr int STAGE_BYTES = 2 * KV_BYTES;
-  static constexpr int RING_BYTES = STAGES * STAGE_BYTES;      // per warp
-  static constexpr int PS_BYTES = (TPS * G + G) * 4;           // per warp: p[TPS][G], alpha[G]
-  static constexpr int RED_BYTES = NW * RPI * G * D * 4;       // end-of-CTA merge buffer
-  static constexpr int MAIN_BYTES = NW * RING_BYTES > RED_BYTES ? NW * RING_BYTES : RED_BYTES;
-  static constexpr int SMEM_BYTES = MAIN_BYTES + NW * PS_BYTES + NW * G * 2 * 4;
-  static constexpr int LOADS_PER_LANE = 2 * TPS * CPR / 32;    // cp.async per lane per stage
-  static_assert(NT >= 1 && NT * RPI == TPS, "stage must cover whole row groups");
-  static_assert(LPR * CPL == CPR, "lanes x chunks must cover a row");
-  static_assert((2 * TPS * CPR) % 32 == 0, "stage copies must split evenly over the warp");
+struct DecCfg {
+  static constexpr int BK = 128;                   // keys per tile (MMA M for S^T)
+  static constexpr int STAGES = 3;
+  static constexpr int THREADS = 352;              // 4 softmax warps, 6 producer warps, MMA warp
+  static constexpr int NPROD = 64;                 // producer threads per group (one group per stage)
+  static constexpr int MMA_WARP = 10;
+  static constexpr int NSM = 128;                  // softmax threads
+  static constexpr int NS = 16;                    // S^T columns: query heads padded to 16
+  static constexpr int NPV = (G <= 8) ? 16 : 32;   // O^T columns: hi heads then lo heads
+  static constexpr int HALF = NPV / 2;
+  static constexpr int NCB = D / 64;               // 128-byte column blocks per K/V row
+  static constexpr int TILE = BK * D * 2;          // one K (or V) tile
+  static constexpr int ZERO = (D == 64) ? BK * 128 : 0;   // pads V^T to M = 128 when D = 64
+  static constexpr int STAGE_BYTES = 2 * TILE + ZERO;     // K | V | zero block
+  static constexpr int QBUFS = 4;
+  static constexpr int Q_BYTES = NS * D * 2;
+  static constexpr int P_BYTES = NPV * BK * 2;
+  static constexpr int Q_OFF = STAGES * STAGE_BYTES;
+  static constexpr int P_OFF = Q_OFF + QBUFS * Q_BYTES;   // 2 buffers
+  static constexpr int RED_OFF = P_OFF + 2 * P_BYTES;     // [2][4 warps][16] floats (max), [4][16] (sum)
+  static constexpr int BAR_OFF = RED_OFF + 3 * 4 * 16 * 4;
+  // barriers: full[3], empty[3], s_full[2], p_full[2], pv_done[2], then tmem slot, error flag
+  static constexpr int NBAR = 3 + 3 + 2 + 2 + 2;
+  static constexpr int SMEM_BYTES = BAR_OFF + NBAR * 8 + 16;
+  static constexpr int CPR = D / 8;                      // 16-byte chunks per K/V row
+  static constexpr int KV_IT = BK * CPR / NPROD;          // cp.async per producer thread per K tile
+  static constexpr uint32_t TMEM_S0 = 0;           // S^T buffers at columns 0 and 16
+  static constexpr uint32_t TMEM_O = 32;
+  static constexpr uint32_t TMEM_COLS = 64;
+  static constexpr uint32_t IDESC_S = tc::idesc_bf16_f32(128, NS, false, false);
+  static constexpr uint32_t IDESC_PV = tc::idesc_bf16_f32(128, NPV, true, false);  // A (V^T) MN-major
+  static_assert(G <= 16, "at most 16 query heads per KV head");
+  static_assert(TMEM_O + NPV <= TMEM_COLS, "tensor-memory budget");
+  static_assert(STAGE_BYTES % 1024 == 0 && Q_OFF % 1024 == 0 && P_OFF % 1024 == 0 && Q_BYTES % 1024 == 0 &&
+                    P_BYTES % 1024 == 0,
+                "swizzle atoms must be 1024-byte aligned");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
-// Transpose-reduction over the LPR lanes of a row group.  Input: v[0..N) partial sums in
-// every lane.  Each step pairs the lower and upper halves of the live values; the lane whose
-// step bit is set keeps the upper half and receives its partner's copy of it.  After the
-// steps the lane holds N/LPR finished sums (or 1, replicated, when N < LPR).
-template <int N, int M>
-struct TReduce {
-  static __device__ __forceinline__ void run(float* v, int lane) {
-    if constexpr (M >= 1) {
-      if constexpr (N >= 2) {
-        const bool up = (lane & M) != 0;
-#pragma unroll
-        for (int i = 0; i < N / 2; ++i) {
-          const float send = up ? v[i] : v[i + N / 2];
-          const float keep = up ? v[i + N / 2] : v[i];
-          v[i] = keep + __shfl_xor_sync(kFullMask, send, M);
-        }
-        TReduce<N / 2, M / 2>::run(v, lane);
-      } else {
-        v[0] += __shfl_xor_sync(kFullMask, v[0], M);
-        TReduce<1, M / 2>::run(v, lane);
-      }
-    }
-  }
-};
-
-// Which lane bits decide the head of a finished score (the "head mask"), and which mark
-// replicas (lanes holding copies of the same score).  Everything else distinguishes keys.
-template <int D, int G>
-struct LaneRoles {
-  using C = DecodeCfg<D, G>;
-  static constexpr unsigned compute_head_mask() {
-    unsigned mask = 0;
-    int n = C::NV;
-    for (int m = C::LPR / 2; m >= 1; m /= 2) {
-      if (n >= 2) {
-        if (n / 2 < G) mask |= (unsigned)m;  // this step chose an index bit below log2(G)
-        n /= 2;
-      }
-    }
-    return mask;
-  }
-  static constexpr unsigned compute_replica_mask() {
-    unsigned mask = 0;
-    int n = C::NV;
-    for (int m = C::LPR / 2; m >= 1; m /= 2) {
-      if (n >= 2) n /= 2; else mask |= (unsigned)m;
-    }
-    return mask;
-  }
-  static constexpr unsigned kHead = compute_head_mask();
-  static constexpr unsigned kReplica = compute_replica_mask();
-  static constexpr unsigned kKey = 31u & ~kHead & ~kReplica;  // lane bits that select keys
-};
-
-// Butterfly over the lane bits in MASK (compile-time), max or sum.
-template <unsigned MASK, bool IS_MAX>
-__device__ __forceinline__ float butterfly(float x) {
-#pragma unroll
-  for (int m = 16; m >= 1; m /= 2) {
-    if (MASK & (unsigned)m) {
-      const float y = __shfl_xor_sync(kFullMask, x, m);
-      x = IS_MAX ? fmaxf(x, y) : x + y;
-    }
-  }
-  return x;
+__device__ __forceinline__ void sts16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
 
-// Index of the first finished score a lane holds (position in the [NT][G] score list).
-template <int D, int G>
-__device__ __forceinline__ int finished_base(int lane) {
-  using C = DecodeCfg<D, G>;
-  int base = 0, n = C::NV;
-#pragma unroll
-  for (int m = C::LPR / 2; m >= 1; m /= 2) {
-    if (n >= 2) {
-      if (lane & m) base += n / 2;
-      n /= 2;
+__device__ __forceinline__ void sts128_zero(uint32_t addr) {
+  asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(addr), "r"(0) : "memory");
+}
+
+// Walks the tiles of one chunk: a tile never crosses a request boundary.
+struct TileIter {
+  int b, start, end;  // current tile: flat keys [start, end) of request b
+  __device__ __forceinline__ void first(const int32_t* ind, int B, int lo, int hi) {
+    int l = 0, h = B - 1;  // largest b with ind[b] <= lo
+    while (l < h) {
+      const int m = (l + h + 1) >> 1;
+      if (__ldg(ind + m) <= lo) l = m; else h = m - 1;
     }
+    b = l;
+    start = lo;
+    end = min(start + 128, min(hi, __ldg(ind + b + 1)));
   }
-  return base;
+  __device__ __forceinline__ void next(const int32_t* ind, int B, int hi) {
+    const int piece_end = min(hi, __ldg(ind + b + 1));
+    if (end < piece_end) {
+      start = end;
+    } else {
+      do { ++b; } while (b < B && __ldg(ind + b + 1) <= __ldg(ind + b));  // skip empty requests
+      start = (b < B) ? __ldg(ind + b) : hi;
+      if (start > hi) start = hi;
+    }
+    end = (start < hi) ? min(start + 128, min(hi, __ldg(ind + b + 1))) : start;
+  }
+  __device__ __forceinline__ bool valid(int hi) const { return start < hi; }
+  __device__ __forceinline__ bool opens_piece(const int32_t* ind, int lo) const { return start == max(lo, __ldg(ind + b)); }
+  __device__ __forceinline__ bool closes_piece(const int32_t* ind, int hi) const { return end == min(hi, __ldg(ind + b + 1)); }
+};
+
+// Bounded wait that gives up (and raises the CTA's error flag) on timeout or once the flag is up.
+__device__ __forceinline__ bool wait_or_fail(uint32_t bar, uint32_t parity, volatile int* err) {
+  if (*err) return false;
+  if (tc::mbar_wait(bar, parity)) return true;
+  *err = 1;
+  return false;
+}
+
+// Byte offset of 16-byte chunk c of row r in a 128-byte-swizzled K-major tile whose
+// 64-element column blocks each hold `rows` rows.
+__device__ __forceinline__ uint32_t sw128(int r, int c, int rows) {
+  return (uint32_t)((c >> 3) * rows * 128 + (r >> 3) * 1024 + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(128, 3) decode_split_kernel(const DecodeParams p) {
-  using C = DecodeCfg<D, G>;
-  using R = LaneRoles<D, G>;
-  extern __shared__ __align__(128) unsigned char smem[];
+__global__ void __launch_bounds__(352, 1) decode_split_tc_kernel(const DecodeParams p) {
+  using C = DecCfg<D, G>;
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const uint32_t sbase = smem_u32(smem);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int kvh = blockIdx.y, cx = blockIdx.x;
+  const int B = p.batch;
+  const int32_t* ind = p.kv_indptr;
 
-  const int s = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rg = lane / C::LPR, sub = lane % C::LPR;
+  const int T = __ldg(ind + B);
+  const int CL = decode_chunk_len(T, gridDim.x, p.min_chunk, p.part_pitch);
+  const int lo = (int)min((int64_t)cx * CL, (int64_t)T), hi = min(lo + CL, T);
+  if (lo >= hi) return;
+  if ((sbase & 1023u) != 0) return;  // swizzle atoms need a 1024-byte aligned window
 
-  // ---- this CTA's key range [lo, hi) of request b, and this warp's share [wlo, whi)
-  const int n = __ldg(p.seq_lens + b);
-  const int S = p.num_splits;
-  const int chunk = (n + S - 1) / S;
-  const int lo = min(s * chunk, n), hi = min(lo + chunk, n);
-  const int per_warp = (((hi - lo) + C::TPS * C::NW - 1) / (C::TPS * C::NW)) * C::TPS;
-  const int wlo = min(lo + warp * per_warp, hi), whi = min(wlo + per_warp, hi);
-  const int nst = (whi - wlo + C::TPS - 1) / C::TPS;
+  const uint32_t bars = sbase + C::BAR_OFF;
+  auto full = [&](int s) { return bars + 8u * s; };
+  auto empty = [&](int s) { return bars + 8u * (3 + s); };
+  auto s_full = [&](int i) { return bars + 8u * (6 + i); };
+  auto p_full = [&](int i) { return bars + 8u * (8 + i); };
+  auto pv_done = [&](int i) { return bars + 8u * (10 + i); };
+  const uint32_t slot = bars + 8u * C::NBAR;
+  volatile int* err = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 8 * C::NBAR + 4);
+  float* red = reinterpret_cast<float*>(smem + C::RED_OFF);
 
-  const uint32_t ring = smem_u32(smem) + warp * C::RING_BYTES;
-  float* ps = reinterpret_cast<float*>(smem + C::MAIN_BYTES + warp * C::PS_BYTES);  // p[TPS][G], alpha[G]
-  const uint32_t ps_addr = smem_u32(ps);
-
-  const int32_t* r2t = p.req_to_token + (int64_t)b * p.r2t_stride;
-  const size_t head_stride = (size_t)p.num_kv_heads * D;
-  const uint16_t* kbase = p.k_pool + (size_t)kvh * D;
-  const uint16_t* vbase = p.v_pool + (size_t)kvh * D;
-
-  // ---- slot ids: lane i holds the slot of key (blk + i); two 32-key blocks kept in registers
-  auto load_ids = [&](int first) -> int {
-    const int t = first + lane;
-    return (t < whi) ? ldg_nc_i32(r2t + t) : 0;
-  };
-  int ids_cur = load_ids(wlo), ids_nxt = load_ids(wlo + 32);
-
-  // ---- query rows of the G heads sharing kvh, pre-scaled by sm_scale*log2(e)
-  float2 q2[G][C::CPL * 4];
-  {
-    const uint16_t* qrow = p.q + ((size_t)b * p.num_qo_heads + (size_t)kvh * G) * D;
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-      for (int c = 0; c < C::CPL; ++c) {
-        const uint4 w = __ldg(reinterpret_cast<const uint4*>(qrow + (size_t)g * D + (sub + c * C::LPR) * 8));
-        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 f = bf16x2_to_float2(ww[j]);
-          q2[g][c * 4 + j] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
-        }
-      }
+  // ---- set-up: barriers, TMEM, zero padding (P rows of absent heads, V^T pad block)
+  if (tid == 0) {
+    for (int s = 0; s < 3; ++s) {
+      tc::mbar_init(full(s), C::NPROD);
+      tc::mbar_init(empty(s), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(s_full(i), 1);
+      tc::mbar_init(p_full(i), C::NSM);
+      tc::mbar_init(pv_done(i), 1);
+    }
+    *err = 0;
+    tc::fence_mbarrier_init();
   }
+  if (warp == C::MMA_WARP) tc::tmem_alloc<C::TMEM_COLS>(slot);
+  // P^T rows of absent heads and Q rows of absent heads stay zero for the whole kernel
+  for (int i = tid; i < 2 * C::P_BYTES / 16; i += C::THREADS) sts128_zero(sbase + C::P_OFF + i * 16);
+  for (int i = tid; i < C::QBUFS * C::Q_BYTES / 16; i += C::THREADS) sts128_zero(sbase + C::Q_OFF + i * 16);
+  if constexpr (C::ZERO > 0) {
+    for (int st = 0; st < C::STAGES; ++st)
+      for (int i = tid; i < C::ZERO / 16; i += C::THREADS)
+        sts128_zero(sbase + st * C::STAGE_BYTES + 2 * C::TILE + i * 16);
+  }
+  tc::fence_proxy_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::BAR_OFF + 8 * C::NBAR);
+  // let the combine kernel's CTAs launch now; they wait for this grid's memory to be visible
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  // ---- issue stage `st` (keys wlo + st*TPS ...) into ring slot st % STAGES
-  auto issue = [&](int st) {
-    if (st < nst) {
-      const int off = st * C::TPS;                   // keys since wlo
-      if ((off & 31) == 0 && off > 0) {              // entering a new 32-key block
-        ids_cur = ids_nxt;
-        ids_nxt = load_ids(wlo + off + 32);
-      }
-      const uint32_t dst_stage = ring + (st % C::STAGES) * C::STAGE_BYTES;
-#pragma unroll
-      for (int it = 0; it < C::LOADS_PER_LANE; ++it) {
-        const int flat = it * 32 + lane;
-        const int kv = flat / (C::TPS * C::CPR);
-        const int rem = flat % (C::TPS * C::CPR);
-        const int r = rem / C::CPR, ch = rem % C::CPR;
-        const int slot = __shfl_sync(kFullMask, ids_cur, (off & 31) + r);
-        const bool valid = wlo + off + r < whi;
-        const uint16_t* src = (kv == 0 ? kbase : vbase) + (valid ? (size_t)slot * head_stride : 0) + ch * 8;
-        cp_async16(dst_stage + kv * C::KV_BYTES + r * C::ROW_BYTES + ch * 16, src, valid);
-      }
+  if (warp >= 4 && warp < 10) {
+    // ======================= producers: group g fills ring stage g with tiles g, g+3, ...
+    const int grp = (warp - 4) >> 1;             // 0..2 = the stage this group owns
+    const int pt = tid - C::NSM - grp * C::NPROD;  // 0..63 within the group
+    TileIter it;
+    it.first(ind, B, lo, hi);
+    int piece = 0;
+    for (int k = 0; k < grp && it.valid(hi); ++k) {  // advance to tile grp
+      if (it.closes_piece(ind, hi)) ++piece;
+      it.next(ind, B, hi);
     }
-    cp_async_commit();  // possibly empty: keeps the group count uniform
-  };
-
-  float m_run[C::NF], l_run[C::NF];
+    const size_t head_stride = (size_t)p.num_kv_heads * D;
+    // thread pt copies chunk (pt % CPR) of keys (i * NPROD + pt) / CPR, i = 0 .. KV_IT-1
+    int ids[C::KV_IT];
+    auto load_ids = [&](const TileIter& t) {
 #pragma unroll
-  for (int k = 0; k < C::NF; ++k) { m_run[k] = -CUDART_INF_F; l_run[k] = 0.f; }
-  float2 acc[G][C::CPL * 4];
+      for (int i = 0; i < C::KV_IT; ++i) {
+        const int key = (i * C::NPROD + pt) / C::CPR;
+        const int flat = t.start + key;
+        ids[i] = (t.valid(hi) && flat < t.end)
+                     ? ldg_nc_i32(p.req_to_token + (int64_t)t.b * p.r2t_stride + (flat - __ldg(ind + t.b)))
+                     : -1;
+      }
+    };
+    load_ids(it);
+    for (int round = 0; it.valid(hi); ++round) {
+      if (round > 0 && !wait_or_fail(empty(grp), (uint32_t)((round - 1) & 1), err)) break;
+      const uint32_t kst = sbase + grp * C::STAGE_BYTES, vst = kst + C::TILE;
 #pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int j = 0; j < C::CPL * 4; ++j) acc[g][j] = make_float2(0.f, 0.f);
-
-  const int fbase = finished_base<D, G>(lane);
-
-#pragma unroll
-  for (int st = 0; st < C::STAGES - 1; ++st) issue(st);
-
-  for (int st = 0; st < nst; ++st) {
-    issue(st + C::STAGES - 1);
-    cp_async_wait<C::STAGES - 1>();
-    __syncwarp();
-    const uint32_t kt = ring + (st % C::STAGES) * C::STAGE_BYTES;
-    const uint32_t vt = kt + C::KV_BYTES;
-    const int t0 = wlo + st * C::TPS;
-
-    // -- scores: partial dot products of this lane's slice, then transpose-reduce
-    float sc[C::NV];
-#pragma unroll
-    for (int t = 0; t < C::NT; ++t) {
-      const int row = rg + C::RPI * t;
-      float2 part[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) part[g] = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int c = 0; c < C::CPL; ++c) {
-        const uint4 kw = lds128(kt + row * C::ROW_BYTES + (sub + c * C::LPR) * 16);
-        const float2 k0 = bf16x2_to_float2(kw.x), k1 = bf16x2_to_float2(kw.y);
-        const float2 k2 = bf16x2_to_float2(kw.z), k3 = bf16x2_to_float2(kw.w);
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          part[g] = __ffma2_rn(q2[g][c * 4 + 0], k0, part[g]);
-          part[g] = __ffma2_rn(q2[g][c * 4 + 1], k1, part[g]);
-          part[g] = __ffma2_rn(q2[g][c * 4 + 2], k2, part[g]);
-          part[g] = __ffma2_rn(q2[g][c * 4 + 3], k3, part[g]);
+      for (int i = 0; i < C::KV_IT; ++i) {
+        const int flat = i * C::NPROD + pt;
+        const int key = flat / C::CPR, c = flat % C::CPR;
+        const bool valid = ids[i] >= 0;
+        const size_t off = valid ? (size_t)ids[i] * head_stride + (size_t)kvh * D + c * 8 : 0;
+        const uint32_t o = sw128(key, c, C::BK);
+        cp_async16(kst + o, p.k_pool + off, valid);
+        cp_async16(vst + o, p.v_pool + off, valid);
+      }
+      if (it.opens_piece(ind, lo)) {  // first tile of a piece: its G query rows
+        const uint32_t qb = sbase + C::Q_OFF + (piece % C::QBUFS) * C::Q_BYTES;
+        const uint16_t* qsrc = p.q + ((size_t)it.b * p.num_qo_heads + (size_t)kvh * G) * D;
+        for (int i = pt; i < G * C::CPR; i += C::NPROD) {
+          const int g = i / C::CPR, c = i % C::CPR;
+          cp_async16(qb + sw128(g, c, C::NS), qsrc + (size_t)g * D + c * 8, true);
         }
       }
-#pragma unroll
-      for (int g = 0; g < G; ++g) sc[t * G + g] = part[g].x + part[g].y;
+      cp_async_commit();
+      // advance three tiles (this group's next one) and prefetch its slot ids
+      for (int k = 0; k < C::STAGES && it.valid(hi); ++k) {
+        if (it.closes_piece(ind, hi)) ++piece;
+        it.next(ind, B, hi);
+      }
+      load_ids(it);
+      cp_async_wait<0>();
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(full(grp));
     }
-    TReduce<C::NV, C::LPR / 2>::run(sc, lane);
-
-    // -- online softmax on the finished scores (base 2)
-    bool moved = false;
+  } else if (warp == C::MMA_WARP) {
+    // ======================= MMA issuer (one thread)
+    // Two streams issued as their inputs become ready, polled without blocking so that
+    // neither can hold up the other: S^T of tile k (needs tile k resident and S buffer k&1
+    // released by the softmax of tile k-2) and O^T += V^T P^T of tile k (needs P of tile k).
+    if (lane == 0) {
+      TileIter s_it, v_it;
+      s_it.first(ind, B, lo, hi);
+      v_it.first(ind, B, lo, hi);
+      int s_piece = 0, ns = 0, nv = 0;
+      long long idle_since = clock64();
+      while (v_it.valid(hi)) {
+        bool progress = false;
+        if (s_it.valid(hi) && ns <= nv + 1 && tc::mbar_test(full(ns % C::STAGES), (uint32_t)((ns / C::STAGES) & 1))) {
+          tc::fence_after_sync();
+          const uint32_t kst = sbase + (ns % C::STAGES) * C::STAGE_BYTES;
+          const uint32_t qb = sbase + C::Q_OFF + (s_piece % C::QBUFS) * C::Q_BYTES;
 #pragma unroll
-    for (int k = 0; k < C::NF; ++k) {
-      const int idx = fbase + k;
-      const int tl = idx / G, g = idx % G;
-      const int key = rg + C::RPI * tl;
-      const float sv = (t0 + key < whi) ? sc[k] : -CUDART_INF_F;
-      const float tmax = butterfly<R::kKey, true>(sv);
-      const float m_new = fmaxf(m_run[k], tmax);
-      const float alpha = exp2f(m_run[k] - m_new);   // 0 on the first stage (m_run = -inf)
-      const float pk = exp2f(sv - m_new);
-      l_run[k] = l_run[k] * alpha + pk;
-      moved |= (m_new != m_run[k]);
-      m_run[k] = m_new;
-      ps[key * G + g] = pk;
-      ps[C::TPS * G + g] = alpha;   // every lane holding head g writes the same value
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t ad = tc::smem_desc_sw128(kst + (kk >> 2) * (C::BK * 128) + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = tc::smem_desc_sw128(qb + (kk >> 2) * (C::NS * 128) + (kk & 3) * 32, 16, 1024);
+            tc::mma_bf16_ss(tmem + C::TMEM_S0 + (ns & 1) * 16, ad, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
+          }
+          tc::mma_commit(s_full(ns & 1));
+          if (s_it.closes_piece(ind, hi)) ++s_piece;
+          s_it.next(ind, B, hi);
+          ++ns;
+          progress = true;
+        }
+        if (nv < ns && tc::mbar_test(p_full(nv & 1), (uint32_t)((nv >> 1) & 1))) {
+          tc::fence_after_sync();
+          const uint32_t vst = sbase + (nv % C::STAGES) * C::STAGE_BYTES + C::TILE;
+          const uint32_t pb = sbase + C::P_OFF + (nv & 1) * C::P_BYTES;
+          const bool opens = v_it.opens_piece(ind, lo);
+#pragma unroll
+          for (int kk = 0; kk < C::BK / 16; ++kk) {
+            // A = V^T: M = head_dim (MN-major; second 64-column block at +BK*128 bytes, which
+            // is the zero block when head_dim = 64), K = 16 keys per step
+            const uint64_t ad = tc::smem_desc_sw128(vst + kk * 16 * 128, C::BK * 128, 1024);
+            const uint64_t bd = tc::smem_desc_sw128(pb + (kk >> 2) * (C::NPV * 128) + (kk & 3) * 32, 16, 1024);
+            tc::mma_bf16_ss(tmem + C::TMEM_O, ad, bd, C::IDESC_PV, (opens && kk == 0) ? 0u : 1u);
+          }
+          tc::mma_commit(empty(nv % C::STAGES));
+          tc::mma_commit(pv_done(nv & 1));
+          v_it.next(ind, B, hi);
+          ++nv;
+          progress = true;
+        }
+        if (progress) {
+          idle_since = clock64();
+        } else if (*err || clock64() - idle_since > (1ll << 31)) {  // ~1 s without progress
+          *err = 1;
+          break;
+        } else {
+          __nanosleep(32);
+        }
+      }
     }
-    const bool any_moved = __any_sync(kFullMask, moved);
-    __syncwarp();
-
-    // -- rescale only when some running max moved
-    if (any_moved) {
+  } else {
+    // ======================= softmax warps 0-3 (thread t = key t = TMEM lane t)
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    TileIter it;
+    it.first(ind, B, lo, hi);
+    float m_run[G], l_thr[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) { m_run[g] = -CUDART_INF_F; l_thr[g] = 0.f; }
+    const float scale = p.scale_log2;
+    for (int j = 0; it.valid(hi); ++j) {
+      const bool opens = it.opens_piece(ind, lo), closes = it.closes_piece(ind, hi);
+      if (!wait_or_fail(s_full(j & 1), (uint32_t)((j >> 1) & 1), err)) break;
+      tc::fence_after_sync();
+      const bool kvalid = it.start + tid < it.end;
+      float sv[G];
+      {
+        uint32_t r[16];
+        tc::tmem_ld16(tmem + lane_base + C::TMEM_S0 + (j & 1) * 16, r);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int g = 0; g < G; ++g) sv[g] = kvalid ? __uint_as_float(r[g]) * scale : -CUDART_INF_F;
+      }
+      // per-head max over the tile's 128 keys (exchange buffer alternates with j)
+      float* rmax = red + (j & 1) * 64;
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        const float a = ps[C::TPS * G + g];
-        const float2 a2 = make_float2(a, a);
+        float x = sv[g];
 #pragma unroll
-        for (int j = 0; j < C::CPL * 4; ++j) acc[g][j] = __fmul2_rn(acc[g][j], a2);
+        for (int o = 16; o >= 1; o >>= 1) x = fmaxf(x, __shfl_xor_sync(kFullMask, x, o));
+        if (lane == 0) rmax[warp * 16 + g] = x;
       }
-    }
+      tc::named_bar_sync(1, C::NSM);
+      float alpha[G];
+      bool moved = false;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float tmax = fmaxf(fmaxf(rmax[g], rmax[16 + g]), fmaxf(rmax[32 + g], rmax[48 + g]));
+        const float m_new = fmaxf(m_run[g], tmax);  // finite: the tile has at least one key
+        alpha[g] = exp2f(m_run[g] - m_new);          // 0 on the first tile of a piece
+        moved |= (m_new != m_run[g]);
+        m_run[g] = m_new;
+      }
+      // P^T buffer j&1 was last read by O^T += V^T P^T of tile j-2
+      if (j >= 2 && !wait_or_fail(pv_done(j & 1), (uint32_t)(((j - 2) >> 1) & 1), err)) break;
+      const uint32_t pb = sbase + C::P_OFF + (j & 1) * C::P_BYTES;
+      const int col_chunk = (tid & 63) >> 3, blk = tid >> 6, within = (tid & 7) * 2;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float pg = exp2f(sv[g] - m_run[g]);  // 0 for keys past the piece
+        l_thr[g] = l_thr[g] * alpha[g] + pg;
+        const uint32_t hi16 = float2_to_bf16x2_rn(pg, 0.f) & 0xffffu;
+        const float lo_f = pg - __uint_as_float(hi16 << 16);
+        const uint32_t lo16 = float2_to_bf16x2_rn(lo_f, 0.f) & 0xffffu;
+        const int gl = C::HALF + g;
+        sts16(pb + blk * (C::NPV * 128) + (g >> 3) * 1024 + (g & 7) * 128 + ((col_chunk ^ (g & 7)) << 4) + within,
+              (uint16_t)hi16);
+        sts16(pb + blk * (C::NPV * 128) + (gl >> 3) * 1024 + (gl & 7) * 128 + ((col_chunk ^ (gl & 7)) << 4) + within,
+              (uint16_t)lo16);
+      }
+      // rescale the live O^T columns when a running max moved (CTA-uniform decision)
+      if (moved && !opens) {
+        if (!wait_or_fail(pv_done((j - 1) & 1), (uint32_t)(((j - 1) >> 1) & 1), err)) break;
+        tc::fence_after_sync();
+        if constexpr (C::NPV == 16) {
+          uint32_t o[16];
+          tc::tmem_ld16(tmem + lane_base + C::TMEM_O, o);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            o[g] = __float_as_uint(__uint_as_float(o[g]) * alpha[g]);
+            o[C::HALF + g] = __float_as_uint(__uint_as_float(o[C::HALF + g]) * alpha[g]);
+          }
+          tc::tmem_st16(tmem + lane_base + C::TMEM_O, o);
+        } else {
+          uint32_t o[32];
+          tc::tmem_ld32(tmem + lane_base + C::TMEM_O, o);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            o[g] = __float_as_uint(__uint_as_float(o[g]) * alpha[g]);
+            o[C::HALF + g] = __float_as_uint(__uint_as_float(o[C::HALF + g]) * alpha[g]);
+          }
+          tc::tmem_st32(tmem + lane_base + C::TMEM_O, o);
+        }
+        tc::tmem_st_wait();
+      }
+      tc::fence_proxy_async_smem();
+      tc::fence_before_sync();
+      tc::mbar_arrive(p_full(j & 1));
 
-    // -- P V
-#pragma unroll
-    for (int t = 0; t < C::NT; ++t) {
-      const int row = rg + C::RPI * t;
-      float pg[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) pg[g] = ps[row * G + g];
-#pragma unroll
-      for (int c = 0; c < C::CPL; ++c) {
-        const uint4 vw = lds128(vt + row * C::ROW_BYTES + (sub + c * C::LPR) * 16);
-        const float2 v0 = bf16x2_to_float2(vw.x), v1 = bf16x2_to_float2(vw.y);
-        const float2 v2 = bf16x2_to_float2(vw.z), v3 = bf16x2_to_float2(vw.w);
+      if (closes) {
+        // piece finished: O^T += V^T P^T of this tile must land, then write the partial
+        if (!wait_or_fail(pv_done(j & 1), (uint32_t)((j >> 1) & 1), err)) break;
+        tc::fence_after_sync();
+        float* rsum = red + 128;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          const float2 pp = make_float2(pg[g], pg[g]);
-          acc[g][c * 4 + 0] = __ffma2_rn(pp, v0, acc[g][c * 4 + 0]);
-          acc[g][c * 4 + 1] = __ffma2_rn(pp, v1, acc[g][c * 4 + 1]);
-          acc[g][c * 4 + 2] = __ffma2_rn(pp, v2, acc[g][c * 4 + 2]);
-          acc[g][c * 4 + 3] = __ffma2_rn(pp, v3, acc[g][c * 4 + 3]);
+          float x = l_thr[g];
+#pragma unroll
+          for (int o = 16; o >= 1; o >>= 1) x += __shfl_xor_sync(kFullMask, x, o);
+          if (lane == 0) rsum[warp * 16 + g] = x;
         }
+        float og[G];
+        if constexpr (C::NPV == 16) {
+          uint32_t o[16];
+          tc::tmem_ld16(tmem + lane_base + C::TMEM_O, o);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int g = 0; g < G; ++g) og[g] = __uint_as_float(o[g]) + __uint_as_float(o[C::HALF + g]);
+        } else {
+          uint32_t o[32];
+          tc::tmem_ld32(tmem + lane_base + C::TMEM_O, o);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int g = 0; g < G; ++g) og[g] = __uint_as_float(o[g]) + __uint_as_float(o[C::HALF + g]);
+        }
+        tc::named_bar_sync(1, C::NSM);
+        const int b = it.b;
+        const int rb = __ldg(ind + b), re = __ldg(ind + b + 1);
+        if (p.out != nullptr && rb >= lo && re <= hi) {
+          // the whole request lies in this chunk: normalise and write the output directly
+          // (the combine skips requests that occupy a single chunk)
+          if (tid < D) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+              const float L = rsum[g] + rsum[16 + g] + rsum[32 + g] + rsum[48 + g];
+              const float v = og[g] / L;
+              const __nv_bfloat16 h = __float2bfloat16_rn(v);
+              p.out[((size_t)b * p.num_qo_heads + (size_t)kvh * G + g) * D + tid] =
+                  *reinterpret_cast<const uint16_t*>(&h);
+            }
+          }
+        } else {
+          const int s = cx - rb / CL;  // partial slot of this piece
+          const size_t row0 = ((size_t)b * p.num_qo_heads + (size_t)kvh * G) * p.part_pitch + s;
+          if (tid < D) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) p.o_part[(row0 + (size_t)g * p.part_pitch) * D + tid] = og[g];
+          }
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            if (tid == g) {
+              p.ml_part[(row0 + (size_t)g * p.part_pitch) * 2 + 0] = m_run[g] * kLn2;  // natural-log units
+              p.ml_part[(row0 + (size_t)g * p.part_pitch) * 2 + 1] =
+                  rsum[g] + rsum[16 + g] + rsum[32 + g] + rsum[48 + g];
+            }
+          }
+        }
+        tc::named_bar_sync(1, C::NSM);  // sums read before the next piece reuses the buffer
+#pragma unroll
+        for (int g = 0; g < G; ++g) { m_run[g] = -CUDART_INF_F; l_thr[g] = 0.f; }
       }
+      it.next(ind, B, hi);
     }
-    __syncwarp();
   }
-  cp_async_wait<0>();
 
-  // ---- per-warp (m, l): sum l over the lanes that hold different keys of the same head
-  float* wml = reinterpret_cast<float*>(smem + C::MAIN_BYTES + C::NW * C::PS_BYTES);  // [NW][G][2]
-#pragma unroll
-  for (int k = 0; k < C::NF; ++k) {
-    const float lsum = butterfly<R::kKey, false>(l_run[k]);
-    const int g = (fbase + k) % G;
-    if ((lane & (R::kKey | R::kReplica)) == 0) {
-      wml[(warp * G + g) * 2 + 0] = m_run[k];
-      wml[(warp * G + g) * 2 + 1] = lsum;
-    }
-  }
-  if (nst == 0) {  // this warp saw no keys: neutral (m, l)
-    if (lane < G) {
-      wml[(warp * G + lane) * 2 + 0] = -CUDART_INF_F;
-      wml[(warp * G + lane) * 2 + 1] = 0.f;
-    }
-  }
-  __syncthreads();  // every warp is done with its ring: reuse it as the merge buffer
-
-  // ---- accumulators to shared memory: red[warp][rg][g][D]
-  float* red = reinterpret_cast<float*>(smem);
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int c = 0; c < C::CPL; ++c) {
-      float* dst = red + (((size_t)warp * C::RPI + rg) * G + g) * D + (sub + c * C::LPR) * 8;
-      reinterpret_cast<float4*>(dst)[0] = make_float4(acc[g][c * 4 + 0].x, acc[g][c * 4 + 0].y,
-                                                      acc[g][c * 4 + 1].x, acc[g][c * 4 + 1].y);
-      reinterpret_cast<float4*>(dst)[1] = make_float4(acc[g][c * 4 + 2].x, acc[g][c * 4 + 2].y,
-                                                      acc[g][c * 4 + 3].x, acc[g][c * 4 + 3].y);
-    }
+  // ---- teardown: every role has finished (all issued MMAs were waited on by the softmax
+  //      warps through pv_done of the final tile)
+  tc::fence_before_sync();
   __syncthreads();
-
-  // ---- merge warps (log-sum-exp) and write the split partial
-  for (int o = threadIdx.x; o < G * (D / 4); o += blockDim.x) {
-    const int g = o / (D / 4), d4 = o % (D / 4);
-    float M = -CUDART_INF_F;
-#pragma unroll
-    for (int w = 0; w < C::NW; ++w) M = fmaxf(M, wml[(w * G + g) * 2]);
-    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-    float L = 0.f;
-    if (M != -CUDART_INF_F) {
-#pragma unroll
-      for (int w = 0; w < C::NW; ++w) {
-        const float f = exp2f(wml[(w * G + g) * 2] - M);
-        L += f * wml[(w * G + g) * 2 + 1];
-#pragma unroll
-        for (int r = 0; r < C::RPI; ++r) {
-          const float4 a = reinterpret_cast<const float4*>(red + (((size_t)w * C::RPI + r) * G + g) * D)[d4];
-          O.x += f * a.x; O.y += f * a.y; O.z += f * a.z; O.w += f * a.w;
-        }
-      }
-    }
-    const int h = kvh * G + g;
-    const size_t row = ((size_t)b * p.num_qo_heads + h) * p.part_pitch + s;
-    reinterpret_cast<float4*>(p.o_part + row * D)[d4] = O;
-    if (d4 == 0) {
-      p.ml_part[row * 2 + 0] = (M == -CUDART_INF_F) ? M : M * kLn2;  // natural-log units
-      p.ml_part[row * 2 + 1] = L;
+  if (warp == C::MMA_WARP) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc<C::TMEM_COLS>(tmem);
+  }
+  if (*err && tid < D) {  // a wait timed out: poison what this CTA owns so the call reads as failed
+    TileIter it;
+    it.first(ind, B, lo, hi);
+    for (; it.valid(hi); it.next(ind, B, hi)) {
+      if (!it.closes_piece(ind, hi)) continue;
+      const int s = cx - __ldg(ind + it.b) / CL;
+      const size_t row0 = ((size_t)it.b * p.num_qo_heads + (size_t)kvh * G) * p.part_pitch + s;
+      for (int g = 0; g < G; ++g) p.o_part[(row0 + (size_t)g * p.part_pitch) * D + tid] = CUDART_NAN_F;
     }
   }
 }
 
-// One warp per (request, query head): merge the S partials and write bf16.
+// One warp per (request, query head): merge the request's partials and write bf16.
 template <int D>
 __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams p) {
   constexpr int VPL = D / 32;  // output elements per lane
   const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
+  // launched as a programmatic dependent of the split kernel: wait until its writes are visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (wid >= p.batch * p.num_qo_heads) return;
+  const int b = wid / p.num_qo_heads;
+  int S;
+  if (p.kv_indptr != nullptr) {  // token-balanced chunks: the chunks that overlap request b
+    const int T = __ldg(p.kv_indptr + p.batch);
+    const int CL = decode_chunk_len(T, p.num_splits, p.min_chunk, p.part_pitch);
+    const int a = __ldg(p.kv_indptr + b), e = __ldg(p.kv_indptr + b + 1);
+    S = (e > a) ? (e - 1) / CL - a / CL + 1 : 0;
+    if (S == 1 && !p.combine_all) return;  // written directly by the split kernel
+  } else {                       // explicit count (partials supplied by the caller)
+    S = p.num_splits;
+  }
   const size_t base = (size_t)wid * p.part_pitch;
-  const int S = p.num_splits;
   const float* ml = p.ml_part + base * 2;
 
   float M = -CUDART_INF_F;
   for (int s = lane; s < S; s += 32) M = fmaxf(M, ml[2 * s]);
-  M = butterfly<31u, true>(M);
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, o));
 
   float acc[VPL];
 #pragma unroll
@@ -430,31 +559,32 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
 
 template <int D, int G>
 cudaError_t launch_split_t(const DecodeParams& p, cudaStream_t stream) {
-  using C = DecodeCfg<D, G>;
-  static bool attr_set = false;  // per process; the attribute is per function and device-agnostic here
+  using C = DecCfg<D, G>;
+  static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(decode_split_tc_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 grid(p.num_splits, p.num_kv_heads, p.batch);
-  decode_split_kernel<D, G><<<grid, C::NW * 32, C::SMEM_BYTES, stream>>>(p);
+  dim3 grid(p.num_splits, p.num_kv_heads);
+  decode_split_tc_kernel<D, G><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 bool decode_supported(int head_dim, int group) {
-  return (head_dim == 64 || head_dim == 128) && (group == 1 || group == 2 || group == 4 || group == 8);
+  return (head_dim == 64 || head_dim == 128) &&
+         (group == 1 || group == 2 || group == 4 || group == 8 || group == 16);
 }
 
 cudaError_t launch_decode_split(const DecodeParams& p, cudaStream_t stream) {
   const int G = p.num_qo_heads / p.num_kv_heads;
 #define ASTR_DEC_CASE(DD, GG) \
   if (p.head_dim == DD && G == GG) return launch_split_t<DD, GG>(p, stream);
-  ASTR_DEC_CASE(128, 4) ASTR_DEC_CASE(128, 1) ASTR_DEC_CASE(128, 2) ASTR_DEC_CASE(128, 8)
-  ASTR_DEC_CASE(64, 4) ASTR_DEC_CASE(64, 1) ASTR_DEC_CASE(64, 2) ASTR_DEC_CASE(64, 8)
+  ASTR_DEC_CASE(128, 4) ASTR_DEC_CASE(128, 1) ASTR_DEC_CASE(128, 2) ASTR_DEC_CASE(128, 8) ASTR_DEC_CASE(128, 16)
+  ASTR_DEC_CASE(64, 4) ASTR_DEC_CASE(64, 1) ASTR_DEC_CASE(64, 2) ASTR_DEC_CASE(64, 8) ASTR_DEC_CASE(64, 16)
 #undef ASTR_DEC_CASE
   return cudaErrorInvalidValue;
 }
@@ -463,9 +593,21 @@ cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream) {
   const int rows = p.batch * p.num_qo_heads;
   const int warps_per_block = 8;
   dim3 grid((rows + warps_per_block - 1) / warps_per_block);
-  if (p.head_dim == 128) decode_combine_kernel<128><<<grid, warps_per_block * 32, 0, stream>>>(p);
-  else if (p.head_dim == 64) decode_combine_kernel<64><<<grid, warps_per_block * 32, 0, stream>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(warps_per_block * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlap with the split kernel's tail
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
+  if (p.head_dim == 128) e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<128>, p);
+  else if (p.head_dim == 64) e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<64>, p);
   else return cudaErrorInvalidValue;
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

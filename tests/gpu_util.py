@@ -43,6 +43,17 @@ def prefill_dims(w):
                         w.max_seq_len, total_q=w.total_q, max_q_len=w.max_q_len)
 
 
+def decode_chunk_len(w, n_chunks, max_splits):
+    """Keys per split-kernel chunk, as documented for astr_attn_paged_decode."""
+    T = int(w.kv_indptr[-1])
+    if max_splits <= 1:
+        return max(T, 1)
+    c = -(-T // n_chunks)
+    c = (c + 15) // 16 * 16
+    floor = max(16, -(-w.max_seq_len // (max_splits - 1)))
+    return max(c, floor)
+
+
 def run_decode(w, t=None, max_splits=32, num_splits=0, stream=None, return_parts=False):
     torch = _torch()
     t = t or upload(w)
@@ -53,11 +64,11 @@ def run_decode(w, t=None, max_splits=32, num_splits=0, stream=None, return_parts
                               w.sm_scale, stream=stream)
     torch.cuda.synchronize()
     if return_parts:
-        S = pa.astr_attn_decode_num_splits(dims, torch.cuda.current_device())
+        n_chunks = pa.astr_attn_decode_num_splits(dims, torch.cuda.current_device())
         B, Hq, D = w.batch, w.num_qo_heads, w.head_dim
-        o = o_part.view(B, Hq, max_splits, D)[:, :, :S].cpu().numpy().astype(np.float64)
-        ml = ml_part.view(B, Hq, max_splits, 2)[:, :, :S].cpu().numpy().astype(np.float64)
-        return out, o, ml, S
+        o = o_part.view(B, Hq, max_splits, D).cpu().numpy().astype(np.float64)
+        ml = ml_part.view(B, Hq, max_splits, 2).cpu().numpy().astype(np.float64)
+        return out, o, ml, n_chunks
     return out
 
 

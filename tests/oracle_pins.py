@@ -265,6 +265,30 @@ def pin_split_combine(lib):
                     assert np.all(np.isfinite(ml[b, :, s]))
 
 
+def pin_chunk_partials_combine(lib):
+    """Token-balanced chunks (boundaries anywhere in the flat key space, so chunks straddle
+    requests): chunk partials + combine == unsplit attention, for several chunk lengths."""
+    w = _small_decode(seed=73, B=6, lo=0, hi=45)
+    w.seq_lens[2] = 0   # an empty request owns no chunk
+    w.kv_indptr[1:] = np.cumsum(w.seq_lens)
+    ref = oracle.decode(w, lib=lib)
+    T = int(w.kv_indptr[-1])
+    for C in (1, 7, 16, 33, T, T + 5):
+        ns = oracle.chunk_split_counts(w.kv_indptr, C)
+        pitch = max(1, int(ns.max()))
+        o, ml, ns2 = oracle.decode_chunk_partials(w, C, pitch, lib=lib)
+        assert np.array_equal(ns, ns2)
+        # brute force: count (request, chunk) overlaps key by key
+        overlaps = {(b, j // C) for b in range(w.batch) for j in range(w.kv_indptr[b], w.kv_indptr[b + 1])}
+        assert int(ns.sum()) == len(overlaps)
+        got = oracle.combine(np.nan_to_num(o), np.where(np.isnan(ml), -np.inf, ml), nsplit=ns, lib=lib)
+        err = np.abs(got - ref).max()
+        assert err <= 1e-12, f"chunk combine C={C}: {err}"
+        # every written slot is a proper partial: finite m, positive l
+        for b in range(w.batch):
+            assert np.all(np.isfinite(ml[b, :, :ns[b], 0])) and np.all(ml[b, :, :ns[b], 1] > 0)
+
+
 def pin_partial_is_softmax_piece(lib):
     """One split's (m, l, o): m is the max logit, l*exp(m) the sum of exp(logit), o/l the
     softmax attention over that split's keys alone (checked against fp64 SDPA of that piece)."""
@@ -312,6 +336,6 @@ def pin_prefill_row_is_decode(lib):
 ALL_PINS = [
     pin_sdpa_decode, pin_sdpa_prefill, pin_prefix0_is_textbook_causal, pin_golden,
     pin_q_zero_is_mean_of_visible_v, pin_single_key_returns_v, pin_per_request_marker, pin_dominant_key,
-    pin_slot_permutation, pin_key_shift, pin_unreferenced_slots_unread, pin_split_combine,
+    pin_slot_permutation, pin_key_shift, pin_unreferenced_slots_unread, pin_split_combine, pin_chunk_partials_combine,
     pin_partial_is_softmax_piece, pin_prefill_row_is_decode,
 ]

@@ -87,17 +87,24 @@ def test_int_arrays_need_only_4_byte_alignment(lib):
     (dict(head_dim=96), pa.ASTR_ERR_UNSUPPORTED),
     (dict(head_dim=256), pa.ASTR_ERR_UNSUPPORTED),
     (dict(num_qo_heads=30, num_kv_heads=8), pa.ASTR_ERR_UNSUPPORTED),
-    (dict(num_qo_heads=128, num_kv_heads=4), pa.ASTR_ERR_UNSUPPORTED),   # decode group 32 not built
+    (dict(num_qo_heads=128, num_kv_heads=4), pa.ASTR_ERR_UNSUPPORTED),   # group 32 not built
     (dict(batch=-1), pa.ASTR_ERR_INVALID_ARG),
     (dict(num_kv_heads=0), pa.ASTR_ERR_INVALID_ARG),
     (dict(r2t_stride=100), pa.ASTR_ERR_INVALID_ARG),                      # stride below max_seq_len
     (dict(max_splits=0), pa.ASTR_ERR_INVALID_ARG),
-    (dict(num_splits=9), pa.ASTR_ERR_WORKSPACE_TOO_SMALL),
     (dict(num_splits=-1), pa.ASTR_ERR_INVALID_ARG),
     (dict(num_slots=0), pa.ASTR_ERR_INVALID_ARG),
 ])
 def test_decode_bad_dims(lib, kw, status):
     assert _dec(_dims(**kw)) == status
+
+
+def test_combine_explicit_layout_needs_capacity(lib):
+    # kv_indptr NULL: num_splits partials per row, which must fit in max_splits
+    st = pa.astr_attn_decode_combine(A, A, None, None, A, _dims(num_splits=9), stream=0, check=False)
+    assert st == pa.ASTR_ERR_WORKSPACE_TOO_SMALL
+    st = pa.astr_attn_decode_combine(A, A, None, None, A, _dims(num_splits=0), stream=0, check=False)
+    assert st == pa.ASTR_ERR_INVALID_ARG
 
 
 def test_decode_non_finite_scale(lib):

@@ -16,7 +16,7 @@ if not torch.cuda.is_available():
     pytest.skip("no CUDA device", allow_module_level=True)
 
 import prefill_attention_gb300 as pa  # noqa: E402
-from gpu_util import TOL, run_decode, sample_rows, to_f64, upload, decode_dims  # noqa: E402
+from gpu_util import TOL, decode_chunk_len, decode_dims, run_decode, sample_rows, to_f64, upload  # noqa: E402
 
 
 def _err(got, ref):
@@ -41,42 +41,71 @@ def test_decode_config_sampled(cfg):
     assert np.isfinite(out).all()
 
 
-@pytest.mark.parametrize("S", [1, 2, 3, 5, 16, 32])
-def test_forced_split_counts(S):
+@pytest.mark.parametrize("n_chunks", [1, 2, 3, 5, 16, 32, 200])
+def test_forced_chunk_counts(n_chunks):
     w = workload.config(1)
-    got = to_f64(run_decode(w, max_splits=32, num_splits=S))
+    got = to_f64(run_decode(w, max_splits=32, num_splits=n_chunks))
     assert _err(got, oracle.decode(w)) <= TOL
 
 
-@pytest.mark.parametrize("d,Hq,Hkv", [(128, 32, 8), (128, 8, 8), (128, 16, 8), (128, 64, 8),
-                                      (64, 8, 2), (64, 4, 4), (64, 8, 4), (64, 16, 2)])
+@pytest.mark.parametrize("max_splits", [1, 2, 3, 64])
+def test_workspace_capacity_floor(max_splits):
+    """A small partial capacity raises the chunk floor; results stay correct."""
+    w = workload.config(2)
+    got = to_f64(run_decode(w, max_splits=max_splits))
+    assert _err(got, oracle.decode(w)) <= TOL
+
+
+@pytest.mark.parametrize("d,Hq,Hkv", [(128, 32, 8), (128, 8, 8), (128, 16, 8), (128, 64, 8), (128, 128, 8),
+                                      (64, 8, 2), (64, 4, 4), (64, 8, 4), (64, 16, 2), (64, 32, 2)])
 def test_head_shapes_and_ragged_tails(d, Hq, Hkv):
     rng = np.random.default_rng(d * 1000 + Hq * 10 + Hkv)
-    seq = [1, 7, 8, 9, 31, 33, 64, 65, 200, 257]
+    seq = [1, 7, 8, 9, 31, 33, 64, 65, 127, 128, 129, 200, 257, 0, 600]
     w = make_from_lengths(rng, kind="decode", name="shapes", seq_lens=seq, q_lens=None, Hq=Hq, Hkv=Hkv, d=d)
-    for S in (0, 1, 4):
-        got = to_f64(run_decode(w, num_splits=S))
-        assert _err(got, oracle.decode(w)) <= TOL, f"S={S}"
+    for n in (0, 1, 4, 37):
+        got = to_f64(run_decode(w, num_splits=n))
+        assert _err(got, oracle.decode(w)) <= TOL, f"n_chunks={n}"
 
 
-def test_partials_match_oracle_split():
+def test_partials_match_oracle_chunks():
     w = workload.config(1)
-    S = 3
-    out, o, ml, S_used = run_decode(w, max_splits=8, num_splits=S, return_parts=True)
-    assert S_used == S
-    o_ref, ml_ref = oracle.decode_split_partials(w, S)
-    m, l = ml[..., 0], ml[..., 1]
-    assert np.array_equal(np.isneginf(m), np.isneginf(ml_ref[..., 0]))
-    fin = np.isfinite(ml_ref[..., 0])
-    assert np.abs(m[fin] - ml_ref[..., 0][fin]).max() <= 1e-3
-    assert np.abs(l[fin] / ml_ref[..., 1][fin] - 1).max() <= 1e-3
-    np.testing.assert_array_equal(l[~fin], 0)
-    norm = o[fin] / l[fin][:, None]
-    norm_ref = o_ref[fin] / ml_ref[..., 1][fin][:, None]
-    assert np.abs(norm - norm_ref).max() <= TOL
+    max_splits, n = 8, 5
+    out, o, ml, n_used = run_decode(w, max_splits=max_splits, num_splits=n, return_parts=True)
+    assert n_used == n
+    C = decode_chunk_len(w, n, max_splits)
+    o_ref, ml_ref, ns = oracle.decode_chunk_partials(w, C, max_splits)
+    assert ns.max() <= max_splits
+    assert (ns >= 2).any()
+    for b in range(w.batch):
+        k = int(ns[b])
+        if k < 2:   # single-chunk requests are written to `out` directly, without partials
+            continue
+        m, l = ml[b, :, :k, 0], ml[b, :, :k, 1]
+        assert np.abs(m - ml_ref[b, :, :k, 0]).max() <= 1e-3
+        assert np.abs(l / ml_ref[b, :, :k, 1] - 1).max() <= 1e-3
+        norm = o[b, :, :k] / l[..., None]
+        norm_ref = o_ref[b, :, :k] / ml_ref[b, :, :k, 1][..., None]
+        assert np.abs(norm - norm_ref).max() <= TOL
+    assert _err(to_f64(out), oracle.decode(w)) <= TOL
 
 
-def test_combine_alone_on_oracle_partials():
+def test_combine_alone_on_oracle_chunk_partials():
+    w = workload.config(1)
+    max_splits, n = 8, 7
+    dims = decode_dims(w, max_splits=max_splits, num_splits=n)
+    C = decode_chunk_len(w, n, max_splits)
+    o_ref, ml_ref, ns = oracle.decode_chunk_partials(w, C, max_splits)
+    o_part = torch.from_numpy(np.nan_to_num(o_ref).astype(np.float32)).cuda().contiguous()
+    ml_part = torch.from_numpy(np.nan_to_num(ml_ref).astype(np.float32)).cuda().contiguous()
+    out = torch.empty((w.batch, w.num_qo_heads, w.head_dim), dtype=torch.bfloat16, device="cuda")
+    kvi = torch.from_numpy(w.kv_indptr).cuda()
+    pa.astr_attn_decode_combine(o_part, ml_part, None, kvi, out, dims)
+    torch.cuda.synchronize()
+    assert _err(to_f64(out), oracle.decode(w)) <= TOL
+
+
+def test_combine_alone_explicit_layout():
+    """kv_indptr = NULL: every (b, h) row holds num_splits partials (here an even split)."""
     w = workload.config(1)
     S = 4
     o_ref, ml_ref = oracle.decode_split_partials(w, S)
@@ -224,3 +253,20 @@ def test_guard_bands_untouched():
         assert torch.all(buf[:pad] == val) and torch.all(buf[pad + n:] == val)
     got = to_f64(out_buf[pad:pad + n_out].view(w.batch, w.num_qo_heads, w.head_dim))
     assert _err(got, oracle.decode(w)) <= TOL
+
+
+def test_split_then_combine_entry_points():
+    """astr_attn_decode_split + astr_attn_decode_combine == astr_attn_paged_decode (bit-exact)."""
+    w = workload.config(2)
+    t = upload(w)
+    dims = decode_dims(w, max_splits=16)
+    o_part, ml_part = pa.alloc_decode_workspace(dims)
+    out = torch.empty_like(t["q"])
+    pa.astr_attn_decode_split(t["q"], t["k"], t["v"], t["r2t"], t["seq"], t["kvi"], o_part, ml_part, dims,
+                              w.sm_scale)
+    pa.astr_attn_decode_combine(o_part, ml_part, t["seq"], t["kvi"], out, dims)
+    torch.cuda.synchronize()
+    got = to_f64(out)
+    assert _err(got, oracle.decode(w)) <= TOL
+    ref = run_decode(w, t, max_splits=16)
+    assert np.abs(got - to_f64(ref)).max() <= TOL
