@@ -29,6 +29,13 @@ __device__ __forceinline__ uint32_t float2_to_bf16x2_rn(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// 2^x with the MUFU approximation (relative error ~2^-22); 2^-inf = +0.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ---------------------------------------------------------------- shared-memory addressing
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

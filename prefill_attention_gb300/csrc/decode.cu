@@ -59,6 +59,8 @@ __device__ __forceinline__ int decode_chunk_len(int T, int n_chunks, int min_chu
 
 namespace {
 
+constexpr float kRescaleLog2 = 8.f;  // lazy-rescale threshold (base-2 logit units)
+
 template <int D, int G>
 struct DecCfg {
   static constexpr int BK = 128;                   // keys per tile (MMA M for S^T)
@@ -344,25 +346,38 @@ __global__ void __launch_bounds__(352, 1) decode_split_tc_kernel(const DecodePar
 #pragma unroll
         for (int g = 0; g < G; ++g) sv[g] = kvalid ? __uint_as_float(r[g]) * scale : -CUDART_INF_F;
       }
-      // per-head max over the tile's 128 keys (exchange buffer alternates with j)
-      float* rmax = red + (j & 1) * 64;
+      // Lazy rescale: a head's reference max moves only on the first tile of a piece or
+      // when some score exceeds it by more than 2^8, so O^T is rarely rescaled, P stays
+      // below 2^8, and the result is exact because P, l and O share one reference max.
+      // Common case: one barrier vote that no score is that far above its reference.
+      bool over = false;
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float x = sv[g];
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) x = fmaxf(x, __shfl_xor_sync(kFullMask, x, o));
-        if (lane == 0) rmax[warp * 16 + g] = x;
-      }
-      tc::named_bar_sync(1, C::NSM);
+      for (int g = 0; g < G; ++g) over |= sv[g] > m_run[g] + kRescaleLog2;
+      const bool exchange = opens || tc::named_bar_or(1, C::NSM, over);
       float alpha[G];
       bool moved = false;
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float tmax = fmaxf(fmaxf(rmax[g], rmax[16 + g]), fmaxf(rmax[32 + g], rmax[48 + g]));
-        const float m_new = fmaxf(m_run[g], tmax);  // finite: the tile has at least one key
-        alpha[g] = exp2f(m_run[g] - m_new);          // 0 on the first tile of a piece
-        moved |= (m_new != m_run[g]);
-        m_run[g] = m_new;
+      for (int g = 0; g < G; ++g) alpha[g] = 1.f;
+      if (exchange) {  // per-head tile max over the 128 keys (exchange buffer alternates with j)
+        float* rmax = red + (j & 1) * 64;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float x = sv[g];
+#pragma unroll
+          for (int o = 16; o >= 1; o >>= 1) x = fmaxf(x, __shfl_xor_sync(kFullMask, x, o));
+          if (lane == 0) rmax[warp * 16 + g] = x;
+        }
+        tc::named_bar_sync(1, C::NSM);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float tmax = fmaxf(fmaxf(rmax[g], rmax[16 + g]), fmaxf(rmax[32 + g], rmax[48 + g]));
+          // tmax is finite: the tile has at least one key
+          const bool up = opens || tmax > m_run[g] + kRescaleLog2;
+          const float m_new = up ? fmaxf(m_run[g], tmax) : m_run[g];
+          alpha[g] = fast_exp2(m_run[g] - m_new);  // 0 on the first tile of a piece
+          moved |= (up && !opens);
+          m_run[g] = m_new;
+        }
       }
       // P^T buffer j&1 was last read by O^T += V^T P^T of tile j-2
       if (j >= 2 && !wait_or_fail(pv_done(j & 1), (uint32_t)(((j - 2) >> 1) & 1), err)) break;
@@ -370,7 +385,7 @@ __global__ void __launch_bounds__(352, 1) decode_split_tc_kernel(const DecodePar
       const int col_chunk = (tid & 63) >> 3, blk = tid >> 6, within = (tid & 7) * 2;
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        const float pg = exp2f(sv[g] - m_run[g]);  // 0 for keys past the piece
+        const float pg = fast_exp2(sv[g] - m_run[g]);  // 0 for keys past the piece
         l_thr[g] = l_thr[g] * alpha[g] + pg;
         const uint32_t hi16 = float2_to_bf16x2_rn(pg, 0.f) & 0xffffu;
         const float lo_f = pg - __uint_as_float(hi16 << 16);
@@ -381,8 +396,8 @@ __global__ void __launch_bounds__(352, 1) decode_split_tc_kernel(const DecodePar
         sts16(pb + blk * (C::NPV * 128) + (gl >> 3) * 1024 + (gl & 7) * 128 + ((col_chunk ^ (gl & 7)) << 4) + within,
               (uint16_t)lo16);
       }
-      // rescale the live O^T columns when a running max moved (CTA-uniform decision)
-      if (moved && !opens) {
+      // rescale the live O^T columns when a reference max moved (CTA-uniform decision)
+      if (moved) {
         if (!wait_or_fail(pv_done((j - 1) & 1), (uint32_t)(((j - 1) >> 1) & 1), err)) break;
         tc::fence_after_sync();
         if constexpr (C::NPV == 16) {
