@@ -164,6 +164,29 @@ int astr_attn_prefill_ragged(const uint16_t* q, const int32_t* qo_indptr, const 
                              const int32_t* kv_indptr, uint16_t* out, const astr_attn_dims* dims, float sm_scale,
                              void* stream);
 
+/*
+ * Paged decode that allocates nothing (no counterpart in the source pages; this is a
+ * service of this library).  Same computation, arguments, rules and errors as
+ * astr_attn_paged_decode minus o_part / ml_part: the split-KV partials go to a 16 MiB
+ * array compiled into the library instead of caller memory.  It is for callers that
+ * cannot hand the library a workspace -- an operator inside an inference runtime whose
+ * memory planner owns all device memory and forwards only inputs and outputs, or a
+ * process that must not grow device memory after start-up.  Every GPU that loads the
+ * library holds the array until the process exits.
+ *   - Size limit: batch * Hq * max_splits * (head_dim + 2) * 4 bytes (plus alignment
+ *     padding of at most 255 bytes) must fit in 16 MiB, else WORKSPACE_TOO_SMALL before
+ *     anything is launched.
+ *   - The first call on a device resolves the array's device address with that device
+ *     current; make that first call before any stream capture.
+ *   - All calls share the one array: calls that overlap on the GPU race and must be
+ *     serialised by the caller.  The array keeps the previous call's contents; nothing in
+ *     it needs to start at zero.
+ *   - Calls no cudaMalloc / cudaFree or any allocating routine.
+ */
+int astr_attn_paged_decode_noalloc(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
+                                   const int32_t* req_to_token, const int32_t* seq_lens, const int32_t* kv_indptr,
+                                   uint16_t* out, const astr_attn_dims* dims, float sm_scale, void* stream);
+
 /* Static description of a status code (never NULL). */
 const char* astr_attn_status_string(int status);
 

@@ -18,6 +18,7 @@ from typing import Optional
 __all__ = [
     "Dims", "AstrAttnError", "load", "lib_path", "make_dims",
     "astr_attn_paged_decode", "astr_attn_decode_split", "astr_attn_decode_combine", "astr_attn_prefill_ragged",
+    "astr_attn_paged_decode_noalloc",
     "astr_attn_decode_num_splits", "astr_attn_decode_workspace_bytes", "astr_attn_status_string",
     "astr_attn_version", "alloc_decode_workspace",
     "ASTR_OK", "ASTR_ERR_INVALID_ARG", "ASTR_ERR_UNSUPPORTED", "ASTR_ERR_MISALIGNED",
@@ -39,7 +40,7 @@ _lib = None
 EXPORTED_SYMBOLS = [
     "astr_attn_decode_num_splits", "astr_attn_decode_workspace_bytes", "astr_attn_paged_decode",
     "astr_attn_decode_combine", "astr_attn_prefill_ragged", "astr_attn_status_string", "astr_attn_version",
-    "astr_attn_decode_split",
+    "astr_attn_decode_split", "astr_attn_paged_decode_noalloc",
 ]
 
 
@@ -80,12 +81,14 @@ def load():
     lib.astr_attn_paged_decode.argtypes = [P, P, P, P, P, P, P, P, P, D, F, P]
     lib.astr_attn_decode_split.argtypes = [P, P, P, P, P, P, P, P, D, F, P]
     lib.astr_attn_decode_combine.argtypes = [P, P, P, P, P, D, P]
+    lib.astr_attn_paged_decode_noalloc.argtypes = [P, P, P, P, P, P, P, D, F, P]
     lib.astr_attn_prefill_ragged.argtypes = [P, P, P, P, P, P, P, P, D, F, P]
     lib.astr_attn_status_string.argtypes = [I32]
     lib.astr_attn_status_string.restype = ctypes.c_char_p
     lib.astr_attn_version.argtypes = []
     for f in ("astr_attn_decode_num_splits", "astr_attn_decode_workspace_bytes", "astr_attn_paged_decode",
-              "astr_attn_decode_split", "astr_attn_decode_combine", "astr_attn_prefill_ragged", "astr_attn_version"):
+              "astr_attn_decode_split", "astr_attn_decode_combine", "astr_attn_prefill_ragged", "astr_attn_version",
+              "astr_attn_paged_decode_noalloc"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -158,6 +161,19 @@ def astr_attn_decode_split(q, k_pool, v_pool, req_to_token, seq_lens, kv_indptr,
                                        _ptr(kv_indptr), _ptr(o_part), _ptr(ml_part), ctypes.byref(dims),
                                        float(sm_scale), _stream(stream))
     return _check(st, "astr_attn_decode_split", check)
+
+
+def astr_attn_paged_decode_noalloc(q, k_pool, v_pool, req_to_token, seq_lens, kv_indptr, out, dims: Dims,
+                                   sm_scale: float, stream=None, check: bool = True) -> int:
+    """Paged decode with the split partials in the library's own fixed device array.
+
+    For callers that cannot pass a workspace (see include/astr_attn.h): no allocation
+    happens anywhere in the call.  Calls that overlap on the GPU share the array and race.
+    """
+    st = load().astr_attn_paged_decode_noalloc(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(req_to_token),
+                                               _ptr(seq_lens), _ptr(kv_indptr), _ptr(out), ctypes.byref(dims),
+                                               float(sm_scale), _stream(stream))
+    return _check(st, "astr_attn_paged_decode_noalloc", check)
 
 
 def astr_attn_decode_combine(o_part, ml_part, seq_lens, kv_indptr, out, dims: Dims, stream=None,

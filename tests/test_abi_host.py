@@ -147,3 +147,24 @@ def test_prefill_kv_indptr_may_be_null_and_empty_batch_is_noop(lib):
 def test_workspace_bytes(lib):
     ob, mb = pa.astr_attn_decode_workspace_bytes(_dims(batch=32, max_splits=5))
     assert ob == 32 * 32 * 5 * 128 * 4 and mb == 32 * 32 * 5 * 2 * 4
+
+
+def test_noalloc_rejects_oversize_and_null_dims_without_gpu(lib):
+    # 256 x 32 heads x 64 splits x 130 floats = 272 MB > the fixed 16 MiB array
+    st = pa.astr_attn_paged_decode_noalloc(A, A, A, A, A, A, A, _dims(batch=256, max_splits=64), 0.1, stream=0,
+                                           check=False)
+    assert st == pa.ASTR_ERR_WORKSPACE_TOO_SMALL
+    st = lib.astr_attn_paged_decode_noalloc(A, A, A, A, A, A, A, None, ctypes.c_float(0.1), None)
+    assert st == pa.ASTR_ERR_INVALID_ARG
+
+
+def test_library_imports_no_device_allocator(lib):
+    """No entry point can allocate: the library does not even import cudaMalloc/cudaFree."""
+    import shutil
+    import subprocess
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    syms = subprocess.run([nm, "-D", "--undefined-only", pa.lib_path()], capture_output=True, text=True).stdout
+    for bad in ("cudaMalloc", "cudaFree", "cudaMallocAsync", "cudaFreeAsync", "cudaMallocManaged"):
+        assert f" {bad}" not in syms and f"U {bad}@" not in syms, bad
