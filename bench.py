@@ -446,7 +446,7 @@ def main():
                    "kv_bytes_per_call": nbytes["kv"], "total_keys": int(w.seq_lens.sum()),
                    "l2": f"rotating {POOL_COPIES} KV-pool copies ({POOL_COPIES * nbytes['kv'] / 1e6:.0f} MB > L2)",
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "kernel": "decode_split_tc_kernel<128,4>", "achieved": round(split_gbs, 2),
+        "roofline": {"bound": "hbm", "kernel": "decode_split_kernel<128,4>", "achieved": round(split_gbs, 2),
                      "peak": peaks["hbm_gbs"], "peak_source": f"hbm_gbs ({peaks_src})", "unit": "GB/s",
                      "frac": round(split_gbs / peaks["hbm_gbs"], 4), "us_per_launch": round(t_split * 1e6, 3),
                      "traffic": traffic},

@@ -1,4 +1,4 @@
-// decode.cu -- split-KV paged decode for sm_103a on the 5th-generation tensor core.
+// decode.cu -- split-KV paged decode for sm_103a.
 //
 // Method (AstrAI commit log, page "astrai/extension @6f67ba8"):
 //   * CUDA-backend commit: req_to_token is the page table with one token per page, so
@@ -17,30 +17,32 @@
 //     whole batch (T = kv_indptr[B]) is cut into equal chunks of C keys, one CTA per chunk,
 //     so every CTA moves the same number of bytes however skewed seq_lens is.  A chunk may
 //     hold the tail of one request and the head of the next; each such piece produces one
-//     partial, indexed by (chunk - first chunk of the request).  C depends only on T, the
-//     grid and a host-supplied floor, so the combine recomputes it identically.
+//     partial, indexed by (chunk - first chunk of the request), and a request that lies
+//     inside one chunk is written to the output directly.  C depends only on T, the grid
+//     and a host-supplied floor, so the combine recomputes it identically.
 //   * One persistent CTA per SM, warp specialised:
 //       warps 4-9 (producers) -- three groups of two warps, group g owning ring stage g
-//               (tiles g, g+3, ...): a group gathers the K and V rows of its 128-key tile slot
-//               by slot with 16-byte cp.async into the 128-byte-swizzled layout the tensor
-//               core reads (XOR of the 16-byte chunk index with the row), waits for its own
-//               copies, fences them to the async proxy and arrives on the stage's full
-//               barrier.  Three tiles are in flight and each is published as soon as it
-//               lands.  (TMA tile::gather4 was measured first: at one
-//               128-byte row per gathered row it delivered ~12 GB/s per SM, well below the
-//               ~45 GB/s per SM the HBM roofline needs, so the gather stays on the LSU path.)
-//       warp 10 (MMA)     -- one thread issues S^T = K Q^T (M = 128 keys, N = 16 padded
-//               query heads) into a double-buffered TMEM accumulator, one tile ahead of the
-//               softmax, then O^T += V^T P^T (M = head_dim, V read MN-major from the same
-//               tile) and releases the stage with tcgen05.commit.
-//       warps 0-3 (softmax) -- thread t owns key t of the tile: it reads its S^T row from
-//               TMEM, the per-head max goes through warp shuffles and a 4-entry exchange,
-//               exp2 runs on the CUDA cores (the scale carries log2 e), and P^T is written
-//               as two bf16 planes, hi = bf16(p) and lo = bf16(p - hi), side by side in the
-//               N dimension, so O^T accumulates p to ~2^-17 relative precision.  At the end
-//               of a request piece the same warps read O^T (thread = head_dim row) and
-//               write the partial.
-//     All G query heads of a KV head are served by each K/V tile.
+//               (tiles g, g+3, ...): a group gathers the K and V rows of its 128-key tile
+//               slot by slot with 16-byte cp.async into a 128-byte-swizzled layout (16-byte
+//               chunk c of row r at c ^ (r & 7), so 8 consecutive rows of one chunk hit 8
+//               different bank groups), waits for its own copies and arrives on the
+//               stage's full barrier.  Three 64 KB tiles are in flight and each is published
+//               as soon as it lands.
+//       warps 0-3 (consumers) -- warp w owns keys 32w .. 32w+31 of every tile and keeps its
+//               own online-softmax state: S = Q K^T and O += P V as warp-level bf16 tensor
+//               core MMAs (m16n8k16, fp32 accumulators in registers, operands via ldmatrix
+//               from the swizzled tiles).  The 16 MMA rows are the G query heads sharing the
+//               KV head (zero-padded), so one K/V load serves all of them.  P is split into
+//               hi = bf16(p) and lo = bf16(p - hi) and both halves go through the MMA, which
+//               keeps p to ~2^-17 relative precision.  Softmax in base 2 (the scale carries
+//               log2 e) with a lazy rescale: a warp moves its reference max only when a
+//               score exceeds it by more than 2^8.  The four warps merge once per request
+//               piece through shared memory; there is no per-tile CTA synchronisation.
+//     Measured alternatives (see the profiles): a CUDA-core version was issue bound
+//     (~550 instructions per 4 KB of K/V); a tcgen05 version with S^T / O^T accumulators in
+//     tensor memory spent ~150 cycles per M=128 x N=16 x K=16 MMA, ~2400 cycles per 64 KB
+//     tile on the critical path; TMA tile::gather4 for the row gather delivered ~12 GB/s
+//     per SM.
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
@@ -63,50 +65,63 @@ constexpr float kRescaleLog2 = 8.f;  // lazy-rescale threshold (base-2 logit uni
 
 template <int D, int G>
 struct DecCfg {
-  static constexpr int BK = 128;                   // keys per tile (MMA M for S^T)
+  static constexpr int BK = 128;                   // keys per tile
   static constexpr int STAGES = 3;
-  static constexpr int THREADS = 352;              // 4 softmax warps, 6 producer warps, MMA warp
+  static constexpr int NCONS = 4;                  // consumer warps (32 keys each)
+  static constexpr int THREADS = 320;              // 4 consumer warps, 6 producer warps
   static constexpr int NPROD = 64;                 // producer threads per group (one group per stage)
-  static constexpr int MMA_WARP = 10;
-  static constexpr int NSM = 128;                  // softmax threads
-  static constexpr int NS = 16;                    // S^T columns: query heads padded to 16
-  static constexpr int NPV = (G <= 8) ? 16 : 32;   // O^T columns: hi heads then lo heads
-  static constexpr int HALF = NPV / 2;
-  static constexpr int NCB = D / 64;               // 128-byte column blocks per K/V row
+  static constexpr int CPR = D / 8;                // 16-byte chunks per K/V row
+  static constexpr int KV_IT = BK * CPR / NPROD;   // cp.async per producer thread per K tile
   static constexpr int TILE = BK * D * 2;          // one K (or V) tile
-  static constexpr int ZERO = (D == 64) ? BK * 128 : 0;   // pads V^T to M = 128 when D = 64
-  static constexpr int STAGE_BYTES = 2 * TILE + ZERO;     // K | V | zero block
+  static constexpr int STAGE_BYTES = 2 * TILE;     // K | V
+  static constexpr int QROWS = 16;                 // MMA rows: query heads, zero padded
   static constexpr int QBUFS = 4;
-  static constexpr int Q_BYTES = NS * D * 2;
-  static constexpr int P_BYTES = NPV * BK * 2;
+  static constexpr int Q_BYTES = QROWS * D * 2;
+  static constexpr int HG = (D == 128) ? 8 : 16;   // head rows merged per pass at a piece end
+  static constexpr int MERGE_BYTES = NCONS * HG * D * 4;
   static constexpr int Q_OFF = STAGES * STAGE_BYTES;
-  static constexpr int P_OFF = Q_OFF + QBUFS * Q_BYTES;   // 2 buffers
-  static constexpr int RED_OFF = P_OFF + 2 * P_BYTES;     // [2][4 warps][16] floats (max), [4][16] (sum)
-  static constexpr int BAR_OFF = RED_OFF + 3 * 4 * 16 * 4;
-  // barriers: full[3], empty[3], s_full[2], p_full[2], pv_done[2], then tmem slot, error flag
-  static constexpr int NBAR = 3 + 3 + 2 + 2 + 2;
+  static constexpr int MERGE_OFF = Q_OFF + QBUFS * Q_BYTES;
+  static constexpr int ML_OFF = MERGE_OFF + MERGE_BYTES;   // [NCONS][16] m, then [NCONS][16] l
+  static constexpr int BAR_OFF = ML_OFF + 2 * NCONS * 16 * 4;
+  static constexpr int NBAR = 2 * STAGES + 1;      // full[3], empty[3], consumer merge barrier
   static constexpr int SMEM_BYTES = BAR_OFF + NBAR * 8 + 16;
-  static constexpr int CPR = D / 8;                      // 16-byte chunks per K/V row
-  static constexpr int KV_IT = BK * CPR / NPROD;          // cp.async per producer thread per K tile
-  static constexpr uint32_t TMEM_S0 = 0;           // S^T buffers at columns 0 and 16
-  static constexpr uint32_t TMEM_O = 32;
-  static constexpr uint32_t TMEM_COLS = 64;
-  static constexpr uint32_t IDESC_S = tc::idesc_bf16_f32(128, NS, false, false);
-  static constexpr uint32_t IDESC_PV = tc::idesc_bf16_f32(128, NPV, true, false);  // A (V^T) MN-major
+  static constexpr int KSTEPS = D / 16;            // MMA k-steps over head_dim
+  static constexpr int NT_D = D / 8;               // 8-wide n-tiles over head_dim
   static_assert(G <= 16, "at most 16 query heads per KV head");
-  static_assert(TMEM_O + NPV <= TMEM_COLS, "tensor-memory budget");
-  static_assert(STAGE_BYTES % 1024 == 0 && Q_OFF % 1024 == 0 && P_OFF % 1024 == 0 && Q_BYTES % 1024 == 0 &&
-                    P_BYTES % 1024 == 0,
-                "swizzle atoms must be 1024-byte aligned");
+  static_assert(STAGE_BYTES % 1024 == 0 && Q_OFF % 1024 == 0 && Q_BYTES % 1024 == 0, "swizzle atoms");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
-__device__ __forceinline__ void sts16(uint32_t addr, uint16_t v) {
-  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
-}
-
 __device__ __forceinline__ void sts128_zero(uint32_t addr) {
   asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(addr), "r"(0) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// D += A * B for one m16n8k16 bf16 tile with fp32 accumulation.
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Byte offset of 16-byte chunk c of row r in a 128-byte-swizzled tile whose 64-element
+// column blocks each hold `rows` rows.
+__device__ __forceinline__ uint32_t sw128(int r, int c, int rows) {
+  return (uint32_t)((c >> 3) * rows * 128 + (r >> 3) * 1024 + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
 // Walks the tiles of one chunk: a tile never crosses a request boundary.
@@ -146,14 +161,8 @@ __device__ __forceinline__ bool wait_or_fail(uint32_t bar, uint32_t parity, vola
   return false;
 }
 
-// Byte offset of 16-byte chunk c of row r in a 128-byte-swizzled K-major tile whose
-// 64-element column blocks each hold `rows` rows.
-__device__ __forceinline__ uint32_t sw128(int r, int c, int rows) {
-  return (uint32_t)((c >> 3) * rows * 128 + (r >> 3) * 1024 + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4));
-}
-
 template <int D, int G>
-__global__ void __launch_bounds__(352, 1) decode_split_tc_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(320, 1) decode_split_kernel(const DecodeParams p) {
   using C = DecCfg<D, G>;
   extern __shared__ __align__(1024) unsigned char smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -170,49 +179,29 @@ __global__ void __launch_bounds__(352, 1) decode_split_tc_kernel(const DecodePar
 
   const uint32_t bars = sbase + C::BAR_OFF;
   auto full = [&](int s) { return bars + 8u * s; };
-  auto empty = [&](int s) { return bars + 8u * (3 + s); };
-  auto s_full = [&](int i) { return bars + 8u * (6 + i); };
-  auto p_full = [&](int i) { return bars + 8u * (8 + i); };
-  auto pv_done = [&](int i) { return bars + 8u * (10 + i); };
-  const uint32_t slot = bars + 8u * C::NBAR;
-  volatile int* err = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 8 * C::NBAR + 4);
-  float* red = reinterpret_cast<float*>(smem + C::RED_OFF);
+  auto empty = [&](int s) { return bars + 8u * (C::STAGES + s); };
+  const uint32_t cbar = bars + 8u * (2 * C::STAGES);  // the four consumer warps, bounded waits
+  volatile int* err = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 8 * C::NBAR);
 
-  // ---- set-up: barriers, TMEM, zero padding (P rows of absent heads, V^T pad block)
+  // ---- set-up: barriers; Q rows of absent heads stay zero for the whole kernel
   if (tid == 0) {
-    for (int s = 0; s < 3; ++s) {
+    for (int s = 0; s < C::STAGES; ++s) {
       tc::mbar_init(full(s), C::NPROD);
-      tc::mbar_init(empty(s), 1);
+      tc::mbar_init(empty(s), C::NCONS * 32);
     }
-    for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(s_full(i), 1);
-      tc::mbar_init(p_full(i), C::NSM);
-      tc::mbar_init(pv_done(i), 1);
-    }
+    tc::mbar_init(cbar, C::NCONS * 32);
     *err = 0;
     tc::fence_mbarrier_init();
   }
-  if (warp == C::MMA_WARP) tc::tmem_alloc<C::TMEM_COLS>(slot);
-  // P^T rows of absent heads and Q rows of absent heads stay zero for the whole kernel
-  for (int i = tid; i < 2 * C::P_BYTES / 16; i += C::THREADS) sts128_zero(sbase + C::P_OFF + i * 16);
   for (int i = tid; i < C::QBUFS * C::Q_BYTES / 16; i += C::THREADS) sts128_zero(sbase + C::Q_OFF + i * 16);
-  if constexpr (C::ZERO > 0) {
-    for (int st = 0; st < C::STAGES; ++st)
-      for (int i = tid; i < C::ZERO / 16; i += C::THREADS)
-        sts128_zero(sbase + st * C::STAGE_BYTES + 2 * C::TILE + i * 16);
-  }
-  tc::fence_proxy_async_smem();
-  tc::fence_before_sync();
   __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::BAR_OFF + 8 * C::NBAR);
   // let the combine kernel's CTAs launch now; they wait for this grid's memory to be visible
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  if (warp >= 4 && warp < 10) {
+  if (warp >= C::NCONS) {
     // ======================= producers: group g fills ring stage g with tiles g, g+3, ...
-    const int grp = (warp - 4) >> 1;             // 0..2 = the stage this group owns
-    const int pt = tid - C::NSM - grp * C::NPROD;  // 0..63 within the group
+    const int grp = (warp - C::NCONS) >> 1;             // 0..2 = the stage this group owns
+    const int pt = tid - C::NCONS * 32 - grp * C::NPROD;  // 0..63 within the group
     TileIter it;
     it.first(ind, B, lo, hi);
     int piece = 0;
@@ -244,7 +233,7 @@ __global__ void __launch_bounds__(352, 1) decode_split_tc_kernel(const DecodePar
         const bool valid = ids[i] >= 0;
         const size_t off = valid ? (size_t)ids[i] * head_stride + (size_t)kvh * D + c * 8 : 0;
         const uint32_t o = sw128(key, c, C::BK);
-        cp_async16(kst + o, p.k_pool + off, valid);
+        cp_async16(kst + o, p.k_pool + off, valid);  // rows past the piece are zero-filled
         cp_async16(vst + o, p.v_pool + off, valid);
       }
       if (it.opens_piece(ind, lo)) {  // first tile of a piece: its G query rows
@@ -252,7 +241,7 @@ __global__ void __launch_bounds__(352, 1) decode_split_tc_kernel(const DecodePar
         const uint16_t* qsrc = p.q + ((size_t)it.b * p.num_qo_heads + (size_t)kvh * G) * D;
         for (int i = pt; i < G * C::CPR; i += C::NPROD) {
           const int g = i / C::CPR, c = i % C::CPR;
-          cp_async16(qb + sw128(g, c, C::NS), qsrc + (size_t)g * D + c * 8, true);
+          cp_async16(qb + sw128(g, c, C::QROWS), qsrc + (size_t)g * D + c * 8, true);
         }
       }
       cp_async_commit();
@@ -263,252 +252,225 @@ __global__ void __launch_bounds__(352, 1) decode_split_tc_kernel(const DecodePar
       }
       load_ids(it);
       cp_async_wait<0>();
-      tc::fence_proxy_async_smem();
-      tc::mbar_arrive(full(grp));
+      tc::mbar_arrive(full(grp));  // release: the copies are visible to the consumers' loads
     }
-  } else if (warp == C::MMA_WARP) {
-    // ======================= MMA issuer (one thread)
-    // Two streams issued as their inputs become ready, polled without blocking so that
-    // neither can hold up the other: S^T of tile k (needs tile k resident and S buffer k&1
-    // released by the softmax of tile k-2) and O^T += V^T P^T of tile k (needs P of tile k).
-    if (lane == 0) {
-      TileIter s_it, v_it;
-      s_it.first(ind, B, lo, hi);
-      v_it.first(ind, B, lo, hi);
-      int s_piece = 0, ns = 0, nv = 0;
-      long long idle_since = clock64();
-      while (v_it.valid(hi)) {
-        bool progress = false;
-        if (s_it.valid(hi) && ns <= nv + 1 && tc::mbar_test(full(ns % C::STAGES), (uint32_t)((ns / C::STAGES) & 1))) {
-          tc::fence_after_sync();
-          const uint32_t kst = sbase + (ns % C::STAGES) * C::STAGE_BYTES;
-          const uint32_t qb = sbase + C::Q_OFF + (s_piece % C::QBUFS) * C::Q_BYTES;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t ad = tc::smem_desc_sw128(kst + (kk >> 2) * (C::BK * 128) + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = tc::smem_desc_sw128(qb + (kk >> 2) * (C::NS * 128) + (kk & 3) * 32, 16, 1024);
-            tc::mma_bf16_ss(tmem + C::TMEM_S0 + (ns & 1) * 16, ad, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
-          }
-          tc::mma_commit(s_full(ns & 1));
-          if (s_it.closes_piece(ind, hi)) ++s_piece;
-          s_it.next(ind, B, hi);
-          ++ns;
-          progress = true;
-        }
-        if (nv < ns && tc::mbar_test(p_full(nv & 1), (uint32_t)((nv >> 1) & 1))) {
-          tc::fence_after_sync();
-          const uint32_t vst = sbase + (nv % C::STAGES) * C::STAGE_BYTES + C::TILE;
-          const uint32_t pb = sbase + C::P_OFF + (nv & 1) * C::P_BYTES;
-          const bool opens = v_it.opens_piece(ind, lo);
-#pragma unroll
-          for (int kk = 0; kk < C::BK / 16; ++kk) {
-            // A = V^T: M = head_dim (MN-major; second 64-column block at +BK*128 bytes, which
-            // is the zero block when head_dim = 64), K = 16 keys per step
-            const uint64_t ad = tc::smem_desc_sw128(vst + kk * 16 * 128, C::BK * 128, 1024);
-            const uint64_t bd = tc::smem_desc_sw128(pb + (kk >> 2) * (C::NPV * 128) + (kk & 3) * 32, 16, 1024);
-            tc::mma_bf16_ss(tmem + C::TMEM_O, ad, bd, C::IDESC_PV, (opens && kk == 0) ? 0u : 1u);
-          }
-          tc::mma_commit(empty(nv % C::STAGES));
-          tc::mma_commit(pv_done(nv & 1));
-          v_it.next(ind, B, hi);
-          ++nv;
-          progress = true;
-        }
-        if (progress) {
-          idle_since = clock64();
-        } else if (*err || clock64() - idle_since > (1ll << 31)) {  // ~1 s without progress
-          *err = 1;
-          break;
-        } else {
-          __nanosleep(32);
-        }
-      }
-    }
+    cp_async_wait<0>();
   } else {
-    // ======================= softmax warps 0-3 (thread t = key t = TMEM lane t)
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    // ======================= consumers: warp w owns keys 32w .. 32w+31 of every tile
+    const int g4 = lane >> 2, t4 = lane & 3;  // fragment row / column-pair index
+    const int lrow = lane & 7, lmat = lane >> 3;  // ldmatrix: row within / index of the 8x8 matrix
+    const float scale = p.scale_log2;
+    float* mw = reinterpret_cast<float*>(smem + C::ML_OFF);  // [NCONS][16]
+    float* lw = mw + C::NCONS * 16;                           // [NCONS][16]
+    float* mrg = reinterpret_cast<float*>(smem + C::MERGE_OFF);
+
     TileIter it;
     it.first(ind, B, lo, hi);
-    float m_run[G], l_thr[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) { m_run[g] = -CUDART_INF_F; l_thr[g] = 0.f; }
-    const float scale = p.scale_log2;
+    int piece = 0;
+    uint32_t cphase = 0;            // completed phases of the consumer merge barrier
+    auto cons_sync = [&]() -> bool {  // barrier over the consumer warps that cannot hang
+      tc::mbar_arrive(cbar);
+      return wait_or_fail(cbar, (cphase++) & 1u, err);
+    };
+    uint32_t qa[C::KSTEPS][4];      // Q as the A operand (rows = heads), per k-step
+    float acc[C::NT_D][4];          // O rows g4 (c0,c1) and g4+8 (c2,c3) over head_dim
+    float m_run[2], l_thr[2];       // rows g4 and g4+8 of this warp
     for (int j = 0; it.valid(hi); ++j) {
+      const int st = j % C::STAGES;
       const bool opens = it.opens_piece(ind, lo), closes = it.closes_piece(ind, hi);
-      if (!wait_or_fail(s_full(j & 1), (uint32_t)((j >> 1) & 1), err)) break;
-      tc::fence_after_sync();
-      const bool kvalid = it.start + tid < it.end;
-      float sv[G];
-      {
-        uint32_t r[16];
-        tc::tmem_ld16(tmem + lane_base + C::TMEM_S0 + (j & 1) * 16, r);
-        tc::tmem_ld_wait();
+      if (!wait_or_fail(full(st), (uint32_t)((j / C::STAGES) & 1), err)) break;
+      const uint32_t kst = sbase + st * C::STAGE_BYTES, vst = kst + C::TILE;
+
+      if (opens) {  // new request piece: its query rows, fresh softmax state
+        const uint32_t qb = sbase + C::Q_OFF + (piece % C::QBUFS) * C::Q_BYTES;
 #pragma unroll
-        for (int g = 0; g < G; ++g) sv[g] = kvalid ? __uint_as_float(r[g]) * scale : -CUDART_INF_F;
+        for (int kk = 0; kk < C::KSTEPS; ++kk) {
+          // matrices: (rows 0-7, chunk 2kk), (rows 8-15, 2kk), (rows 0-7, 2kk+1), (rows 8-15, 2kk+1)
+          const int r = lrow + (lmat & 1) * 8, c = 2 * kk + (lmat >> 1);
+          ldsm_x4(qb + sw128(r, c, C::QROWS), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+        }
+#pragma unroll
+        for (int n = 0; n < C::NT_D; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+        m_run[0] = m_run[1] = -CUDART_INF_F;
+        l_thr[0] = l_thr[1] = 0.f;
       }
-      // Lazy rescale: a head's reference max moves only on the first tile of a piece or
-      // when some score exceeds it by more than 2^8, so O^T is rarely rescaled, P stays
-      // below 2^8, and the result is exact because P, l and O share one reference max.
-      // Common case: one barrier vote that no score is that far above its reference.
-      bool over = false;
+
+      // ---- S = Q K^T for this warp's 32 keys: 4 n-tiles of 8 keys
+      const int kbase = warp * 32;
+      float s[4][4];
 #pragma unroll
-      for (int g = 0; g < G; ++g) over |= sv[g] > m_run[g] + kRescaleLog2;
-      const bool exchange = opens || tc::named_bar_or(1, C::NSM, over);
-      float alpha[G];
+      for (int n = 0; n < 4; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < C::KSTEPS; ++kk) {
+#pragma unroll
+        for (int np = 0; np < 2; ++np) {  // two n-tiles per ldmatrix.x4
+          // matrices: (keys n, chunk 2kk), (keys n, 2kk+1), (keys n+8, 2kk), (keys n+8, 2kk+1)
+          const int key = kbase + np * 16 + lrow + (lmat >> 1) * 8, c = 2 * kk + (lmat & 1);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(kst + sw128(key, c, C::BK), b0, b1, b2, b3);
+          mma16816(s[2 * np], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+          mma16816(s[2 * np + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
+        }
+      }
+
+      // ---- online softmax (base 2) on rows g4 (c0,c1) and g4+8 (c2,c3)
+      const int nkeys = it.end - it.start;  // valid keys of the tile; the rest are masked
+      float rmax[2] = {-CUDART_INF_F, -CUDART_INF_F};
+#pragma unroll
+      for (int n = 0; n < 4; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int key = kbase + n * 8 + 2 * t4 + (e & 1);
+          const float x = (key < nkeys) ? s[n][e] * scale : -CUDART_INF_F;
+          s[n][e] = x;
+          rmax[e >> 1] = fmaxf(rmax[e >> 1], x);
+        }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        rmax[h] = fmaxf(rmax[h], __shfl_xor_sync(kFullMask, rmax[h], 1));
+        rmax[h] = fmaxf(rmax[h], __shfl_xor_sync(kFullMask, rmax[h], 2));
+      }
+      float alpha[2] = {1.f, 1.f};
       bool moved = false;
 #pragma unroll
-      for (int g = 0; g < G; ++g) alpha[g] = 1.f;
-      if (exchange) {  // per-head tile max over the 128 keys (exchange buffer alternates with j)
-        float* rmax = red + (j & 1) * 64;
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          float x = sv[g];
-#pragma unroll
-          for (int o = 16; o >= 1; o >>= 1) x = fmaxf(x, __shfl_xor_sync(kFullMask, x, o));
-          if (lane == 0) rmax[warp * 16 + g] = x;
-        }
-        tc::named_bar_sync(1, C::NSM);
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float tmax = fmaxf(fmaxf(rmax[g], rmax[16 + g]), fmaxf(rmax[32 + g], rmax[48 + g]));
-          // tmax is finite: the tile has at least one key
-          const bool up = opens || tmax > m_run[g] + kRescaleLog2;
-          const float m_new = up ? fmaxf(m_run[g], tmax) : m_run[g];
-          alpha[g] = fast_exp2(m_run[g] - m_new);  // 0 on the first tile of a piece
-          moved |= (up && !opens);
-          m_run[g] = m_new;
+      for (int h = 0; h < 2; ++h) {
+        // a warp whose keys are all masked keeps m = -inf; nothing it adds is nonzero
+        if (rmax[h] > m_run[h] + kRescaleLog2) {
+          alpha[h] = fast_exp2(m_run[h] - rmax[h]);  // 0 when m_run = -inf
+          m_run[h] = rmax[h];
+          moved = true;
         }
       }
-      // P^T buffer j&1 was last read by O^T += V^T P^T of tile j-2
-      if (j >= 2 && !wait_or_fail(pv_done(j & 1), (uint32_t)(((j - 2) >> 1) & 1), err)) break;
-      const uint32_t pb = sbase + C::P_OFF + (j & 1) * C::P_BYTES;
-      const int col_chunk = (tid & 63) >> 3, blk = tid >> 6, within = (tid & 7) * 2;
+      if (__any_sync(kFullMask, moved)) {
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float pg = fast_exp2(sv[g] - m_run[g]);  // 0 for keys past the piece
-        l_thr[g] = l_thr[g] * alpha[g] + pg;
-        const uint32_t hi16 = float2_to_bf16x2_rn(pg, 0.f) & 0xffffu;
-        const float lo_f = pg - __uint_as_float(hi16 << 16);
-        const uint32_t lo16 = float2_to_bf16x2_rn(lo_f, 0.f) & 0xffffu;
-        const int gl = C::HALF + g;
-        sts16(pb + blk * (C::NPV * 128) + (g >> 3) * 1024 + (g & 7) * 128 + ((col_chunk ^ (g & 7)) << 4) + within,
-              (uint16_t)hi16);
-        sts16(pb + blk * (C::NPV * 128) + (gl >> 3) * 1024 + (gl & 7) * 128 + ((col_chunk ^ (gl & 7)) << 4) + within,
-              (uint16_t)lo16);
-      }
-      // rescale the live O^T columns when a reference max moved (CTA-uniform decision)
-      if (moved) {
-        if (!wait_or_fail(pv_done((j - 1) & 1), (uint32_t)(((j - 1) >> 1) & 1), err)) break;
-        tc::fence_after_sync();
-        if constexpr (C::NPV == 16) {
-          uint32_t o[16];
-          tc::tmem_ld16(tmem + lane_base + C::TMEM_O, o);
-          tc::tmem_ld_wait();
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            o[g] = __float_as_uint(__uint_as_float(o[g]) * alpha[g]);
-            o[C::HALF + g] = __float_as_uint(__uint_as_float(o[C::HALF + g]) * alpha[g]);
-          }
-          tc::tmem_st16(tmem + lane_base + C::TMEM_O, o);
-        } else {
-          uint32_t o[32];
-          tc::tmem_ld32(tmem + lane_base + C::TMEM_O, o);
-          tc::tmem_ld_wait();
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            o[g] = __float_as_uint(__uint_as_float(o[g]) * alpha[g]);
-            o[C::HALF + g] = __float_as_uint(__uint_as_float(o[C::HALF + g]) * alpha[g]);
-          }
-          tc::tmem_st32(tmem + lane_base + C::TMEM_O, o);
+        for (int n = 0; n < C::NT_D; ++n) {
+          acc[n][0] *= alpha[0]; acc[n][1] *= alpha[0];
+          acc[n][2] *= alpha[1]; acc[n][3] *= alpha[1];
         }
-        tc::tmem_st_wait();
+        l_thr[0] *= alpha[0];
+        l_thr[1] *= alpha[1];
       }
-      tc::fence_proxy_async_smem();
-      tc::fence_before_sync();
-      tc::mbar_arrive(p_full(j & 1));
+      // P = exp2(s - m) as hi / lo bf16 A fragments, two k-steps of 16 keys
+      uint32_t ph[2][4], pl[2][4];
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        float pv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float mr = m_run[e >> 1];
+          pv[e] = (mr == -CUDART_INF_F) ? 0.f : fast_exp2(s[n][e] - mr);
+          l_thr[e >> 1] += pv[e];
+        }
+        const uint32_t h01 = float2_to_bf16x2_rn(pv[0], pv[1]), h23 = float2_to_bf16x2_rn(pv[2], pv[3]);
+        const float2 f01 = bf16x2_to_float2(h01), f23 = bf16x2_to_float2(h23);
+        const uint32_t l01 = float2_to_bf16x2_rn(pv[0] - f01.x, pv[1] - f01.y);
+        const uint32_t l23 = float2_to_bf16x2_rn(pv[2] - f23.x, pv[3] - f23.y);
+        // n-tile n covers keys 8n..8n+7 of the warp: k-step n/2, low (a0a1,a2a3) or high (a4a5,a6a7) half
+        const int ks = n >> 1, hi8 = (n & 1) * 2;
+        ph[ks][hi8 + 0] = h01; ph[ks][hi8 + 1] = h23;
+        pl[ks][hi8 + 0] = l01; pl[ks][hi8 + 1] = l23;
+      }
+
+      // ---- O += P V over the warp's 32 keys: 2 k-steps x head_dim / 8 n-tiles
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks) {
+#pragma unroll
+        for (int np = 0; np < C::NT_D / 2; ++np) {  // two d n-tiles per ldmatrix.x4.trans
+          // matrices: (keys 0-7, chunk 2np), (keys 8-15, 2np), (keys 0-7, 2np+1), (keys 8-15, 2np+1)
+          const int key = kbase + ks * 16 + lrow + (lmat & 1) * 8, c = 2 * np + (lmat >> 1);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(vst + sw128(key, c, C::BK), b0, b1, b2, b3);
+          mma16816(acc[2 * np], ph[ks][0], ph[ks][1], ph[ks][2], ph[ks][3], b0, b1);
+          mma16816(acc[2 * np], pl[ks][0], pl[ks][1], pl[ks][2], pl[ks][3], b0, b1);
+          mma16816(acc[2 * np + 1], ph[ks][0], ph[ks][1], ph[ks][2], ph[ks][3], b2, b3);
+          mma16816(acc[2 * np + 1], pl[ks][0], pl[ks][1], pl[ks][2], pl[ks][3], b2, b3);
+        }
+      }
+      __syncwarp();
+      tc::mbar_arrive(empty(st));  // this warp is done reading stage st
 
       if (closes) {
-        // piece finished: O^T += V^T P^T of this tile must land, then write the partial
-        if (!wait_or_fail(pv_done(j & 1), (uint32_t)((j >> 1) & 1), err)) break;
-        tc::fence_after_sync();
-        float* rsum = red + 128;
+        // ---- piece finished: merge the four warps (log-sum-exp) and write it out
+        float lsum[2];
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          float x = l_thr[g];
-#pragma unroll
-          for (int o = 16; o >= 1; o >>= 1) x += __shfl_xor_sync(kFullMask, x, o);
-          if (lane == 0) rsum[warp * 16 + g] = x;
+        for (int h = 0; h < 2; ++h) {
+          float x = l_thr[h];
+          x += __shfl_xor_sync(kFullMask, x, 1);
+          x += __shfl_xor_sync(kFullMask, x, 2);
+          lsum[h] = x;
         }
-        float og[G];
-        if constexpr (C::NPV == 16) {
-          uint32_t o[16];
-          tc::tmem_ld16(tmem + lane_base + C::TMEM_O, o);
-          tc::tmem_ld_wait();
-#pragma unroll
-          for (int g = 0; g < G; ++g) og[g] = __uint_as_float(o[g]) + __uint_as_float(o[C::HALF + g]);
-        } else {
-          uint32_t o[32];
-          tc::tmem_ld32(tmem + lane_base + C::TMEM_O, o);
-          tc::tmem_ld_wait();
-#pragma unroll
-          for (int g = 0; g < G; ++g) og[g] = __uint_as_float(o[g]) + __uint_as_float(o[C::HALF + g]);
+        if (t4 == 0) {
+          mw[warp * 16 + g4] = m_run[0];
+          mw[warp * 16 + g4 + 8] = m_run[1];
+          lw[warp * 16 + g4] = lsum[0];
+          lw[warp * 16 + g4 + 8] = lsum[1];
         }
-        tc::named_bar_sync(1, C::NSM);
         const int b = it.b;
         const int rb = __ldg(ind + b), re = __ldg(ind + b + 1);
-        if (p.out != nullptr && rb >= lo && re <= hi) {
-          // the whole request lies in this chunk: normalise and write the output directly
-          // (the combine skips requests that occupy a single chunk)
-          if (tid < D) {
+        const bool direct = (p.out != nullptr) && rb >= lo && re <= hi;  // whole request in this chunk
+        const int slot = cx - rb / CL;
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-              const float L = rsum[g] + rsum[16 + g] + rsum[32 + g] + rsum[48 + g];
-              const float v = og[g] / L;
-              const __nv_bfloat16 h = __float2bfloat16_rn(v);
-              p.out[((size_t)b * p.num_qo_heads + (size_t)kvh * G + g) * D + tid] =
-                  *reinterpret_cast<const uint16_t*>(&h);
+        for (int h0 = 0; h0 < G; h0 += C::HG) {
+          // this warp's accumulator rows h0 .. h0+HG-1 to shared memory: mrg[warp][row][d]
+#pragma unroll
+          for (int n = 0; n < C::NT_D; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int row = g4 + (e >> 1) * 8 - h0;
+              if (row >= 0 && row < C::HG && row + h0 < G)
+                mrg[(warp * C::HG + row) * D + n * 8 + 2 * t4 + (e & 1)] = acc[n][e];
+            }
+          if (!cons_sync()) break;
+          // 128 threads: thread -> (row, d) pairs of this head group
+          for (int idx = tid; idx < C::HG * D; idx += C::NCONS * 32) {
+            const int row = idx / D, d = idx % D, h = h0 + row;
+            if (h >= G) continue;
+            float M = -CUDART_INF_F;
+#pragma unroll
+            for (int w = 0; w < C::NCONS; ++w) M = fmaxf(M, mw[w * 16 + h]);
+            float O = 0.f, L = 0.f;
+            if (M != -CUDART_INF_F) {
+#pragma unroll
+              for (int w = 0; w < C::NCONS; ++w) {
+                const float f = fast_exp2(mw[w * 16 + h] - M);  // 0 for warps that saw no key
+                O += f * mrg[(w * C::HG + row) * D + d];
+                L += f * lw[w * 16 + h];
+              }
+            }
+            const size_t qh = (size_t)b * p.num_qo_heads + (size_t)kvh * G + h;
+            if (direct) {
+              const __nv_bfloat16 v = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+              p.out[qh * D + d] = *reinterpret_cast<const uint16_t*>(&v);
+            } else {
+              const size_t row0 = qh * p.part_pitch + slot;
+              p.o_part[row0 * D + d] = O;
+              if (d == 0) {
+                p.ml_part[row0 * 2 + 0] = (M == -CUDART_INF_F) ? M : M * kLn2;  // natural-log units
+                p.ml_part[row0 * 2 + 1] = L;
+              }
             }
           }
-        } else {
-          const int s = cx - rb / CL;  // partial slot of this piece
-          const size_t row0 = ((size_t)b * p.num_qo_heads + (size_t)kvh * G) * p.part_pitch + s;
-          if (tid < D) {
-#pragma unroll
-            for (int g = 0; g < G; ++g) p.o_part[(row0 + (size_t)g * p.part_pitch) * D + tid] = og[g];
-          }
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            if (tid == g) {
-              p.ml_part[(row0 + (size_t)g * p.part_pitch) * 2 + 0] = m_run[g] * kLn2;  // natural-log units
-              p.ml_part[(row0 + (size_t)g * p.part_pitch) * 2 + 1] =
-                  rsum[g] + rsum[16 + g] + rsum[32 + g] + rsum[48 + g];
-            }
-          }
+          if (!cons_sync()) break;  // merge buffer and m / l free again
         }
-        tc::named_bar_sync(1, C::NSM);  // sums read before the next piece reuses the buffer
-#pragma unroll
-        for (int g = 0; g < G; ++g) { m_run[g] = -CUDART_INF_F; l_thr[g] = 0.f; }
+        if (*err) break;
+        ++piece;
       }
       it.next(ind, B, hi);
     }
   }
-
-  // ---- teardown: every role has finished (all issued MMAs were waited on by the softmax
-  //      warps through pv_done of the final tile)
-  tc::fence_before_sync();
   __syncthreads();
-  if (warp == C::MMA_WARP) {
-    tc::fence_after_sync();
-    tc::tmem_dealloc<C::TMEM_COLS>(tmem);
-  }
-  if (*err && tid < D) {  // a wait timed out: poison what this CTA owns so the call reads as failed
+  if (*err && tid < C::NCONS * 32) {
+    // a wait timed out: poison every partial this CTA owns so the call reads as failed
     TileIter it;
     it.first(ind, B, lo, hi);
     for (; it.valid(hi); it.next(ind, B, hi)) {
       if (!it.closes_piece(ind, hi)) continue;
       const int s = cx - __ldg(ind + it.b) / CL;
-      const size_t row0 = ((size_t)it.b * p.num_qo_heads + (size_t)kvh * G) * p.part_pitch + s;
-      for (int g = 0; g < G; ++g) p.o_part[(row0 + (size_t)g * p.part_pitch) * D + tid] = CUDART_NAN_F;
+      for (int i = tid; i < G * D; i += C::NCONS * 32) {
+        const size_t qh = (size_t)it.b * p.num_qo_heads + (size_t)kvh * G + i / D;
+        p.o_part[(qh * p.part_pitch + s) * D + i % D] = CUDART_NAN_F;
+        if (p.out != nullptr) p.out[qh * D + i % D] = 0x7fc0;
+      }
     }
   }
 }
@@ -577,13 +539,13 @@ cudaError_t launch_split_t(const DecodeParams& p, cudaStream_t stream) {
   using C = DecCfg<D, G>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_split_tc_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM_BYTES);
+    cudaError_t e =
+        cudaFuncSetAttribute(decode_split_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   dim3 grid(p.num_splits, p.num_kv_heads);
-  decode_split_tc_kernel<D, G><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(p);
+  decode_split_kernel<D, G><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
 }
 
