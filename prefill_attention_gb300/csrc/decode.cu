@@ -25,19 +25,23 @@
 //               (tiles g, g+3, ...): a group gathers the K and V rows of its 128-key tile
 //               slot by slot with 16-byte cp.async into a 128-byte-swizzled layout (16-byte
 //               chunk c of row r at c ^ (r & 7), so 8 consecutive rows of one chunk hit 8
-//               different bank groups), waits for its own copies and arrives on the
-//               stage's full barrier.  Three 64 KB tiles are in flight and each is published
-//               as soon as it lands.
-//       warps 0-3 (consumers) -- warp w owns keys 32w .. 32w+31 of every tile and keeps its
-//               own online-softmax state: S = Q K^T and O += P V as warp-level bf16 tensor
-//               core MMAs (m16n8k16, fp32 accumulators in registers, operands via ldmatrix
-//               from the swizzled tiles).  The 16 MMA rows are the G query heads sharing the
-//               KV head (zero-padded), so one K/V load serves all of them.  P is split into
-//               hi = bf16(p) and lo = bf16(p - hi) and both halves go through the MMA, which
-//               keeps p to ~2^-17 relative precision.  Softmax in base 2 (the scale carries
-//               log2 e) with a lazy rescale: a warp moves its reference max only when a
-//               score exceeds it by more than 2^8.  The four warps merge once per request
-//               piece through shared memory; there is no per-tile CTA synchronisation.
+//               different bank groups).  Each 32-key quarter of a tile is its own cp.async
+//               group with its own full barrier, so a quarter is published as soon as it
+//               lands.  Three 64 KB tiles are in flight.
+//       warps 0-3 (consumers) -- warp w takes quarter (w + j) mod 4 of tile j and keeps its
+//               own online-softmax state.  The products are computed transposed, S^T = K Q^T
+//               and O^T += V^T P^T, as warp-level bf16 MMAs (m16n8k16, fp32 accumulators in
+//               registers, operands via ldmatrix from the swizzled tiles): the 16-row MMA
+//               side is keys or head_dim and the 8-wide side the G query heads of the KV
+//               head, so one K/V load serves all of them with little padding.  P goes from
+//               the S^T accumulator layout to the B-operand layout with movmatrix.  P is
+//               split into hi = bf16(p) and lo = bf16(p - hi) and both halves go through the
+//               MMA, which keeps p to ~2^-17 relative precision.  Softmax in base 2 (the
+//               scale carries log2 e) with a lazy rescale: a warp moves its reference max
+//               only when a score exceeds it by more than 2^8.  A quarter with no valid key
+//               (the ragged end of a piece) is skipped; rotating the quarters spreads those
+//               savings over the warps.  The four warps merge once per request piece
+//               through shared memory; there is no per-tile CTA synchronisation.
 //     Measured alternatives (see the profiles): a CUDA-core version was issue bound
 //     (~550 instructions per 4 KB of K/V); a tcgen05 version with S^T / O^T accumulators in
 //     tensor memory spent ~150 cycles per M=128 x N=16 x K=16 MMA, ~2400 cycles per 64 KB
@@ -67,14 +71,16 @@ template <int D, int G>
 struct DecCfg {
   static constexpr int BK = 128;                   // keys per tile
   static constexpr int STAGES = 3;
-  static constexpr int NCONS = 4;                  // consumer warps (32 keys each)
+  static constexpr int NCONS = 4;                  // consumer warps; a tile is 4 quarters of 32 keys
   static constexpr int THREADS = 320;              // 4 consumer warps, 6 producer warps
   static constexpr int NPROD = 64;                 // producer threads per group (one group per stage)
   static constexpr int CPR = D / 8;                // 16-byte chunks per K/V row
   static constexpr int KV_IT = BK * CPR / NPROD;   // cp.async per producer thread per K tile
+  static constexpr int KV_IT_Q = KV_IT / NCONS;    // ... per quarter
   static constexpr int TILE = BK * D * 2;          // one K (or V) tile
   static constexpr int STAGE_BYTES = 2 * TILE;     // K | V
-  static constexpr int QROWS = 16;                 // MMA rows: query heads, zero padded
+  static constexpr int NH = (G + 7) / 8;           // 8-wide MMA n-tiles over the query heads
+  static constexpr int QROWS = 8 * NH;             // query rows in shared memory, zero padded
   static constexpr int QBUFS = 4;
   static constexpr int Q_BYTES = QROWS * D * 2;
   static constexpr int HG = (D == 128) ? 8 : 16;   // head rows merged per pass at a piece end
@@ -83,11 +89,12 @@ struct DecCfg {
   static constexpr int MERGE_OFF = Q_OFF + QBUFS * Q_BYTES;
   static constexpr int ML_OFF = MERGE_OFF + MERGE_BYTES;   // [NCONS][16] m, then [NCONS][16] l
   static constexpr int BAR_OFF = ML_OFF + 2 * NCONS * 16 * 4;
-  static constexpr int NBAR = 2 * STAGES + 1;      // full[3], empty[3], consumer merge barrier
+  static constexpr int NBAR = STAGES * NCONS + STAGES + 1;  // full[stage][quarter], empty[stage], merge
   static constexpr int SMEM_BYTES = BAR_OFF + NBAR * 8 + 16;
-  static constexpr int KSTEPS = D / 16;            // MMA k-steps over head_dim
-  static constexpr int NT_D = D / 8;               // 8-wide n-tiles over head_dim
+  static constexpr int KSTEPS = D / 16;            // MMA k-steps over head_dim (S^T = K Q^T)
+  static constexpr int MT_D = D / 16;              // 16-row m-tiles over head_dim (O^T = V^T P^T)
   static_assert(G <= 16, "at most 16 query heads per KV head");
+  static_assert(KV_IT % NCONS == 0, "quarters split the producer loop evenly");
   static_assert(STAGE_BYTES % 1024 == 0 && Q_OFF % 1024 == 0 && Q_BYTES % 1024 == 0, "swizzle atoms");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
@@ -106,6 +113,13 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
+}
+
+// Transpose of one 8x8 b16 matrix held one packed pair per lane (row lane/4, columns 2(lane%4), +1).
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
 }
 
 // D += A * B for one m16n8k16 bf16 tile with fp32 accumulation.
@@ -164,6 +178,7 @@ __device__ __forceinline__ bool wait_or_fail(uint32_t bar, uint32_t parity, vola
 template <int D, int G>
 __global__ void __launch_bounds__(320, 1) decode_split_kernel(const DecodeParams p) {
   using C = DecCfg<D, G>;
+  constexpr int NH = C::NH;
   extern __shared__ __align__(1024) unsigned char smem[];
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -171,22 +186,18 @@ __global__ void __launch_bounds__(320, 1) decode_split_kernel(const DecodeParams
   const int B = p.batch;
   const int32_t* ind = p.kv_indptr;
 
-  const int T = __ldg(ind + B);
-  const int CL = decode_chunk_len(T, gridDim.x, p.min_chunk, p.part_pitch);
-  const int lo = (int)min((int64_t)cx * CL, (int64_t)T), hi = min(lo + CL, T);
-  if (lo >= hi) return;
   if ((sbase & 1023u) != 0) return;  // swizzle atoms need a 1024-byte aligned window
 
   const uint32_t bars = sbase + C::BAR_OFF;
-  auto full = [&](int s) { return bars + 8u * s; };
-  auto empty = [&](int s) { return bars + 8u * (C::STAGES + s); };
-  const uint32_t cbar = bars + 8u * (2 * C::STAGES);  // the four consumer warps, bounded waits
+  auto full = [&](int s, int q) { return bars + 8u * (s * C::NCONS + q); };
+  auto empty = [&](int s) { return bars + 8u * (C::STAGES * C::NCONS + s); };
+  const uint32_t cbar = bars + 8u * (C::NBAR - 1);  // the four consumer warps, bounded waits
   volatile int* err = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 8 * C::NBAR);
 
-  // ---- set-up: barriers; Q rows of absent heads stay zero for the whole kernel
+  // ---- set-up (shared memory only): barriers; Q rows of absent heads stay zero throughout
   if (tid == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      tc::mbar_init(full(s), C::NPROD);
+      for (int q = 0; q < C::NCONS; ++q) tc::mbar_init(full(s, q), C::NPROD);
       tc::mbar_init(empty(s), C::NCONS * 32);
     }
     tc::mbar_init(cbar, C::NCONS * 32);
@@ -195,8 +206,17 @@ __global__ void __launch_bounds__(320, 1) decode_split_kernel(const DecodeParams
   }
   for (int i = tid; i < C::QBUFS * C::Q_BYTES / 16; i += C::THREADS) sts128_zero(sbase + C::Q_OFF + i * 16);
   __syncthreads();
+  // Launched as a programmatic dependent of the previous kernel in the stream: the set-up
+  // above overlapped its tail; from here on its writes are visible and its reads are done,
+  // so no global memory is touched before this point.  (A no-op for an ordinary launch.)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // let the combine kernel's CTAs launch now; they wait for this grid's memory to be visible
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  const int T = __ldg(ind + B);
+  const int CL = decode_chunk_len(T, gridDim.x, p.min_chunk, p.part_pitch);
+  const int lo = (int)min((int64_t)cx * CL, (int64_t)T), hi = min(lo + CL, T);
+  if (lo >= hi) return;  // uniform over the CTA; no barrier follows for it
 
   if (warp >= C::NCONS) {
     // ======================= producers: group g fills ring stage g with tiles g, g+3, ...
@@ -210,7 +230,8 @@ __global__ void __launch_bounds__(320, 1) decode_split_kernel(const DecodeParams
       it.next(ind, B, hi);
     }
     const size_t head_stride = (size_t)p.num_kv_heads * D;
-    // thread pt copies chunk (pt % CPR) of keys (i * NPROD + pt) / CPR, i = 0 .. KV_IT-1
+    // thread pt copies chunk (pt % CPR) of keys (i * NPROD + pt) / CPR, i = 0 .. KV_IT-1;
+    // iterations [q * KV_IT_Q, (q + 1) * KV_IT_Q) cover exactly the keys of quarter q
     int ids[C::KV_IT];
     auto load_ids = [&](const TileIter& t) {
 #pragma unroll
@@ -226,17 +247,7 @@ __global__ void __launch_bounds__(320, 1) decode_split_kernel(const DecodeParams
     for (int round = 0; it.valid(hi); ++round) {
       if (round > 0 && !wait_or_fail(empty(grp), (uint32_t)((round - 1) & 1), err)) break;
       const uint32_t kst = sbase + grp * C::STAGE_BYTES, vst = kst + C::TILE;
-#pragma unroll
-      for (int i = 0; i < C::KV_IT; ++i) {
-        const int flat = i * C::NPROD + pt;
-        const int key = flat / C::CPR, c = flat % C::CPR;
-        const bool valid = ids[i] >= 0;
-        const size_t off = valid ? (size_t)ids[i] * head_stride + (size_t)kvh * D + c * 8 : 0;
-        const uint32_t o = sw128(key, c, C::BK);
-        cp_async16(kst + o, p.k_pool + off, valid);  // rows past the piece are zero-filled
-        cp_async16(vst + o, p.v_pool + off, valid);
-      }
-      if (it.opens_piece(ind, lo)) {  // first tile of a piece: its G query rows
+      if (it.opens_piece(ind, lo)) {  // first tile of a piece: its G query rows (with quarter 0)
         const uint32_t qb = sbase + C::Q_OFF + (piece % C::QBUFS) * C::Q_BYTES;
         const uint16_t* qsrc = p.q + ((size_t)it.b * p.num_qo_heads + (size_t)kvh * G) * D;
         for (int i = pt; i < G * C::CPR; i += C::NPROD) {
@@ -244,19 +255,41 @@ __global__ void __launch_bounds__(320, 1) decode_split_kernel(const DecodeParams
           cp_async16(qb + sw128(g, c, C::QROWS), qsrc + (size_t)g * D + c * 8, true);
         }
       }
-      cp_async_commit();
+#pragma unroll
+      for (int q = 0; q < C::NCONS; ++q) {  // one cp.async group per quarter
+#pragma unroll
+        for (int i = q * C::KV_IT_Q; i < (q + 1) * C::KV_IT_Q; ++i) {
+          const int flat = i * C::NPROD + pt;
+          const int key = flat / C::CPR, c = flat % C::CPR;
+          const bool valid = ids[i] >= 0;
+          const size_t off = valid ? (size_t)ids[i] * head_stride + (size_t)kvh * D + c * 8 : 0;
+          const uint32_t o = sw128(key, c, C::BK);
+          cp_async16(kst + o, p.k_pool + off, valid);  // rows past the piece are zero-filled
+          cp_async16(vst + o, p.v_pool + off, valid);
+        }
+        cp_async_commit();
+      }
       // advance three tiles (this group's next one) and prefetch its slot ids
       for (int k = 0; k < C::STAGES && it.valid(hi); ++k) {
         if (it.closes_piece(ind, hi)) ++piece;
         it.next(ind, B, hi);
       }
       load_ids(it);
+      // publish each quarter as soon as this thread's copies of it have landed
+      cp_async_wait<3>();
+      tc::mbar_arrive(full(grp, 0));
+      cp_async_wait<2>();
+      tc::mbar_arrive(full(grp, 1));
+      cp_async_wait<1>();
+      tc::mbar_arrive(full(grp, 2));
       cp_async_wait<0>();
-      tc::mbar_arrive(full(grp));  // release: the copies are visible to the consumers' loads
+      tc::mbar_arrive(full(grp, 3));
     }
     cp_async_wait<0>();
   } else {
-    // ======================= consumers: warp w owns keys 32w .. 32w+31 of every tile
+    // ======================= consumers: warp w takes quarter (w + j) % 4 of tile j
+    // Transposed products so the 16-row MMA side is keys / head_dim, not the few heads:
+    //   S^T (32 keys x 8 heads) = K Q^T,   O^T (D x 8 heads) += V^T P^T.
     const int g4 = lane >> 2, t4 = lane & 3;  // fragment row / column-pair index
     const int lrow = lane & 7, lmat = lane >> 3;  // ldmatrix: row within / index of the 8x8 matrix
     const float scale = p.scale_log2;
@@ -272,138 +305,186 @@ __global__ void __launch_bounds__(320, 1) decode_split_kernel(const DecodeParams
       tc::mbar_arrive(cbar);
       return wait_or_fail(cbar, (cphase++) & 1u, err);
     };
-    uint32_t qa[C::KSTEPS][4];      // Q as the A operand (rows = heads), per k-step
-    float acc[C::NT_D][4];          // O rows g4 (c0,c1) and g4+8 (c2,c3) over head_dim
-    float m_run[2], l_thr[2];       // rows g4 and g4+8 of this warp
+    uint32_t qb[NH][C::KSTEPS][2];  // Q^T as the B operand (n = heads), per k-step
+    float acc[C::MT_D][NH][4];      // O^T: rows d = 16md + g4 (+8), heads 8nh + 2t4 (+1)
+    float m_run[NH][2], l_thr[NH][2];  // heads 8nh + 2t4 + e of this warp
     for (int j = 0; it.valid(hi); ++j) {
       const int st = j % C::STAGES;
+      const int quarter = (warp + j) & (C::NCONS - 1);
       const bool opens = it.opens_piece(ind, lo), closes = it.closes_piece(ind, hi);
-      if (!wait_or_fail(full(st), (uint32_t)((j / C::STAGES) & 1), err)) break;
+      const int kbase = quarter * 32;
+      const int nkeys = it.end - it.start;  // valid keys of the tile; the rest are masked
+      const bool work = kbase < nkeys;      // quarters wholly past the piece are skipped
+      if (!wait_or_fail(full(st, quarter), (uint32_t)((j / C::STAGES) & 1), err)) break;
       const uint32_t kst = sbase + st * C::STAGE_BYTES, vst = kst + C::TILE;
 
       if (opens) {  // new request piece: its query rows, fresh softmax state
-        const uint32_t qb = sbase + C::Q_OFF + (piece % C::QBUFS) * C::Q_BYTES;
+        const uint32_t qbuf = sbase + C::Q_OFF + (piece % C::QBUFS) * C::Q_BYTES;
+#pragma unroll
+        for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+          for (int kk = 0; kk < C::KSTEPS; kk += 2) {
+            // matrices: heads 8nh .. 8nh+7 at chunks 2kk, 2kk+1, 2kk+2, 2kk+3
+            ldsm_x4(qbuf + sw128(8 * nh + lrow, 2 * kk + lmat, C::QROWS), qb[nh][kk][0], qb[nh][kk][1],
+                    qb[nh][kk + 1][0], qb[nh][kk + 1][1]);
+          }
+#pragma unroll
+        for (int md = 0; md < C::MT_D; ++md)
+#pragma unroll
+          for (int nh = 0; nh < NH; ++nh) acc[md][nh][0] = acc[md][nh][1] = acc[md][nh][2] = acc[md][nh][3] = 0.f;
+#pragma unroll
+        for (int nh = 0; nh < NH; ++nh) {
+          m_run[nh][0] = m_run[nh][1] = -CUDART_INF_F;
+          l_thr[nh][0] = l_thr[nh][1] = 0.f;
+        }
+      }
+
+      if (work) {
+        // ---- S^T = K Q^T: 2 m-tiles of 16 keys; even / odd k-steps in separate accumulators
+        float s[2][NH][4], s2[2][NH][4];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s[mt][nh][e] = s2[mt][nh][e] = 0.f;
 #pragma unroll
         for (int kk = 0; kk < C::KSTEPS; ++kk) {
-          // matrices: (rows 0-7, chunk 2kk), (rows 8-15, 2kk), (rows 0-7, 2kk+1), (rows 8-15, 2kk+1)
-          const int r = lrow + (lmat & 1) * 8, c = 2 * kk + (lmat >> 1);
-          ldsm_x4(qb + sw128(r, c, C::QROWS), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
-        }
 #pragma unroll
-        for (int n = 0; n < C::NT_D; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-        m_run[0] = m_run[1] = -CUDART_INF_F;
-        l_thr[0] = l_thr[1] = 0.f;
-      }
+          for (int mt = 0; mt < 2; ++mt) {
+            // matrices: (keys 0-7, chunk 2kk), (keys 8-15, 2kk), (keys 0-7, 2kk+1), (keys 8-15, 2kk+1)
+            const int key = kbase + mt * 16 + lrow + (lmat & 1) * 8, c = 2 * kk + (lmat >> 1);
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(kst + sw128(key, c, C::BK), a0, a1, a2, a3);
+#pragma unroll
+            for (int nh = 0; nh < NH; ++nh) {
+              if (kk & 1) mma16816(s2[mt][nh], a0, a1, a2, a3, qb[nh][kk][0], qb[nh][kk][1]);
+              else mma16816(s[mt][nh], a0, a1, a2, a3, qb[nh][kk][0], qb[nh][kk][1]);
+            }
+          }
+        }
 
-      // ---- S = Q K^T for this warp's 32 keys: 4 n-tiles of 8 keys
-      const int kbase = warp * 32;
-      float s[4][4];
+        // ---- online softmax (base 2) per head; this lane holds keys 16mt + g4 (+8)
+        float rmax[NH][2];
 #pragma unroll
-      for (int n = 0; n < 4; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+        for (int nh = 0; nh < NH; ++nh) rmax[nh][0] = rmax[nh][1] = -CUDART_INF_F;
 #pragma unroll
-      for (int kk = 0; kk < C::KSTEPS; ++kk) {
+        for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-        for (int np = 0; np < 2; ++np) {  // two n-tiles per ldmatrix.x4
-          // matrices: (keys n, chunk 2kk), (keys n, 2kk+1), (keys n+8, 2kk), (keys n+8, 2kk+1)
-          const int key = kbase + np * 16 + lrow + (lmat >> 1) * 8, c = 2 * kk + (lmat & 1);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(kst + sw128(key, c, C::BK), b0, b1, b2, b3);
-          mma16816(s[2 * np], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
-          mma16816(s[2 * np + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
+          for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int key = kbase + mt * 16 + g4 + (e >> 1) * 8;
+              const float x = (key < nkeys) ? (s[mt][nh][e] + s2[mt][nh][e]) * scale : -CUDART_INF_F;
+              s[mt][nh][e] = x;
+              rmax[nh][e & 1] = fmaxf(rmax[nh][e & 1], x);
+            }
+#pragma unroll
+        for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float x = rmax[nh][h];
+            x = fmaxf(x, __shfl_xor_sync(kFullMask, x, 4));
+            x = fmaxf(x, __shfl_xor_sync(kFullMask, x, 8));
+            x = fmaxf(x, __shfl_xor_sync(kFullMask, x, 16));
+            rmax[nh][h] = x;
+          }
+        float alpha[NH][2];
+        bool moved = false;
+#pragma unroll
+        for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            alpha[nh][h] = 1.f;
+            // a warp whose keys are all masked keeps m = -inf; nothing it adds is nonzero
+            if (rmax[nh][h] > m_run[nh][h] + kRescaleLog2) {
+              alpha[nh][h] = fast_exp2(m_run[nh][h] - rmax[nh][h]);  // 0 when m_run = -inf
+              m_run[nh][h] = rmax[nh][h];
+              moved = true;
+            }
+          }
+        if (__any_sync(kFullMask, moved)) {
+#pragma unroll
+          for (int md = 0; md < C::MT_D; ++md)
+#pragma unroll
+            for (int nh = 0; nh < NH; ++nh) {
+              acc[md][nh][0] *= alpha[nh][0]; acc[md][nh][1] *= alpha[nh][1];
+              acc[md][nh][2] *= alpha[nh][0]; acc[md][nh][3] *= alpha[nh][1];
+            }
+#pragma unroll
+          for (int nh = 0; nh < NH; ++nh) {
+            l_thr[nh][0] *= alpha[nh][0];
+            l_thr[nh][1] *= alpha[nh][1];
+          }
         }
-      }
+        // P = exp2(s - m) as hi / lo bf16 pairs, transposed into P^T B fragments
+        uint32_t ph[2][NH][2], pl[2][NH][2];  // [k-step = m-tile][nh][keys 0-7 | 8-15]
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              float pv[2];
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const float mr = m_run[nh][e];
+                pv[e] = (mr == -CUDART_INF_F) ? 0.f : fast_exp2(s[mt][nh][2 * half + e] - mr);
+                l_thr[nh][e] += pv[e];
+              }
+              const uint32_t h01 = float2_to_bf16x2_rn(pv[0], pv[1]);
+              const float2 f01 = bf16x2_to_float2(h01);
+              const uint32_t l01 = float2_to_bf16x2_rn(pv[0] - f01.x, pv[1] - f01.y);
+              // (key g4 + 8 half, heads 2t4, 2t4+1) -> (head g4, keys 8 half + 2t4, +1)
+              ph[mt][nh][half] = movmatrix_t(h01);
+              pl[mt][nh][half] = movmatrix_t(l01);
+            }
 
-      // ---- online softmax (base 2) on rows g4 (c0,c1) and g4+8 (c2,c3)
-      const int nkeys = it.end - it.start;  // valid keys of the tile; the rest are masked
-      float rmax[2] = {-CUDART_INF_F, -CUDART_INF_F};
+        // ---- O^T += V^T P^T over the quarter's 32 keys: 2 k-steps x D / 16 m-tiles
 #pragma unroll
-      for (int n = 0; n < 4; ++n)
+        for (int ks = 0; ks < 2; ++ks) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int key = kbase + n * 8 + 2 * t4 + (e & 1);
-          const float x = (key < nkeys) ? s[n][e] * scale : -CUDART_INF_F;
-          s[n][e] = x;
-          rmax[e >> 1] = fmaxf(rmax[e >> 1], x);
-        }
+          for (int md = 0; md < C::MT_D; ++md) {
+            // matrices (transposed on load): (d 0-7, keys 0-7), (d 8-15, keys 0-7), (d 0-7, keys 8-15), (d 8-15, keys 8-15)
+            const int key = kbase + ks * 16 + lrow + (lmat >> 1) * 8, c = 2 * md + (lmat & 1);
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_t(vst + sw128(key, c, C::BK), a0, a1, a2, a3);
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        rmax[h] = fmaxf(rmax[h], __shfl_xor_sync(kFullMask, rmax[h], 1));
-        rmax[h] = fmaxf(rmax[h], __shfl_xor_sync(kFullMask, rmax[h], 2));
-      }
-      float alpha[2] = {1.f, 1.f};
-      bool moved = false;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        // a warp whose keys are all masked keeps m = -inf; nothing it adds is nonzero
-        if (rmax[h] > m_run[h] + kRescaleLog2) {
-          alpha[h] = fast_exp2(m_run[h] - rmax[h]);  // 0 when m_run = -inf
-          m_run[h] = rmax[h];
-          moved = true;
+            for (int nh = 0; nh < NH; ++nh) {
+              mma16816(acc[md][nh], a0, a1, a2, a3, ph[ks][nh][0], ph[ks][nh][1]);
+              mma16816(acc[md][nh], a0, a1, a2, a3, pl[ks][nh][0], pl[ks][nh][1]);
+            }
+          }
         }
       }
-      if (__any_sync(kFullMask, moved)) {
-#pragma unroll
-        for (int n = 0; n < C::NT_D; ++n) {
-          acc[n][0] *= alpha[0]; acc[n][1] *= alpha[0];
-          acc[n][2] *= alpha[1]; acc[n][3] *= alpha[1];
-        }
-        l_thr[0] *= alpha[0];
-        l_thr[1] *= alpha[1];
-      }
-      // P = exp2(s - m) as hi / lo bf16 A fragments, two k-steps of 16 keys
-      uint32_t ph[2][4], pl[2][4];
-#pragma unroll
-      for (int n = 0; n < 4; ++n) {
-        float pv[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float mr = m_run[e >> 1];
-          pv[e] = (mr == -CUDART_INF_F) ? 0.f : fast_exp2(s[n][e] - mr);
-          l_thr[e >> 1] += pv[e];
-        }
-        const uint32_t h01 = float2_to_bf16x2_rn(pv[0], pv[1]), h23 = float2_to_bf16x2_rn(pv[2], pv[3]);
-        const float2 f01 = bf16x2_to_float2(h01), f23 = bf16x2_to_float2(h23);
-        const uint32_t l01 = float2_to_bf16x2_rn(pv[0] - f01.x, pv[1] - f01.y);
-        const uint32_t l23 = float2_to_bf16x2_rn(pv[2] - f23.x, pv[3] - f23.y);
-        // n-tile n covers keys 8n..8n+7 of the warp: k-step n/2, low (a0a1,a2a3) or high (a4a5,a6a7) half
-        const int ks = n >> 1, hi8 = (n & 1) * 2;
-        ph[ks][hi8 + 0] = h01; ph[ks][hi8 + 1] = h23;
-        pl[ks][hi8 + 0] = l01; pl[ks][hi8 + 1] = l23;
-      }
-
-      // ---- O += P V over the warp's 32 keys: 2 k-steps x head_dim / 8 n-tiles
-#pragma unroll
-      for (int ks = 0; ks < 2; ++ks) {
-#pragma unroll
-        for (int np = 0; np < C::NT_D / 2; ++np) {  // two d n-tiles per ldmatrix.x4.trans
-          // matrices: (keys 0-7, chunk 2np), (keys 8-15, 2np), (keys 0-7, 2np+1), (keys 8-15, 2np+1)
-          const int key = kbase + ks * 16 + lrow + (lmat & 1) * 8, c = 2 * np + (lmat >> 1);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(vst + sw128(key, c, C::BK), b0, b1, b2, b3);
-          mma16816(acc[2 * np], ph[ks][0], ph[ks][1], ph[ks][2], ph[ks][3], b0, b1);
-          mma16816(acc[2 * np], pl[ks][0], pl[ks][1], pl[ks][2], pl[ks][3], b0, b1);
-          mma16816(acc[2 * np + 1], ph[ks][0], ph[ks][1], ph[ks][2], ph[ks][3], b2, b3);
-          mma16816(acc[2 * np + 1], pl[ks][0], pl[ks][1], pl[ks][2], pl[ks][3], b2, b3);
-        }
-      }
+      // Quarters land in order, so seeing the last one means all of round j / STAGES is in.
+      // The next warp to wait on this stage's barriers may hold another quarter; with this
+      // wait, no barrier of the stage can still be a phase behind when it does.
+      if (!wait_or_fail(full(st, C::NCONS - 1), (uint32_t)((j / C::STAGES) & 1), err)) break;
       __syncwarp();
       tc::mbar_arrive(empty(st));  // this warp is done reading stage st
 
       if (closes) {
         // ---- piece finished: merge the four warps (log-sum-exp) and write it out
-        float lsum[2];
+        float lsum[NH][2];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          float x = l_thr[h];
-          x += __shfl_xor_sync(kFullMask, x, 1);
-          x += __shfl_xor_sync(kFullMask, x, 2);
-          lsum[h] = x;
-        }
-        if (t4 == 0) {
-          mw[warp * 16 + g4] = m_run[0];
-          mw[warp * 16 + g4 + 8] = m_run[1];
-          lw[warp * 16 + g4] = lsum[0];
-          lw[warp * 16 + g4 + 8] = lsum[1];
+        for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float x = l_thr[nh][h];
+            x += __shfl_xor_sync(kFullMask, x, 4);
+            x += __shfl_xor_sync(kFullMask, x, 8);
+            x += __shfl_xor_sync(kFullMask, x, 16);
+            lsum[nh][h] = x;
+          }
+        if (g4 == 0) {
+#pragma unroll
+          for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              mw[warp * 16 + 8 * nh + 2 * t4 + h] = m_run[nh][h];
+              lw[warp * 16 + 8 * nh + 2 * t4 + h] = lsum[nh][h];
+            }
         }
         const int b = it.b;
         const int rb = __ldg(ind + b), re = __ldg(ind + b + 1);
@@ -413,13 +494,15 @@ __global__ void __launch_bounds__(320, 1) decode_split_kernel(const DecodeParams
         for (int h0 = 0; h0 < G; h0 += C::HG) {
           // this warp's accumulator rows h0 .. h0+HG-1 to shared memory: mrg[warp][row][d]
 #pragma unroll
-          for (int n = 0; n < C::NT_D; ++n)
+          for (int md = 0; md < C::MT_D; ++md)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int row = g4 + (e >> 1) * 8 - h0;
-              if (row >= 0 && row < C::HG && row + h0 < G)
-                mrg[(warp * C::HG + row) * D + n * 8 + 2 * t4 + (e & 1)] = acc[n][e];
-            }
+            for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int row = 8 * nh + 2 * t4 + (e & 1) - h0;
+                if (row >= 0 && row < C::HG && row + h0 < G)
+                  mrg[(warp * C::HG + row) * D + md * 16 + g4 + (e >> 1) * 8] = acc[md][nh][e];
+              }
           if (!cons_sync()) break;
           // 128 threads: thread -> (row, d) pairs of this head group
           for (int idx = tid; idx < C::HG * D; idx += C::NCONS * 32) {
@@ -483,6 +566,8 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
   const int lane = threadIdx.x & 31;
   // launched as a programmatic dependent of the split kernel: wait until its writes are visible
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the next kernel in the stream may start its shared-memory set-up now
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (wid >= p.batch * p.num_qo_heads) return;
   const int b = wid / p.num_qo_heads;
   int S;
@@ -544,8 +629,18 @@ cudaError_t launch_split_t(const DecodeParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 grid(p.num_splits, p.num_kv_heads);
-  decode_split_kernel<D, G><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.num_splits, p.num_kv_heads);
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // set-up overlaps the previous kernel
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, decode_split_kernel<D, G>, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
