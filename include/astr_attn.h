@@ -88,13 +88,14 @@ typedef struct astr_attn_dims {
  * Decode split schedule (P3, shared-helpers commit: the split count is chosen per call;
  * P3, kv_indptr commit: kv_indptr is built once per step and drives it here).
  * The batch's keys are laid end to end in kv_indptr order, T = kv_indptr[batch], and for
- * every KV head cut into `num_splits` chunks of C keys, one CTA per chunk:
+ * every KV head cut into `num_splits` chunks of C keys, each read by one warp pair
+ * (a producer and a consumer warp; four chunks per CTA):
  *   C = max(round_up(ceil(T / num_splits), 16), F),  F = max(16, ceil(max_seq_len / (max_splits - 1)))
- *   (C = T when max_splits == 1), so every CTA reads the same number of K/V bytes.
+ *   (C = T when max_splits == 1), so every chunk holds the same number of keys.
  * Request b overlaps chunks kv_indptr[b] / C .. (kv_indptr[b+1] - 1) / C; the piece of it
  * in chunk c becomes partial slot c - kv_indptr[b] / C of (b, h), and the floor F keeps
  * that below max_splits.  This call returns num_splits as planned for `device`: the
- * forced dims->num_splits if > 0, else ceil(#SMs / Hkv) (one persistent CTA per SM).
+ * forced dims->num_splits if > 0, else 4 * ceil(#SMs / Hkv) (one persistent CTA per SM).
  * Depends only on host-known values, never on the contents of seq_lens.
  * Errors: INVALID_ARG (null, bad dims), DEVICE (device query failed).
  */

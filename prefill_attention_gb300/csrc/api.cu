@@ -54,13 +54,14 @@ int check_common(const astr_attn_dims* d) {
   return ASTR_OK;
 }
 
-// Key chunks per KV head: one wave of persistent CTAs, kv heads x chunks = SMs.
+// Key chunks per KV head: one wave of persistent CTAs (kv heads x CTAs = SMs), each CTA
+// running kDecodeChunksPerCta chunks.
 int plan_splits(const astr_attn_dims* d, int sms) {
   if (d->num_splits > 0) return d->num_splits;
   const int64_t target = (int64_t)sms * kDecodeCtasPerSm;
   int64_t s = (target + d->num_kv_heads - 1) / d->num_kv_heads;
   if (s < 1) s = 1;
-  return (int)s;
+  return (int)(s * astr::kDecodeChunksPerCta);
 }
 
 // Floor on the chunk length: a request of max_seq_len keys overlaps at most

@@ -7,6 +7,9 @@
 
 namespace astr {
 
+// Decode split kernel: a CTA runs this many independent warp pairs, one key chunk each.
+constexpr int kDecodeChunksPerCta = 4;
+
 // Decode: one launch of the split kernel followed by one launch of the combine kernel.
 struct DecodeParams {
   const uint16_t* q;             // [B, Hq, D]
@@ -21,7 +24,7 @@ struct DecodeParams {
   int64_t r2t_stride;
   int64_t num_slots;             // rows of k_pool / v_pool (sizes the gather tensor maps)
   int batch, num_qo_heads, num_kv_heads, head_dim;
-  int num_splits;                // key chunks per KV head (grid x of the split kernel)
+  int num_splits;                // key chunks per KV head (kDecodeChunksPerCta per CTA)
   int part_pitch;                // partial slots per (b, h) row of o_part (= max_splits)
   int min_chunk;                 // floor on the chunk length so no request needs > part_pitch slots
   float scale_log2;              // sm_scale * log2(e): logits are kept in base-2 units on chip

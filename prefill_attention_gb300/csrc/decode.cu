@@ -69,33 +69,29 @@ constexpr float kRescaleLog2 = 8.f;  // lazy-rescale threshold (base-2 logit uni
 
 template <int D, int G>
 struct DecCfg {
-  static constexpr int BK = 128;                   // keys per tile
-  static constexpr int STAGES = 3;
-  static constexpr int NCONS = 4;                  // consumer warps; a tile is 4 quarters of 32 keys
-  static constexpr int THREADS = 320;              // 4 consumer warps, 6 producer warps
-  static constexpr int NPROD = 64;                 // producer threads per group (one group per stage)
+  static constexpr int NPAIR = kDecodeChunksPerCta;  // independent (producer, consumer) warp pairs
+  static constexpr int THREADS = 2 * NPAIR * 32;   // warps 0..3 consume, warps 4..7 produce
+  static constexpr int BK = 32;                    // keys per ring slot
   static constexpr int CPR = D / 8;                // 16-byte chunks per K/V row
-  static constexpr int KV_IT = BK * CPR / NPROD;   // cp.async per producer thread per K tile
-  static constexpr int KV_IT_Q = KV_IT / NCONS;    // ... per quarter
-  static constexpr int TILE = BK * D * 2;          // one K (or V) tile
-  static constexpr int STAGE_BYTES = 2 * TILE;     // K | V
+  static constexpr int KV_IT = BK * CPR / 32;      // cp.async per producer lane per K slot
   static constexpr int NH = (G + 7) / 8;           // 8-wide MMA n-tiles over the query heads
-  static constexpr int QROWS = 8 * NH;             // query rows in shared memory, zero padded
-  static constexpr int QBUFS = 4;
+  static constexpr int QROWS = 8 * NH;             // query rows in a slot, zero padded
+  static constexpr int KV_BYTES = BK * D * 2;      // K (or V) part of a slot
   static constexpr int Q_BYTES = QROWS * D * 2;
-  static constexpr int HG = (D == 128) ? 8 : 16;   // head rows merged per pass at a piece end
-  static constexpr int MERGE_BYTES = NCONS * HG * D * 4;
-  static constexpr int Q_OFF = STAGES * STAGE_BYTES;
-  static constexpr int MERGE_OFF = Q_OFF + QBUFS * Q_BYTES;
-  static constexpr int ML_OFF = MERGE_OFF + MERGE_BYTES;   // [NCONS][16] m, then [NCONS][16] l
-  static constexpr int BAR_OFF = ML_OFF + 2 * NCONS * 16 * 4;
-  static constexpr int NBAR = STAGES * NCONS + STAGES + 1;  // full[stage][quarter], empty[stage], merge
-  static constexpr int SMEM_BYTES = BAR_OFF + NBAR * 8 + 16;
+  static constexpr int SLOT = 2 * KV_BYTES + Q_BYTES;   // K | V | Q
+  static constexpr int STAGES_FIT = (220 * 1024) / (NPAIR * SLOT);
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;  // ring slots per pair
+  static constexpr int RING = STAGES * SLOT;
+  static constexpr int BAR_OFF = NPAIR * RING;
+  static constexpr int NBAR = NPAIR * 2 * STAGES;  // full[pair][slot], empty[pair][slot]
+  static constexpr int SMEM_BYTES = BAR_OFF + NBAR * 8 + 16 * 4;  // + per-pair error flags
   static constexpr int KSTEPS = D / 16;            // MMA k-steps over head_dim (S^T = K Q^T)
   static constexpr int MT_D = D / 16;              // 16-row m-tiles over head_dim (O^T = V^T P^T)
+  static constexpr int STG_PITCH = D + 4;          // fp32 staging row pitch (conflict-free writes)
   static_assert(G <= 16, "at most 16 query heads per KV head");
-  static_assert(KV_IT % NCONS == 0, "quarters split the producer loop evenly");
-  static_assert(STAGE_BYTES % 1024 == 0 && Q_OFF % 1024 == 0 && Q_BYTES % 1024 == 0, "swizzle atoms");
+  static_assert(STAGES >= 2, "a ring needs two slots");
+  static_assert(SLOT % 1024 == 0 && KV_BYTES % 1024 == 0, "swizzle atoms");
+  static_assert((QROWS * STG_PITCH + 2 * QROWS) * 4 <= 2 * KV_BYTES, "piece staging fits in K | V");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
@@ -132,15 +128,22 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Arrive on an mbarrier once every cp.async this thread has issued so far has landed
+// (the arrival counts toward the barrier's expected count; it does not add to it).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 // Byte offset of 16-byte chunk c of row r in a 128-byte-swizzled tile whose 64-element
 // column blocks each hold `rows` rows.
 __device__ __forceinline__ uint32_t sw128(int r, int c, int rows) {
   return (uint32_t)((c >> 3) * rows * 128 + (r >> 3) * 1024 + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
-// Walks the tiles of one chunk: a tile never crosses a request boundary.
+// Walks the slots of one chunk: BK keys at a time, never across a request boundary.
+template <int BK>
 struct TileIter {
-  int b, start, end;  // current tile: flat keys [start, end) of request b
+  int b, start, end;  // current slot: flat keys [start, end) of request b
   __device__ __forceinline__ void first(const int32_t* ind, int B, int lo, int hi) {
     int l = 0, h = B - 1;  // largest b with ind[b] <= lo
     while (l < h) {
@@ -149,7 +152,13 @@ struct TileIter {
     }
     b = l;
     start = lo;
-    end = min(start + 128, min(hi, __ldg(ind + b + 1)));
+    end = min(start + BK, min(hi, __ldg(ind + b + 1)));
+  }
+  // Same as first() for a chunk whose first request b0 and its end ind[b0 + 1] are known.
+  __device__ __forceinline__ void start_at(int b0, int b0_end, int lo, int hi) {
+    b = b0;
+    start = lo;
+    end = min(start + BK, min(hi, b0_end));
   }
   __device__ __forceinline__ void next(const int32_t* ind, int B, int hi) {
     const int piece_end = min(hi, __ldg(ind + b + 1));
@@ -160,14 +169,49 @@ struct TileIter {
       start = (b < B) ? __ldg(ind + b) : hi;
       if (start > hi) start = hi;
     }
-    end = (start < hi) ? min(start + 128, min(hi, __ldg(ind + b + 1))) : start;
+    end = (start < hi) ? min(start + BK, min(hi, __ldg(ind + b + 1))) : start;
   }
   __device__ __forceinline__ bool valid(int hi) const { return start < hi; }
   __device__ __forceinline__ bool opens_piece(const int32_t* ind, int lo) const { return start == max(lo, __ldg(ind + b)); }
   __device__ __forceinline__ bool closes_piece(const int32_t* ind, int hi) const { return end == min(hi, __ldg(ind + b + 1)); }
 };
 
-// Bounded wait that gives up (and raises the CTA's error flag) on timeout or once the flag is up.
+// Warp-cooperative lookup of the request that holds flat key `lo` (largest b with
+// ind[b] <= lo, so empty requests are stepped over), with ind[b] and ind[b + 1].
+// Each round samples ind at 128 evenly spaced points of the bracket [l, h) (every point
+// once the bracket is that narrow) and keeps the two samples around lo, so a batch of up
+// to 128 requests takes one round of loads and 16384 take two.  Needs ind[l] <= lo <
+// ind[h] on entry, i.e. l = 0, h = B, ind_h = ind[B] > lo.
+__device__ __forceinline__ int pick4(const int (&v)[4], int k) {  // v[k] without local memory
+  return k == 0 ? v[0] : k == 1 ? v[1] : k == 2 ? v[2] : v[3];
+}
+struct ReqBracket {
+  int b, start, end;
+};
+__device__ __forceinline__ ReqBracket locate_request(const int32_t* ind, int B, int lo, int ind_B, int lane) {
+  int l = 0, h = B, ind_l = 0, ind_h = ind_B;
+  while (h - l > 1) {
+    int v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) v[k] = __ldg(ind + l + (int)((int64_t)(h - l) * (lane * 4 + k) / 128));
+    int c = 0;  // samples with ind <= lo; they are samples 0 .. c-1 (ind and positions ascend)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) c += __popc(__ballot_sync(kFullMask, v[k] <= lo));
+    const int i_lo = c - 1;  // >= 0: sample 0 is ind[l] <= lo
+    const int vl = __shfl_sync(kFullMask, pick4(v, i_lo & 3), i_lo >> 2);
+    const int nl = l + (int)((int64_t)(h - l) * i_lo / 128);
+    if (c < 128) {
+      const int vh = __shfl_sync(kFullMask, pick4(v, c & 3), c >> 2);
+      h = l + (int)((int64_t)(h - l) * c / 128);
+      ind_h = vh;
+    }
+    l = nl;
+    ind_l = vl;
+  }
+  return ReqBracket{l, ind_l, ind_h};
+}
+
+// Bounded wait that gives up (and raises the pair's error flag) on timeout or once the flag is up.
 __device__ __forceinline__ bool wait_or_fail(uint32_t bar, uint32_t parity, volatile int* err) {
   if (*err) return false;
   if (tc::mbar_wait(bar, parity)) return true;
@@ -176,35 +220,35 @@ __device__ __forceinline__ bool wait_or_fail(uint32_t bar, uint32_t parity, vola
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(320, 1) decode_split_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(const DecodeParams p) {
   using C = DecCfg<D, G>;
   constexpr int NH = C::NH;
   extern __shared__ __align__(1024) unsigned char smem[];
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int kvh = blockIdx.y, cx = blockIdx.x;
+  const int pair = warp & (C::NPAIR - 1);
+  const bool is_producer = warp >= C::NPAIR;
+  const int kvh = blockIdx.y;
   const int B = p.batch;
   const int32_t* ind = p.kv_indptr;
-
   if ((sbase & 1023u) != 0) return;  // swizzle atoms need a 1024-byte aligned window
 
-  const uint32_t bars = sbase + C::BAR_OFF;
-  auto full = [&](int s, int q) { return bars + 8u * (s * C::NCONS + q); };
-  auto empty = [&](int s) { return bars + 8u * (C::STAGES * C::NCONS + s); };
-  const uint32_t cbar = bars + 8u * (C::NBAR - 1);  // the four consumer warps, bounded waits
-  volatile int* err = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 8 * C::NBAR);
+  const uint32_t ring = sbase + pair * C::RING;
+  const uint32_t bars = sbase + C::BAR_OFF + 8u * (pair * 2 * C::STAGES);
+  auto full = [&](int s) { return bars + 8u * s; };
+  auto empty = [&](int s) { return bars + 8u * (C::STAGES + s); };
+  volatile int* err = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 8 * C::NBAR) + pair;
 
   // ---- set-up (shared memory only): barriers; Q rows of absent heads stay zero throughout
   if (tid == 0) {
-    for (int s = 0; s < C::STAGES; ++s) {
-      for (int q = 0; q < C::NCONS; ++q) tc::mbar_init(full(s, q), C::NPROD);
-      tc::mbar_init(empty(s), C::NCONS * 32);
-    }
-    tc::mbar_init(cbar, C::NCONS * 32);
-    *err = 0;
+    for (int i = 0; i < C::NPAIR * 2 * C::STAGES; ++i) tc::mbar_init(sbase + C::BAR_OFF + 8u * i, 32);
+    for (int i = 0; i < C::NPAIR; ++i) reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 8 * C::NBAR)[i] = 0;
     tc::fence_mbarrier_init();
   }
-  for (int i = tid; i < C::QBUFS * C::Q_BYTES / 16; i += C::THREADS) sts128_zero(sbase + C::Q_OFF + i * 16);
+  for (int i = tid; i < C::NPAIR * C::STAGES * (C::Q_BYTES / 16); i += C::THREADS) {
+    const int slot = i / (C::Q_BYTES / 16), c = i % (C::Q_BYTES / 16);
+    sts128_zero(sbase + slot * C::SLOT + 2 * C::KV_BYTES + c * 16);
+  }
   __syncthreads();
   // Launched as a programmatic dependent of the previous kernel in the stream: the set-up
   // above overlapped its tail; from here on its writes are visible and its reads are done,
@@ -213,119 +257,83 @@ __global__ void __launch_bounds__(320, 1) decode_split_kernel(const DecodeParams
   // let the combine kernel's CTAs launch now; they wait for this grid's memory to be visible
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
+  // ---- this pair's chunk (chunk index vc of the KV head) and its first request
+  const int vc = blockIdx.x * C::NPAIR + pair;
   const int T = __ldg(ind + B);
-  const int CL = decode_chunk_len(T, gridDim.x, p.min_chunk, p.part_pitch);
-  const int lo = (int)min((int64_t)cx * CL, (int64_t)T), hi = min(lo + CL, T);
-  if (lo >= hi) return;  // uniform over the CTA; no barrier follows for it
+  const int CL = decode_chunk_len(T, p.num_splits, p.min_chunk, p.part_pitch);
+  const int lo = (vc < p.num_splits) ? (int)min((int64_t)vc * CL, (int64_t)T) : T;
+  const int hi = min(lo + CL, T);
+  ReqBracket first{0, 0, T};
+  if (lo < hi) first = locate_request(ind, B, lo, T, lane);
 
-  if (warp >= C::NCONS) {
-    // ======================= producers: group g fills ring stage g with tiles g, g+3, ...
-    const int grp = (warp - C::NCONS) >> 1;             // 0..2 = the stage this group owns
-    const int pt = tid - C::NCONS * 32 - grp * C::NPROD;  // 0..63 within the group
-    TileIter it;
-    it.first(ind, B, lo, hi);
-    int piece = 0;
-    for (int k = 0; k < grp && it.valid(hi); ++k) {  // advance to tile grp
-      if (it.closes_piece(ind, hi)) ++piece;
-      it.next(ind, B, hi);
-    }
+  if (lo < hi && is_producer) {
+    // ======================= producer warp: gathers the chunk's K / V rows slot by slot
+    TileIter<C::BK> it;
+    it.start_at(first.b, first.end, lo, hi);
     const size_t head_stride = (size_t)p.num_kv_heads * D;
-    // thread pt copies chunk (pt % CPR) of keys (i * NPROD + pt) / CPR, i = 0 .. KV_IT-1;
-    // iterations [q * KV_IT_Q, (q + 1) * KV_IT_Q) cover exactly the keys of quarter q
-    int ids[C::KV_IT];
-    auto load_ids = [&](const TileIter& t) {
-#pragma unroll
-      for (int i = 0; i < C::KV_IT; ++i) {
-        const int key = (i * C::NPROD + pt) / C::CPR;
-        const int flat = t.start + key;
-        ids[i] = (t.valid(hi) && flat < t.end)
-                     ? ldg_nc_i32(p.req_to_token + (int64_t)t.b * p.r2t_stride + (flat - __ldg(ind + t.b)))
-                     : -1;
-      }
+    const unsigned nslots = (unsigned)p.num_slots;
+    auto slot_id = [&](const TileIter<C::BK>& t) {  // lane k: slot id of key k of the slot, or -1
+      const int flat = t.start + lane;
+      return (t.valid(hi) && flat < t.end)
+                 ? ldg_nc_i32(p.req_to_token + (int64_t)t.b * p.r2t_stride + (flat - __ldg(ind + t.b)))
+                 : -1;
     };
-    load_ids(it);
-    for (int round = 0; it.valid(hi); ++round) {
-      if (round > 0 && !wait_or_fail(empty(grp), (uint32_t)((round - 1) & 1), err)) break;
-      const uint32_t kst = sbase + grp * C::STAGE_BYTES, vst = kst + C::TILE;
-      if (it.opens_piece(ind, lo)) {  // first tile of a piece: its G query rows (with quarter 0)
-        const uint32_t qb = sbase + C::Q_OFF + (piece % C::QBUFS) * C::Q_BYTES;
+    int my_id = slot_id(it);
+    for (int i = 0; it.valid(hi); ++i) {
+      const int s = i % C::STAGES;
+      if (i >= C::STAGES && !wait_or_fail(empty(s), (uint32_t)((i / C::STAGES - 1) & 1), err)) break;
+      const uint32_t kst = ring + s * C::SLOT, vst = kst + C::KV_BYTES, qst = vst + C::KV_BYTES;
+      if (it.opens_piece(ind, lo)) {  // first slot of a piece: its G query rows
         const uint16_t* qsrc = p.q + ((size_t)it.b * p.num_qo_heads + (size_t)kvh * G) * D;
-        for (int i = pt; i < G * C::CPR; i += C::NPROD) {
-          const int g = i / C::CPR, c = i % C::CPR;
-          cp_async16(qb + sw128(g, c, C::QROWS), qsrc + (size_t)g * D + c * 8, true);
+        for (int j = lane; j < G * C::CPR; j += 32) {
+          const int g = j / C::CPR, c = j % C::CPR;
+          cp_async16(qst + sw128(g, c, C::QROWS), qsrc + (size_t)g * D + c * 8, true);
         }
       }
+      // lane -> chunk (lane % CPR) of keys (r * 32 + lane) / CPR, r = 0 .. KV_IT-1
 #pragma unroll
-      for (int q = 0; q < C::NCONS; ++q) {  // one cp.async group per quarter
-#pragma unroll
-        for (int i = q * C::KV_IT_Q; i < (q + 1) * C::KV_IT_Q; ++i) {
-          const int flat = i * C::NPROD + pt;
-          const int key = flat / C::CPR, c = flat % C::CPR;
-          const bool valid = ids[i] >= 0;
-          const size_t off = valid ? (size_t)ids[i] * head_stride + (size_t)kvh * D + c * 8 : 0;
-          const uint32_t o = sw128(key, c, C::BK);
-          cp_async16(kst + o, p.k_pool + off, valid);  // rows past the piece are zero-filled
-          cp_async16(vst + o, p.v_pool + off, valid);
-        }
-        cp_async_commit();
+      for (int r = 0; r < C::KV_IT; ++r) {
+        const int flat = r * 32 + lane;
+        const int key = flat / C::CPR, c = flat % C::CPR;
+        const int id = __shfl_sync(kFullMask, my_id, key);
+        const bool valid = (unsigned)id < nslots;  // padding and out-of-range ids read as zeros
+        const size_t off = valid ? (size_t)id * head_stride + (size_t)kvh * D + c * 8 : 0;
+        const uint32_t o = sw128(key, c, C::BK);
+        cp_async16(kst + o, p.k_pool + off, valid);
+        cp_async16(vst + o, p.v_pool + off, valid);
       }
-      // advance three tiles (this group's next one) and prefetch its slot ids
-      for (int k = 0; k < C::STAGES && it.valid(hi); ++k) {
-        if (it.closes_piece(ind, hi)) ++piece;
-        it.next(ind, B, hi);
-      }
-      load_ids(it);
-      // publish each quarter as soon as this thread's copies of it have landed
-      cp_async_wait<3>();
-      tc::mbar_arrive(full(grp, 0));
-      cp_async_wait<2>();
-      tc::mbar_arrive(full(grp, 1));
-      cp_async_wait<1>();
-      tc::mbar_arrive(full(grp, 2));
-      cp_async_wait<0>();
-      tc::mbar_arrive(full(grp, 3));
+      cp_async_arrive_noinc(full(s));  // completes once this lane's copies (and older ones) land
+      it.next(ind, B, hi);
+      my_id = slot_id(it);
     }
     cp_async_wait<0>();
-  } else {
-    // ======================= consumers: warp w takes quarter (w + j) % 4 of tile j
+  } else if (lo < hi) {
+    // ======================= consumer warp: online softmax over the chunk's slots
     // Transposed products so the 16-row MMA side is keys / head_dim, not the few heads:
     //   S^T (32 keys x 8 heads) = K Q^T,   O^T (D x 8 heads) += V^T P^T.
     const int g4 = lane >> 2, t4 = lane & 3;  // fragment row / column-pair index
     const int lrow = lane & 7, lmat = lane >> 3;  // ldmatrix: row within / index of the 8x8 matrix
     const float scale = p.scale_log2;
-    float* mw = reinterpret_cast<float*>(smem + C::ML_OFF);  // [NCONS][16]
-    float* lw = mw + C::NCONS * 16;                           // [NCONS][16]
-    float* mrg = reinterpret_cast<float*>(smem + C::MERGE_OFF);
-
-    TileIter it;
-    it.first(ind, B, lo, hi);
-    int piece = 0;
-    uint32_t cphase = 0;            // completed phases of the consumer merge barrier
-    auto cons_sync = [&]() -> bool {  // barrier over the consumer warps that cannot hang
-      tc::mbar_arrive(cbar);
-      return wait_or_fail(cbar, (cphase++) & 1u, err);
-    };
+    TileIter<C::BK> it;
+    it.start_at(first.b, first.end, lo, hi);
     uint32_t qb[NH][C::KSTEPS][2];  // Q^T as the B operand (n = heads), per k-step
     float acc[C::MT_D][NH][4];      // O^T: rows d = 16md + g4 (+8), heads 8nh + 2t4 (+1)
-    float m_run[NH][2], l_thr[NH][2];  // heads 8nh + 2t4 + e of this warp
-    for (int j = 0; it.valid(hi); ++j) {
-      const int st = j % C::STAGES;
-      const int quarter = (warp + j) & (C::NCONS - 1);
+    float m_run[NH][2], l_thr[NH][2];  // heads 8nh + 2t4 + e: reference max (lazy), sum
+    float m_max[NH][2];                // exact running max, for the (max, sum) partial
+    for (int i = 0; it.valid(hi); ++i) {
+      const int s = i % C::STAGES;
       const bool opens = it.opens_piece(ind, lo), closes = it.closes_piece(ind, hi);
-      const int kbase = quarter * 32;
-      const int nkeys = it.end - it.start;  // valid keys of the tile; the rest are masked
-      const bool work = kbase < nkeys;      // quarters wholly past the piece are skipped
-      if (!wait_or_fail(full(st, quarter), (uint32_t)((j / C::STAGES) & 1), err)) break;
-      const uint32_t kst = sbase + st * C::STAGE_BYTES, vst = kst + C::TILE;
+      const int nkeys = it.end - it.start;  // valid keys of the slot; the rest are masked
+      if (!wait_or_fail(full(s), (uint32_t)((i / C::STAGES) & 1), err)) break;
+      const uint32_t kst = ring + s * C::SLOT, vst = kst + C::KV_BYTES, qst = vst + C::KV_BYTES;
 
       if (opens) {  // new request piece: its query rows, fresh softmax state
-        const uint32_t qbuf = sbase + C::Q_OFF + (piece % C::QBUFS) * C::Q_BYTES;
 #pragma unroll
         for (int nh = 0; nh < NH; ++nh)
 #pragma unroll
           for (int kk = 0; kk < C::KSTEPS; kk += 2) {
             // matrices: heads 8nh .. 8nh+7 at chunks 2kk, 2kk+1, 2kk+2, 2kk+3
-            ldsm_x4(qbuf + sw128(8 * nh + lrow, 2 * kk + lmat, C::QROWS), qb[nh][kk][0], qb[nh][kk][1],
+            ldsm_x4(qst + sw128(8 * nh + lrow, 2 * kk + lmat, C::QROWS), qb[nh][kk][0], qb[nh][kk][1],
                     qb[nh][kk + 1][0], qb[nh][kk + 1][1]);
           }
 #pragma unroll
@@ -335,221 +343,208 @@ __global__ void __launch_bounds__(320, 1) decode_split_kernel(const DecodeParams
 #pragma unroll
         for (int nh = 0; nh < NH; ++nh) {
           m_run[nh][0] = m_run[nh][1] = -CUDART_INF_F;
+          m_max[nh][0] = m_max[nh][1] = -CUDART_INF_F;
           l_thr[nh][0] = l_thr[nh][1] = 0.f;
         }
       }
 
-      if (work) {
-        // ---- S^T = K Q^T: 2 m-tiles of 16 keys; even / odd k-steps in separate accumulators
-        float s[2][NH][4], s2[2][NH][4];
+      // ---- S^T = K Q^T: 2 m-tiles of 16 keys; even / odd k-steps in separate accumulators
+      float sc[2][NH][4], s2[2][NH][4];
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-          for (int nh = 0; nh < NH; ++nh)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) s[mt][nh][e] = s2[mt][nh][e] = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < C::KSTEPS; ++kk) {
-#pragma unroll
-          for (int mt = 0; mt < 2; ++mt) {
-            // matrices: (keys 0-7, chunk 2kk), (keys 8-15, 2kk), (keys 0-7, 2kk+1), (keys 8-15, 2kk+1)
-            const int key = kbase + mt * 16 + lrow + (lmat & 1) * 8, c = 2 * kk + (lmat >> 1);
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(kst + sw128(key, c, C::BK), a0, a1, a2, a3);
-#pragma unroll
-            for (int nh = 0; nh < NH; ++nh) {
-              if (kk & 1) mma16816(s2[mt][nh], a0, a1, a2, a3, qb[nh][kk][0], qb[nh][kk][1]);
-              else mma16816(s[mt][nh], a0, a1, a2, a3, qb[nh][kk][0], qb[nh][kk][1]);
-            }
-          }
-        }
-
-        // ---- online softmax (base 2) per head; this lane holds keys 16mt + g4 (+8)
-        float rmax[NH][2];
-#pragma unroll
-        for (int nh = 0; nh < NH; ++nh) rmax[nh][0] = rmax[nh][1] = -CUDART_INF_F;
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-          for (int nh = 0; nh < NH; ++nh)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int key = kbase + mt * 16 + g4 + (e >> 1) * 8;
-              const float x = (key < nkeys) ? (s[mt][nh][e] + s2[mt][nh][e]) * scale : -CUDART_INF_F;
-              s[mt][nh][e] = x;
-              rmax[nh][e & 1] = fmaxf(rmax[nh][e & 1], x);
-            }
+      for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
         for (int nh = 0; nh < NH; ++nh)
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            float x = rmax[nh][h];
-            x = fmaxf(x, __shfl_xor_sync(kFullMask, x, 4));
-            x = fmaxf(x, __shfl_xor_sync(kFullMask, x, 8));
-            x = fmaxf(x, __shfl_xor_sync(kFullMask, x, 16));
-            rmax[nh][h] = x;
-          }
-        float alpha[NH][2];
-        bool moved = false;
+          for (int e = 0; e < 4; ++e) sc[mt][nh][e] = s2[mt][nh][e] = 0.f;
 #pragma unroll
-        for (int nh = 0; nh < NH; ++nh)
+      for (int kk = 0; kk < C::KSTEPS; ++kk) {
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            alpha[nh][h] = 1.f;
-            // a warp whose keys are all masked keeps m = -inf; nothing it adds is nonzero
-            if (rmax[nh][h] > m_run[nh][h] + kRescaleLog2) {
-              alpha[nh][h] = fast_exp2(m_run[nh][h] - rmax[nh][h]);  // 0 when m_run = -inf
-              m_run[nh][h] = rmax[nh][h];
-              moved = true;
-            }
-          }
-        if (__any_sync(kFullMask, moved)) {
-#pragma unroll
-          for (int md = 0; md < C::MT_D; ++md)
-#pragma unroll
-            for (int nh = 0; nh < NH; ++nh) {
-              acc[md][nh][0] *= alpha[nh][0]; acc[md][nh][1] *= alpha[nh][1];
-              acc[md][nh][2] *= alpha[nh][0]; acc[md][nh][3] *= alpha[nh][1];
-            }
+        for (int mt = 0; mt < 2; ++mt) {
+          // matrices: (keys 0-7, chunk 2kk), (keys 8-15, 2kk), (keys 0-7, 2kk+1), (keys 8-15, 2kk+1)
+          const int key = mt * 16 + lrow + (lmat & 1) * 8, c = 2 * kk + (lmat >> 1);
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(kst + sw128(key, c, C::BK), a0, a1, a2, a3);
 #pragma unroll
           for (int nh = 0; nh < NH; ++nh) {
-            l_thr[nh][0] *= alpha[nh][0];
-            l_thr[nh][1] *= alpha[nh][1];
-          }
-        }
-        // P = exp2(s - m) as hi / lo bf16 pairs, transposed into P^T B fragments
-        uint32_t ph[2][NH][2], pl[2][NH][2];  // [k-step = m-tile][nh][keys 0-7 | 8-15]
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-          for (int nh = 0; nh < NH; ++nh)
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              float pv[2];
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const float mr = m_run[nh][e];
-                pv[e] = (mr == -CUDART_INF_F) ? 0.f : fast_exp2(s[mt][nh][2 * half + e] - mr);
-                l_thr[nh][e] += pv[e];
-              }
-              const uint32_t h01 = float2_to_bf16x2_rn(pv[0], pv[1]);
-              const float2 f01 = bf16x2_to_float2(h01);
-              const uint32_t l01 = float2_to_bf16x2_rn(pv[0] - f01.x, pv[1] - f01.y);
-              // (key g4 + 8 half, heads 2t4, 2t4+1) -> (head g4, keys 8 half + 2t4, +1)
-              ph[mt][nh][half] = movmatrix_t(h01);
-              pl[mt][nh][half] = movmatrix_t(l01);
-            }
-
-        // ---- O^T += V^T P^T over the quarter's 32 keys: 2 k-steps x D / 16 m-tiles
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-#pragma unroll
-          for (int md = 0; md < C::MT_D; ++md) {
-            // matrices (transposed on load): (d 0-7, keys 0-7), (d 8-15, keys 0-7), (d 0-7, keys 8-15), (d 8-15, keys 8-15)
-            const int key = kbase + ks * 16 + lrow + (lmat >> 1) * 8, c = 2 * md + (lmat & 1);
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4_t(vst + sw128(key, c, C::BK), a0, a1, a2, a3);
-#pragma unroll
-            for (int nh = 0; nh < NH; ++nh) {
-              mma16816(acc[md][nh], a0, a1, a2, a3, ph[ks][nh][0], ph[ks][nh][1]);
-              mma16816(acc[md][nh], a0, a1, a2, a3, pl[ks][nh][0], pl[ks][nh][1]);
-            }
+            if (kk & 1) mma16816(s2[mt][nh], a0, a1, a2, a3, qb[nh][kk][0], qb[nh][kk][1]);
+            else mma16816(sc[mt][nh], a0, a1, a2, a3, qb[nh][kk][0], qb[nh][kk][1]);
           }
         }
       }
-      // Quarters land in order, so seeing the last one means all of round j / STAGES is in.
-      // The next warp to wait on this stage's barriers may hold another quarter; with this
-      // wait, no barrier of the stage can still be a phase behind when it does.
-      if (!wait_or_fail(full(st, C::NCONS - 1), (uint32_t)((j / C::STAGES) & 1), err)) break;
-      __syncwarp();
-      tc::mbar_arrive(empty(st));  // this warp is done reading stage st
+
+      // ---- online softmax (base 2) per head; this lane holds keys 16mt + g4 (+8)
+      float rmax[NH][2];
+#pragma unroll
+      for (int nh = 0; nh < NH; ++nh) rmax[nh][0] = rmax[nh][1] = -CUDART_INF_F;
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int key = mt * 16 + g4 + (e >> 1) * 8;
+            const float x = (key < nkeys) ? (sc[mt][nh][e] + s2[mt][nh][e]) * scale : -CUDART_INF_F;
+            sc[mt][nh][e] = x;
+            rmax[nh][e & 1] = fmaxf(rmax[nh][e & 1], x);
+          }
+#pragma unroll
+      for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float x = rmax[nh][h];
+          x = fmaxf(x, __shfl_xor_sync(kFullMask, x, 4));
+          x = fmaxf(x, __shfl_xor_sync(kFullMask, x, 8));
+          x = fmaxf(x, __shfl_xor_sync(kFullMask, x, 16));
+          rmax[nh][h] = x;
+          m_max[nh][h] = fmaxf(m_max[nh][h], x);
+        }
+      float alpha[NH][2];
+      bool moved = false;
+#pragma unroll
+      for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          alpha[nh][h] = 1.f;
+          // a slot whose keys are all masked keeps m = -inf; nothing it adds is nonzero
+          if (rmax[nh][h] > m_run[nh][h] + kRescaleLog2) {
+            alpha[nh][h] = fast_exp2(m_run[nh][h] - rmax[nh][h]);  // 0 when m_run = -inf
+            m_run[nh][h] = rmax[nh][h];
+            moved = true;
+          }
+        }
+      if (__any_sync(kFullMask, moved)) {
+#pragma unroll
+        for (int md = 0; md < C::MT_D; ++md)
+#pragma unroll
+          for (int nh = 0; nh < NH; ++nh) {
+            acc[md][nh][0] *= alpha[nh][0]; acc[md][nh][1] *= alpha[nh][1];
+            acc[md][nh][2] *= alpha[nh][0]; acc[md][nh][3] *= alpha[nh][1];
+          }
+#pragma unroll
+        for (int nh = 0; nh < NH; ++nh) {
+          l_thr[nh][0] *= alpha[nh][0];
+          l_thr[nh][1] *= alpha[nh][1];
+        }
+      }
+      // P = exp2(s - m) as hi / lo bf16 pairs, transposed into P^T B fragments
+      uint32_t ph[2][NH][2], pl[2][NH][2];  // [k-step = m-tile][nh][keys 0-7 | 8-15]
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            float pv[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const float mr = m_run[nh][e];
+              pv[e] = (mr == -CUDART_INF_F) ? 0.f : fast_exp2(sc[mt][nh][2 * half + e] - mr);
+              l_thr[nh][e] += pv[e];
+            }
+            const uint32_t h01 = float2_to_bf16x2_rn(pv[0], pv[1]);
+            const float2 f01 = bf16x2_to_float2(h01);
+            const uint32_t l01 = float2_to_bf16x2_rn(pv[0] - f01.x, pv[1] - f01.y);
+            // (key g4 + 8 half, heads 2t4, 2t4+1) -> (head g4, keys 8 half + 2t4, +1)
+            ph[mt][nh][half] = movmatrix_t(h01);
+            pl[mt][nh][half] = movmatrix_t(l01);
+          }
+
+      // ---- O^T += V^T P^T over the slot's 32 keys: 2 k-steps x D / 16 m-tiles
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks) {
+#pragma unroll
+        for (int md = 0; md < C::MT_D; ++md) {
+          // matrices (transposed on load): (d 0-7, keys 0-7), (d 8-15, keys 0-7), (d 0-7, keys 8-15), (d 8-15, keys 8-15)
+          const int key = ks * 16 + lrow + (lmat >> 1) * 8, c = 2 * md + (lmat & 1);
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_t(vst + sw128(key, c, C::BK), a0, a1, a2, a3);
+#pragma unroll
+          for (int nh = 0; nh < NH; ++nh) {
+            mma16816(acc[md][nh], a0, a1, a2, a3, ph[ks][nh][0], ph[ks][nh][1]);
+            mma16816(acc[md][nh], a0, a1, a2, a3, pl[ks][nh][0], pl[ks][nh][1]);
+          }
+        }
+      }
 
       if (closes) {
-        // ---- piece finished: merge the four warps (log-sum-exp) and write it out
-        float lsum[NH][2];
+        // ---- piece finished: stage O (and m, l) in the slot's K | V area, then write it out
+        __syncwarp();  // every lane's ldmatrix reads of K and V are done
+        float* stg = reinterpret_cast<float*>(smem + (kst - sbase));   // [QROWS][STG_PITCH]
+        float* stg_ml = stg + C::QROWS * C::STG_PITCH;                 // [QROWS][2]
+        // move the reference from the lazy max to the exact one: factor 2^(m_run - m_max) in [2^-8, 1]
+        float f[NH][2];
 #pragma unroll
         for (int nh = 0; nh < NH; ++nh)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
+            f[nh][h] = (m_run[nh][h] == -CUDART_INF_F) ? 1.f : fast_exp2(m_run[nh][h] - m_max[nh][h]);
             float x = l_thr[nh][h];
             x += __shfl_xor_sync(kFullMask, x, 4);
             x += __shfl_xor_sync(kFullMask, x, 8);
             x += __shfl_xor_sync(kFullMask, x, 16);
-            lsum[nh][h] = x;
+            if (g4 == 0) {
+              stg_ml[(8 * nh + 2 * t4 + h) * 2 + 0] = m_max[nh][h];
+              stg_ml[(8 * nh + 2 * t4 + h) * 2 + 1] = x * f[nh][h];
+            }
           }
-        if (g4 == 0) {
+#pragma unroll
+        for (int md = 0; md < C::MT_D; ++md)
 #pragma unroll
           for (int nh = 0; nh < NH; ++nh)
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              mw[warp * 16 + 8 * nh + 2 * t4 + h] = m_run[nh][h];
-              lw[warp * 16 + 8 * nh + 2 * t4 + h] = lsum[nh][h];
-            }
-        }
+            for (int e = 0; e < 4; ++e)
+              stg[(8 * nh + 2 * t4 + (e & 1)) * C::STG_PITCH + md * 16 + g4 + (e >> 1) * 8] =
+                  acc[md][nh][e] * f[nh][e & 1];
+        __syncwarp();
         const int b = it.b;
         const int rb = __ldg(ind + b), re = __ldg(ind + b + 1);
         const bool direct = (p.out != nullptr) && rb >= lo && re <= hi;  // whole request in this chunk
-        const int slot = cx - rb / CL;
-#pragma unroll
-        for (int h0 = 0; h0 < G; h0 += C::HG) {
-          // this warp's accumulator rows h0 .. h0+HG-1 to shared memory: mrg[warp][row][d]
-#pragma unroll
-          for (int md = 0; md < C::MT_D; ++md)
-#pragma unroll
-            for (int nh = 0; nh < NH; ++nh)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int row = 8 * nh + 2 * t4 + (e & 1) - h0;
-                if (row >= 0 && row < C::HG && row + h0 < G)
-                  mrg[(warp * C::HG + row) * D + md * 16 + g4 + (e >> 1) * 8] = acc[md][nh][e];
-              }
-          if (!cons_sync()) break;
-          // 128 threads: thread -> (row, d) pairs of this head group
-          for (int idx = tid; idx < C::HG * D; idx += C::NCONS * 32) {
-            const int row = idx / D, d = idx % D, h = h0 + row;
-            if (h >= G) continue;
-            float M = -CUDART_INF_F;
-#pragma unroll
-            for (int w = 0; w < C::NCONS; ++w) M = fmaxf(M, mw[w * 16 + h]);
-            float O = 0.f, L = 0.f;
-            if (M != -CUDART_INF_F) {
-#pragma unroll
-              for (int w = 0; w < C::NCONS; ++w) {
-                const float f = fast_exp2(mw[w * 16 + h] - M);  // 0 for warps that saw no key
-                O += f * mrg[(w * C::HG + row) * D + d];
-                L += f * lw[w * 16 + h];
-              }
-            }
-            const size_t qh = (size_t)b * p.num_qo_heads + (size_t)kvh * G + h;
-            if (direct) {
-              const __nv_bfloat16 v = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
-              p.out[qh * D + d] = *reinterpret_cast<const uint16_t*>(&v);
-            } else {
-              const size_t row0 = qh * p.part_pitch + slot;
-              p.o_part[row0 * D + d] = O;
-              if (d == 0) {
-                p.ml_part[row0 * 2 + 0] = (M == -CUDART_INF_F) ? M : M * kLn2;  // natural-log units
-                p.ml_part[row0 * 2 + 1] = L;
-              }
-            }
+        const size_t qh0 = (size_t)b * p.num_qo_heads + (size_t)kvh * G;
+        if (direct) {
+          // lane -> 8 consecutive d of one head: bf16(O / l), 16-byte stores
+          for (int j = lane; j < G * (D / 8); j += 32) {
+            const int h = j / (D / 8), d0 = (j % (D / 8)) * 8;
+            const float L = stg_ml[h * 2 + 1];
+            const float inv = (L > 0.f) ? 1.f / L : 0.f;
+            const float* src = stg + h * C::STG_PITCH + d0;
+            uint4 v;
+            v.x = float2_to_bf16x2_rn(src[0] * inv, src[1] * inv);
+            v.y = float2_to_bf16x2_rn(src[2] * inv, src[3] * inv);
+            v.z = float2_to_bf16x2_rn(src[4] * inv, src[5] * inv);
+            v.w = float2_to_bf16x2_rn(src[6] * inv, src[7] * inv);
+            *reinterpret_cast<uint4*>(p.out + (qh0 + h) * D + d0) = v;
           }
-          if (!cons_sync()) break;  // merge buffer and m / l free again
+        } else {
+          const int slot = vc - rb / CL;
+          for (int j = lane; j < G * (D / 4); j += 32) {
+            const int h = j / (D / 4), d0 = (j % (D / 4)) * 4;
+            const float* src = stg + h * C::STG_PITCH + d0;
+            *reinterpret_cast<float4*>(p.o_part + ((qh0 + h) * p.part_pitch + slot) * D + d0) =
+                make_float4(src[0], src[1], src[2], src[3]);
+          }
+          for (int h = lane; h < G; h += 32) {
+            const float M = stg_ml[h * 2 + 0];
+            float2 ml;
+            ml.x = (M == -CUDART_INF_F) ? M : M * kLn2;  // natural-log units
+            ml.y = stg_ml[h * 2 + 1];
+            *reinterpret_cast<float2*>(p.ml_part + ((qh0 + h) * p.part_pitch + slot) * 2) = ml;
+          }
         }
-        if (*err) break;
-        ++piece;
       }
+      __syncwarp();
+      tc::mbar_arrive(empty(s));  // this slot may be refilled
       it.next(ind, B, hi);
     }
   }
   __syncthreads();
-  if (*err && tid < C::NCONS * 32) {
-    // a wait timed out: poison every partial this CTA owns so the call reads as failed
-    TileIter it;
+  if (*err && lo < hi && !is_producer) {
+    // a wait timed out: poison every output this pair owns so the call reads as failed
+    TileIter<C::BK> it;
     it.first(ind, B, lo, hi);
     for (; it.valid(hi); it.next(ind, B, hi)) {
       if (!it.closes_piece(ind, hi)) continue;
-      const int s = cx - __ldg(ind + it.b) / CL;
-      for (int i = tid; i < G * D; i += C::NCONS * 32) {
+      const int s = vc - __ldg(ind + it.b) / CL;
+      for (int i = lane; i < G * D; i += 32) {
         const size_t qh = (size_t)it.b * p.num_qo_heads + (size_t)kvh * G + i / D;
         p.o_part[(qh * p.part_pitch + s) * D + i % D] = CUDART_NAN_F;
         if (p.out != nullptr) p.out[qh * D + i % D] = 0x7fc0;
@@ -630,7 +625,7 @@ cudaError_t launch_split_t(const DecodeParams& p, cudaStream_t stream) {
     attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.num_splits, p.num_kv_heads);
+  cfg.gridDim = dim3((p.num_splits + C::NPAIR - 1) / C::NPAIR, p.num_kv_heads);  // NPAIR chunks per CTA
   cfg.blockDim = dim3(C::THREADS);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = stream;
