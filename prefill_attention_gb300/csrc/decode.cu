@@ -50,6 +50,8 @@
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "tcgen05.cuh"
 
@@ -577,31 +579,68 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
   }
   const size_t base = (size_t)wid * p.part_pitch;
   const float* ml = p.ml_part + base * 2;
-
-  float M = -CUDART_INF_F;
-  for (int s = lane; s < S; s += 32) M = fmaxf(M, ml[2 * s]);
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, o));
-
+  using VecT = typename std::conditional<VPL == 4, float4, float2>::type;
+  const VecT* o = reinterpret_cast<const VecT*>(p.o_part + base * D) + lane;  // slot s at o[s * 32]
+  auto fma_vec = [](float (&a)[VPL], float w, const VecT& v) {
+    if constexpr (VPL == 4) {
+      a[0] += w * v.x; a[1] += w * v.y; a[2] += w * v.z; a[3] += w * v.w;
+    } else {
+      a[0] += w * v.x; a[1] += w * v.y;
+    }
+  };
   float acc[VPL];
 #pragma unroll
   for (int e = 0; e < VPL; ++e) acc[e] = 0.f;
   float L = 0.f;
-  if (M != -CUDART_INF_F) {
-    for (int s = 0; s < S; ++s) {
-      const float m = ml[2 * s];
-      const float w = (m == -CUDART_INF_F) ? 0.f : exp2f((m - M) * kLog2e);
-      L += w * ml[2 * s + 1];
-      const float* o = p.o_part + (base + s) * D + lane * VPL;
-      if constexpr (VPL == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(o);
-        acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
-      } else {
-        const float2 v = *reinterpret_cast<const float2*>(o);
-        acc[0] += w * v.x; acc[1] += w * v.y;
+  constexpr int kFast = 8;  // up to this many slots: every load of the row in one round
+  if (S <= kFast) {
+    float2 mlj = make_float2(-CUDART_INF_F, 0.f);
+    if (lane < S) mlj = *reinterpret_cast<const float2*>(ml + 2 * lane);
+    VecT v[kFast];
+#pragma unroll
+    for (int k = 0; k < kFast; ++k)
+      if (k < S) v[k] = o[k * 32];
+    float M = mlj.x;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, off));
+    if (M != -CUDART_INF_F) {
+      const float wj = (mlj.x == -CUDART_INF_F) ? 0.f : exp2f((mlj.x - M) * kLog2e);
+      L = wj * mlj.y;
+#pragma unroll
+      for (int k = 0; k < kFast; ++k)
+        if (k < S) fma_vec(acc, __shfl_sync(kFullMask, wj, k), v[k]);
+    }
+  } else {
+    float M = -CUDART_INF_F;
+    for (int s = lane; s < S; s += 32) M = fmaxf(M, ml[2 * s]);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, off));
+    // O = sum_s w_s o_s, L = sum_s w_s l_s with w_s = e^(m_s - M), 32 slots at a time:
+    // lane j computes w of slot s0 + j; the o_s loads of four slots are issued together.
+    if (M != -CUDART_INF_F) {
+      for (int s0 = 0; s0 < S; s0 += 32) {
+        float wj = 0.f;
+        if (s0 + lane < S) {
+          const float2 mlj = *reinterpret_cast<const float2*>(ml + 2 * (s0 + lane));
+          wj = (mlj.x == -CUDART_INF_F) ? 0.f : exp2f((mlj.x - M) * kLog2e);
+          L += wj * mlj.y;
+        }
+        const int n = min(32, S - s0);
+        int j = 0;
+        for (; j + 4 <= n; j += 4) {
+          const VecT v0 = o[(s0 + j) * 32], v1 = o[(s0 + j + 1) * 32];
+          const VecT v2 = o[(s0 + j + 2) * 32], v3 = o[(s0 + j + 3) * 32];
+          fma_vec(acc, __shfl_sync(kFullMask, wj, j), v0);
+          fma_vec(acc, __shfl_sync(kFullMask, wj, j + 1), v1);
+          fma_vec(acc, __shfl_sync(kFullMask, wj, j + 2), v2);
+          fma_vec(acc, __shfl_sync(kFullMask, wj, j + 3), v3);
+        }
+        for (; j < n; ++j) fma_vec(acc, __shfl_sync(kFullMask, wj, j), o[(s0 + j) * 32]);
       }
     }
   }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(kFullMask, L, off);
   const float inv = (L > 0.f) ? 1.f / L : 0.f;
   uint16_t* dst = p.out + (size_t)wid * D + lane * VPL;
   if constexpr (VPL == 4) {
