@@ -238,13 +238,17 @@ int astr_attn_prefill_ragged(const uint16_t* q, const int32_t* qo_indptr, const 
   p.num_qo_heads = d->num_qo_heads;
   p.num_kv_heads = d->num_kv_heads;
   p.head_dim = d->head_dim;
+  p.num_slots = d->num_slots;
   p.total_q = d->total_q;
-  const int bq = astr::prefill_rows_per_tile() / G;  // query positions per tile
+  const int bq = astr::prefill_rows_per_cta() / G;  // query positions per CTA
   const int64_t by_total = ((int64_t)d->total_q + bq - 1) / bq + d->batch;
   const int64_t by_max = (int64_t)d->batch * (((int64_t)d->max_q_len + bq - 1) / bq);
   const int64_t tiles = by_total < by_max ? by_total : by_max;
   if (tiles > 0x7fffffffLL) return ASTR_ERR_INVALID_ARG;
   p.num_q_tiles = (int)tiles;
+  int sms = 0;
+  if ((st = sm_count(dev, &sms)) != ASTR_OK) return st;
+  p.num_ctas = sms;
   p.scale_log2 = sm_scale * 1.4426950408889634f;
   if (astr::launch_prefill(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ASTR_ERR_LAUNCH_FAILED;
   return ASTR_OK;

@@ -41,9 +41,11 @@ struct PrefillParams {
   const int32_t* seq_lens;       // [B]
   uint16_t* out;                 // [total_q, Hq, D]
   int64_t r2t_stride;
+  int64_t num_slots;             // rows of k_pool / v_pool (slot ids outside read as zeros)
   int batch, num_qo_heads, num_kv_heads, head_dim;
   int total_q;
-  int num_q_tiles;               // grid upper bound on (request, query tile) pairs
+  int num_q_tiles;               // upper bound on (request, query-tile pair) work items per KV head
+  int num_ctas;                  // persistent CTAs to launch (one per SM)
   float scale_log2;
 };
 
@@ -55,6 +57,6 @@ cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream);
 // Whether the kernels exist for this (head_dim, group size).
 bool decode_supported(int head_dim, int group);
 bool prefill_supported(int head_dim, int group);
-int prefill_rows_per_tile();  // query-head rows per tensor-core tile (M)
+int prefill_rows_per_cta();  // query-head rows per CTA (two tensor-core tiles of M = 128)
 
 }  // namespace astr

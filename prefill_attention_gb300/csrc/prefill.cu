@@ -40,31 +40,41 @@ namespace {
 
 template <int D, int G>
 struct PrefillCfg {
-  static constexpr int M = 128;                        // tile rows = query positions x heads
+  static constexpr int M = 128;                        // rows of one query tile = positions x heads
   static constexpr int BQ = M / G;                     // query positions per tile
+  static constexpr int NQ = 2;                         // query tiles per work item (consecutive, same request)
   static constexpr int BN = 64;                        // keys per KV tile
-  static constexpr int THREADS = 128;
+  static constexpr int STAGES = 4;                     // K/V ring; one producer warp per stage
+  static constexpr int MMA_WARP = 4 * NQ;              // warps 0-3: softmax of tile A, 4-7: tile B
+  static constexpr int PROD_WARP0 = MMA_WARP + 1;
+  static constexpr int THREADS = (PROD_WARP0 + STAGES) * 32;
   static constexpr int CPR = D / 8;                    // 16-byte chunks per row
   static constexpr int Q_BYTES = M * D * 2;
   static constexpr int KV_BYTES = BN * D * 2;          // one K (or V) tile
-  static constexpr int Q_OFF = 0;
-  static constexpr int K_OFF = Q_OFF + Q_BYTES;        // 2 stages
-  static constexpr int V_OFF = K_OFF + 2 * KV_BYTES;   // 2 stages
-  static constexpr int BAR_OFF = V_OFF + 2 * KV_BYTES; // bar_s, bar_o, tmem slot
-  static constexpr int SMEM_BYTES = BAR_OFF + 32;
-  static constexpr uint32_t TMEM_O = 0;                // O: columns [0, D)
-  static constexpr uint32_t TMEM_S = D;                // S: columns [D, D + BN)
-  static constexpr uint32_t TMEM_PH = D + BN;          // P high part, bf16 pairs: BN/2 columns
-  static constexpr uint32_t TMEM_PL = D + BN + BN / 2; // P low part (p - bf16(p)), BN/2 columns
-  static constexpr uint32_t TMEM_COLS = 256;           // D + 2 BN <= 256
-  static constexpr int Q_IT = M * CPR / THREADS;       // cp.async per thread for Q
-  static constexpr int KV_IT = BN * CPR / THREADS;     // cp.async per thread per K (and per V) tile
+  static constexpr int Q_OFF = 0;                      // NQ tiles
+  static constexpr int K_OFF = Q_OFF + NQ * Q_BYTES;   // STAGES tiles
+  static constexpr int V_OFF = K_OFF + STAGES * KV_BYTES;
+  static constexpr int BAR_OFF = V_OFF + STAGES * KV_BYTES;
+  // barriers: kv_full[STAGES], kv_empty[STAGES], q_full, q_free, s_full[NQ][2], p_full[NQ][2],
+  // pv_done[NQ], o_done[NQ], o_free[NQ], fin
+  static constexpr int NBAR = 2 * STAGES + 2 + 7 * NQ + 1;
+  // work order: items sorted by cost, and the per-request item offsets (when they fit)
+  static constexpr int MAX_SORT_ITEMS = 8192;
+  static constexpr int MAX_SORT_REQS = 1024;
+  static constexpr int ORD_OFF = BAR_OFF + NBAR * 8 + 16;
+  static constexpr int PST_OFF = ORD_OFF + MAX_SORT_ITEMS * 2;
+  static constexpr int SMEM_BYTES = PST_OFF + (MAX_SORT_REQS + 1) * 4;
+  static constexpr uint32_t TMEM_TILE = 256;           // tile t: O at 256 t, S buffers at 256 t + D + {0, BN}
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr int Q_IT = NQ * M * CPR / (32 * STAGES);  // cp.async per producer lane for its share of Q
+  static constexpr int KV_IT = BN * CPR / 32;          // cp.async per producer lane per K (and per V) tile
   static constexpr uint32_t IDESC_S = tc::idesc_bf16_f32(M, BN, false, false);   // K-major A and B
   static constexpr uint32_t IDESC_PV = tc::idesc_bf16_f32(M, D, false, true);    // B (V) MN-major
   static constexpr float kRescaleThreshold = 8.f;     // log2 units
-  static_assert(Q_IT * THREADS == M * CPR && KV_IT * THREADS == BN * CPR, "even copy split");
-  static_assert((Q_OFF | K_OFF | V_OFF) % 1024 == 0, "swizzle atoms must be 1024-byte aligned");
-  static_assert(D + 2 * BN <= (int)TMEM_COLS, "tensor-memory budget");
+  static_assert((Q_OFF | K_OFF | V_OFF | Q_BYTES) % 1024 == 0, "swizzle atoms must be 1024-byte aligned");
+  static_assert(D + 2 * BN <= (int)TMEM_TILE, "tensor-memory budget per tile");
+  static_assert(Q_IT * 32 * STAGES == NQ * M * CPR, "producers split the query tiles evenly");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
 // Byte offset of 16-byte chunk c of row r in a 128-byte-swizzled K-major tile whose
@@ -73,257 +83,536 @@ __device__ __forceinline__ uint32_t sw128(int r, int c, int rows) {
   return (uint32_t)((c >> 3) * rows * 128 + (r >> 3) * 1024 + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
+// One work item: KV head kvh, request b, query-tile pair pr (tiles 2 pr and 2 pr + 1 of the
+// request, the second possibly absent).  Items are numbered pair-major, KV-head-minor.
+struct PrefillItem {
+  int b, kvh, q0, q_len, cb, first0, nq, n_tiles;
+};
+
+// Fills the item's fields once its request b and pair pr are known.
+template <int BQ2, int BQ, int BN>
+__device__ __forceinline__ void fill_item(const PrefillParams& p, int b, int pr, int kvh, PrefillItem& it) {
+  it.b = b;
+  it.kvh = kvh;
+  it.q0 = __ldg(p.qo_indptr + b);
+  it.q_len = __ldg(p.qo_indptr + b + 1) - it.q0;
+  it.cb = __ldg(p.seq_lens + b) - it.q_len;
+  it.first0 = pr * BQ2;
+  it.nq = min(BQ2 / BQ, (it.q_len - it.first0 + BQ - 1) / BQ);
+  const int last = min(it.q_len, it.first0 + it.nq * BQ) - 1;
+  it.n_tiles = (it.cb + last + 1 + BN - 1) / BN;
+}
+
+// Decodes item w.  With `pst` (per-request first pair index, in shared memory) a binary
+// search; without it a warp-parallel prefix scan of per-request pair counts (all 32 lanes
+// call it and get the same answer).  False once w is past the last item.
+template <int BQ2, int BQ, int BN>
+__device__ __forceinline__ bool decode_item(const PrefillParams& p, int w, int lane, PrefillItem& it,
+                                            const int* pst) {
+  const int pair_idx = w / p.num_kv_heads;
+  if (pst != nullptr) {
+    if (pair_idx >= pst[p.batch]) return false;
+    int l = 0, h = p.batch - 1;  // largest b with pst[b] <= pair_idx
+    while (l < h) {
+      const int m = (l + h + 1) >> 1;
+      if (pst[m] <= pair_idx) l = m; else h = m - 1;
+    }
+    fill_item<BQ2, BQ, BN>(p, l, pair_idx - pst[l], w % p.num_kv_heads, it);
+    return true;
+  }
+  int acc = 0;
+  for (int base = 0; base < p.batch; base += 32) {
+    const int bb = base + lane;
+    int np = 0;
+    if (bb < p.batch) np = (__ldg(p.qo_indptr + bb + 1) - __ldg(p.qo_indptr + bb) + BQ2 - 1) / BQ2;
+    int inc = np;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFullMask, inc, o);
+      if (lane >= o) inc += y;
+    }
+    const int total = __shfl_sync(kFullMask, inc, 31);
+    if (pair_idx < acc + total) {
+      const unsigned ball = __ballot_sync(kFullMask, pair_idx < acc + inc);
+      const int first = __ffs(ball) - 1;
+      const int excl = __shfl_sync(kFullMask, inc - np, first);
+      fill_item<BQ2, BQ, BN>(p, base + first, pair_idx - acc - excl, w % p.num_kv_heads, it);
+      return true;
+    }
+    acc += total;
+  }
+  return false;
+}
 
 template <int D, int G>
-__global__ void __launch_bounds__(128, 2) prefill_kernel(const PrefillParams p) {
+__global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(const PrefillParams p) {
   using C = PrefillCfg<D, G>;
+  constexpr int BQ2 = C::NQ * C::BQ;
   extern __shared__ __align__(1024) unsigned char smem[];
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int kvh = blockIdx.y;
-
-  // ---- (request, query tile) of this CTA from qo_indptr: warp-parallel prefix scan of
-  //      per-request tile counts (every warp computes the same answer)
-  int b = -1, qt = 0;
-  {
-    const int x = blockIdx.x;
-    int acc = 0;
-    for (int base = 0; base < p.batch; base += 32) {
-      const int bb = base + lane;
-      int nt = 0;
-      if (bb < p.batch) {
-        const int ql = __ldg(p.qo_indptr + bb + 1) - __ldg(p.qo_indptr + bb);
-        nt = (ql + C::BQ - 1) / C::BQ;
-      }
-      int inc = nt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(kFullMask, inc, o);
-        if (lane >= o) inc += y;
-      }
-      const int total = __shfl_sync(kFullMask, inc, 31);
-      if (x < acc + total) {
-        const unsigned ball = __ballot_sync(kFullMask, x < acc + inc);
-        const int first = __ffs(ball) - 1;
-        const int excl = __shfl_sync(kFullMask, inc - nt, first);
-        b = base + first;
-        qt = x - acc - excl;
-        break;
-      }
-      acc += total;
-    }
-  }
-  if (b < 0) return;                  // grid upper bound exceeds the real tile count
   if ((sbase & 1023u) != 0) return;   // swizzle atoms need a 1024-byte aligned window
 
-  const int q0 = __ldg(p.qo_indptr + b);
-  const int q_len = __ldg(p.qo_indptr + b + 1) - q0;
-  const int cb = __ldg(p.seq_lens + b) - q_len;       // causal offset
-  const int qi_first = qt * C::BQ;
-  const int qi_last = min(q_len, qi_first + C::BQ) - 1;
-  const int kv_end = cb + qi_last + 1;                 // keys any row of the tile sees
-  const int n_tiles = (kv_end + C::BN - 1) / C::BN;
-
-  const int qi = qi_first + tid / G;                   // this thread's row (= TMEM lane)
-  const int g = tid % G;
-  const bool row_valid = qi <= qi_last;
-  const int limit = cb + min(qi, qi_last);             // last key this row attends
-
-  const uint32_t bar_s = sbase + C::BAR_OFF, bar_o = bar_s + 8, slot = bar_s + 16;
+  const uint32_t bars = sbase + C::BAR_OFF;
+  auto kv_full = [&](int s) { return bars + 8u * s; };
+  auto kv_empty = [&](int s) { return bars + 8u * (C::STAGES + s); };
+  const uint32_t q_full = bars + 8u * (2 * C::STAGES), q_free = q_full + 8;
+  const uint32_t tb = q_free + 8;  // per-tile barriers
+  // S / P of the g-th KV tile of query tile t live in buffer g & 1 (g counts over all items);
+  // each buffer has its own barriers, so no waiter is ever more than one phase behind.
+  auto s_full = [&](int t, int buf) { return tb + 8u * (2 * t + buf); };
+  auto p_full = [&](int t, int buf) { return tb + 8u * (2 * C::NQ + 2 * t + buf); };
+  auto pv_done = [&](int t) { return tb + 8u * (4 * C::NQ + t); };
+  auto o_done = [&](int t) { return tb + 8u * (5 * C::NQ + t); };
+  auto o_free = [&](int t) { return tb + 8u * (6 * C::NQ + t); };
+  const uint32_t fin = tb + 8u * (7 * C::NQ);
+  volatile int* err = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 8 * C::NBAR);
+  const uint32_t slot = sbase + C::BAR_OFF + 8 * C::NBAR + 4;
   if (tid == 0) {
-    tc::mbar_init(bar_s, 1);
-    tc::mbar_init(bar_o, 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      tc::mbar_init(kv_full(s), 32);
+      tc::mbar_init(kv_empty(s), 1);
+    }
+    tc::mbar_init(q_full, 32 * C::STAGES);
+    tc::mbar_init(q_free, 1);
+    for (int t = 0; t < C::NQ; ++t) {
+      for (int buf = 0; buf < 2; ++buf) {
+        tc::mbar_init(s_full(t, buf), 1);
+        tc::mbar_init(p_full(t, buf), 128);
+      }
+      tc::mbar_init(pv_done(t), 1);
+      tc::mbar_init(o_done(t), 1);
+      tc::mbar_init(o_free(t), 128);
+    }
+    tc::mbar_init(fin, 1);
+    *err = 0;
     tc::fence_mbarrier_init();
   }
   if (warp == 0) tc::tmem_alloc<C::TMEM_COLS>(slot);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::BAR_OFF + 16);
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::BAR_OFF + 8 * C::NBAR + 4);
 
-  // ---- Q tile: rows (position, head) contiguous in the packed q array
-  {
-    const uint16_t* qbase = p.q + ((size_t)q0 * p.num_qo_heads + (size_t)kvh * G) * D;
+  // ---- work order, computed identically by every CTA (no cross-CTA communication): items
+  // sorted by cost (KV tiles x query tiles, descending; ties by index) and dealt out in snake
+  // order (CTA c takes sorted positions c, 2G-1-c, 2G+c, ... for G CTAs), which keeps the
+  // per-CTA totals within a few percent of each other.  Problems too large for the tables
+  // fall back to the natural item order.
+  uint16_t* order = reinterpret_cast<uint16_t*>(smem + C::ORD_OFF);
+  int* pst = reinterpret_cast<int*>(smem + C::PST_OFF);
+  bool sorted = p.batch <= C::MAX_SORT_REQS;
+  if (sorted) {
+    if (warp == 0) {  // pst[b] = first pair index of request b, pst[B] = number of pairs
+      int acc = 0;
+      for (int base = 0; base < p.batch; base += 32) {
+        const int bb = base + lane;
+        int np = 0;
+        if (bb < p.batch) np = (__ldg(p.qo_indptr + bb + 1) - __ldg(p.qo_indptr + bb) + BQ2 - 1) / BQ2;
+        int inc = np;
 #pragma unroll
-    for (int it = 0; it < C::Q_IT; ++it) {
-      const int flat = it * C::THREADS + tid;
-      const int row = flat / C::CPR, c = flat % C::CPR;
-      const int rqi = qi_first + row / G;
-      const bool valid = rqi <= qi_last;
-      const uint16_t* src = valid ? qbase + ((size_t)rqi * p.num_qo_heads + row % G) * D + c * 8 : p.q;
-      cp_async16(sbase + C::Q_OFF + sw128(row, c, C::M), src, valid);
-    }
-  }
-
-  // ---- K/V gather through the slot table
-  const int32_t* r2t = p.req_to_token + (size_t)b * p.r2t_stride;
-  const size_t head_stride = (size_t)p.num_kv_heads * D;
-  int ids[C::KV_IT];
-  auto load_ids = [&](int tile) {
-#pragma unroll
-    for (int it = 0; it < C::KV_IT; ++it) {
-      const int key = (it * C::THREADS + tid) / C::CPR;
-      const int j = tile * C::BN + key;
-      ids[it] = (tile < n_tiles && j < kv_end) ? ldg_nc_i32(r2t + j) : -1;
-    }
-  };
-  auto issue_kv = [&](int tile) {
-    const uint32_t kdst = sbase + C::K_OFF + (tile & 1) * C::KV_BYTES;
-    const uint32_t vdst = sbase + C::V_OFF + (tile & 1) * C::KV_BYTES;
-#pragma unroll
-    for (int it = 0; it < C::KV_IT; ++it) {
-      const int flat = it * C::THREADS + tid;
-      const int key = flat / C::CPR, c = flat % C::CPR;
-      const bool valid = ids[it] >= 0;
-      const size_t off = valid ? (size_t)ids[it] * head_stride + (size_t)kvh * D + c * 8 : 0;
-      const uint32_t o = sw128(key, c, C::BN);
-      cp_async16(kdst + o, p.k_pool + off, valid);
-      cp_async16(vdst + o, p.v_pool + off, valid);
-    }
-    cp_async_commit();
-  };
-
-  load_ids(0);
-  issue_kv(0);  // group 0 = Q + KV tile 0
-  load_ids(1);
-
-  float m_run = -CUDART_INF_F, l_run = 0.f;
-  bool ok = true;
-  const float scale = p.scale_log2;
-
-  for (int j = 0; j < n_tiles; ++j) {
-    const int stage = j & 1;
-    // A. tile j is resident and visible to the tensor core; stop early if any wait timed out
-    cp_async_wait<0>();
-    tc::fence_proxy_async_smem();
-    tc::fence_before_sync();
-    ok = __syncthreads_and(ok ? 1 : 0) != 0;
-    tc::fence_after_sync();
-    if (!ok) break;
-
-    // B. S = Q K_j^T  (fp32 in TMEM columns [D, D+BN))
-    if (tid == 0) {
-      const uint32_t qa = sbase + C::Q_OFF, ka = sbase + C::K_OFF + stage * C::KV_BYTES;
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t ad = tc::smem_desc_sw128(qa + (kk >> 2) * (C::M * 128) + (kk & 3) * 32, 16, 1024);
-        const uint64_t bd = tc::smem_desc_sw128(ka + (kk >> 2) * (C::BN * 128) + (kk & 3) * 32, 16, 1024);
-        tc::mma_bf16_ss(tmem + C::TMEM_S, ad, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
-      }
-      tc::mma_commit(bar_s);
-    }
-
-    // C. S_j done (and, in issue order, P V_{j-1}: P buffer, O and stage j+1 are free)
-    ok &= tc::mbar_wait(bar_s, (uint32_t)(j & 1));
-    tc::fence_after_sync();
-
-    // D. prefetch tile j+1 and the slot ids of tile j+2
-    if (j + 1 < n_tiles) {
-      issue_kv(j + 1);
-      load_ids(j + 2);
-    }
-
-    // E. softmax of this thread's row
-    float s[C::BN];
-    {
-      uint32_t raw[32];
-#pragma unroll
-      for (int half = 0; half < C::BN / 32; ++half) {
-        tc::tmem_ld32(tmem + lane_base + C::TMEM_S + half * 32, raw);
-        tc::tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < 32; ++c) s[half * 32 + c] = __uint_as_float(raw[c]);
-      }
-    }
-    const int j0 = j * C::BN;
-    float mx = -CUDART_INF_F;
-#pragma unroll
-    for (int c = 0; c < C::BN; ++c) {
-      const float x = (j0 + c <= limit) ? s[c] * scale : -CUDART_INF_F;
-      s[c] = x;
-      mx = fmaxf(mx, x);
-    }
-    const float m_new = fmaxf(m_run, mx);
-    const bool need = m_new > m_run + C::kRescaleThreshold;   // always true on the first tile
-    if (__any_sync(kFullMask, need)) {
-      if (j > 0) {
-        const float alpha = exp2f(m_run - m_new);
-        l_run *= alpha;
-#pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t o[32];
-          tc::tmem_ld32(tmem + lane_base + C::TMEM_O + cc * 32, o);
-          tc::tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-          tc::tmem_st32(tmem + lane_base + C::TMEM_O + cc * 32, o);
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(kFullMask, inc, o);
+          if (lane >= o) inc += y;
         }
-        tc::tmem_st_wait();
+        if (bb < p.batch) pst[bb] = acc + inc - np;
+        acc += __shfl_sync(kFullMask, inc, 31);
       }
-      m_run = m_new;
+      if (lane == 0) pst[p.batch] = acc;
     }
-    // P = exp2(s - m) split into bf16 high and low parts (p = hi + lo to ~2^-17 relative),
-    // stored to this row's TMEM lane; P V then runs as two MMAs so P is not rounded to bf16.
-    float lsum = 0.f;
-    {
-      uint32_t ph[C::BN / 2], pl[C::BN / 2];
-#pragma unroll
-      for (int e = 0; e < C::BN / 2; ++e) {
-        const float p0 = exp2f(s[2 * e] - m_run);
-        const float p1 = exp2f(s[2 * e + 1] - m_run);
-        lsum += p0 + p1;
-        ph[e] = float2_to_bf16x2_rn(p0, p1);
-        const float2 h = bf16x2_to_float2(ph[e]);
-        pl[e] = float2_to_bf16x2_rn(p0 - h.x, p1 - h.y);
-      }
-      tc::tmem_st32(tmem + lane_base + C::TMEM_PH, ph);
-      tc::tmem_st32(tmem + lane_base + C::TMEM_PL, pl);
-      tc::tmem_st_wait();
-    }
-    l_run += lsum;
-
-    // F. P and any O rescale are in tensor memory before the MMA is issued
-    tc::fence_before_sync();
     __syncthreads();
-    tc::fence_after_sync();
-
-    // G. O += P V_j  (fp32 in TMEM columns [0, D)); completion is observed through the
-    //    next commit (S_{j+1}) or the final one.
-    if (tid == 0) {
-      const uint32_t va = sbase + C::V_OFF + stage * C::KV_BYTES;
+    sorted = (int64_t)pst[p.batch] * p.num_kv_heads <= C::MAX_SORT_ITEMS;
+  }
+  const int n_items = sorted ? pst[p.batch] * p.num_kv_heads : 0;
+  if (sorted) {
+    uint16_t* key = reinterpret_cast<uint16_t*>(smem + C::K_OFF);  // scratch: the KV ring is not in use yet
+    int* cnt = reinterpret_cast<int*>(smem + C::V_OFF);               // [256] bucket counts, then offsets
+    for (int w = tid; w < n_items; w += C::THREADS) {
+      const int pair_idx = w / p.num_kv_heads;
+      int l = 0, h = p.batch - 1;
+      while (l < h) {
+        const int m = (l + h + 1) >> 1;
+        if (pst[m] <= pair_idx) l = m; else h = m - 1;
+      }
+      PrefillItem it;
+      fill_item<BQ2, C::BQ, C::BN>(p, l, pair_idx - pst[l], 0, it);
+      int c = 2;  // fixed part of an item, in KV-tile units
+      for (int t = 0; t < it.nq; ++t) c += (it.cb + min(it.q_len, it.first0 + (t + 1) * C::BQ) + C::BN - 1) / C::BN;
+      key[w] = (uint16_t)(255 - min(c, 255));  // ascending key = descending cost
+    }
+    for (int i = tid; i < 256; i += C::THREADS) cnt[i] = 0;
+    __syncthreads();
+    if (warp == 0) {  // stable counting sort, one warp, chunks of 32 items in index order
+      for (int base = 0; base < n_items; base += 32) {
+        const int w = base + lane;
+        const int k = (w < n_items) ? key[w] : -1;
+        const unsigned peers = __match_any_sync(kFullMask, k);
+        if (w < n_items && (peers & ((1u << lane) - 1u)) == 0u) cnt[k] += __popc(peers);
+        __syncwarp();
+      }
+      int run = 0;  // exclusive scan of the 256 counts, 8 per lane
+      int v[8];
 #pragma unroll
-      for (int kk = 0; kk < C::BN / 16; ++kk) {
-        const uint64_t bd = tc::smem_desc_sw128(va + kk * 16 * 128, C::BN * 128, 1024);
-        tc::mma_bf16_ts(tmem + C::TMEM_O, tmem + C::TMEM_PH + kk * 8, bd, C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
-        tc::mma_bf16_ts(tmem + C::TMEM_O, tmem + C::TMEM_PL + kk * 8, bd, C::IDESC_PV, 1u);
+      for (int i = 0; i < 8; ++i) v[i] = cnt[lane * 8 + i];
+      int tot = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) tot += v[i];
+      int inc = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFullMask, inc, o);
+        if (lane >= o) inc += y;
+      }
+      run = inc - tot;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        cnt[lane * 8 + i] = run;
+        run += v[i];
+      }
+      __syncwarp();
+      for (int base = 0; base < n_items; base += 32) {
+        const int w = base + lane;
+        const int k = (w < n_items) ? key[w] : -1;
+        const unsigned peers = __match_any_sync(kFullMask, k);
+        if (w < n_items) order[cnt[k] + __popc(peers & ((1u << lane) - 1u))] = (uint16_t)w;
+        __syncwarp();
+        if (w < n_items && (peers & ((1u << lane) - 1u)) == 0u) cnt[k] += __popc(peers);
+        __syncwarp();
       }
     }
+    __syncthreads();
   }
+  // the k-th item of this CTA, or -1
+  auto item_at = [&](int k) -> int {
+    const int r = k, c = blockIdx.x;
+    const int pos = r * (int)gridDim.x + ((r & 1) ? (int)gridDim.x - 1 - c : c);
+    if (sorted) return pos < n_items ? (int)order[pos] : -1;
+    return pos;  // natural order; decode_item reports the end
+  };
+  const int* pst_or_null = sorted ? pst : nullptr;
 
-  // ---- epilogue: O / l -> bf16 rows of out
-  cp_async_wait<0>();
-  if (tid == 0) tc::mma_commit(bar_o);
-  if (ok) ok = tc::mbar_wait(bar_o, 0);
-  tc::fence_after_sync();
-  const bool all_ok = __syncthreads_and(ok ? 1 : 0) != 0;
-  const float inv = all_ok ? 1.f / l_run : CUDART_NAN_F;   // a timed-out wait poisons the tile
-  uint16_t* orow = p.out + ((size_t)(q0 + qi) * p.num_qo_heads + (size_t)kvh * G + g) * D;
-#pragma unroll
-  for (int cc = 0; cc < D / 32; ++cc) {
-    uint32_t o[32];
-    tc::tmem_ld32(tmem + lane_base + C::TMEM_O + cc * 32, o);
-    tc::tmem_ld_wait();
-    if (row_valid) {
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        uint4 v;
-        v.x = float2_to_bf16x2_rn(__uint_as_float(o[q4 * 8 + 0]) * inv, __uint_as_float(o[q4 * 8 + 1]) * inv);
-        v.y = float2_to_bf16x2_rn(__uint_as_float(o[q4 * 8 + 2]) * inv, __uint_as_float(o[q4 * 8 + 3]) * inv);
-        v.z = float2_to_bf16x2_rn(__uint_as_float(o[q4 * 8 + 4]) * inv, __uint_as_float(o[q4 * 8 + 5]) * inv);
-        v.w = float2_to_bf16x2_rn(__uint_as_float(o[q4 * 8 + 6]) * inv, __uint_as_float(o[q4 * 8 + 7]) * inv);
-        reinterpret_cast<uint4*>(orow + cc * 32)[q4] = v;
+  // Bounded wait, agreed by the whole warp (so warp-collective tcgen05 ops after it stay
+  // converged); a timeout, or an error raised elsewhere, makes every later wait fail.
+  auto wait_or_fail = [&](uint32_t bar, uint32_t parity) -> bool {
+    bool ok = (*err == 0) && tc::mbar_wait(bar, parity);
+    ok = __all_sync(kFullMask, ok);
+    if (!ok) *err = 1;
+    return ok;
+  };
+
+  if (warp >= C::PROD_WARP0) {
+    // ======================= producers: warp PROD_WARP0 + s fills stage s with every KV tile
+    //                         g = s mod STAGES (g counts over all items) and loads a quarter
+    //                         of each item's query rows
+    const int st = warp - C::PROD_WARP0;
+    const size_t head_stride = (size_t)p.num_kv_heads * D;
+    const unsigned nslots = (unsigned)p.num_slots;
+    int g_base = 0;  // global index of the current item's KV tile 0
+    bool ok = true;
+    PrefillItem it;
+    for (int n_item = 0; ok; ++n_item) {
+      const int w = item_at(n_item);
+      if (w < 0 || !decode_item<BQ2, C::BQ, C::BN>(p, w, lane, it, pst_or_null)) break;
+      const int kvh = it.kvh;
+      const int32_t* r2t = p.req_to_token + (size_t)it.b * p.r2t_stride;
+      const int kv_end = min(it.cb + min(it.q_len, it.first0 + BQ2), it.cb + it.q_len);
+      // query rows (position, head) of both tiles; this warp takes chunks st, st + STAGES, ...
+      if (n_item > 0 && !(ok = wait_or_fail(q_free, (uint32_t)((n_item - 1) & 1)))) break;
+      {
+        const uint16_t* qbase = p.q + ((size_t)it.q0 * p.num_qo_heads + (size_t)kvh * G) * D;
+#pragma unroll 4
+        for (int i = 0; i < C::Q_IT; ++i) {
+          const int flat = (i * C::STAGES + st) * 32 + lane;       // over both tiles' chunks
+          const int t = flat / (C::M * C::CPR), rem = flat % (C::M * C::CPR);
+          const int row = rem / C::CPR, c = rem % C::CPR;
+          const int rqi = it.first0 + t * C::BQ + row / G;
+          const bool valid = t < it.nq && rqi < it.q_len && rqi < it.first0 + (t + 1) * C::BQ;
+          const uint16_t* src = valid ? qbase + ((size_t)rqi * p.num_qo_heads + row % G) * D + c * 8 : p.q;
+          cp_async16(sbase + C::Q_OFF + t * C::Q_BYTES + sw128(row, c, C::M), src, valid);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+        tc::fence_proxy_async_smem();
+        tc::mbar_arrive(q_full);
       }
+      // this warp's KV tiles of the item
+      const int j_first = (st - g_base % C::STAGES + C::STAGES) % C::STAGES;
+      auto ids_of = [&](int j, int half) {  // slot id of key 32 half + lane of item tile j, or -1
+        const int key = j * C::BN + half * 32 + lane;
+        return (j < it.n_tiles && key < kv_end) ? ldg_nc_i32(r2t + key) : -1;
+      };
+      int id0 = ids_of(j_first, 0), id1 = ids_of(j_first, 1);
+      for (int j = j_first; j < it.n_tiles; j += C::STAGES) {
+        const int g = g_base + j;
+        if (g >= C::STAGES && !(ok = wait_or_fail(kv_empty(st), (uint32_t)(((g / C::STAGES) - 1) & 1)))) break;
+        const uint32_t kdst = sbase + C::K_OFF + st * C::KV_BYTES, vdst = sbase + C::V_OFF + st * C::KV_BYTES;
+#pragma unroll 8
+        for (int i = 0; i < C::KV_IT; ++i) {
+          const int flat = i * 32 + lane;
+          const int key = flat / C::CPR, c = flat % C::CPR;  // key < 32 exactly for the first half of `i`
+          const int id = __shfl_sync(kFullMask, (i < C::KV_IT / 2) ? id0 : id1, key & 31);
+          const bool valid = (unsigned)id < nslots;  // padding and out-of-range ids read as zeros
+          const size_t off = valid ? (size_t)id * head_stride + (size_t)kvh * D + c * 8 : 0;
+          const uint32_t o = sw128(key, c, C::BN);
+          cp_async16(kdst + o, p.k_pool + off, valid);
+          cp_async16(vdst + o, p.v_pool + off, valid);
+        }
+        cp_async_commit();
+        id0 = ids_of(j + C::STAGES, 0);  // next tile of this stage: its slot ids load meanwhile
+        id1 = ids_of(j + C::STAGES, 1);
+        cp_async_wait<0>();
+        tc::fence_proxy_async_smem();  // the tensor core reads the tile through the async proxy
+        tc::mbar_arrive(kv_full(st));
+      }
+      g_base += it.n_tiles;
+    }
+    cp_async_wait<0>();
+  } else if (warp == C::MMA_WARP) {
+    // ======================= MMA issue, lane 0 alone.  tcgen05.mma issue runs nearly in step
+    // with execution, so the thread must not stall between MMAs: the barrier each group needs
+    // is tested (without blocking) in the middle of the group before it.  Per KV tile j of an
+    // item: S_t(j+1) = Q_t K_{j+1}^T for both tiles (other S buffer), then O_t += P_t(j) V_j as
+    // soon as the softmax warps of tile t have written P_t(j).
+    int g_base = 0;                   // global index of the item's KV tile 0
+    int gs[C::NQ] = {};               // S tiles issued so far per query tile (buffer / phase counter)
+    int n_used[C::NQ] = {};           // items so far that had query tile t (o_done / o_free phases)
+    bool ok = true;
+    PrefillItem it;
+    for (int n_item = 0; ok; ++n_item) {
+      const int w = item_at(n_item);
+      if (w < 0 || !decode_item<BQ2, C::BQ, C::BN>(p, w, lane, it, pst_or_null)) break;
+      if (lane == 0) {
+        int nk[C::NQ];
+#pragma unroll
+        for (int t = 0; t < C::NQ; ++t)
+          nk[t] = (t < it.nq) ? (it.cb + min(it.q_len, it.first0 + (t + 1) * C::BQ) - 1 + 1 + C::BN - 1) / C::BN : 0;
+        const int n = it.n_tiles;
+        auto wait_one = [&](uint32_t bar, uint32_t parity, bool ready) {  // blocking only if not pre-tested ready
+          if (ok && !ready && !tc::mbar_wait(bar, parity)) {
+            *err = 1;
+            ok = false;
+          }
+          tc::fence_after_sync();
+        };
+        auto kv_ready = [&](int j) { return kv_full((g_base + j) % C::STAGES); };
+        auto kv_par = [&](int j) { return (uint32_t)(((g_base + j) / C::STAGES) & 1); };
+        auto sbuf = [&](int t, int j) { return (gs[t] + j) & 1; };
+        auto s_par = [&](int t, int j) { return (uint32_t)(((gs[t] + j) >> 1) & 1); };
+        // issue S_t(j); while it runs, test barrier `nb` (parity `np`); returns that test
+        auto issue_s = [&](int t, int j, uint32_t nb, uint32_t np) -> bool {
+          const uint32_t qa = sbase + C::Q_OFF + t * C::Q_BYTES;
+          const uint32_t ka = sbase + C::K_OFF + ((g_base + j) % C::STAGES) * C::KV_BYTES;
+          const uint32_t sd = tmem + t * C::TMEM_TILE + D + sbuf(t, j) * C::BN;
+          bool r = false;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t ad = tc::smem_desc_sw128(qa + (kk >> 2) * (C::M * 128) + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = tc::smem_desc_sw128(ka + (kk >> 2) * (C::BN * 128) + (kk & 3) * 32, 16, 1024);
+            tc::mma_bf16_ss(sd, ad, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
+            if (kk == D / 32) r = nb != 0u && tc::mbar_test(nb, np);
+          }
+          tc::mma_commit(s_full(t, sbuf(t, j)));
+          return r;
+        };
+        auto issue_pv = [&](int t, int j, uint32_t nb, uint32_t np) -> bool {
+          const uint32_t va = sbase + C::V_OFF + ((g_base + j) % C::STAGES) * C::KV_BYTES;
+          const uint32_t od = tmem + t * C::TMEM_TILE, pa = od + D + sbuf(t, j) * C::BN;  // P hi [0,32), lo [32,64)
+          bool r = false;
+#pragma unroll
+          for (int kk = 0; kk < C::BN / 16; ++kk) {
+            const uint64_t bd = tc::smem_desc_sw128(va + kk * 16 * 128, C::BN * 128, 1024);
+            tc::mma_bf16_ts(od, pa + kk * 8, bd, C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+            tc::mma_bf16_ts(od, pa + C::BN / 2 + kk * 8, bd, C::IDESC_PV, 1u);
+            if (kk == 1) r = nb != 0u && tc::mbar_test(nb, np);
+          }
+          tc::mma_commit(pv_done(t));
+          if (j == nk[t] - 1) tc::mma_commit(o_done(t));
+          return r;
+        };
+
+        wait_one(q_full, (uint32_t)(n_item & 1), false);
+        wait_one(kv_ready(0), kv_par(0), false);
+        bool ready = false;  // pre-test result for the next wait
+        for (int t = 0; ok && t < it.nq; ++t)
+          ready = issue_s(t, 0, t == it.nq - 1 && n > 1 ? kv_ready(1) : 0u, kv_par(1));
+        if (n == 1) tc::mma_commit(q_free);  // every S of the item issued: Q may be reloaded
+        for (int j = 0; ok && j < n; ++j) {
+          // S of KV tile j + 1 for both query tiles
+          if (j + 1 < n) {
+            wait_one(kv_ready(j + 1), kv_par(j + 1), ready);
+            ready = false;
+            for (int t = 0; ok && t < it.nq; ++t) {
+              if (j + 1 >= nk[t]) continue;
+              const bool last = (t == it.nq - 1);
+              const bool r = issue_s(t, j + 1, last && j < nk[0] ? p_full(0, sbuf(0, j)) : 0u, s_par(0, j));
+              if (last) ready = r;
+            }
+            if (j + 2 == n) tc::mma_commit(q_free);
+          }
+          // O_t += P_t(j) V_j (the first P V of an item overwrites O once the epilogue of the
+          // item before has read it)
+          for (int t = 0; ok && t < it.nq; ++t) {
+            if (j >= nk[t]) continue;
+            if (j == 0 && n_used[t] > 0) wait_one(o_free(t), (uint32_t)((n_used[t] - 1) & 1), false);
+            wait_one(p_full(t, sbuf(t, j)), s_par(t, j), ready);
+            uint32_t nb = 0u, np = 0u;  // next wait: P of the following tile, else the next KV tile
+            if (t + 1 < it.nq && j < nk[t + 1]) {
+              nb = p_full(t + 1, sbuf(t + 1, j));
+              np = s_par(t + 1, j);
+            } else if (j + 2 < n) {
+              nb = kv_ready(j + 2);
+              np = kv_par(j + 2);
+            }
+            ready = issue_pv(t, j, nb, np);
+          }
+          tc::mma_commit(kv_empty((g_base + j) % C::STAGES));  // stage free once every MMA on it is done
+        }
+#pragma unroll
+        for (int t = 0; t < C::NQ; ++t) {
+          gs[t] += nk[t];
+          if (t < it.nq) ++n_used[t];
+        }
+      }
+      ok = __shfl_sync(kFullMask, ok ? 1 : 0, 0) != 0;
+      g_base += it.n_tiles;
+    }
+    if (lane == 0) {
+      // every MMA this thread issued has completed before the CTA may release tensor memory
+      tc::mma_commit(fin);
+      if (!tc::mbar_wait(fin, 0)) *err = 1;
+    }
+    __syncwarp();
+  } else {
+    // ======================= softmax: warp group t = warp / 4; thread owns row tid % 128
+    const int t = warp >> 2;
+    const int row = tid & 127;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t o_col = tmem + lane_base + t * C::TMEM_TILE;
+    const float scale = p.scale_log2;
+    const bool pos_scale = scale >= 0.f;
+    int gs = 0, n_used = 0;  // same counters as the MMA thread, for this query tile
+    bool ok = true;
+    PrefillItem it;
+    for (int n_item = 0; ok; ++n_item) {
+      const int w = item_at(n_item);
+      if (w < 0 || !decode_item<BQ2, C::BQ, C::BN>(p, w, lane, it, pst_or_null)) break;
+      if (t >= it.nq) continue;
+      const int qf = it.first0 + t * C::BQ, ql = min(it.q_len, qf + C::BQ) - 1;
+      const int n_keys = (it.cb + ql + 1 + C::BN - 1) / C::BN;
+      const int qi = qf + row / G;                       // this thread's query position
+      const int g = row % G;
+      const bool row_valid = qi <= ql;
+      const int limit = it.cb + min(qi, ql);             // last key this row attends
+      const int mask_from = (it.cb + qf + 1) / C::BN;    // tiles >= this one hold a masked key for some row
+      float m_run = -CUDART_INF_F, l_run = 0.f;
+      for (int j = 0; j < n_keys; ++j) {
+        const int gb = gs + j;
+        const uint32_t sb = o_col + D + (gb & 1) * C::BN;  // S_t(j), then P_t(j)
+        if (!(ok = wait_or_fail(s_full(t, gb & 1), (uint32_t)((gb >> 1) & 1)))) break;
+        tc::fence_after_sync();
+        float s[C::BN];
+        {
+          uint32_t raw[32];
+#pragma unroll
+          for (int half = 0; half < C::BN / 32; ++half) {
+            tc::tmem_ld32(sb + half * 32, raw);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) s[half * 32 + c] = __uint_as_float(raw[c]);
+          }
+        }
+        // row max of sm_scale * s in base-2 units: max (or min for a negative scale) of the
+        // raw scores times the scale; masked keys are left out here and get p = 0 below
+        const bool masked = j >= mask_from;
+        const int j0 = j * C::BN;
+        float ext = pos_scale ? -CUDART_INF_F : CUDART_INF_F;
+        if (masked) {
+#pragma unroll
+          for (int c = 0; c < C::BN; ++c)
+            if (j0 + c <= limit) ext = pos_scale ? fmaxf(ext, s[c]) : fminf(ext, s[c]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < C::BN; ++c) ext = pos_scale ? fmaxf(ext, s[c]) : fminf(ext, s[c]);
+        }
+        const float m_tile = (j0 > limit) ? -CUDART_INF_F : ext * scale;  // -inf: no visible key
+        const bool need = m_tile > m_run + C::kRescaleThreshold;  // true on the first visible tile
+        if (__any_sync(kFullMask, need)) {
+          const float alpha = need ? fast_exp2(m_run - m_tile) : 1.f;  // 0 while m_run = -inf
+          if (j > 0) {
+            // O holds P V of KV tiles < j once P V_{j-1} completes (S_t(j) done implies
+            // P V_{j-2} done, so pv_done is at most one phase behind here)
+            if (!(ok = wait_or_fail(pv_done(t), (uint32_t)((gb - 1) & 1)))) break;
+            tc::fence_after_sync();
+#pragma unroll 1
+            for (int cc = 0; cc < D / 16; ++cc) {
+              uint32_t o[16];
+              tc::tmem_ld16(o_col + cc * 16, o);
+              tc::tmem_ld_wait();
+#pragma unroll
+              for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+              tc::tmem_st16(o_col + cc * 16, o);
+            }
+          }
+          l_run *= alpha;
+          if (need) m_run = m_tile;
+        }
+        // P = 2^(scale s - m) as bf16 hi / lo planes in the S columns just read (p = hi + lo
+        // to ~2^-17 relative); P V then runs as two MMAs so P is not rounded to bf16.
+        const float neg_m = (m_run == -CUDART_INF_F) ? 0.f : -m_run;
+        float lsum = 0.f;
+#pragma unroll
+        for (int half = 0; half < C::BN / 32; ++half) {
+          uint32_t ph[16], pl[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int c0 = half * 32 + 2 * e;
+            float p0 = fast_exp2(fmaf(s[c0], scale, neg_m));
+            float p1 = fast_exp2(fmaf(s[c0 + 1], scale, neg_m));
+            if (masked) {
+              p0 = (j0 + c0 <= limit) ? p0 : 0.f;
+              p1 = (j0 + c0 + 1 <= limit) ? p1 : 0.f;
+            }
+            lsum += p0 + p1;
+            ph[e] = float2_to_bf16x2_rn(p0, p1);
+            const float2 h = bf16x2_to_float2(ph[e]);
+            pl[e] = float2_to_bf16x2_rn(p0 - h.x, p1 - h.y);
+          }
+          tc::tmem_st16(sb + half * 16, ph);
+          tc::tmem_st16(sb + C::BN / 2 + half * 16, pl);
+        }
+        l_run += lsum;
+        tc::tmem_st_wait();
+        tc::fence_before_sync();
+        tc::mbar_arrive(p_full(t, gb & 1));
+      }
+      if (!ok) break;
+
+      // ---- epilogue: O / l -> bf16 rows of out, once the last P V of this tile has landed
+      ok = wait_or_fail(o_done(t), (uint32_t)(n_used & 1));
+      tc::fence_after_sync();
+      const float inv = (ok && !*err) ? 1.f / l_run : CUDART_NAN_F;   // a timed-out wait poisons the tile
+      uint16_t* orow = p.out + ((size_t)(it.q0 + qi) * p.num_qo_heads + (size_t)it.kvh * G + g) * D;
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t o[32];
+        tc::tmem_ld32(o_col + cc * 32, o);
+        tc::tmem_ld_wait();
+        if (row_valid) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 v;
+            v.x = float2_to_bf16x2_rn(__uint_as_float(o[q4 * 8 + 0]) * inv, __uint_as_float(o[q4 * 8 + 1]) * inv);
+            v.y = float2_to_bf16x2_rn(__uint_as_float(o[q4 * 8 + 2]) * inv, __uint_as_float(o[q4 * 8 + 3]) * inv);
+            v.z = float2_to_bf16x2_rn(__uint_as_float(o[q4 * 8 + 4]) * inv, __uint_as_float(o[q4 * 8 + 5]) * inv);
+            v.w = float2_to_bf16x2_rn(__uint_as_float(o[q4 * 8 + 6]) * inv, __uint_as_float(o[q4 * 8 + 7]) * inv);
+            reinterpret_cast<uint4*>(orow + cc * 32)[q4] = v;
+          }
+        }
+      }
+      tc::fence_before_sync();
+      tc::mbar_arrive(o_free(t));  // O of this tile may be overwritten by the next item
+      gs += n_keys;
+      ++n_used;
     }
   }
 
@@ -345,14 +634,17 @@ cudaError_t launch_prefill_t(const PrefillParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 grid(p.num_q_tiles, p.num_kv_heads);
+  // persistent CTAs, one per SM, each walking items blockIdx.x, + gridDim.x, ...
+  const int64_t items = (int64_t)p.num_q_tiles * p.num_kv_heads;
+  const int grid = (int)(items < p.num_ctas ? items : p.num_ctas);
+  if (grid <= 0) return cudaSuccess;
   prefill_kernel<D, G><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-int prefill_rows_per_tile() { return 128; }
+int prefill_rows_per_cta() { return 256; }
 
 bool prefill_supported(int head_dim, int group) {
   return (head_dim == 64 || head_dim == 128) && (group == 1 || group == 2 || group == 4 || group == 8 || group == 16);
