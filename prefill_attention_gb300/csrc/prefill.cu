@@ -46,7 +46,7 @@ struct PrefillCfg {
   static constexpr int BN = 64;                        // keys per KV tile
   static constexpr int STAGES = 4;                     // K/V ring; one producer warp per stage
   static constexpr int MMA_WARP = 4 * NQ;              // warps 0-3: softmax of tile A, 4-7: tile B
-  static constexpr int PROD_WARP0 = MMA_WARP + 1;
+  static constexpr int PROD_WARP0 = MMA_WARP + NQ;     // one MMA-issuing warp per query tile
   static constexpr int THREADS = (PROD_WARP0 + STAGES) * 32;
   static constexpr int CPR = D / 8;                    // 16-byte chunks per row
   static constexpr int Q_BYTES = M * D * 2;
@@ -81,6 +81,34 @@ struct PrefillCfg {
 // 64-element column blocks each hold `rows` rows.
 __device__ __forceinline__ uint32_t sw128(int r, int c, int rows) {
   return (uint32_t)((c >> 3) * rows * 128 + (r >> 3) * 1024 + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+// tcgen05.mma with the shared-memory descriptors passed as 32-bit halves.  The start address
+// lives in bits 0-13 of the low half, so a descriptor for base + off is (lo + off / 16, hi)
+// for the operand offsets used here (all smem addresses are below 256 KB).
+__device__ __forceinline__ void mma_ss_h(uint32_t d, uint32_t alo, uint32_t ahi, uint32_t blo, uint32_t bhi,
+                                         uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 a, b;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\tmov.b64 a, {%1, %2};\n\tmov.b64 b, {%3, %4};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, p;\n\t}" ::"r"(d),
+      "r"(alo), "r"(ahi), "r"(blo), "r"(bhi), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_h(uint32_t d, uint32_t a_tmem, uint32_t blo, uint32_t bhi, uint32_t idesc,
+                                         uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 b;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\tmov.b64 b, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b, %4, p;\n\t}" ::"r"(d),
+      "r"(a_tmem), "r"(blo), "r"(bhi), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// Keeps the values in registers at this point (they are computed before it, not between MMAs).
+template <int N>
+__device__ __forceinline__ void keep_regs(uint32_t (&v)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(v[i]));
 }
 
 // One work item: KV head kvh, request b, query-tile pair pr (tiles 2 pr and 2 pr + 1 of the
@@ -171,10 +199,10 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
   if (tid == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       tc::mbar_init(kv_full(s), 32);
-      tc::mbar_init(kv_empty(s), 1);
+      tc::mbar_init(kv_empty(s), C::NQ);  // one commit per MMA thread
     }
     tc::mbar_init(q_full, 32 * C::STAGES);
-    tc::mbar_init(q_free, 1);
+    tc::mbar_init(q_free, C::NQ);
     for (int t = 0; t < C::NQ; ++t) {
       for (int buf = 0; buf < 2; ++buf) {
         tc::mbar_init(s_full(t, buf), 1);
@@ -184,7 +212,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
       tc::mbar_init(o_done(t), 1);
       tc::mbar_init(o_free(t), 128);
     }
-    tc::mbar_init(fin, 1);
+    tc::mbar_init(fin, C::NQ);
     *err = 0;
     tc::fence_mbarrier_init();
   }
@@ -367,25 +395,35 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
       g_base += it.n_tiles;
     }
     cp_async_wait<0>();
-  } else if (warp == C::MMA_WARP) {
-    // ======================= MMA issue, lane 0 alone.  tcgen05.mma issue runs nearly in step
-    // with execution, so the thread must not stall between MMAs: the barrier each group needs
-    // is tested (without blocking) in the middle of the group before it.  Per KV tile j of an
-    // item: S_t(j+1) = Q_t K_{j+1}^T for both tiles (other S buffer), then O_t += P_t(j) V_j as
-    // soon as the softmax warps of tile t have written P_t(j).
-    int g_base = 0;                   // global index of the item's KV tile 0
-    int gs[C::NQ] = {};               // S tiles issued so far per query tile (buffer / phase counter)
-    int n_used[C::NQ] = {};           // items so far that had query tile t (o_done / o_free phases)
+  } else if (warp >= C::MMA_WARP) {
+    // ======================= MMA issue: warp MMA_WARP + t, lane 0 alone, for query tile t.
+    // tcgen05.mma issue runs nearly in step with execution, so whatever the issuing thread
+    // does between MMAs (waits, fences, commits) idles the tensor core unless another thread
+    // has MMAs queued: the two query tiles therefore have their own issuing threads, and the
+    // barrier each group needs is tested (without blocking) in the middle of the group before
+    // it.  Per KV tile j: S_t(j+1) = Q_t K_{j+1}^T into the other S buffer, then
+    // O_t += P_t(j) V_j once the softmax warps of tile t have written P_t(j).  Both threads
+    // commit every KV tile (after it has landed) and every item's Q, used or not, so the shared
+    // barriers count two arrivals per phase.
+    const int t = warp - C::MMA_WARP;
+    // descriptor halves of Q tile t, K stage 0 (K-major) and V stage 0 (MN-major)
+    const uint64_t qd0 = tc::smem_desc_sw128(sbase + C::Q_OFF + t * C::Q_BYTES, 16, 1024);
+    const uint64_t kd0 = tc::smem_desc_sw128(sbase + C::K_OFF, 16, 1024);
+    const uint64_t vd0 = tc::smem_desc_sw128(sbase + C::V_OFF, C::BN * 128, 1024);
+    const uint32_t q_lo = (uint32_t)qd0, q_hi = (uint32_t)(qd0 >> 32);
+    const uint32_t k_lo = (uint32_t)kd0, k_hi = (uint32_t)(kd0 >> 32);
+    const uint32_t v_lo = (uint32_t)vd0, v_hi = (uint32_t)(vd0 >> 32);
+    const uint32_t od = tmem + t * C::TMEM_TILE;  // O of tile t; S / P buffers at od + D + {0, BN}
+    int g_base = 0;   // global index of the item's KV tile 0
+    int gs = 0;       // KV tiles of tile t so far (S buffer / phase counter)
+    int n_used = 0;   // items so far that had tile t (o_done / o_free phases)
     bool ok = true;
     PrefillItem it;
     for (int n_item = 0; ok; ++n_item) {
       const int w = item_at(n_item);
       if (w < 0 || !decode_item<BQ2, C::BQ, C::BN>(p, w, lane, it, pst_or_null)) break;
       if (lane == 0) {
-        int nk[C::NQ];
-#pragma unroll
-        for (int t = 0; t < C::NQ; ++t)
-          nk[t] = (t < it.nq) ? (it.cb + min(it.q_len, it.first0 + (t + 1) * C::BQ) - 1 + 1 + C::BN - 1) / C::BN : 0;
+        const int nk = (t < it.nq) ? (it.cb + min(it.q_len, it.first0 + (t + 1) * C::BQ) + C::BN - 1) / C::BN : 0;
         const int n = it.n_tiles;
         auto wait_one = [&](uint32_t bar, uint32_t parity, bool ready) {  // blocking only if not pre-tested ready
           if (ok && !ready && !tc::mbar_wait(bar, parity)) {
@@ -396,82 +434,78 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
         };
         auto kv_ready = [&](int j) { return kv_full((g_base + j) % C::STAGES); };
         auto kv_par = [&](int j) { return (uint32_t)(((g_base + j) / C::STAGES) & 1); };
-        auto sbuf = [&](int t, int j) { return (gs[t] + j) & 1; };
-        auto s_par = [&](int t, int j) { return (uint32_t)(((gs[t] + j) >> 1) & 1); };
-        // issue S_t(j); while it runs, test barrier `nb` (parity `np`); returns that test
-        auto issue_s = [&](int t, int j, uint32_t nb, uint32_t np) -> bool {
-          const uint32_t qa = sbase + C::Q_OFF + t * C::Q_BYTES;
-          const uint32_t ka = sbase + C::K_OFF + ((g_base + j) % C::STAGES) * C::KV_BYTES;
-          const uint32_t sd = tmem + t * C::TMEM_TILE + D + sbuf(t, j) * C::BN;
+        auto sbuf = [&](int j) { return (gs + j) & 1; };
+        auto s_par = [&](int j) { return (uint32_t)(((gs + j) >> 1) & 1); };
+        // issue S_t(j); while it runs, test barrier `nb` (parity `np`); returns that test.
+        // Descriptors are formed before the first MMA so the MMAs issue back to back.
+        auto issue_s = [&](int j, uint32_t nb, uint32_t np) -> bool {
+          const uint32_t sd = od + D + sbuf(j) * C::BN;
+          const uint32_t klo = k_lo + (uint32_t)(((g_base + j) % C::STAGES) * C::KV_BYTES >> 4);
+          uint32_t al[D / 16], bl[D / 16];
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            al[kk] = q_lo + (uint32_t)(((kk >> 2) * (C::M * 128) + (kk & 3) * 32) >> 4);
+            bl[kk] = klo + (uint32_t)(((kk >> 2) * (C::BN * 128) + (kk & 3) * 32) >> 4);
+          }
+          keep_regs(al);
+          keep_regs(bl);
           bool r = false;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t ad = tc::smem_desc_sw128(qa + (kk >> 2) * (C::M * 128) + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = tc::smem_desc_sw128(ka + (kk >> 2) * (C::BN * 128) + (kk & 3) * 32, 16, 1024);
-            tc::mma_bf16_ss(sd, ad, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
+            mma_ss_h(sd, al[kk], q_hi, bl[kk], k_hi, C::IDESC_S, kk > 0 ? 1u : 0u);
             if (kk == D / 32) r = nb != 0u && tc::mbar_test(nb, np);
           }
-          tc::mma_commit(s_full(t, sbuf(t, j)));
+          tc::mma_commit(s_full(t, sbuf(j)));
           return r;
         };
-        auto issue_pv = [&](int t, int j, uint32_t nb, uint32_t np) -> bool {
-          const uint32_t va = sbase + C::V_OFF + ((g_base + j) % C::STAGES) * C::KV_BYTES;
-          const uint32_t od = tmem + t * C::TMEM_TILE, pa = od + D + sbuf(t, j) * C::BN;  // P hi [0,32), lo [32,64)
+        auto issue_pv = [&](int j, uint32_t nb, uint32_t np) -> bool {
+          const uint32_t pa = od + D + sbuf(j) * C::BN;  // P hi in [0, 32), lo in [32, 64)
+          const uint32_t vlo = v_lo + (uint32_t)(((g_base + j) % C::STAGES) * C::KV_BYTES >> 4);
+          uint32_t bl[C::BN / 16];
+#pragma unroll
+          for (int kk = 0; kk < C::BN / 16; ++kk) bl[kk] = vlo + (uint32_t)((kk * 16 * 128) >> 4);
+          keep_regs(bl);
+          const uint32_t acc0 = j > 0 ? 1u : 0u;
           bool r = false;
 #pragma unroll
           for (int kk = 0; kk < C::BN / 16; ++kk) {
-            const uint64_t bd = tc::smem_desc_sw128(va + kk * 16 * 128, C::BN * 128, 1024);
-            tc::mma_bf16_ts(od, pa + kk * 8, bd, C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
-            tc::mma_bf16_ts(od, pa + C::BN / 2 + kk * 8, bd, C::IDESC_PV, 1u);
+            mma_ts_h(od, pa + kk * 8, bl[kk], v_hi, C::IDESC_PV, kk > 0 ? 1u : acc0);
+            mma_ts_h(od, pa + C::BN / 2 + kk * 8, bl[kk], v_hi, C::IDESC_PV, 1u);
             if (kk == 1) r = nb != 0u && tc::mbar_test(nb, np);
           }
           tc::mma_commit(pv_done(t));
-          if (j == nk[t] - 1) tc::mma_commit(o_done(t));
+          if (j == nk - 1) tc::mma_commit(o_done(t));
           return r;
         };
 
         wait_one(q_full, (uint32_t)(n_item & 1), false);
-        wait_one(kv_ready(0), kv_par(0), false);
         bool ready = false;  // pre-test result for the next wait
-        for (int t = 0; ok && t < it.nq; ++t)
-          ready = issue_s(t, 0, t == it.nq - 1 && n > 1 ? kv_ready(1) : 0u, kv_par(1));
-        if (n == 1) tc::mma_commit(q_free);  // every S of the item issued: Q may be reloaded
+        if (nk > 0) {
+          wait_one(kv_ready(0), kv_par(0), false);
+          ready = issue_s(0, nk > 1 ? kv_ready(1) : 0u, kv_par(1));
+        }
+        if (nk <= 1) tc::mma_commit(q_free);  // every S of tile t in this item issued
         for (int j = 0; ok && j < n; ++j) {
-          // S of KV tile j + 1 for both query tiles
-          if (j + 1 < n) {
-            wait_one(kv_ready(j + 1), kv_par(j + 1), ready);
-            ready = false;
-            for (int t = 0; ok && t < it.nq; ++t) {
-              if (j + 1 >= nk[t]) continue;
-              const bool last = (t == it.nq - 1);
-              const bool r = issue_s(t, j + 1, last && j < nk[0] ? p_full(0, sbuf(0, j)) : 0u, s_par(0, j));
-              if (last) ready = r;
+          if (j < nk) {
+            if (j + 1 < nk) {  // S of KV tile j + 1 into the other buffer
+              wait_one(kv_ready(j + 1), kv_par(j + 1), ready);
+              ready = issue_s(j + 1, p_full(t, sbuf(j)), s_par(j));
+              if (j + 2 == nk) tc::mma_commit(q_free);
             }
-            if (j + 2 == n) tc::mma_commit(q_free);
+            // O_t += P_t(j) V_j (the item's first P V overwrites O once the epilogue of the
+            // item before has read it)
+            if (j == 0 && n_used > 0) wait_one(o_free(t), (uint32_t)((n_used - 1) & 1), false);
+            wait_one(p_full(t, sbuf(j)), s_par(j), ready);
+            ready = issue_pv(j, j + 2 < nk ? kv_ready(j + 2) : 0u, kv_par(j + 2));
           }
-          // O_t += P_t(j) V_j (the first P V of an item overwrites O once the epilogue of the
-          // item before has read it)
-          for (int t = 0; ok && t < it.nq; ++t) {
-            if (j >= nk[t]) continue;
-            if (j == 0 && n_used[t] > 0) wait_one(o_free(t), (uint32_t)((n_used[t] - 1) & 1), false);
-            wait_one(p_full(t, sbuf(t, j)), s_par(t, j), ready);
-            uint32_t nb = 0u, np = 0u;  // next wait: P of the following tile, else the next KV tile
-            if (t + 1 < it.nq && j < nk[t + 1]) {
-              nb = p_full(t + 1, sbuf(t + 1, j));
-              np = s_par(t + 1, j);
-            } else if (j + 2 < n) {
-              nb = kv_ready(j + 2);
-              np = kv_par(j + 2);
-            }
-            ready = issue_pv(t, j, nb, np);
-          }
-          tc::mma_commit(kv_empty((g_base + j) % C::STAGES));  // stage free once every MMA on it is done
+          // a KV tile this query tile does not need still gets this thread's commit, but only
+          // once it has landed: otherwise the commit could run ahead and count toward an
+          // earlier phase of the stage's empty barrier
+          if (j >= nk) wait_one(kv_ready(j), kv_par(j), false);
+          tc::mma_commit(kv_empty((g_base + j) % C::STAGES));  // this thread's MMAs on the stage are done
         }
-#pragma unroll
-        for (int t = 0; t < C::NQ; ++t) {
-          gs[t] += nk[t];
-          if (t < it.nq) ++n_used[t];
-        }
+        gs += nk;
+        if (nk > 0) ++n_used;
       }
       ok = __shfl_sync(kFullMask, ok ? 1 : 0, 0) != 0;
       g_base += it.n_tiles;
