@@ -56,8 +56,8 @@ struct PrefillCfg {
   static constexpr int V_OFF = K_OFF + STAGES * KV_BYTES;
   static constexpr int BAR_OFF = V_OFF + STAGES * KV_BYTES;
   // barriers: kv_full[STAGES], kv_empty[STAGES], q_full, q_free, s_full[NQ][2], p_full[NQ][2],
-  // pv_done[NQ], o_done[NQ], o_free[NQ], fin
-  static constexpr int NBAR = 2 * STAGES + 2 + 7 * NQ + 1;
+  // o_done[NQ], o_free[NQ], fin
+  static constexpr int NBAR = 2 * STAGES + 2 + 6 * NQ + 1;
   // work order: items sorted by cost, and the per-request item offsets (when they fit)
   static constexpr int MAX_SORT_ITEMS = 8192;
   static constexpr int MAX_SORT_REQS = 1024;
@@ -190,10 +190,9 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
   // each buffer has its own barriers, so no waiter is ever more than one phase behind.
   auto s_full = [&](int t, int buf) { return tb + 8u * (2 * t + buf); };
   auto p_full = [&](int t, int buf) { return tb + 8u * (2 * C::NQ + 2 * t + buf); };
-  auto pv_done = [&](int t) { return tb + 8u * (4 * C::NQ + t); };
-  auto o_done = [&](int t) { return tb + 8u * (5 * C::NQ + t); };
-  auto o_free = [&](int t) { return tb + 8u * (6 * C::NQ + t); };
-  const uint32_t fin = tb + 8u * (7 * C::NQ);
+  auto o_done = [&](int t) { return tb + 8u * (4 * C::NQ + t); };
+  auto o_free = [&](int t) { return tb + 8u * (5 * C::NQ + t); };
+  const uint32_t fin = tb + 8u * (6 * C::NQ);
   volatile int* err = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 8 * C::NBAR);
   const uint32_t slot = sbase + C::BAR_OFF + 8 * C::NBAR + 4;
   if (tid == 0) {
@@ -208,7 +207,6 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
         tc::mbar_init(s_full(t, buf), 1);
         tc::mbar_init(p_full(t, buf), 128);
       }
-      tc::mbar_init(pv_done(t), 1);
       tc::mbar_init(o_done(t), 1);
       tc::mbar_init(o_free(t), 128);
     }
@@ -473,7 +471,6 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
             mma_ts_h(od, pa + C::BN / 2 + kk * 8, bl[kk], v_hi, C::IDESC_PV, 1u);
             if (kk == 1) r = nb != 0u && tc::mbar_test(nb, np);
           }
-          tc::mma_commit(pv_done(t));
           if (j == nk - 1) tc::mma_commit(o_done(t));
           return r;
         };
@@ -525,12 +522,16 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
     const float scale = p.scale_log2;
     const bool pos_scale = scale >= 0.f;
     int gs = 0, n_used = 0;  // same counters as the MMA thread, for this query tile
+    int g_base = 0;          // global index of the item's KV tile 0
     bool ok = true;
     PrefillItem it;
     for (int n_item = 0; ok; ++n_item) {
       const int w = item_at(n_item);
       if (w < 0 || !decode_item<BQ2, C::BQ, C::BN>(p, w, lane, it, pst_or_null)) break;
-      if (t >= it.nq) continue;
+      if (t >= it.nq) {
+        g_base += it.n_tiles;
+        continue;
+      }
       const int qf = it.first0 + t * C::BQ, ql = min(it.q_len, qf + C::BQ) - 1;
       const int n_keys = (it.cb + ql + 1 + C::BN - 1) / C::BN;
       const int qi = qf + row / G;                       // this thread's query position
@@ -573,9 +574,11 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
         if (__any_sync(kFullMask, need)) {
           const float alpha = need ? fast_exp2(m_run - m_tile) : 1.f;  // 0 while m_run = -inf
           if (j > 0) {
-            // O holds P V of KV tiles < j once P V_{j-1} completes (S_t(j) done implies
-            // P V_{j-2} done, so pv_done is at most one phase behind here)
-            if (!(ok = wait_or_fail(pv_done(t), (uint32_t)((gb - 1) & 1)))) break;
+            // O holds P V of KV tiles < j once P V_{j-1} completes; the issuing thread commits
+            // that KV tile's empty barrier right after it, so wait for that phase (rare: only
+            // when the row max grows by more than the threshold)
+            const int gp = g_base + j - 1;
+            if (!(ok = wait_or_fail(kv_empty(gp % C::STAGES), (uint32_t)((gp / C::STAGES) & 1)))) break;
             tc::fence_after_sync();
 #pragma unroll 1
             for (int cc = 0; cc < D / 16; ++cc) {
@@ -647,6 +650,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
       tc::mbar_arrive(o_free(t));  // O of this tile may be overwritten by the next item
       gs += n_keys;
       ++n_used;
+      g_base += it.n_tiles;
     }
   }
 
