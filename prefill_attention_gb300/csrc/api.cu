@@ -165,6 +165,7 @@ int astr_attn_paged_decode(const uint16_t* q, const uint16_t* k_pool, const uint
   p.kv_indptr = kv_indptr; p.o_part = o_part; p.ml_part = ml_part; p.out = out;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (astr::launch_decode_split(p, s) != cudaSuccess) return ASTR_ERR_LAUNCH_FAILED;
+  p.indptr_before_wait = 1;  // the combine follows this call's split kernel directly
   if (astr::launch_decode_combine(p, s) != cudaSuccess) return ASTR_ERR_LAUNCH_FAILED;
   return ASTR_OK;
 }

@@ -29,6 +29,8 @@ struct DecodeParams {
   int min_chunk;                 // floor on the chunk length so no request needs > part_pitch slots
   float scale_log2;              // sm_scale * log2(e): logits are kept in base-2 units on chip
   int combine_all;               // combine even single-chunk requests (partials supplied by the caller)
+  int indptr_before_wait;        // combine: kv_indptr may be read before the dependency wait (the
+                                 // previous kernel is this call's split kernel, which does not write it)
 };
 
 // Prefill/extend: one launch of the tensor-core kernel.

@@ -561,22 +561,28 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
   constexpr int VPL = D / 32;  // output elements per lane
   const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  // launched as a programmatic dependent of the split kernel: wait until its writes are visible
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  // the next kernel in the stream may start its shared-memory set-up now
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (wid >= p.batch * p.num_qo_heads) return;
-  const int b = wid / p.num_qo_heads;
-  int S;
-  if (p.kv_indptr != nullptr) {  // token-balanced chunks: the chunks that overlap request b
+  const bool live = wid < p.batch * p.num_qo_heads;
+  const int b = live ? wid / p.num_qo_heads : 0;
+  // Split count of request b: the chunks that overlap it (token-balanced schedule), or the
+  // caller's explicit count.
+  auto split_count = [&]() {
+    if (p.kv_indptr == nullptr) return p.num_splits;
     const int T = __ldg(p.kv_indptr + p.batch);
     const int CL = decode_chunk_len(T, p.num_splits, p.min_chunk, p.part_pitch);
     const int a = __ldg(p.kv_indptr + b), e = __ldg(p.kv_indptr + b + 1);
-    S = (e > a) ? (e - 1) / CL - a / CL + 1 : 0;
-    if (S == 1 && !p.combine_all) return;  // written directly by the split kernel
-  } else {                       // explicit count (partials supplied by the caller)
-    S = p.num_splits;
-  }
+    return (e > a) ? (e - 1) / CL - a / CL + 1 : 0;
+  };
+  // Right after this call's split kernel, kv_indptr (an input the split kernel does not write)
+  // is read before the wait: that kernel has already passed its own wait on the kernels before
+  // it.  After any other kernel it is read only once the wait has returned.
+  int S = (live && p.indptr_before_wait) ? split_count() : 0;
+  // launched as a programmatic dependent of the previous kernel: wait until its writes are visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (live && !p.indptr_before_wait) S = split_count();
+  // the next kernel in the stream may start its shared-memory set-up now
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (!live) return;
+  if (p.kv_indptr != nullptr && S == 1 && !p.combine_all) return;  // written directly by the split kernel
   const size_t base = (size_t)wid * p.part_pitch;
   const float* ml = p.ml_part + base * 2;
   using VecT = typename std::conditional<VPL == 4, float4, float2>::type;

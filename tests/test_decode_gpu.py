@@ -270,3 +270,14 @@ def test_split_then_combine_entry_points():
     assert _err(got, oracle.decode(w)) <= TOL
     ref = run_decode(w, t, max_splits=16)
     assert np.abs(got - to_f64(ref)).max() <= TOL
+
+
+@pytest.mark.parametrize("scale", [-0.125, 0.0, 0.3])
+def test_scale_sign_and_zero(scale):
+    rng = np.random.default_rng(44)
+    seq = [1, 33, 200, 517, 0, 64]
+    w = make_from_lengths(rng, kind="decode", name="scale", seq_lens=seq, q_lens=None, Hq=8, Hkv=2, d=64,
+                          sm_scale=scale)
+    for n in (0, 3):
+        got = to_f64(run_decode(w, num_splits=n))
+        assert _err(got, oracle.decode(w)) <= TOL, f"n_chunks={n}"

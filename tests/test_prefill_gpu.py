@@ -127,3 +127,37 @@ def test_cuda_graph_replay_bit_exact():
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+
+
+@pytest.mark.parametrize("scale", [-0.125, 0.0, 0.3])
+def test_scale_sign_and_zero(scale):
+    """The row max turns into a min for a negative scale; a zero scale gives the mean of the
+    visible V rows (every logit 0)."""
+    rng = np.random.default_rng(41)
+    ql = np.array([1, 17, 64, 130])
+    pre = np.array([0, 40, 3, 200])
+    w = make_from_lengths(rng, kind="prefill", name="scale", seq_lens=pre + ql, q_lens=ql, Hq=8, Hkv=2, d=64,
+                          sm_scale=scale)
+    assert _err(to_f64(run_prefill(w)), oracle.prefill(w)) <= TOL
+
+
+def test_many_requests_natural_order():
+    """More requests than the kernel's shared-memory work-order table holds: the items are then
+    dealt out in their natural order (the path every large batch takes)."""
+    rng = np.random.default_rng(42)
+    B = 1100
+    ql = rng.integers(1, 5, B)
+    pre = rng.integers(0, 21, B)
+    w = make_from_lengths(rng, kind="prefill", name="many-req", seq_lens=pre + ql, q_lens=ql, Hq=8, Hkv=2, d=64)
+    assert _err(to_f64(run_prefill(w)), oracle.prefill(w)) <= TOL
+
+
+def test_many_items_natural_order():
+    """Fewer requests than that limit but more work items (KV head x query-tile pair) than the
+    sorted order holds."""
+    rng = np.random.default_rng(43)
+    B = 600                          # 600 requests x 2 pairs x 8 KV heads = 9600 items
+    ql = rng.integers(257, 281, B)   # G = 1: two 128-row tiles per pair, two pairs per request
+    pre = rng.integers(0, 21, B)
+    w = make_from_lengths(rng, kind="prefill", name="many-items", seq_lens=pre + ql, q_lens=ql, Hq=8, Hkv=8, d=64)
+    assert _err(to_f64(run_prefill(w)), oracle.prefill(w)) <= TOL
