@@ -83,6 +83,36 @@ __device__ __forceinline__ uint32_t sw128(int r, int c, int rows) {
   return (uint32_t)((c >> 3) * rows * 128 + (r >> 3) * 1024 + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
+// Packed fp32 pairs (f32x2 arithmetic on sm_100-family SMs) and three-input max / min.
+__device__ __forceinline__ uint64_t pk2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void upk2(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+__device__ __forceinline__ float min3(float a, float b, float c) {
+  float r;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // tcgen05.mma with the shared-memory descriptors passed as 32-bit halves.  The start address
 // lives in bits 0-13 of the low half, so a descriptor for base + off is (lo + off / 16, hi)
 // for the operand offsets used here (all smem addresses are below 256 KB).
@@ -556,19 +586,27 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
             for (int c = 0; c < 32; ++c) s[half * 32 + c] = __uint_as_float(raw[c]);
           }
         }
-        // row max of sm_scale * s in base-2 units: max (or min for a negative scale) of the
-        // raw scores times the scale; masked keys are left out here and get p = 0 below
+        // row max of sm_scale * s in base-2 units: max (or min for a negative scale) of the raw
+        // scores times the scale; on tiles that cross the causal edge, keys past this row's
+        // limit are set to the extreme that the max / min ignores, and get p = 0 below
         const bool masked = j >= mask_from;
         const int j0 = j * C::BN;
-        float ext = pos_scale ? -CUDART_INF_F : CUDART_INF_F;
+        const float skip = pos_scale ? -CUDART_INF_F : CUDART_INF_F;
         if (masked) {
 #pragma unroll
-          for (int c = 0; c < C::BN; ++c)
-            if (j0 + c <= limit) ext = pos_scale ? fmaxf(ext, s[c]) : fminf(ext, s[c]);
-        } else {
-#pragma unroll
-          for (int c = 0; c < C::BN; ++c) ext = pos_scale ? fmaxf(ext, s[c]) : fminf(ext, s[c]);
+          for (int c = 0; c < C::BN; ++c) s[c] = (j0 + c <= limit) ? s[c] : skip;
         }
+        float e4[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {  // four independent 3-input chains over 16 scores each
+          float e = skip;
+#pragma unroll
+          for (int c = q * 16; c < q * 16 + 16; c += 2)
+            e = pos_scale ? max3(e, s[c], s[c + 1]) : min3(e, s[c], s[c + 1]);
+          e4[q] = e;
+        }
+        const float ext = pos_scale ? max3(max3(e4[0], e4[1], e4[2]), e4[3], skip)
+                                    : min3(min3(e4[0], e4[1], e4[2]), e4[3], skip);
         const float m_tile = (j0 > limit) ? -CUDART_INF_F : ext * scale;  // -inf: no visible key
         const bool need = m_tile > m_run + C::kRescaleThreshold;  // true on the first visible tile
         if (__any_sync(kFullMask, need)) {
@@ -593,30 +631,40 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
           l_run *= alpha;
           if (need) m_run = m_tile;
         }
-        // P = 2^(scale s - m) as bf16 hi / lo planes in the S columns just read (p = hi + lo
-        // to ~2^-17 relative); P V then runs as two MMAs so P is not rounded to bf16.
+        // P = 2^(scale s - m) as bf16 hi / lo planes in the S columns just read: hi = p with its
+        // low 16 bits cleared (exactly a bf16), lo = bf16(p - hi), so p = hi + lo to ~2^-17
+        // relative; P V then runs as two MMAs and P is not rounded to bf16.  Pairs of scores
+        // go through packed fp32x2 arithmetic.
         const float neg_m = (m_run == -CUDART_INF_F) ? 0.f : -m_run;
-        float lsum = 0.f;
+        const uint64_t sc2 = pk2(scale, scale), nm2 = pk2(neg_m, neg_m), minus1 = pk2(-1.f, -1.f);
+        uint64_t lsum2 = pk2(0.f, 0.f);
 #pragma unroll
         for (int half = 0; half < C::BN / 32; ++half) {
           uint32_t ph[16], pl[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int c0 = half * 32 + 2 * e;
-            float p0 = fast_exp2(fmaf(s[c0], scale, neg_m));
-            float p1 = fast_exp2(fmaf(s[c0 + 1], scale, neg_m));
+            float x0, x1;
+            upk2(fma2(pk2(s[c0], s[c0 + 1]), sc2, nm2), x0, x1);
+            float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
             if (masked) {
               p0 = (j0 + c0 <= limit) ? p0 : 0.f;
               p1 = (j0 + c0 + 1 <= limit) ? p1 : 0.f;
             }
-            lsum += p0 + p1;
-            ph[e] = float2_to_bf16x2_rn(p0, p1);
-            const float2 h = bf16x2_to_float2(ph[e]);
-            pl[e] = float2_to_bf16x2_rn(p0 - h.x, p1 - h.y);
+            const uint64_t p2 = pk2(p0, p1);
+            lsum2 = add2(lsum2, p2);
+            const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+            ph[e] = __byte_perm(b0, b1, 0x7632);  // upper halves: truncated bf16 of p0 (low), p1 (high)
+            float l0, l1;
+            upk2(fma2(pk2(__uint_as_float(b0 & 0xffff0000u), __uint_as_float(b1 & 0xffff0000u)), minus1, p2), l0, l1);
+            pl[e] = float2_to_bf16x2_rn(l0, l1);
           }
           tc::tmem_st16(sb + half * 16, ph);
           tc::tmem_st16(sb + C::BN / 2 + half * 16, pl);
         }
+        float ls0, ls1;
+        upk2(lsum2, ls0, ls1);
+        const float lsum = ls0 + ls1;
         l_run += lsum;
         tc::tmem_st_wait();
         tc::fence_before_sync();
