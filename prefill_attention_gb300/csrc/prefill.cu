@@ -10,25 +10,29 @@
 //     absolute position of the first query row.
 //
 // GB300 design:
-//   * One CTA = one (request, query tile, KV head).  The 128-row MMA tile packs BQ = 128/G
-//     query positions x the G query heads that share the KV head, so each gathered K/V
-//     tile feeds all G heads (row r = position r / G, head r % G).
-//   * S = Q K^T and O += P V run as tcgen05.mma (bf16 in, fp32 accumulate) with both
-//     accumulators in tensor memory: S in BN = 64 columns, O in D columns.  One thread
-//     issues the MMAs; an mbarrier armed by tcgen05.commit reports completion.
-//   * K/V rows are gathered slot by slot with 16-byte cp.async into 128-byte-swizzled
-//     shared-memory tiles (double buffered: tile j+1 loads while tile j is in softmax).
-//     The same tile layout serves K as a K-major operand and V as an MN-major operand.
-//   * Softmax: thread t owns TMEM lane t (one row).  Base-2 online softmax with a lazy
-//     rescale: O and l are rescaled only when a row's max grows by more than 8 (so
-//     unnormalised P stays below 2^8), which keeps the result exact because the same
-//     reference max is used for P, l and O.
-//   * P never goes through shared memory: each thread stores its row of P into tensor
-//     memory as two bf16 planes, hi = bf16(p) and lo = bf16(p - hi), and O accumulates
-//     P_hi V + P_lo V (A operand read from TMEM).  p is thus carried to ~2^-17 relative
-//     instead of bf16's 2^-9, so the only bf16 rounding left is the final output's.
-//   * Two CTAs share an SM (96 KB of tiles each), so one CTA's softmax overlaps the
-//     other's MMAs and loads.
+//   * Persistent CTAs, one per SM.  A work item is (request, two consecutive query tiles,
+//     KV head).  A 128-row MMA tile packs BQ = 128/G query positions x the G query heads
+//     that share the KV head (row r = position r / G, head r % G), so each gathered K/V tile
+//     feeds 2 x 128 rows.  Every CTA computes the same cost-sorted order of the items in its
+//     prologue and takes its share in snake order.
+//   * Warp roles (15 warps): 0-7 softmax and epilogue, four per query tile, thread = row =
+//     TMEM lane; 8-9 issue the MMAs, one thread per query tile; 10-13 gather K/V, one warp
+//     per ring stage; 14 loads the query tiles by TMA (a box of BQ positions x G heads x 64
+//     columns is exactly 128 rows of the swizzled operand layout).
+//   * S = Q K^T and O += P V run as tcgen05.mma (bf16 in, fp32 accumulate); S is double
+//     buffered and O stays in tensor memory.  A K/V ring stage is refilled once the P V that
+//     read its V (and so the S that read its K) has completed.
+//   * Query tiles go through a ring of three slots, so the next item's first tile loads
+//     while the current item runs (its second once the current item's first tile is done).
+//     A finished tile's slot then stages its output rows, which leave as 512-byte coalesced
+//     stores; O in tensor memory is released as soon as it is read.
+//   * Softmax: base-2 online softmax with a lazy rescale (O and l rescaled only when a row's
+//     max grows by more than 8), exact because P, l and O share one reference max.
+//   * P stays in tensor memory as two bf16 planes, hi (p truncated to bf16) and lo =
+//     bf16(p - hi); O accumulates P_hi V + P_lo V, which carries p to ~2^-17 relative
+//     instead of bf16's 2^-9, so the only bf16 rounding left is the output's.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
@@ -45,35 +49,39 @@ struct PrefillCfg {
   static constexpr int NQ = 2;                         // query tiles per work item (consecutive, same request)
   static constexpr int BN = 64;                        // keys per KV tile
   static constexpr int STAGES = 4;                     // K/V ring; one producer warp per stage
-  static constexpr int MMA_WARP = 4 * NQ;              // warps 0-3: softmax of tile A, 4-7: tile B
-  static constexpr int PROD_WARP0 = MMA_WARP + NQ;     // one MMA-issuing warp per query tile
-  static constexpr int THREADS = (PROD_WARP0 + STAGES) * 32;
+  static constexpr int Q_SLOTS = 3;                    // query-tile ring
+  static constexpr int MMA_WARP = 4 * NQ;              // warps 0-3: softmax of tile 0, 4-7: tile 1
+  static constexpr int KV_WARP0 = MMA_WARP + NQ;       // one MMA-issuing warp per query tile
+  static constexpr int Q_WARP = KV_WARP0 + STAGES;     // query-tile loads
+  static constexpr int THREADS = (Q_WARP + 1) * 32;
   static constexpr int CPR = D / 8;                    // 16-byte chunks per row
-  static constexpr int Q_BYTES = M * D * 2;
+  static constexpr int Q_BYTES = M * D * 2;            // one query tile
   static constexpr int KV_BYTES = BN * D * 2;          // one K (or V) tile
-  static constexpr int Q_OFF = 0;                      // NQ tiles
-  static constexpr int K_OFF = Q_OFF + NQ * Q_BYTES;   // STAGES tiles
+  static constexpr int Q_OFF = 0;                      // Q_SLOTS query tiles
+  static constexpr int K_OFF = Q_OFF + Q_SLOTS * Q_BYTES;  // STAGES tiles
   static constexpr int V_OFF = K_OFF + STAGES * KV_BYTES;
   static constexpr int BAR_OFF = V_OFF + STAGES * KV_BYTES;
-  // barriers: kv_full[STAGES], kv_empty[STAGES], q_full, q_free, s_full[NQ][2], p_full[NQ][2],
-  // o_done[NQ], o_free[NQ], fin
-  static constexpr int NBAR = 2 * STAGES + 2 + 6 * NQ + 1;
-  // work order: items sorted by cost, and the per-request item offsets (when they fit)
-  static constexpr int MAX_SORT_ITEMS = 8192;
+  // barriers: kv_full, kv_empty [STAGES]; q_full, q_free [Q_SLOTS]; s_full, p_full [NQ][2];
+  // o_done, o_free [NQ]; fin.  Then the error flag and TMEM address.
+  static constexpr int NBAR = 2 * STAGES + 2 * Q_SLOTS + 6 * NQ + 1;
+  static constexpr int LIST_OFF = (BAR_OFF + NBAR * 8 + 8 + 15) & ~15;
+  // this CTA's items in order, as (request, pair within the request, KV head)
+  static constexpr int MAX_CTA_ITEMS = 128;
+  static constexpr int SMEM_BYTES = LIST_OFF + MAX_CTA_ITEMS * 12;
+  // prologue scratch in the K/V ring: per-request pair offsets, 256 counts, keys, order
   static constexpr int MAX_SORT_REQS = 1024;
-  static constexpr int ORD_OFF = BAR_OFF + NBAR * 8 + 16;
-  static constexpr int PST_OFF = ORD_OFF + MAX_SORT_ITEMS * 2;
-  static constexpr int SMEM_BYTES = PST_OFF + (MAX_SORT_REQS + 1) * 4;
+  static constexpr int MAX_SORT_PAIRS = 8192;
   static constexpr uint32_t TMEM_TILE = 256;           // tile t: O at 256 t, S buffers at 256 t + D + {0, BN}
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr int Q_IT = NQ * M * CPR / (32 * STAGES);  // cp.async per producer lane for its share of Q
-  static constexpr int KV_IT = BN * CPR / 32;          // cp.async per producer lane per K (and per V) tile
+  static constexpr int KV_IT = BN * CPR / 32;          // cp.async per producer lane per K (or V) tile
+  static constexpr int RPI = 32 / CPR;                 // output rows per coalesced warp store
   static constexpr uint32_t IDESC_S = tc::idesc_bf16_f32(M, BN, false, false);   // K-major A and B
   static constexpr uint32_t IDESC_PV = tc::idesc_bf16_f32(M, D, false, true);    // B (V) MN-major
   static constexpr float kRescaleThreshold = 8.f;     // log2 units
-  static_assert((Q_OFF | K_OFF | V_OFF | Q_BYTES) % 1024 == 0, "swizzle atoms must be 1024-byte aligned");
+  static_assert((Q_OFF | K_OFF | V_OFF | Q_BYTES | KV_BYTES) % 1024 == 0, "swizzle atoms must be 1024-byte aligned");
   static_assert(D + 2 * BN <= (int)TMEM_TILE, "tensor-memory budget per tile");
-  static_assert(Q_IT * 32 * STAGES == NQ * M * CPR, "producers split the query tiles evenly");
+  static_assert(KV_IT * 32 == BN * CPR && D % 64 == 0, "whole warp iterations, whole 128-byte column blocks");
+  static_assert((MAX_SORT_REQS + 1 + 256) * 4 + MAX_SORT_PAIRS * 4 <= 2 * STAGES * KV_BYTES, "prologue scratch");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
@@ -161,23 +169,11 @@ __device__ __forceinline__ void fill_item(const PrefillParams& p, int b, int pr,
   it.n_tiles = (it.cb + last + 1 + BN - 1) / BN;
 }
 
-// Decodes item w.  With `pst` (per-request first pair index, in shared memory) a binary
-// search; without it a warp-parallel prefix scan of per-request pair counts (all 32 lanes
-// call it and get the same answer).  False once w is past the last item.
+// Decodes item w of the natural order by a warp-parallel prefix scan of the per-request pair
+// counts (all 32 lanes call it and get the same answer).  False once w is past the last item.
 template <int BQ2, int BQ, int BN>
-__device__ __forceinline__ bool decode_item(const PrefillParams& p, int w, int lane, PrefillItem& it,
-                                            const int* pst) {
+__device__ __forceinline__ bool scan_item(const PrefillParams& p, int w, int lane, PrefillItem& it) {
   const int pair_idx = w / p.num_kv_heads;
-  if (pst != nullptr) {
-    if (pair_idx >= pst[p.batch]) return false;
-    int l = 0, h = p.batch - 1;  // largest b with pst[b] <= pair_idx
-    while (l < h) {
-      const int m = (l + h + 1) >> 1;
-      if (pst[m] <= pair_idx) l = m; else h = m - 1;
-    }
-    fill_item<BQ2, BQ, BN>(p, l, pair_idx - pst[l], w % p.num_kv_heads, it);
-    return true;
-  }
   int acc = 0;
   for (int base = 0; base < p.batch; base += 32) {
     const int bb = base + lane;
@@ -202,8 +198,19 @@ __device__ __forceinline__ bool decode_item(const PrefillParams& p, int w, int l
   return false;
 }
 
+// Largest b with pst[b] <= x (pst ascending, pst[0] = 0).
+__device__ __forceinline__ int upper_index(const int* pst, int n, int x) {
+  int l = 0, h = n - 1;
+  while (l < h) {
+    const int m = (l + h + 1) >> 1;
+    if (pst[m] <= x) l = m; else h = m - 1;
+  }
+  return l;
+}
+
 template <int D, int G>
-__global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(const PrefillParams p) {
+__global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(const PrefillParams p,
+                                                                                const __grid_constant__ CUtensorMap q_map) {
   using C = PrefillCfg<D, G>;
   constexpr int BQ2 = C::NQ * C::BQ;
   extern __shared__ __align__(1024) unsigned char smem[];
@@ -214,8 +221,12 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
   const uint32_t bars = sbase + C::BAR_OFF;
   auto kv_full = [&](int s) { return bars + 8u * s; };
   auto kv_empty = [&](int s) { return bars + 8u * (C::STAGES + s); };
-  const uint32_t q_full = bars + 8u * (2 * C::STAGES), q_free = q_full + 8;
-  const uint32_t tb = q_free + 8;  // per-tile barriers
+  // query tile number u (counted over the CTA's items, in order) lives in slot u % Q_SLOTS
+  auto q_full = [&](int u) { return bars + 8u * (2 * C::STAGES + u % C::Q_SLOTS); };
+  auto q_free = [&](int u) { return bars + 8u * (2 * C::STAGES + C::Q_SLOTS + u % C::Q_SLOTS); };
+  auto q_par = [&](int u) { return (uint32_t)((u / C::Q_SLOTS) & 1); };
+  auto q_slot = [&](int u) { return sbase + C::Q_OFF + (u % C::Q_SLOTS) * C::Q_BYTES; };
+  const uint32_t tb = bars + 8u * (2 * C::STAGES + 2 * C::Q_SLOTS);  // per-tile barriers
   // S / P of the g-th KV tile of query tile t live in buffer g & 1 (g counts over all items);
   // each buffer has its own barriers, so no waiter is ever more than one phase behind.
   auto s_full = [&](int t, int buf) { return tb + 8u * (2 * t + buf); };
@@ -230,8 +241,12 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
       tc::mbar_init(kv_full(s), 32);
       tc::mbar_init(kv_empty(s), C::NQ);  // one commit per MMA thread
     }
-    tc::mbar_init(q_full, 32 * C::STAGES);
-    tc::mbar_init(q_free, C::NQ);
+    for (int u = 0; u < C::Q_SLOTS; ++u) {
+      tc::mbar_init(q_full(u), 1);  // arrive + TMA transaction bytes
+      // lane 0 of the four softmax warps of the tile (after its output rows left the slot) and
+      // every MMA thread (once it has seen the tile)
+      tc::mbar_init(q_free(u), 4 + C::NQ);
+    }
     for (int t = 0; t < C::NQ; ++t) {
       for (int buf = 0; buf < 2; ++buf) {
         tc::mbar_init(s_full(t, buf), 1);
@@ -253,10 +268,16 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
   // ---- work order, computed identically by every CTA (no cross-CTA communication): items
   // sorted by cost (KV tiles x query tiles, descending; ties by index) and dealt out in snake
   // order (CTA c takes sorted positions c, 2G-1-c, 2G+c, ... for G CTAs), which keeps the
-  // per-CTA totals within a few percent of each other.  Problems too large for the tables
-  // fall back to the natural item order.
-  uint16_t* order = reinterpret_cast<uint16_t*>(smem + C::ORD_OFF);
-  int* pst = reinterpret_cast<int*>(smem + C::PST_OFF);
+  // per-CTA totals within a few percent of each other.  The KV heads of one query-tile pair
+  // cost the same and have consecutive indices, so the pairs are sorted and then expanded.
+  // Each CTA keeps only its own list; problems too large for it use the natural order.
+  int* list = reinterpret_cast<int*>(smem + C::LIST_OFF);
+  int* pst = reinterpret_cast<int*>(smem + C::K_OFF);  // scratch: the K/V ring is not in use yet
+  int* cnt = pst + C::MAX_SORT_REQS + 1;
+  uint16_t* key = reinterpret_cast<uint16_t*>(cnt + 256);
+  uint16_t* order = key + C::MAX_SORT_PAIRS;
+  const int H = p.num_kv_heads;
+  int per_cta = 0;
   bool sorted = p.batch <= C::MAX_SORT_REQS;
   if (sorted) {
     if (warp == 0) {  // pst[b] = first pair index of request b, pst[B] = number of pairs
@@ -277,37 +298,31 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
       if (lane == 0) pst[p.batch] = acc;
     }
     __syncthreads();
-    sorted = (int64_t)pst[p.batch] * p.num_kv_heads <= C::MAX_SORT_ITEMS;
+    const int n_pairs = pst[p.batch];
+    per_cta = (int)(((int64_t)n_pairs * H + gridDim.x - 1) / gridDim.x);
+    sorted = n_pairs <= C::MAX_SORT_PAIRS && per_cta <= C::MAX_CTA_ITEMS;
   }
-  const int n_items = sorted ? pst[p.batch] * p.num_kv_heads : 0;
   if (sorted) {
-    uint16_t* key = reinterpret_cast<uint16_t*>(smem + C::K_OFF);  // scratch: the KV ring is not in use yet
-    int* cnt = reinterpret_cast<int*>(smem + C::V_OFF);               // [256] bucket counts, then offsets
-    for (int w = tid; w < n_items; w += C::THREADS) {
-      const int pair_idx = w / p.num_kv_heads;
-      int l = 0, h = p.batch - 1;
-      while (l < h) {
-        const int m = (l + h + 1) >> 1;
-        if (pst[m] <= pair_idx) l = m; else h = m - 1;
-      }
+    const int n_pairs = pst[p.batch];
+    for (int w = tid; w < n_pairs; w += C::THREADS) {
+      const int b = upper_index(pst, p.batch, w);
       PrefillItem it;
-      fill_item<BQ2, C::BQ, C::BN>(p, l, pair_idx - pst[l], 0, it);
+      fill_item<BQ2, C::BQ, C::BN>(p, b, w - pst[b], 0, it);
       int c = 2;  // fixed part of an item, in KV-tile units
       for (int t = 0; t < it.nq; ++t) c += (it.cb + min(it.q_len, it.first0 + (t + 1) * C::BQ) + C::BN - 1) / C::BN;
       key[w] = (uint16_t)(255 - min(c, 255));  // ascending key = descending cost
     }
     for (int i = tid; i < 256; i += C::THREADS) cnt[i] = 0;
     __syncthreads();
-    if (warp == 0) {  // stable counting sort, one warp, chunks of 32 items in index order
-      for (int base = 0; base < n_items; base += 32) {
+    if (warp == 0) {  // stable counting sort of the pairs, one warp, chunks of 32 in index order
+      for (int base = 0; base < n_pairs; base += 32) {
         const int w = base + lane;
-        const int k = (w < n_items) ? key[w] : -1;
+        const int k = (w < n_pairs) ? key[w] : -1;
         const unsigned peers = __match_any_sync(kFullMask, k);
-        if (w < n_items && (peers & ((1u << lane) - 1u)) == 0u) cnt[k] += __popc(peers);
+        if (w < n_pairs && (peers & ((1u << lane) - 1u)) == 0u) cnt[k] += __popc(peers);
         __syncwarp();
       }
-      int run = 0;  // exclusive scan of the 256 counts, 8 per lane
-      int v[8];
+      int v[8];  // exclusive scan of the 256 counts, 8 per lane
 #pragma unroll
       for (int i = 0; i < 8; ++i) v[i] = cnt[lane * 8 + i];
       int tot = 0;
@@ -319,33 +334,52 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
         const int y = __shfl_up_sync(kFullMask, inc, o);
         if (lane >= o) inc += y;
       }
-      run = inc - tot;
+      int run = inc - tot;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         cnt[lane * 8 + i] = run;
         run += v[i];
       }
       __syncwarp();
-      for (int base = 0; base < n_items; base += 32) {
+      for (int base = 0; base < n_pairs; base += 32) {
         const int w = base + lane;
-        const int k = (w < n_items) ? key[w] : -1;
+        const int k = (w < n_pairs) ? key[w] : -1;
         const unsigned peers = __match_any_sync(kFullMask, k);
-        if (w < n_items) order[cnt[k] + __popc(peers & ((1u << lane) - 1u))] = (uint16_t)w;
+        if (w < n_pairs) order[cnt[k] + __popc(peers & ((1u << lane) - 1u))] = (uint16_t)w;
         __syncwarp();
-        if (w < n_items && (peers & ((1u << lane) - 1u)) == 0u) cnt[k] += __popc(peers);
+        if (w < n_pairs && (peers & ((1u << lane) - 1u)) == 0u) cnt[k] += __popc(peers);
         __syncwarp();
       }
     }
     __syncthreads();
+    for (int k = tid; k < per_cta; k += C::THREADS) {  // this CTA's sorted positions
+      const int c = blockIdx.x, nc = gridDim.x;
+      const int pos = k * nc + ((k & 1) ? nc - 1 - c : c);
+      int* e = list + 3 * k;
+      if (pos < n_pairs * H) {
+        const int pair = order[pos / H];
+        const int b = upper_index(pst, p.batch, pair);
+        e[0] = b;
+        e[1] = pair - pst[b];
+        e[2] = pos % H;
+      } else {
+        e[0] = -1;
+      }
+    }
+    __syncthreads();
   }
-  // the k-th item of this CTA, or -1
-  auto item_at = [&](int k) -> int {
-    const int r = k, c = blockIdx.x;
-    const int pos = r * (int)gridDim.x + ((r & 1) ? (int)gridDim.x - 1 - c : c);
-    if (sorted) return pos < n_items ? (int)order[pos] : -1;
-    return pos;  // natural order; decode_item reports the end
+  // the k-th item of this CTA (called by all 32 lanes of a warp); false past the last one
+  auto get_item = [&](int k, PrefillItem& it) -> bool {
+    if (sorted) {
+      if (k >= per_cta) return false;
+      const int* e = list + 3 * k;
+      if (e[0] < 0) return false;
+      fill_item<BQ2, C::BQ, C::BN>(p, e[0], e[1], e[2], it);
+      return true;
+    }
+    const int c = blockIdx.x, nc = gridDim.x;
+    return scan_item<BQ2, C::BQ, C::BN>(p, k * nc + ((k & 1) ? nc - 1 - c : c), lane, it);
   };
-  const int* pst_or_null = sorted ? pst : nullptr;
 
   // Bounded wait, agreed by the whole warp (so warp-collective tcgen05 ops after it stay
   // converged); a timeout, or an error raised elsewhere, makes every later wait fail.
@@ -356,68 +390,75 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
     return ok;
   };
 
-  if (warp >= C::PROD_WARP0) {
-    // ======================= producers: warp PROD_WARP0 + s fills stage s with every KV tile
-    //                         g = s mod STAGES (g counts over all items) and loads a quarter
-    //                         of each item's query rows
-    const int st = warp - C::PROD_WARP0;
+  if (warp == C::Q_WARP) {
+    // ======================= query tiles by TMA, in order, each as soon as the tile that
+    //                         used its slot before has left it.  Rows past the request's end
+    //                         hold other requests' queries (never stored) or, past the last
+    //                         row, zeros
+    bool ok = true;
+    int u = 0;  // query tiles so far
+    PrefillItem it;
+    for (int n_item = 0; ok; ++n_item) {
+      if (!get_item(n_item, it)) break;
+      for (int t = 0; ok && t < it.nq; ++t, ++u) {
+        if (u >= C::Q_SLOTS && !(ok = wait_or_fail(q_free(u), q_par(u) ^ 1u))) break;
+        if (lane == 0) {
+          tc::mbar_arrive_expect_tx(q_full(u), (uint32_t)C::Q_BYTES);
+          for (int cb = 0; cb < D / 64; ++cb)
+            tc::tma_load_3d(q_slot(u) + cb * (C::M * 128), &q_map, cb * 64, it.kvh * G,
+                            it.q0 + it.first0 + t * C::BQ, q_full(u));
+        }
+        __syncwarp();
+      }
+    }
+  } else if (warp >= C::KV_WARP0) {
+    // ======================= K/V gathers: warp KV_WARP0 + s fills stage s with every KV tile
+    //                         g = s mod STAGES (g counts over all items)
+    const int st = warp - C::KV_WARP0;
     const size_t head_stride = (size_t)p.num_kv_heads * D;
     const unsigned nslots = (unsigned)p.num_slots;
+    const uint32_t kdst = sbase + C::K_OFF + st * C::KV_BYTES, vdst = sbase + C::V_OFF + st * C::KV_BYTES;
     int g_base = 0;  // global index of the current item's KV tile 0
     bool ok = true;
     PrefillItem it;
     for (int n_item = 0; ok; ++n_item) {
-      const int w = item_at(n_item);
-      if (w < 0 || !decode_item<BQ2, C::BQ, C::BN>(p, w, lane, it, pst_or_null)) break;
+      if (!get_item(n_item, it)) break;
       const int kvh = it.kvh;
       const int32_t* r2t = p.req_to_token + (size_t)it.b * p.r2t_stride;
       const int kv_end = min(it.cb + min(it.q_len, it.first0 + BQ2), it.cb + it.q_len);
-      // query rows (position, head) of both tiles; this warp takes chunks st, st + STAGES, ...
-      if (n_item > 0 && !(ok = wait_or_fail(q_free, (uint32_t)((n_item - 1) & 1)))) break;
-      {
-        const uint16_t* qbase = p.q + ((size_t)it.q0 * p.num_qo_heads + (size_t)kvh * G) * D;
-#pragma unroll 4
-        for (int i = 0; i < C::Q_IT; ++i) {
-          const int flat = (i * C::STAGES + st) * 32 + lane;       // over both tiles' chunks
-          const int t = flat / (C::M * C::CPR), rem = flat % (C::M * C::CPR);
-          const int row = rem / C::CPR, c = rem % C::CPR;
-          const int rqi = it.first0 + t * C::BQ + row / G;
-          const bool valid = t < it.nq && rqi < it.q_len && rqi < it.first0 + (t + 1) * C::BQ;
-          const uint16_t* src = valid ? qbase + ((size_t)rqi * p.num_qo_heads + row % G) * D + c * 8 : p.q;
-          cp_async16(sbase + C::Q_OFF + t * C::Q_BYTES + sw128(row, c, C::M), src, valid);
-        }
-        cp_async_commit();
-        cp_async_wait<0>();
-        tc::fence_proxy_async_smem();
-        tc::mbar_arrive(q_full);
-      }
-      // this warp's KV tiles of the item
       const int j_first = (st - g_base % C::STAGES + C::STAGES) % C::STAGES;
       auto ids_of = [&](int j, int half) {  // slot id of key 32 half + lane of item tile j, or -1
         const int key = j * C::BN + half * 32 + lane;
         return (j < it.n_tiles && key < kv_end) ? ldg_nc_i32(r2t + key) : -1;
       };
-      int id0 = ids_of(j_first, 0), id1 = ids_of(j_first, 1);
-      for (int j = j_first; j < it.n_tiles; j += C::STAGES) {
-        const int g = g_base + j;
-        if (g >= C::STAGES && !(ok = wait_or_fail(kv_empty(st), (uint32_t)(((g / C::STAGES) - 1) & 1)))) break;
-        const uint32_t kdst = sbase + C::K_OFF + st * C::KV_BYTES, vdst = sbase + C::V_OFF + st * C::KV_BYTES;
+      // one K/V tile: row `key` comes from the slot id held by lane key % 32 of id0 (keys
+      // 0-31) or id1 (keys 32-63); padding and out-of-range ids read as zeros.  K and V share
+      // each lane's address arithmetic (one loop over both costs the softmax warps on the
+      // same schedulers noticeably fewer issue slots than two)
+      auto gather = [&](int id0, int id1) {
 #pragma unroll 8
         for (int i = 0; i < C::KV_IT; ++i) {
           const int flat = i * 32 + lane;
           const int key = flat / C::CPR, c = flat % C::CPR;  // key < 32 exactly for the first half of `i`
           const int id = __shfl_sync(kFullMask, (i < C::KV_IT / 2) ? id0 : id1, key & 31);
-          const bool valid = (unsigned)id < nslots;  // padding and out-of-range ids read as zeros
+          const bool valid = (unsigned)id < nslots;
           const size_t off = valid ? (size_t)id * head_stride + (size_t)kvh * D + c * 8 : 0;
           const uint32_t o = sw128(key, c, C::BN);
           cp_async16(kdst + o, p.k_pool + off, valid);
           cp_async16(vdst + o, p.v_pool + off, valid);
         }
         cp_async_commit();
+      };
+      int id0 = ids_of(j_first, 0), id1 = ids_of(j_first, 1);
+      for (int j = j_first; j < it.n_tiles; j += C::STAGES) {
+        const int g = g_base + j;
+        const uint32_t par = (uint32_t)(((g / C::STAGES) - 1) & 1);  // phase of tile g - STAGES
+        if (g >= C::STAGES && !(ok = wait_or_fail(kv_empty(st), par))) break;
+        gather(id0, id1);
         id0 = ids_of(j + C::STAGES, 0);  // next tile of this stage: its slot ids load meanwhile
         id1 = ids_of(j + C::STAGES, 1);
         cp_async_wait<0>();
-        tc::fence_proxy_async_smem();  // the tensor core reads the tile through the async proxy
+        tc::fence_proxy_async_smem();  // the tensor core reads the tiles through the async proxy
         tc::mbar_arrive(kv_full(st));
       }
       g_base += it.n_tiles;
@@ -428,31 +469,32 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
     // tcgen05.mma issue runs nearly in step with execution, so whatever the issuing thread
     // does between MMAs (waits, fences, commits) idles the tensor core unless another thread
     // has MMAs queued: the two query tiles therefore have their own issuing threads, and the
-    // barrier each group needs is tested (without blocking) in the middle of the group before
-    // it.  Per KV tile j: S_t(j+1) = Q_t K_{j+1}^T into the other S buffer, then
+    // barriers each group needs are tested (without blocking) in the middle of the group
+    // before it.  Per KV tile j: S_t(j+1) = Q_t K_{j+1}^T into the other S buffer, then
     // O_t += P_t(j) V_j once the softmax warps of tile t have written P_t(j).  Both threads
-    // commit every KV tile (after it has landed) and every item's Q, used or not, so the shared
-    // barriers count two arrivals per phase.
+    // release every KV tile (after it has landed), used or not, so the shared empty barriers
+    // count two arrivals per phase.
     const int t = warp - C::MMA_WARP;
-    // descriptor halves of Q tile t, K stage 0 (K-major) and V stage 0 (MN-major)
-    const uint64_t qd0 = tc::smem_desc_sw128(sbase + C::Q_OFF + t * C::Q_BYTES, 16, 1024);
+    // descriptor halves of query slot 0, K stage 0 (K-major) and V stage 0 (MN-major)
+    const uint64_t qd0 = tc::smem_desc_sw128(sbase + C::Q_OFF, 16, 1024);
     const uint64_t kd0 = tc::smem_desc_sw128(sbase + C::K_OFF, 16, 1024);
     const uint64_t vd0 = tc::smem_desc_sw128(sbase + C::V_OFF, C::BN * 128, 1024);
-    const uint32_t q_lo = (uint32_t)qd0, q_hi = (uint32_t)(qd0 >> 32);
-    const uint32_t k_lo = (uint32_t)kd0, k_hi = (uint32_t)(kd0 >> 32);
-    const uint32_t v_lo = (uint32_t)vd0, v_hi = (uint32_t)(vd0 >> 32);
+    const uint32_t q_hi = (uint32_t)(qd0 >> 32), k_hi = (uint32_t)(kd0 >> 32), v_hi = (uint32_t)(vd0 >> 32);
+    const uint32_t k_lo = (uint32_t)kd0, v_lo = (uint32_t)vd0;
     const uint32_t od = tmem + t * C::TMEM_TILE;  // O of tile t; S / P buffers at od + D + {0, BN}
     int g_base = 0;   // global index of the item's KV tile 0
     int gs = 0;       // KV tiles of tile t so far (S buffer / phase counter)
     int n_used = 0;   // items so far that had tile t (o_done / o_free phases)
+    int u0 = 0;       // query tiles of the items before this one
+    int uw = 0;       // query tiles waited for so far (every thread waits for all, in order)
     bool ok = true;
     PrefillItem it;
     for (int n_item = 0; ok; ++n_item) {
-      const int w = item_at(n_item);
-      if (w < 0 || !decode_item<BQ2, C::BQ, C::BN>(p, w, lane, it, pst_or_null)) break;
+      if (!get_item(n_item, it)) break;
       if (lane == 0) {
         const int nk = (t < it.nq) ? (it.cb + min(it.q_len, it.first0 + (t + 1) * C::BQ) + C::BN - 1) / C::BN : 0;
         const int n = it.n_tiles;
+        const uint32_t q_lo = (uint32_t)qd0 + (uint32_t)((((u0 + t) % C::Q_SLOTS) * C::Q_BYTES) >> 4);
         auto wait_one = [&](uint32_t bar, uint32_t parity, bool ready) {  // blocking only if not pre-tested ready
           if (ok && !ready && !tc::mbar_wait(bar, parity)) {
             *err = 1;
@@ -460,7 +502,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
           }
           tc::fence_after_sync();
         };
-        auto kv_ready = [&](int j) { return kv_full((g_base + j) % C::STAGES); };
+        auto stage = [&](int j) { return (g_base + j) % C::STAGES; };
         auto kv_par = [&](int j) { return (uint32_t)(((g_base + j) / C::STAGES) & 1); };
         auto sbuf = [&](int j) { return (gs + j) & 1; };
         auto s_par = [&](int j) { return (uint32_t)(((gs + j) >> 1) & 1); };
@@ -468,7 +510,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
         // Descriptors are formed before the first MMA so the MMAs issue back to back.
         auto issue_s = [&](int j, uint32_t nb, uint32_t np) -> bool {
           const uint32_t sd = od + D + sbuf(j) * C::BN;
-          const uint32_t klo = k_lo + (uint32_t)(((g_base + j) % C::STAGES) * C::KV_BYTES >> 4);
+          const uint32_t klo = k_lo + (uint32_t)((stage(j) * C::KV_BYTES) >> 4);
           uint32_t al[D / 16], bl[D / 16];
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
@@ -488,7 +530,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
         };
         auto issue_pv = [&](int j, uint32_t nb, uint32_t np) -> bool {
           const uint32_t pa = od + D + sbuf(j) * C::BN;  // P hi in [0, 32), lo in [32, 64)
-          const uint32_t vlo = v_lo + (uint32_t)(((g_base + j) % C::STAGES) * C::KV_BYTES >> 4);
+          const uint32_t vlo = v_lo + (uint32_t)((stage(j) * C::KV_BYTES) >> 4);
           uint32_t bl[C::BN / 16];
 #pragma unroll
           for (int kk = 0; kk < C::BN / 16; ++kk) bl[kk] = vlo + (uint32_t)((kk * 16 * 128) >> 4);
@@ -501,41 +543,49 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
             mma_ts_h(od, pa + C::BN / 2 + kk * 8, bl[kk], v_hi, C::IDESC_PV, 1u);
             if (kk == 1) r = nb != 0u && tc::mbar_test(nb, np);
           }
+          tc::mma_commit(kv_empty(stage(j)));  // the stage may be refilled once P V_j is done
           if (j == nk - 1) tc::mma_commit(o_done(t));
           return r;
         };
 
-        wait_one(q_full, (uint32_t)(n_item & 1), false);
+        // the query tiles are waited for in order, this thread's own and the other's, up to
+        // its own (so no wait is ever more than one phase of a slot away); a tile seen is
+        // released at once: the tensor core's reads of it are covered by its epilogue's
+        // o_done wait
+        for (; ok && uw < u0 + min(t + 1, it.nq); ++uw) {
+          wait_one(q_full(uw), q_par(uw), false);
+          tc::mbar_arrive(q_free(uw));
+        }
         bool ready = false;  // pre-test result for the next wait
         if (nk > 0) {
-          wait_one(kv_ready(0), kv_par(0), false);
-          ready = issue_s(0, nk > 1 ? kv_ready(1) : 0u, kv_par(1));
+          wait_one(kv_full(stage(0)), kv_par(0), false);
+          ready = issue_s(0, nk > 1 ? kv_full(stage(1)) : 0u, kv_par(1));
         }
-        if (nk <= 1) tc::mma_commit(q_free);  // every S of tile t in this item issued
         for (int j = 0; ok && j < n; ++j) {
           if (j < nk) {
             if (j + 1 < nk) {  // S of KV tile j + 1 into the other buffer
-              wait_one(kv_ready(j + 1), kv_par(j + 1), ready);
+              wait_one(kv_full(stage(j + 1)), kv_par(j + 1), ready);
               ready = issue_s(j + 1, p_full(t, sbuf(j)), s_par(j));
-              if (j + 2 == nk) tc::mma_commit(q_free);
             }
             // O_t += P_t(j) V_j (the item's first P V overwrites O once the epilogue of the
             // item before has read it)
             if (j == 0 && n_used > 0) wait_one(o_free(t), (uint32_t)((n_used - 1) & 1), false);
             wait_one(p_full(t, sbuf(j)), s_par(j), ready);
-            ready = issue_pv(j, j + 2 < nk ? kv_ready(j + 2) : 0u, kv_par(j + 2));
+            ready = issue_pv(j, j + 2 < nk ? kv_full(stage(j + 2)) : 0u, kv_par(j + 2));
+          } else {
+            // a KV tile this query tile does not need is still released by this thread, but
+            // only once it has landed: otherwise the release could run ahead and count toward
+            // an earlier phase of the stage's empty barrier
+            wait_one(kv_full(stage(j)), kv_par(j), false);
+            tc::mma_commit(kv_empty(stage(j)));
           }
-          // a KV tile this query tile does not need still gets this thread's commit, but only
-          // once it has landed: otherwise the commit could run ahead and count toward an
-          // earlier phase of the stage's empty barrier
-          if (j >= nk) wait_one(kv_ready(j), kv_par(j), false);
-          tc::mma_commit(kv_empty((g_base + j) % C::STAGES));  // this thread's MMAs on the stage are done
         }
         gs += nk;
         if (nk > 0) ++n_used;
       }
       ok = __shfl_sync(kFullMask, ok ? 1 : 0, 0) != 0;
       g_base += it.n_tiles;
+      u0 += it.nq;
     }
     if (lane == 0) {
       // every MMA this thread issued has completed before the CTA may release tensor memory
@@ -553,11 +603,13 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
     const bool pos_scale = scale >= 0.f;
     int gs = 0, n_used = 0;  // same counters as the MMA thread, for this query tile
     int g_base = 0;          // global index of the item's KV tile 0
+    int u0 = 0;              // query tiles of the items before this one
     bool ok = true;
     PrefillItem it;
     for (int n_item = 0; ok; ++n_item) {
-      const int w = item_at(n_item);
-      if (w < 0 || !decode_item<BQ2, C::BQ, C::BN>(p, w, lane, it, pst_or_null)) break;
+      if (!get_item(n_item, it)) break;
+      const int u = u0 + t;  // this tile's query-tile number
+      u0 += it.nq;
       if (t >= it.nq) {
         g_base += it.n_tiles;
         continue;
@@ -565,8 +617,6 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
       const int qf = it.first0 + t * C::BQ, ql = min(it.q_len, qf + C::BQ) - 1;
       const int n_keys = (it.cb + ql + 1 + C::BN - 1) / C::BN;
       const int qi = qf + row / G;                       // this thread's query position
-      const int g = row % G;
-      const bool row_valid = qi <= ql;
       const int limit = it.cb + min(qi, ql);             // last key this row attends
       const int mask_from = (it.cb + qf + 1) / C::BN;    // tiles >= this one hold a masked key for some row
       float m_run = -CUDART_INF_F, l_run = 0.f;
@@ -672,30 +722,48 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
       }
       if (!ok) break;
 
-      // ---- epilogue: O / l -> bf16 rows of out, once the last P V of this tile has landed
+      // ---- epilogue, once the last P V of this tile has landed: O / l as bf16 into the
+      // tile's query slot (free: every S that read it is complete), release O, then the warp
+      // writes its 32 rows out with coalesced stores and releases the slot
       ok = wait_or_fail(o_done(t), (uint32_t)(n_used & 1));
       tc::fence_after_sync();
+      tc::fence_proxy_async_smem();  // the tensor core's reads of this buffer precede the writes below
       const float inv = (ok && !*err) ? 1.f / l_run : CUDART_NAN_F;   // a timed-out wait poisons the tile
-      uint16_t* orow = p.out + ((size_t)(it.q0 + qi) * p.num_qo_heads + (size_t)it.kvh * G + g) * D;
+      const uint32_t stg = q_slot(u);
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
         tc::tmem_ld32(o_col + cc * 32, o);
         tc::tmem_ld_wait();
-        if (row_valid) {
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint4 v;
-            v.x = float2_to_bf16x2_rn(__uint_as_float(o[q4 * 8 + 0]) * inv, __uint_as_float(o[q4 * 8 + 1]) * inv);
-            v.y = float2_to_bf16x2_rn(__uint_as_float(o[q4 * 8 + 2]) * inv, __uint_as_float(o[q4 * 8 + 3]) * inv);
-            v.z = float2_to_bf16x2_rn(__uint_as_float(o[q4 * 8 + 4]) * inv, __uint_as_float(o[q4 * 8 + 5]) * inv);
-            v.w = float2_to_bf16x2_rn(__uint_as_float(o[q4 * 8 + 6]) * inv, __uint_as_float(o[q4 * 8 + 7]) * inv);
-            reinterpret_cast<uint4*>(orow + cc * 32)[q4] = v;
-          }
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint4 v;
+          v.x = float2_to_bf16x2_rn(__uint_as_float(o[q4 * 8 + 0]) * inv, __uint_as_float(o[q4 * 8 + 1]) * inv);
+          v.y = float2_to_bf16x2_rn(__uint_as_float(o[q4 * 8 + 2]) * inv, __uint_as_float(o[q4 * 8 + 3]) * inv);
+          v.z = float2_to_bf16x2_rn(__uint_as_float(o[q4 * 8 + 4]) * inv, __uint_as_float(o[q4 * 8 + 5]) * inv);
+          v.w = float2_to_bf16x2_rn(__uint_as_float(o[q4 * 8 + 6]) * inv, __uint_as_float(o[q4 * 8 + 7]) * inv);
+          sts128(stg + sw128(row, cc * 4 + q4, C::M), v);
         }
       }
       tc::fence_before_sync();
       tc::mbar_arrive(o_free(t));  // O of this tile may be overwritten by the next item
+      __syncwarp();
+      {
+        const int n_valid = (ql - qf + 1) * G;  // rows [0, n_valid) of the tile are real positions
+        const int r0 = (warp & 3) * 32;
+        uint16_t* obase = p.out + ((size_t)(it.q0 + qf) * p.num_qo_heads + (size_t)it.kvh * G) * D;
+#pragma unroll 4
+        for (int i = 0; i < C::CPR; ++i) {  // RPI rows (512 contiguous bytes when G >= RPI) per store
+          const int r = r0 + i * C::RPI + lane / C::CPR, c = lane % C::CPR;
+          if (r < n_valid) {
+            const uint4 v = lds128(stg + sw128(r, c, C::M));
+            *reinterpret_cast<uint4*>(obase + ((size_t)(r / G) * p.num_qo_heads + r % G) * D + c * 8) = v;
+          }
+        }
+      }
+      tc::fence_proxy_async_smem();  // the next TMA write of this buffer follows these accesses
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(q_free(u));
       gs += n_keys;
       ++n_used;
       g_base += it.n_tiles;
@@ -710,6 +778,20 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
   }
 }
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link against libcuda)
+PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult status{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &status) !=
+            cudaSuccess ||
+        status != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
 template <int D, int G>
 cudaError_t launch_prefill_t(const PrefillParams& p, cudaStream_t stream) {
   using C = PrefillCfg<D, G>;
@@ -720,11 +802,23 @@ cudaError_t launch_prefill_t(const PrefillParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  // persistent CTAs, one per SM, each walking items blockIdx.x, + gridDim.x, ...
+  // persistent CTAs, one per SM, each walking its share of the items
   const int64_t items = (int64_t)p.num_q_tiles * p.num_kv_heads;
   const int grid = (int)(items < p.num_ctas ? items : p.num_ctas);
   if (grid <= 0) return cudaSuccess;
-  prefill_kernel<D, G><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(p);
+  // q as [total_q][Hq][D] bf16; one box = BQ positions x the G heads of a KV head x 64 columns
+  const PFN_cuTensorMapEncodeTiled_v12000 encode = encode_tiled();
+  if (encode == nullptr) return cudaErrorNotSupported;
+  CUtensorMap q_map;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.num_qo_heads, (cuuint64_t)p.total_q};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)p.num_qo_heads * D * 2};
+  const cuuint32_t box[3] = {64u, (cuuint32_t)G, (cuuint32_t)C::BQ};
+  const cuuint32_t elem_strides[3] = {1u, 1u, 1u};
+  if (encode(&q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(p.q), dims, strides, box,
+             elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  prefill_kernel<D, G><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(p, q_map);
   return cudaGetLastError();
 }
 

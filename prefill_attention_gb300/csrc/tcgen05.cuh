@@ -66,43 +66,15 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 
 // ---------------------------------------------------------------- TMA (tensor copies)
 
-// 2-D tiled load of one box at coordinates (x = column, y = row) into shared memory.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y, uint32_t bar) {
+// 3-D tiled load of one box at coordinates (x innermost, y, z) into shared memory; the box's
+// bytes (including zeros filled in for coordinates outside the tensor) complete on `bar`.
+// x times the element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int x, int y, int z, uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          dst),
-      "l"(tmap), "r"(x), "r"(y), "r"(bar)
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
-}
-
-// Gather of four arbitrary rows (one-row box, `x` = first column) into four consecutive
-// shared-memory rows; rows outside the tensor (e.g. -1) are filled with zeros.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int x, int r0, int r1, int r2, int r3,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
-      "%5, %6}], [%7];" ::"r"(dst),
-      "l"(tmap), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
-      : "memory");
-}
-
-// Named barrier for a subset of the CTA's warps.
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
-// Barrier over `threads` threads that also ORs a predicate across them.
-__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t threads, bool pred) {
-  uint32_t out;
-  asm volatile(
-      "{\n\t.reg .pred pi, po;\n\t"
-      "setp.ne.u32 pi, %1, 0;\n\t"
-      "bar.red.or.pred po, %2, %3, pi;\n\t"
-      "selp.u32 %0, 1, 0, po;\n\t}"
-      : "=r"(out)
-      : "r"(pred ? 1u : 0u), "r"(id), "r"(threads)
-      : "memory");
-  return out != 0;
 }
 
 // ---------------------------------------------------------------- proxy / ordering fences

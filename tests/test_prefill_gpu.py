@@ -152,12 +152,24 @@ def test_many_requests_natural_order():
     assert _err(to_f64(run_prefill(w)), oracle.prefill(w)) <= TOL
 
 
-def test_many_items_natural_order():
-    """Fewer requests than that limit but more work items (KV head x query-tile pair) than the
-    sorted order holds."""
+def test_many_items_sorted_order():
+    """Many work items (KV head x query-tile pair), about 64 per CTA: still within the per-CTA
+    list of the sorted order."""
     rng = np.random.default_rng(43)
     B = 600                          # 600 requests x 2 pairs x 8 KV heads = 9600 items
     ql = rng.integers(257, 281, B)   # G = 1: two 128-row tiles per pair, two pairs per request
     pre = rng.integers(0, 21, B)
     w = make_from_lengths(rng, kind="prefill", name="many-items", seq_lens=pre + ql, q_lens=ql, Hq=8, Hkv=8, d=64)
+    assert _err(to_f64(run_prefill(w)), oracle.prefill(w)) <= TOL
+
+
+def test_many_items_natural_order():
+    """More work items than the per-CTA list of the sorted order holds (128 per CTA, i.e.
+    19456 on 152 SMs): the items are then dealt out in their natural order."""
+    rng = np.random.default_rng(44)
+    B = 400                          # 400 requests x 2 pairs x 32 KV heads = 25600 items
+    ql = rng.integers(257, 281, B)
+    pre = rng.integers(0, 21, B)
+    w = make_from_lengths(rng, kind="prefill", name="many-items-natural", seq_lens=pre + ql, q_lens=ql,
+                          Hq=32, Hkv=32, d=64)
     assert _err(to_f64(run_prefill(w)), oracle.prefill(w)) <= TOL
