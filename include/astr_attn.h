@@ -87,14 +87,20 @@ typedef struct astr_attn_dims {
 /*
  * Decode split schedule (P3, shared-helpers commit: the split count is chosen per call;
  * P3, kv_indptr commit: kv_indptr is built once per step and drives it here).
- * The batch's keys are laid end to end in kv_indptr order, T = kv_indptr[batch], and for
- * every KV head cut into `num_splits` chunks of C keys, each read by one warp pair
- * (a producer and a consumer warp; four chunks per CTA):
- *   C = max(round_up(ceil(T / num_splits), 16), F),  F = max(16, ceil(max_seq_len / (max_splits - 1)))
- *   (C = T when max_splits == 1), so every chunk holds the same number of keys.
- * Request b overlaps chunks kv_indptr[b] / C .. (kv_indptr[b+1] - 1) / C; the piece of it
- * in chunk c becomes partial slot c - kv_indptr[b] / C of (b, h), and the floor F keeps
- * that below max_splits.  This call returns num_splits as planned for `device`: the
+ * Each request's keys are cut into slots of 32 keys from its first key (the last slot
+ * possibly short); the batch's slots are laid end to end in request order (request b's first
+ * slot SP_b = sum over b' < b of ceil(seq_len_b' / 32), S = SP_batch) and, for every KV head,
+ * cut into `num_splits` chunks of C slots, each read by one warp pair (a producer and a
+ * consumer warp; four chunks per CTA):
+ *   C = max(ceil(S / num_splits), F),  F = max(1, ceil(ceil(max_seq_len / 32) / (max_splits - 1)))
+ *   (C = S when max_splits == 1), so every chunk holds the same number of 32-key slots (the
+ *   gather pipeline keeps a fixed number of slots in flight, so slots, not keys, set a
+ *   chunk's time).
+ * Request b overlaps chunks SP_b / C .. (SP_b + ceil(seq_len_b / 32) - 1) / C; the piece of it
+ * in chunk c becomes partial slot c - SP_b / C of (b, h), and the floor F keeps the count at
+ * or below max_splits (a request longer than max_seq_len keys would need more; its pieces
+ * past max_splits are not written, which leaves its output wrong but memory intact).
+ * This call returns num_splits as planned for `device`: the
  * forced dims->num_splits if > 0, else 4 * ceil(#SMs / Hkv) (one persistent CTA per SM).
  * Depends only on host-known values, never on the contents of seq_lens.
  * Errors: INVALID_ARG (null, bad dims), DEVICE (device query failed).

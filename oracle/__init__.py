@@ -54,7 +54,7 @@ def _declare(lib):
     lib.oracle_prefill_rows.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _P, _L, _P, _D, _L, _P, _P, _P, _I]
     lib.oracle_decode_split_partials.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _L, _P, _D, _I, _P, _P, _I]
     lib.oracle_combine.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P]
-    lib.oracle_decode_chunk_partials.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _L, _P, _P, _D, _L, _I, _P, _P]
+    lib.oracle_decode_chunk_partials.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _L, _P, _P, _D, _L, _L, _I, _P, _P]
     for f in ("oracle_decode_rows", "oracle_prefill_rows", "oracle_decode_split_partials", "oracle_combine",
               "oracle_decode_chunk_partials"):
         getattr(lib, f).restype = None
@@ -144,8 +144,10 @@ def decode_split_partials(w, S: int, nthreads: Optional[int] = None, lib=None):
     return o, ml
 
 
-def decode_chunk_partials(w, C: int, pitch: int, lib=None):
-    """Token-balanced chunk partials (chunks of C keys over the batch's flat key space).
+def decode_chunk_partials(w, C: int, pitch: int, W: int = 1, lib=None):
+    """Chunk partials: each request's keys in slots of W keys from its first key, the
+    batch's slots end to end in request order, chunks of C slots (W = 1: chunks of C keys
+    of the flat key space).
 
     Returns (o_part [B,Hq,pitch,d], ml_part [B,Hq,pitch,2], nsplit [B]); unused slots hold NaN.
     """
@@ -156,14 +158,16 @@ def decode_chunk_partials(w, C: int, pitch: int, lib=None):
     q, kp, vp = _c(w.q, np.uint16), _c(w.k_pool, np.uint16), _c(w.v_pool, np.uint16)
     r2t, sl, ki = _c(w.req_to_token, np.int32), _c(w.seq_lens, np.int32), _c(w.kv_indptr, np.int32)
     lib.oracle_decode_chunk_partials(B, Hq, Hkv, D, _ptr(q), _ptr(kp), _ptr(vp), _ptr(r2t), r2t.shape[1], _ptr(sl),
-                                     _ptr(ki), float(w.sm_scale), int(C), int(pitch), _ptr(o), _ptr(ml))
-    return o, ml, chunk_split_counts(w.kv_indptr, C)
+                                     _ptr(ki), float(w.sm_scale), int(C), int(W), int(pitch), _ptr(o), _ptr(ml))
+    return o, ml, chunk_split_counts(w.seq_lens, C, W)
 
 
-def chunk_split_counts(kv_indptr, C: int) -> np.ndarray:
-    """Number of C-key chunks that overlap each request."""
-    ind = np.asarray(kv_indptr, dtype=np.int64)
-    a, e = ind[:-1], ind[1:]
+def chunk_split_counts(seq_lens, C: int, W: int = 1) -> np.ndarray:
+    """Number of C-slot chunks that overlap each request (slots of W keys from its first key)."""
+    n = np.maximum(np.asarray(seq_lens, dtype=np.int64), 0)
+    ns = (n + W - 1) // W
+    a = np.concatenate([[0], np.cumsum(ns)[:-1]])
+    e = a + ns
     return np.where(e > a, (e - 1) // C - a // C + 1, 0).astype(np.int32)
 
 

@@ -264,34 +264,41 @@ void oracle_decode_split_partials(int B, int Hq, int Hkv, int D, const uint16_t 
   free(ih);
 }
 
-/* Token-balanced chunk partials.  The batch's keys are laid end to end in kv_indptr order
- * (T = kv_indptr[B]) and cut into chunks of C keys; for every request b and every chunk c
- * that overlaps it, the partial over the overlap is stored in slot c - kv_indptr[b] / C of
- * o_part [B,Hq,pitch,D] / ml_part [B,Hq,pitch,2].  Slots no chunk maps to are not written.
- * This is the split-KV decomposition of the kernel-rename commit with the split boundaries
- * placed by kv_indptr (kv_indptr commit) instead of per request. */
+/* Chunk partials over the batch's slots.  Request b's keys are cut into slots of W keys
+ * starting at its first key (ceil(seq_len_b / W) slots, the last one possibly short); the
+ * slots of all requests are laid end to end in request order (request b's first slot is
+ * SP_b = sum over b' < b of ceil(seq_len_b' / W)) and cut into chunks of C slots.  For every
+ * request b and every chunk c that overlaps it, the partial over the keys of the overlapping
+ * slots is stored in slot c - SP_b / C of o_part [B,Hq,pitch,D] / ml_part [B,Hq,pitch,2].
+ * Slots no chunk maps to are not written.  With W = 1 a slot is a key, so chunks are C
+ * consecutive keys of the flat key space (kv_indptr order).  This is the split-KV
+ * decomposition of the kernel-rename commit with the split boundaries placed over the whole
+ * batch (kv_indptr commit) instead of per request. */
 void oracle_decode_chunk_partials(int B, int Hq, int Hkv, int D, const uint16_t *q, const uint16_t *k_pool,
                                   const uint16_t *v_pool, const int32_t *req_to_token, int64_t r2t_stride,
                                   const int32_t *seq_lens, const int32_t *kv_indptr, double sm_scale, int64_t C,
-                                  int pitch, double *o_part, double *ml_part) {
+                                  int64_t W, int pitch, double *o_part, double *ml_part) {
+  (void)kv_indptr;
   pool_t P;
   P.Hq = Hq; P.Hkv = Hkv; P.D = D; P.k_pool = k_pool; P.v_pool = v_pool; P.sm_scale = sm_scale;
   const int G = Hq / Hkv;
   double *qbuf = (double *)malloc(sizeof(double) * (size_t)D);
+  int64_t sp = 0;  /* first slot of request b */
   for (int b = 0; b < B; ++b) {
-    const int64_t a = kv_indptr[b], e = a + seq_lens[b];
-    if (e <= a) continue;
+    const int64_t n = seq_lens[b] > 0 ? seq_lens[b] : 0;
+    const int64_t ns = (n + W - 1) / W;  /* slots of request b */
     const int32_t *slots = req_to_token + (int64_t)b * r2t_stride;
-    for (int64_t c = a / C; c * C < e; ++c) {
-      int64_t lo = c * C > a ? c * C : a, hi = (c + 1) * C < e ? (c + 1) * C : e;
-      const int64_t s = c - a / C;
+    for (int64_t c = sp / C; ns > 0 && c * C < sp + ns; ++c) {
+      const int64_t g0 = c * C > sp ? c * C : sp, g1 = (c + 1) * C < sp + ns ? (c + 1) * C : sp + ns;
+      const int64_t lo = (g0 - sp) * W, hi = (g1 - sp) * W < n ? (g1 - sp) * W : n;  /* keys of the overlap */
+      const int64_t s = c - sp / C;
       for (int h = 0; h < Hq; ++h) {
         widen_row(q + ((int64_t)b * Hq + h) * D, D, qbuf);
         const int64_t base = ((int64_t)b * Hq + h) * pitch + s;
-        partial(&P, qbuf, h / G, slots, lo - a, hi - a, o_part + base * D, &ml_part[2 * base],
-                &ml_part[2 * base + 1]);
+        partial(&P, qbuf, h / G, slots, lo, hi, o_part + base * D, &ml_part[2 * base], &ml_part[2 * base + 1]);
       }
     }
+    sp += ns;
   }
   free(qbuf);
 }

@@ -64,12 +64,14 @@ int plan_splits(const astr_attn_dims* d, int sms) {
   return (int)(s * astr::kDecodeChunksPerCta);
 }
 
-// Floor on the chunk length: a request of max_seq_len keys overlaps at most
-// ceil(max_seq_len / C) + 1 chunks, which must fit in max_splits partial slots.
+// Floor on the chunk length in 32-key slots: a request of max_seq_len keys has
+// m = ceil(max_seq_len / 32) slots and overlaps at most ceil(m / C) + 1 chunks, which must
+// fit in max_splits partial slots.
 int plan_min_chunk(const astr_attn_dims* d) {
-  if (d->max_splits <= 1) return 1;  // single chunk per KV head (the kernel uses C = T)
-  int64_t c = ((int64_t)d->max_seq_len + d->max_splits - 2) / (d->max_splits - 1);
-  if (c < 16) c = 16;
+  if (d->max_splits <= 1) return 1;  // single chunk per KV head (the kernel uses all slots)
+  const int64_t m = ((int64_t)d->max_seq_len + 31) / 32;
+  int64_t c = (m + d->max_splits - 2) / (d->max_splits - 1);
+  if (c < 1) c = 1;
   return (int)c;
 }
 

@@ -82,4 +82,18 @@ __device__ __forceinline__ int ldg_nc_i32(const int32_t* p) {
   return v;
 }
 
+// Load cached in L2 only: no L1 line is filled, so a value read before another kernel's
+// writes become visible cannot be served stale to a later load of this kernel.
+__device__ __forceinline__ int ldcg_i32(const int32_t* p) {
+  int v;
+  asm volatile("ld.global.cg.b32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+// Hint: bring the 128-byte line holding `p` into L2 (no register result, no fault semantics
+// beyond those of the address; callers keep it inside their buffers).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 }  // namespace astr

@@ -57,12 +57,42 @@
 
 namespace astr {
 
-// Chunk length (keys per CTA) for T keys over n_chunks CTAs; shared by split and combine.
-__device__ __forceinline__ int decode_chunk_len(int T, int n_chunks, int min_chunk, int max_splits) {
-  if (max_splits <= 1) return T > 0 ? T : 1;
-  int c = (T + n_chunks - 1) / n_chunks;
-  c = (c + 15) & ~15;
+// Split schedule, shared by the split and the combine kernels.  Request b's keys are cut
+// into slots of kSlotKeys keys from its first key (the last slot possibly short); the
+// batch's slots lie end to end in request order (request b's first slot is SP_b, the sum of
+// the slot counts of the requests before it) and are cut into chunks of CS slots.  Every
+// chunk thus holds the same number of ring slots, which is what sets a chunk's time: the
+// gather pipeline keeps a fixed number of slots in flight, full or not.
+constexpr int kSlotKeys = 32;
+__device__ __forceinline__ int slots_of(int n) { return n > 0 ? (n + kSlotKeys - 1) / kSlotKeys : 0; }
+
+// Chunk length in slots for S slots over n_chunks chunks.
+__device__ __forceinline__ int decode_chunk_slots(int S, int n_chunks, int min_chunk, int max_splits) {
+  if (max_splits <= 1) return S > 0 ? S : 1;
+  const int c = (S + n_chunks - 1) / n_chunks;
   return c > min_chunk ? c : min_chunk;
+}
+
+// Warp-cooperative: the batch's slot count (x) and the slots of requests b < `before` (y).
+__device__ __forceinline__ int2 slot_totals(const int32_t* ind, int B, int before, int lane) {
+  int tot = 0, pre = 0;
+#pragma unroll 4
+  for (int base = 0; base < B; base += 32) {
+    const int i = base + lane;
+    const int x = __ldg(ind + min(i, B));
+    const int nx = __ldg(ind + min(base + 32, B));
+    int y = __shfl_down_sync(0xffffffffu, x, 1);
+    if (lane == 31) y = nx;
+    const int sl = (i < B) ? slots_of(y - x) : 0;
+    tot += sl;
+    if (i < before) pre += sl;
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    pre += __shfl_xor_sync(0xffffffffu, pre, o);
+  }
+  return make_int2(tot, pre);
 }
 
 namespace {
@@ -142,75 +172,153 @@ __device__ __forceinline__ uint32_t sw128(int r, int c, int rows) {
   return (uint32_t)((c >> 3) * rows * 128 + (r >> 3) * 1024 + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
-// Walks the slots of one chunk: BK keys at a time, never across a request boundary.
+// The request that holds slot g of the batch: b, its first slot, its keys [ind_b, ind_b1).
+struct SlotBracket {
+  int b, spb, ind_b, ind_b1;
+};
+// Warp-cooperative lookup of the request that holds slot `g` (< the batch's slot count):
+// blocks of 32 requests in order, an inclusive scan of their slot counts per block.  A
+// batch of up to 32 requests takes one round of loads (already in L1 after slot_totals).
+__device__ __forceinline__ SlotBracket locate_slot(const int32_t* ind, int B, int g, int lane) {
+  int carry = 0;
+  for (int base = 0; base < B; base += 32) {
+    const int i = base + lane;
+    const int x = __ldg(ind + min(i, B));
+    const int nx = __ldg(ind + min(base + 32, B));
+    int y = __shfl_down_sync(kFullMask, x, 1);
+    if (lane == 31) y = nx;
+    const int sl = (i < B) ? slots_of(y - x) : 0;
+    int incl = sl;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(kFullMask, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const int total = __shfl_sync(kFullMask, incl, 31);
+    if (g < carry + total) {  // warp-uniform
+      const int f = __ffs(__ballot_sync(kFullMask, carry + incl > g)) - 1;
+      SlotBracket r;
+      r.b = base + f;
+      r.spb = carry + __shfl_sync(kFullMask, incl - sl, f);
+      r.ind_b = __shfl_sync(kFullMask, x, f);
+      r.ind_b1 = __shfl_sync(kFullMask, y, f);
+      return r;
+    }
+    carry += total;
+  }
+  return SlotBracket{B, carry, 0, 0};  // g past the last slot (callers never ask)
+}
+
+// Walks the ring slots of one chunk (batch slots [ls, hs)): one request slot at a time,
+// so a ring slot never spans two requests.
 template <int BK>
 struct TileIter {
-  int b, start, end;  // current slot: flat keys [start, end) of request b
-  __device__ __forceinline__ void first(const int32_t* ind, int B, int lo, int hi) {
-    int l = 0, h = B - 1;  // largest b with ind[b] <= lo
-    while (l < h) {
-      const int m = (l + h + 1) >> 1;
-      if (__ldg(ind + m) <= lo) l = m; else h = m - 1;
+  int b, spb, ind_b, ind_b1;  // current request: first batch slot, keys [ind_b, ind_b1)
+  int g;                      // current batch slot
+  int start, end;             // its keys [start, end)
+  __device__ __forceinline__ int nslots() const { return slots_of(ind_b1 - ind_b); }
+  __device__ __forceinline__ void set_keys() {
+    start = ind_b + (g - spb) * BK;
+    end = min(start + BK, ind_b1);
+  }
+  __device__ __forceinline__ void start_at(const SlotBracket& f, int ls) {
+    b = f.b;
+    spb = f.spb;
+    ind_b = f.ind_b;
+    ind_b1 = f.ind_b1;
+    g = ls;
+    set_keys();
+  }
+  __device__ __forceinline__ void next(const int32_t* ind, int B, int hs) {
+    if (++g >= hs) return;
+    while (g >= spb + nslots() && b < B - 1) {  // on to the next request that has keys
+      spb += nslots();
+      ++b;
+      ind_b = ind_b1;
+      ind_b1 = __ldg(ind + b + 1);
     }
-    b = l;
-    start = lo;
-    end = min(start + BK, min(hi, __ldg(ind + b + 1)));
+    set_keys();
   }
-  // Same as first() for a chunk whose first request b0 and its end ind[b0 + 1] are known.
-  __device__ __forceinline__ void start_at(int b0, int b0_end, int lo, int hi) {
-    b = b0;
-    start = lo;
-    end = min(start + BK, min(hi, b0_end));
-  }
-  __device__ __forceinline__ void next(const int32_t* ind, int B, int hi) {
-    const int piece_end = min(hi, __ldg(ind + b + 1));
-    if (end < piece_end) {
-      start = end;
-    } else {
-      do { ++b; } while (b < B && __ldg(ind + b + 1) <= __ldg(ind + b));  // skip empty requests
-      start = (b < B) ? __ldg(ind + b) : hi;
-      if (start > hi) start = hi;
-    }
-    end = (start < hi) ? min(start + BK, min(hi, __ldg(ind + b + 1))) : start;
-  }
-  __device__ __forceinline__ bool valid(int hi) const { return start < hi; }
-  __device__ __forceinline__ bool opens_piece(const int32_t* ind, int lo) const { return start == max(lo, __ldg(ind + b)); }
-  __device__ __forceinline__ bool closes_piece(const int32_t* ind, int hi) const { return end == min(hi, __ldg(ind + b + 1)); }
+  __device__ __forceinline__ bool valid(int hs) const { return g < hs; }
+  __device__ __forceinline__ bool opens_piece(int ls) const { return g == max(ls, spb); }
+  __device__ __forceinline__ bool closes_piece(int hs) const { return g + 1 == min(hs, spb + nslots()); }
 };
 
-// Warp-cooperative lookup of the request that holds flat key `lo` (largest b with
-// ind[b] <= lo, so empty requests are stepped over), with ind[b] and ind[b + 1].
-// Each round samples ind at 128 evenly spaced points of the bracket [l, h) (every point
-// once the bracket is that narrow) and keeps the two samples around lo, so a batch of up
-// to 128 requests takes one round of loads and 16384 take two.  Needs ind[l] <= lo <
-// ind[h] on entry, i.e. l = 0, h = B, ind_h = ind[B] > lo.
-__device__ __forceinline__ int pick4(const int (&v)[4], int k) {  // v[k] without local memory
-  return k == 0 ? v[0] : k == 1 ? v[1] : k == 2 ? v[2] : v[3];
-}
-struct ReqBracket {
-  int b, start, end;
-};
-__device__ __forceinline__ ReqBracket locate_request(const int32_t* ind, int B, int lo, int ind_B, int lane) {
-  int l = 0, h = B, ind_l = 0, ind_h = ind_B;
-  while (h - l > 1) {
-    int v[4];
+// L2 warm-up of a chunk's first ring slots, run before the dependency wait while the
+// previous kernel in the stream may still be writing the tables: kv_indptr and req_to_token
+// are read with L2-only loads (so no stale line stays in L1 past the wait), nothing read is
+// kept, and only prefetch hints for the first request's K/V rows come out (prefetching its
+// query rows as well measured slower).  Every address
+// is clamped to its buffer whatever the values read.  kv_indptr is read in R rounds of 32
+// requests, one coalesced load and one broadcast per round, all rounds issued together (R is
+// picked from the batch size: the unrolled rounds cost latency even when idle); batches of
+// more than 256 requests skip the warm-up.
+template <int D, int G, int BK, int R>
+__device__ __forceinline__ void warm_first_slots(const DecodeParams& p, int vc, int kvh, int n_slots, int lane) {
+  const int B = p.batch;
+  const int32_t* ind = p.kv_indptr;
+  int x[R], y[R];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) v[k] = __ldg(ind + l + (int)((int64_t)(h - l) * (lane * 4 + k) / 128));
-    int c = 0;  // samples with ind <= lo; they are samples 0 .. c-1 (ind and positions ascend)
-#pragma unroll
-    for (int k = 0; k < 4; ++k) c += __popc(__ballot_sync(kFullMask, v[k] <= lo));
-    const int i_lo = c - 1;  // >= 0: sample 0 is ind[l] <= lo
-    const int vl = __shfl_sync(kFullMask, pick4(v, i_lo & 3), i_lo >> 2);
-    const int nl = l + (int)((int64_t)(h - l) * i_lo / 128);
-    if (c < 128) {
-      const int vh = __shfl_sync(kFullMask, pick4(v, c & 3), c >> 2);
-      h = l + (int)((int64_t)(h - l) * c / 128);
-      ind_h = vh;
+  for (int r = 0; r < R; ++r) {
+    if (32 * r < B) {
+      x[r] = ldcg_i32(ind + min(32 * r + lane, B));
+      y[r] = ldcg_i32(ind + min(32 * r + 32, B));  // the same address in every lane
     }
-    l = nl;
-    ind_l = vl;
   }
-  return ReqBracket{l, ind_l, ind_h};
+  int sl[R], incl[R], carry = 0;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    sl[r] = 0;
+    incl[r] = carry;
+    if (32 * r < B) {
+      int nx = __shfl_down_sync(kFullMask, x[r], 1);
+      if (lane == 31) nx = y[r];
+      y[r] = nx;  // y[r] = ind[32 r + lane + 1]
+      sl[r] = (32 * r + lane < B) ? slots_of(y[r] - x[r]) : 0;
+      int c = sl[r];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(kFullMask, c, o);
+        if (lane >= o) c += t;
+      }
+      incl[r] = carry + c;
+      carry += __shfl_sync(kFullMask, c, 31);
+    }
+  }
+  const int S_tot = carry;
+  const int CS = decode_chunk_slots(S_tot, p.num_splits, p.min_chunk, p.part_pitch);
+  const int ls = (vc < p.num_splits) ? (int)min((int64_t)vc * CS, (int64_t)S_tot) : S_tot;
+  if (S_tot <= 0 || ls >= S_tot) return;
+  int b = -1, spb = 0, ib = 0, ib1 = 0;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    if (b < 0 && 32 * r < B) {
+      const unsigned lanes = __ballot_sync(kFullMask, incl[r] > ls);
+      if (lanes != 0u) {
+        const int f = __ffs(lanes) - 1;
+        b = 32 * r + f;
+        spb = __shfl_sync(kFullMask, incl[r] - sl[r], f);
+        ib = __shfl_sync(kFullMask, x[r], f);
+        ib1 = __shfl_sync(kFullMask, y[r], f);
+      }
+    }
+  }
+  if (b < 0 || b >= B) return;
+  const int k0 = (ls - spb) * BK;  // the chunk's first key within request b
+  const size_t head_stride = (size_t)p.num_kv_heads * D;
+  for (int k = lane; k < n_slots * BK; k += 32) {
+    const int key = k0 + k;
+    if (key < 0 || key >= ib1 - ib || (int64_t)key >= p.r2t_stride) continue;
+    const int id = ldcg_i32(p.req_to_token + (int64_t)b * p.r2t_stride + key);
+    if ((uint64_t)(uint32_t)id >= (uint64_t)p.num_slots) continue;  // negative ids wrap past num_slots
+    const uint16_t* kr = p.k_pool + (size_t)id * head_stride + (size_t)kvh * D;
+    const uint16_t* vr = p.v_pool + (size_t)id * head_stride + (size_t)kvh * D;
+#pragma unroll
+    for (int off = 0; off < D; off += 64) {  // 128-byte lines
+      prefetch_l2(kr + off);
+      prefetch_l2(vr + off);
+    }
+  }
 }
 
 // Bounded wait that gives up (and raises the pair's error flag) on timeout or once the flag is up.
@@ -252,40 +360,45 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(
     sts128_zero(sbase + slot * C::SLOT + 2 * C::KV_BYTES + c * 16);
   }
   __syncthreads();
+  // Before the wait: warm L2 with this pair's first ring slots (prefetch hints only, from
+  // tables read through L2 that may still be changing; see warm_first_slots).
+  if (is_producer && B <= 32) warm_first_slots<D, G, C::BK, 1>(p, blockIdx.x * C::NPAIR + pair, kvh, C::STAGES, lane);
+  else if (is_producer && B <= 256) warm_first_slots<D, G, C::BK, 8>(p, blockIdx.x * C::NPAIR + pair, kvh, C::STAGES, lane);
   // Launched as a programmatic dependent of the previous kernel in the stream: the set-up
   // above overlapped its tail; from here on its writes are visible and its reads are done,
-  // so no global memory is touched before this point.  (A no-op for an ordinary launch.)
+  // so nothing read before this point is used.  (A no-op for an ordinary launch.)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // let the combine kernel's CTAs launch now; they wait for this grid's memory to be visible
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  // ---- this pair's chunk (chunk index vc of the KV head) and its first request
+  // ---- this pair's chunk (chunk index vc of the KV head): batch slots [ls, hs), and the
+  // request that holds slot ls
   const int vc = blockIdx.x * C::NPAIR + pair;
-  const int T = __ldg(ind + B);
-  const int CL = decode_chunk_len(T, p.num_splits, p.min_chunk, p.part_pitch);
-  const int lo = (vc < p.num_splits) ? (int)min((int64_t)vc * CL, (int64_t)T) : T;
-  const int hi = min(lo + CL, T);
-  ReqBracket first{0, 0, T};
-  if (lo < hi) first = locate_request(ind, B, lo, T, lane);
+  const int S_tot = slot_totals(ind, B, 0, lane).x;
+  const int CS = decode_chunk_slots(S_tot, p.num_splits, p.min_chunk, p.part_pitch);
+  const int ls = (vc < p.num_splits) ? (int)min((int64_t)vc * CS, (int64_t)S_tot) : S_tot;
+  const int hs = min(ls + CS, S_tot);
+  SlotBracket first{0, 0, 0, 0};
+  if (ls < hs) first = locate_slot(ind, B, ls, lane);
 
-  if (lo < hi && is_producer) {
+  if (ls < hs && is_producer) {
     // ======================= producer warp: gathers the chunk's K / V rows slot by slot
     TileIter<C::BK> it;
-    it.start_at(first.b, first.end, lo, hi);
+    it.start_at(first, ls);
     const size_t head_stride = (size_t)p.num_kv_heads * D;
     const unsigned nslots = (unsigned)p.num_slots;
     auto slot_id = [&](const TileIter<C::BK>& t) {  // lane k: slot id of key k of the slot, or -1
       const int flat = t.start + lane;
-      return (t.valid(hi) && flat < t.end)
-                 ? ldg_nc_i32(p.req_to_token + (int64_t)t.b * p.r2t_stride + (flat - __ldg(ind + t.b)))
+      return (t.valid(hs) && flat < t.end)
+                 ? ldg_nc_i32(p.req_to_token + (int64_t)t.b * p.r2t_stride + (flat - t.ind_b))
                  : -1;
     };
     int my_id = slot_id(it);
-    for (int i = 0; it.valid(hi); ++i) {
+    for (int i = 0; it.valid(hs); ++i) {
       const int s = i % C::STAGES;
       if (i >= C::STAGES && !wait_or_fail(empty(s), (uint32_t)((i / C::STAGES - 1) & 1), err)) break;
       const uint32_t kst = ring + s * C::SLOT, vst = kst + C::KV_BYTES, qst = vst + C::KV_BYTES;
-      if (it.opens_piece(ind, lo)) {  // first slot of a piece: its G query rows
+      if (it.opens_piece(ls)) {  // first slot of a piece: its G query rows
         const uint16_t* qsrc = p.q + ((size_t)it.b * p.num_qo_heads + (size_t)kvh * G) * D;
         for (int j = lane; j < G * C::CPR; j += 32) {
           const int g = j / C::CPR, c = j % C::CPR;
@@ -305,11 +418,11 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(
         cp_async16(vst + o, p.v_pool + off, valid);
       }
       cp_async_arrive_noinc(full(s));  // completes once this lane's copies (and older ones) land
-      it.next(ind, B, hi);
+      it.next(ind, B, hs);
       my_id = slot_id(it);
     }
     cp_async_wait<0>();
-  } else if (lo < hi) {
+  } else if (ls < hs) {
     // ======================= consumer warp: online softmax over the chunk's slots
     // Transposed products so the 16-row MMA side is keys / head_dim, not the few heads:
     //   S^T (32 keys x 8 heads) = K Q^T,   O^T (D x 8 heads) += V^T P^T.
@@ -317,14 +430,14 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(
     const int lrow = lane & 7, lmat = lane >> 3;  // ldmatrix: row within / index of the 8x8 matrix
     const float scale = p.scale_log2;
     TileIter<C::BK> it;
-    it.start_at(first.b, first.end, lo, hi);
+    it.start_at(first, ls);
     uint32_t qb[NH][C::KSTEPS][2];  // Q^T as the B operand (n = heads), per k-step
     float acc[C::MT_D][NH][4];      // O^T: rows d = 16md + g4 (+8), heads 8nh + 2t4 (+1)
     float m_run[NH][2], l_thr[NH][2];  // heads 8nh + 2t4 + e: reference max (lazy), sum
     float m_max[NH][2];                // exact running max, for the (max, sum) partial
-    for (int i = 0; it.valid(hi); ++i) {
+    for (int i = 0; it.valid(hs); ++i) {
       const int s = i % C::STAGES;
-      const bool opens = it.opens_piece(ind, lo), closes = it.closes_piece(ind, hi);
+      const bool opens = it.opens_piece(ls), closes = it.closes_piece(hs);
       const int nkeys = it.end - it.start;  // valid keys of the slot; the rest are masked
       if (!wait_or_fail(full(s), (uint32_t)((i / C::STAGES) & 1), err)) break;
       const uint32_t kst = ring + s * C::SLOT, vst = kst + C::KV_BYTES, qst = vst + C::KV_BYTES;
@@ -499,8 +612,7 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(
                   acc[md][nh][e] * f[nh][e & 1];
         __syncwarp();
         const int b = it.b;
-        const int rb = __ldg(ind + b), re = __ldg(ind + b + 1);
-        const bool direct = (p.out != nullptr) && rb >= lo && re <= hi;  // whole request in this chunk
+        const bool direct = (p.out != nullptr) && it.spb >= ls && it.spb + it.nslots() <= hs;  // whole request here
         const size_t qh0 = (size_t)b * p.num_qo_heads + (size_t)kvh * G;
         if (direct) {
           // lane -> 8 consecutive d of one head: bf16(O / l), 16-byte stores
@@ -516,8 +628,8 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(
             v.w = float2_to_bf16x2_rn(src[6] * inv, src[7] * inv);
             *reinterpret_cast<uint4*>(p.out + (qh0 + h) * D + d0) = v;
           }
-        } else {
-          const int slot = vc - rb / CL;
+        } else if (vc - it.spb / CS < p.part_pitch) {  // (a request past max_seq_len keys is not written)
+          const int slot = vc - it.spb / CS;
           for (int j = lane; j < G * (D / 4); j += 32) {
             const int h = j / (D / 4), d0 = (j % (D / 4)) * 4;
             const float* src = stg + h * C::STG_PITCH + d0;
@@ -535,20 +647,20 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(
       }
       __syncwarp();
       tc::mbar_arrive(empty(s));  // this slot may be refilled
-      it.next(ind, B, hi);
+      it.next(ind, B, hs);
     }
   }
   __syncthreads();
-  if (*err && lo < hi && !is_producer) {
+  if (*err && ls < hs && !is_producer) {
     // a wait timed out: poison every output this pair owns so the call reads as failed
     TileIter<C::BK> it;
-    it.first(ind, B, lo, hi);
-    for (; it.valid(hi); it.next(ind, B, hi)) {
-      if (!it.closes_piece(ind, hi)) continue;
-      const int s = vc - __ldg(ind + it.b) / CL;
+    it.start_at(first, ls);
+    for (; it.valid(hs); it.next(ind, B, hs)) {
+      if (!it.closes_piece(hs)) continue;
+      const int s = vc - it.spb / CS;
       for (int i = lane; i < G * D; i += 32) {
         const size_t qh = (size_t)it.b * p.num_qo_heads + (size_t)kvh * G + i / D;
-        p.o_part[(qh * p.part_pitch + s) * D + i % D] = CUDART_NAN_F;
+        if (s < p.part_pitch) p.o_part[(qh * p.part_pitch + s) * D + i % D] = CUDART_NAN_F;
         if (p.out != nullptr) p.out[qh * D + i % D] = 0x7fc0;
       }
     }
@@ -563,14 +675,14 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
   const int lane = threadIdx.x & 31;
   const bool live = wid < p.batch * p.num_qo_heads;
   const int b = live ? wid / p.num_qo_heads : 0;
-  // Split count of request b: the chunks that overlap it (token-balanced schedule), or the
-  // caller's explicit count.
+  // Split count of request b: the chunks that overlap it (slot schedule above, at most
+  // max_splits), or the caller's explicit count.  Warp-collective.
   auto split_count = [&]() {
     if (p.kv_indptr == nullptr) return p.num_splits;
-    const int T = __ldg(p.kv_indptr + p.batch);
-    const int CL = decode_chunk_len(T, p.num_splits, p.min_chunk, p.part_pitch);
-    const int a = __ldg(p.kv_indptr + b), e = __ldg(p.kv_indptr + b + 1);
-    return (e > a) ? (e - 1) / CL - a / CL + 1 : 0;
+    const int2 tp = slot_totals(p.kv_indptr, p.batch, b, lane);
+    const int CS = decode_chunk_slots(tp.x, p.num_splits, p.min_chunk, p.part_pitch);
+    const int nb = slots_of(__ldg(p.kv_indptr + b + 1) - __ldg(p.kv_indptr + b));
+    return nb > 0 ? min((tp.y + nb - 1) / CS - tp.y / CS + 1, p.part_pitch) : 0;
   };
   // Right after this call's split kernel, kv_indptr (an input the split kernel does not write)
   // is read before the wait: that kernel has already passed its own wait on the kernels before

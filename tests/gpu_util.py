@@ -43,14 +43,18 @@ def prefill_dims(w):
                         w.max_seq_len, total_q=w.total_q, max_q_len=w.max_q_len)
 
 
-def decode_chunk_len(w, n_chunks, max_splits):
-    """Keys per split-kernel chunk, as documented for astr_attn_paged_decode."""
-    T = int(w.kv_indptr[-1])
+SLOT_KEYS = 32  # keys per slot of the decode split schedule
+
+
+def decode_chunk_slots(w, n_chunks, max_splits):
+    """Chunk length in 32-key slots of the decode split schedule, as documented for
+    astr_attn_paged_decode."""
+    n_slots = int(sum(-(-int(n) // SLOT_KEYS) for n in w.seq_lens if n > 0))
     if max_splits <= 1:
-        return max(T, 1)
-    c = -(-T // n_chunks)
-    c = (c + 15) // 16 * 16
-    floor = max(16, -(-w.max_seq_len // (max_splits - 1)))
+        return max(n_slots, 1)
+    c = -(-n_slots // n_chunks)
+    m = -(-w.max_seq_len // SLOT_KEYS)
+    floor = max(1, -(-m // (max_splits - 1)))
     return max(c, floor)
 
 

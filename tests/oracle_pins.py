@@ -266,27 +266,34 @@ def pin_split_combine(lib):
 
 
 def pin_chunk_partials_combine(lib):
-    """Token-balanced chunks (boundaries anywhere in the flat key space, so chunks straddle
-    requests): chunk partials + combine == unsplit attention, for several chunk lengths."""
+    """Chunks over the batch's slots (boundaries anywhere in the end-to-end slot sequence, so
+    chunks straddle requests): chunk partials + combine == unsplit attention, for several
+    chunk lengths and slot widths (W = 1: chunks of the flat key space)."""
     w = _small_decode(seed=73, B=6, lo=0, hi=45)
     w.seq_lens[2] = 0   # an empty request owns no chunk
     w.kv_indptr[1:] = np.cumsum(w.seq_lens)
     ref = oracle.decode(w, lib=lib)
     T = int(w.kv_indptr[-1])
-    for C in (1, 7, 16, 33, T, T + 5):
-        ns = oracle.chunk_split_counts(w.kv_indptr, C)
-        pitch = max(1, int(ns.max()))
-        o, ml, ns2 = oracle.decode_chunk_partials(w, C, pitch, lib=lib)
-        assert np.array_equal(ns, ns2)
-        # brute force: count (request, chunk) overlaps key by key
-        overlaps = {(b, j // C) for b in range(w.batch) for j in range(w.kv_indptr[b], w.kv_indptr[b + 1])}
-        assert int(ns.sum()) == len(overlaps)
-        got = oracle.combine(np.nan_to_num(o), np.where(np.isnan(ml), -np.inf, ml), nsplit=ns, lib=lib)
-        err = np.abs(got - ref).max()
-        assert err <= 1e-12, f"chunk combine C={C}: {err}"
-        # every written slot is a proper partial: finite m, positive l
-        for b in range(w.batch):
-            assert np.all(np.isfinite(ml[b, :, :ns[b], 0])) and np.all(ml[b, :, :ns[b], 1] > 0)
+    for W in (1, 5, 32):
+        n_slots = int(sum(-(-int(n) // W) for n in w.seq_lens))
+        for C in (1, 2, 7, 16, 33, n_slots, n_slots + 5, T):
+            ns = oracle.chunk_split_counts(w.seq_lens, C, W)
+            pitch = max(1, int(ns.max()))
+            o, ml, ns2 = oracle.decode_chunk_partials(w, C, pitch, W, lib=lib)
+            assert np.array_equal(ns, ns2)
+            # brute force: count (request, chunk) overlaps key by key, through each key's slot
+            overlaps, sp = set(), 0
+            for b in range(w.batch):
+                n = int(w.seq_lens[b])
+                overlaps |= {(b, (sp + j // W) // C) for j in range(n)}
+                sp += -(-n // W)
+            assert int(ns.sum()) == len(overlaps)
+            got = oracle.combine(np.nan_to_num(o), np.where(np.isnan(ml), -np.inf, ml), nsplit=ns, lib=lib)
+            err = np.abs(got - ref).max()
+            assert err <= 1e-12, f"chunk combine W={W} C={C}: {err}"
+            # every written slot is a proper partial: finite m, positive l
+            for b in range(w.batch):
+                assert np.all(np.isfinite(ml[b, :, :ns[b], 0])) and np.all(ml[b, :, :ns[b], 1] > 0)
 
 
 def pin_partial_is_softmax_piece(lib):
