@@ -281,3 +281,44 @@ def test_scale_sign_and_zero(scale):
     for n in (0, 3):
         got = to_f64(run_decode(w, num_splits=n))
         assert _err(got, oracle.decode(w)) <= TOL, f"n_chunks={n}"
+
+
+@pytest.mark.parametrize("B", [33, 64, 257, 300])
+def test_batch_sizes_around_warmup_rounds(B):
+    """Batches that take the one-round (B <= 32), partly filled multi-round (33-256) and
+    skipped (B > 256) L2 warm-up before the dependency wait; results must not depend on it."""
+    rng = np.random.default_rng(500 + B)
+    seq = rng.integers(0, 97, B)
+    seq[::17] = 0   # some empty requests
+    w = make_from_lengths(rng, kind="decode", name="warm", seq_lens=seq, q_lens=None, Hq=8, Hkv=2, d=64)
+    for n in (0, 37):
+        got = to_f64(run_decode(w, num_splits=n))
+        assert _err(got, oracle.decode(w)) <= TOL, f"n_chunks={n}"
+
+
+def test_request_longer_than_max_seq_len_stays_in_bounds():
+    """max_seq_len understated for one request: its pieces past max_splits partial slots are
+    not written (its row is then wrong), every other row is right and no byte outside the
+    workspace changes."""
+    rng = np.random.default_rng(611)
+    seq = np.array([20, 33, 200, 7, 40, 1])
+    w = make_from_lengths(rng, kind="decode", name="overlong", seq_lens=seq, q_lens=None, Hq=8, Hkv=2, d=64)
+    t = upload(w)
+    max_splits = 3
+    dims = pa.make_dims(w.batch, w.num_qo_heads, w.num_kv_heads, w.head_dim, w.num_slots, w.r2t_stride, 40,
+                        max_splits=max_splits, num_splits=64)
+    ob, mb = pa.astr_attn_decode_workspace_bytes(dims)
+    pad = 256
+    o_buf = torch.full((ob // 4 + 2 * pad,), 12345.0, device="cuda")
+    m_buf = torch.full((mb // 4 + 2 * pad,), 12345.0, device="cuda")
+    n_out = w.batch * w.num_qo_heads * w.head_dim
+    out_buf = torch.full((n_out + 2 * pad,), 7.0, device="cuda", dtype=torch.bfloat16)
+    pa.astr_attn_paged_decode(t["q"], t["k"], t["v"], t["r2t"], t["seq"], t["kvi"], o_buf[pad:pad + ob // 4],
+                              m_buf[pad:pad + mb // 4], out_buf[pad:pad + n_out], dims, w.sm_scale)
+    torch.cuda.synchronize()
+    for buf, n, val in ((o_buf, ob // 4, 12345.0), (m_buf, mb // 4, 12345.0), (out_buf, n_out, 7.0)):
+        assert torch.all(buf[:pad] == val) and torch.all(buf[pad + n:] == val)
+    got = to_f64(out_buf[pad:pad + n_out].view(w.batch, w.num_qo_heads, w.head_dim))
+    ref = oracle.decode(w)
+    ok_rows = [b for b in range(w.batch) if seq[b] <= 40]
+    assert _err(got[ok_rows], ref[ok_rows]) <= TOL
