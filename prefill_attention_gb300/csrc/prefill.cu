@@ -68,9 +68,10 @@ struct PrefillCfg {
   // this CTA's items in order, as (request, pair within the request, KV head)
   static constexpr int MAX_CTA_ITEMS = 128;
   static constexpr int SMEM_BYTES = LIST_OFF + MAX_CTA_ITEMS * 12;
-  // prologue scratch in the K/V ring: per-request pair offsets, 256 counts, keys, order
+  // prologue scratch in the K/V ring: per-request pair offsets, bucket counts, keys, order
   static constexpr int MAX_SORT_REQS = 1024;
   static constexpr int MAX_SORT_PAIRS = 8192;
+  static constexpr int SORT_BUCKETS = 1024;              // sort key range (estimated cost, clamped)
   static constexpr uint32_t TMEM_TILE = 256;           // tile t: O at 256 t, S buffers at 256 t + D + {0, BN}
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr int KV_IT = BN * CPR / 32;          // cp.async per producer lane per K (or V) tile
@@ -81,7 +82,7 @@ struct PrefillCfg {
   static_assert((Q_OFF | K_OFF | V_OFF | Q_BYTES | KV_BYTES) % 1024 == 0, "swizzle atoms must be 1024-byte aligned");
   static_assert(D + 2 * BN <= (int)TMEM_TILE, "tensor-memory budget per tile");
   static_assert(KV_IT * 32 == BN * CPR && D % 64 == 0, "whole warp iterations, whole 128-byte column blocks");
-  static_assert((MAX_SORT_REQS + 1 + 256) * 4 + MAX_SORT_PAIRS * 4 <= 2 * STAGES * KV_BYTES, "prologue scratch");
+  static_assert((MAX_SORT_REQS + 1 + SORT_BUCKETS) * 4 + MAX_SORT_PAIRS * 4 <= 2 * STAGES * KV_BYTES, "prologue scratch");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
@@ -266,15 +267,18 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::BAR_OFF + 8 * C::NBAR + 4);
 
   // ---- work order, computed identically by every CTA (no cross-CTA communication): items
-  // sorted by cost (KV tiles x query tiles, descending; ties by index) and dealt out in snake
-  // order (CTA c takes sorted positions c, 2G-1-c, 2G+c, ... for G CTAs), which keeps the
-  // per-CTA totals within a few percent of each other.  The KV heads of one query-tile pair
+  // sorted by estimated time (descending; ties by index) and dealt out in snake order (CTA c
+  // takes sorted positions c, 2G-1-c, 2G+c, ... for G CTAs).  The estimate, in half KV tiles,
+  // weighs the KV tiles an item streams (the S -> softmax -> P V chain of each query tile
+  // sets the pace per KV tile), its (query tile, KV tile) MMA units and a fixed per-item cost
+  // (pipeline fill and drain, epilogue): 2 n_tiles + units / 4 + 9, less 3 for a single query
+  // tile, coefficients fitted to measured per-CTA end times.  The KV heads of one query-tile pair
   // cost the same and have consecutive indices, so the pairs are sorted and then expanded.
   // Each CTA keeps only its own list; problems too large for it use the natural order.
   int* list = reinterpret_cast<int*>(smem + C::LIST_OFF);
   int* pst = reinterpret_cast<int*>(smem + C::K_OFF);  // scratch: the K/V ring is not in use yet
   int* cnt = pst + C::MAX_SORT_REQS + 1;
-  uint16_t* key = reinterpret_cast<uint16_t*>(cnt + 256);
+  uint16_t* key = reinterpret_cast<uint16_t*>(cnt + C::SORT_BUCKETS);
   uint16_t* order = key + C::MAX_SORT_PAIRS;
   const int H = p.num_kv_heads;
   int per_cta = 0;
@@ -308,11 +312,12 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
       const int b = upper_index(pst, p.batch, w);
       PrefillItem it;
       fill_item<BQ2, C::BQ, C::BN>(p, b, w - pst[b], 0, it);
-      int c = 2;  // fixed part of an item, in KV-tile units
-      for (int t = 0; t < it.nq; ++t) c += (it.cb + min(it.q_len, it.first0 + (t + 1) * C::BQ) + C::BN - 1) / C::BN;
-      key[w] = (uint16_t)(255 - min(c, 255));  // ascending key = descending cost
+      int units = 0;
+      for (int t = 0; t < it.nq; ++t) units += (it.cb + min(it.q_len, it.first0 + (t + 1) * C::BQ) + C::BN - 1) / C::BN;
+      const int c = 2 * it.n_tiles + (units + 2) / 4 + 9 - (it.nq == 1 ? 3 : 0);
+      key[w] = (uint16_t)(C::SORT_BUCKETS - 1 - min(max(c, 0), C::SORT_BUCKETS - 1));  // ascending key = descending cost
     }
-    for (int i = tid; i < 256; i += C::THREADS) cnt[i] = 0;
+    for (int i = tid; i < C::SORT_BUCKETS; i += C::THREADS) cnt[i] = 0;
     __syncthreads();
     if (warp == 0) {  // stable counting sort of the pairs, one warp, chunks of 32 in index order
       for (int base = 0; base < n_pairs; base += 32) {
@@ -322,12 +327,13 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
         if (w < n_pairs && (peers & ((1u << lane) - 1u)) == 0u) cnt[k] += __popc(peers);
         __syncwarp();
       }
-      int v[8];  // exclusive scan of the 256 counts, 8 per lane
+      constexpr int BPL = C::SORT_BUCKETS / 32;  // exclusive scan of the bucket counts, BPL per lane
+      int v[BPL];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = cnt[lane * 8 + i];
+      for (int i = 0; i < BPL; ++i) v[i] = cnt[lane * BPL + i];
       int tot = 0;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) tot += v[i];
+      for (int i = 0; i < BPL; ++i) tot += v[i];
       int inc = tot;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -336,8 +342,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
       }
       int run = inc - tot;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        cnt[lane * 8 + i] = run;
+      for (int i = 0; i < BPL; ++i) {
+        cnt[lane * BPL + i] = run;
         run += v[i];
       }
       __syncwarp();
