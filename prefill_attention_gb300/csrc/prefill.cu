@@ -61,9 +61,9 @@ struct PrefillCfg {
   static constexpr int K_OFF = Q_OFF + Q_SLOTS * Q_BYTES;  // STAGES tiles
   static constexpr int V_OFF = K_OFF + STAGES * KV_BYTES;
   static constexpr int BAR_OFF = V_OFF + STAGES * KV_BYTES;
-  // barriers: kv_full, kv_empty [STAGES]; q_full, q_free [Q_SLOTS]; s_full, p_full [NQ][2];
-  // o_done, o_free [NQ]; fin.  Then the error flag and TMEM address.
-  static constexpr int NBAR = 2 * STAGES + 2 * Q_SLOTS + 6 * NQ + 1;
+  // barriers: kv_full, kv_empty [STAGES]; q_full, q_free, o_staged [Q_SLOTS]; s_full, p_full
+  // [NQ][2]; o_done, o_free [NQ]; fin.  Then the error flag and TMEM address.
+  static constexpr int NBAR = 2 * STAGES + 3 * Q_SLOTS + 6 * NQ + 1;
   static constexpr int LIST_OFF = (BAR_OFF + NBAR * 8 + 8 + 15) & ~15;
   // this CTA's items in order, as (request, pair within the request, KV head)
   static constexpr int MAX_CTA_ITEMS = 128;
@@ -211,7 +211,8 @@ __device__ __forceinline__ int upper_index(const int* pst, int n, int x) {
 
 template <int D, int G>
 __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(const PrefillParams p,
-                                                                                const __grid_constant__ CUtensorMap q_map) {
+                                                                                const __grid_constant__ CUtensorMap q_map,
+                                                                                const __grid_constant__ CUtensorMap o_map) {
   using C = PrefillCfg<D, G>;
   constexpr int BQ2 = C::NQ * C::BQ;
   extern __shared__ __align__(1024) unsigned char smem[];
@@ -225,9 +226,11 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
   // query tile number u (counted over the CTA's items, in order) lives in slot u % Q_SLOTS
   auto q_full = [&](int u) { return bars + 8u * (2 * C::STAGES + u % C::Q_SLOTS); };
   auto q_free = [&](int u) { return bars + 8u * (2 * C::STAGES + C::Q_SLOTS + u % C::Q_SLOTS); };
+  // output rows of tile u staged in its slot (by the tile's softmax warps)
+  auto o_staged = [&](int u) { return bars + 8u * (2 * C::STAGES + 2 * C::Q_SLOTS + u % C::Q_SLOTS); };
   auto q_par = [&](int u) { return (uint32_t)((u / C::Q_SLOTS) & 1); };
   auto q_slot = [&](int u) { return sbase + C::Q_OFF + (u % C::Q_SLOTS) * C::Q_BYTES; };
-  const uint32_t tb = bars + 8u * (2 * C::STAGES + 2 * C::Q_SLOTS);  // per-tile barriers
+  const uint32_t tb = bars + 8u * (2 * C::STAGES + 3 * C::Q_SLOTS);  // per-tile barriers
   // S / P of the g-th KV tile of query tile t live in buffer g & 1 (g counts over all items);
   // each buffer has its own barriers, so no waiter is ever more than one phase behind.
   auto s_full = [&](int t, int buf) { return tb + 8u * (2 * t + buf); };
@@ -244,9 +247,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
     }
     for (int u = 0; u < C::Q_SLOTS; ++u) {
       tc::mbar_init(q_full(u), 1);  // arrive + TMA transaction bytes
-      // lane 0 of the four softmax warps of the tile (after its output rows left the slot) and
-      // every MMA thread (once it has seen the tile)
-      tc::mbar_init(q_free(u), 4 + C::NQ);
+      tc::mbar_init(q_free(u), C::NQ);  // every MMA thread, once it has seen the tile
+      tc::mbar_init(o_staged(u), 4);    // lane 0 of the tile's four softmax warps
     }
     for (int t = 0; t < C::NQ; ++t) {
       for (int buf = 0; buf < 2; ++buf) {
@@ -397,26 +399,68 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
   };
 
   if (warp == C::Q_WARP) {
-    // ======================= query tiles by TMA, in order, each as soon as the tile that
-    //                         used its slot before has left it.  Rows past the request's end
-    //                         hold other requests' queries (never stored) or, past the last
-    //                         row, zeros
+    // ======================= query tiles in, output tiles out, by TMA, in tile order.  Tile u
+    //                         loads into slot u % Q_SLOTS once the tile that used the slot
+    //                         before (u - Q_SLOTS) has been written out from it; that tile's
+    //                         softmax warps staged its output rows there.  Query rows past the
+    //                         request's end hold other requests' queries (never written out)
+    //                         or, past the last row, zeros.
     bool ok = true;
     int u = 0;  // query tiles so far
+    // where each slot's tile goes (lane k holds slot k): first position, first head, rows
+    int pend_pos = 0, pend_head = 0, pend_rows = 0;
+    // write tile v's staged rows out: one TMA store per 64-column block when all BQ positions
+    // are the request's, else the valid rows with coalesced stores (never past the request)
+    auto write_out = [&](int v) {
+      if (!(ok = wait_or_fail(o_staged(v), q_par(v)))) return;
+      const int k = v % C::Q_SLOTS;
+      const int pos = __shfl_sync(kFullMask, pend_pos, k), head = __shfl_sync(kFullMask, pend_head, k);
+      const int rows = __shfl_sync(kFullMask, pend_rows, k);
+      const uint32_t src = q_slot(v);
+      if (rows == C::M) {
+        if (lane == 0) {
+          for (int cb = 0; cb < D / 64; ++cb) tc::tma_store_3d(&o_map, src + cb * (C::M * 128), cb * 64, head, pos);
+          tc::bulk_commit();
+          tc::bulk_wait_read_all();  // the slot may be refilled once the stores have read it
+        }
+      } else {
+        uint16_t* obase = p.out + ((size_t)pos * p.num_qo_heads + (size_t)head) * D;
+        for (int i = 0; i < C::M * C::CPR / 32; ++i) {
+          const int flat = i * 32 + lane, r = flat / C::CPR, c = flat % C::CPR;
+          if (r < rows) {
+            const uint4 x = lds128(src + sw128(r, c, C::M));
+            *reinterpret_cast<uint4*>(obase + ((size_t)(r / G) * p.num_qo_heads + r % G) * D + c * 8) = x;
+          }
+        }
+        tc::fence_proxy_async_smem();  // the next TMA write of this slot follows these reads
+      }
+      __syncwarp();
+    };
     PrefillItem it;
     for (int n_item = 0; ok; ++n_item) {
       if (!get_item(n_item, it)) break;
       for (int t = 0; ok && t < it.nq; ++t, ++u) {
-        if (u >= C::Q_SLOTS && !(ok = wait_or_fail(q_free(u), q_par(u) ^ 1u))) break;
+        if (u >= C::Q_SLOTS) {
+          write_out(u - C::Q_SLOTS);
+          if (!ok || !(ok = wait_or_fail(q_free(u), q_par(u) ^ 1u))) break;
+        }
+        const int qf = it.first0 + t * C::BQ;
+        if (lane == u % C::Q_SLOTS) {
+          pend_pos = it.q0 + qf;
+          pend_head = it.kvh * G;
+          pend_rows = (min(it.q_len, qf + C::BQ) - qf) * G;
+        }
         if (lane == 0) {
           tc::mbar_arrive_expect_tx(q_full(u), (uint32_t)C::Q_BYTES);
           for (int cb = 0; cb < D / 64; ++cb)
-            tc::tma_load_3d(q_slot(u) + cb * (C::M * 128), &q_map, cb * 64, it.kvh * G,
-                            it.q0 + it.first0 + t * C::BQ, q_full(u));
+            tc::tma_load_3d(q_slot(u) + cb * (C::M * 128), &q_map, cb * 64, it.kvh * G, it.q0 + qf, q_full(u));
         }
         __syncwarp();
       }
     }
+    for (int v = max(0, u - C::Q_SLOTS); ok && v < u; ++v) write_out(v);  // the last tiles
+    if (lane == 0) tc::bulk_wait_all();
+    __syncwarp();
   } else if (warp >= C::KV_WARP0) {
     // ======================= K/V gathers: warp KV_WARP0 + s fills stage s with every KV tile
     //                         g = s mod STAGES (g counts over all items)
@@ -729,8 +773,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
       if (!ok) break;
 
       // ---- epilogue, once the last P V of this tile has landed: O / l as bf16 into the
-      // tile's query slot (free: every S that read it is complete), release O, then the warp
-      // writes its 32 rows out with coalesced stores and releases the slot
+      // tile's query slot (free: every S that read it is complete), release O, and hand the
+      // slot to the query warp, which writes the rows out while these warps go on
       ok = wait_or_fail(o_done(t), (uint32_t)(n_used & 1));
       tc::fence_after_sync();
       tc::fence_proxy_async_smem();  // the tensor core's reads of this buffer precede the writes below
@@ -752,24 +796,10 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
         }
       }
       tc::fence_before_sync();
-      tc::mbar_arrive(o_free(t));  // O of this tile may be overwritten by the next item
+      tc::mbar_arrive(o_free(t));    // O of this tile may be overwritten by the next item
+      tc::fence_proxy_async_smem();  // the staged rows are read by TMA stores (async proxy)
       __syncwarp();
-      {
-        const int n_valid = (ql - qf + 1) * G;  // rows [0, n_valid) of the tile are real positions
-        const int r0 = (warp & 3) * 32;
-        uint16_t* obase = p.out + ((size_t)(it.q0 + qf) * p.num_qo_heads + (size_t)it.kvh * G) * D;
-#pragma unroll 4
-        for (int i = 0; i < C::CPR; ++i) {  // RPI rows (512 contiguous bytes when G >= RPI) per store
-          const int r = r0 + i * C::RPI + lane / C::CPR, c = lane % C::CPR;
-          if (r < n_valid) {
-            const uint4 v = lds128(stg + sw128(r, c, C::M));
-            *reinterpret_cast<uint4*>(obase + ((size_t)(r / G) * p.num_qo_heads + r % G) * D + c * 8) = v;
-          }
-        }
-      }
-      tc::fence_proxy_async_smem();  // the next TMA write of this buffer follows these accesses
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(q_free(u));
+      if (lane == 0) tc::mbar_arrive(o_staged(u));
       gs += n_keys;
       ++n_used;
       g_base += it.n_tiles;
@@ -815,16 +845,20 @@ cudaError_t launch_prefill_t(const PrefillParams& p, cudaStream_t stream) {
   // q as [total_q][Hq][D] bf16; one box = BQ positions x the G heads of a KV head x 64 columns
   const PFN_cuTensorMapEncodeTiled_v12000 encode = encode_tiled();
   if (encode == nullptr) return cudaErrorNotSupported;
-  CUtensorMap q_map;
+  // (out has the same layout; its map writes whole tiles of one request)
+  CUtensorMap q_map, o_map;
   const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.num_qo_heads, (cuuint64_t)p.total_q};
   const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)p.num_qo_heads * D * 2};
   const cuuint32_t box[3] = {64u, (cuuint32_t)G, (cuuint32_t)C::BQ};
   const cuuint32_t elem_strides[3] = {1u, 1u, 1u};
   if (encode(&q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(p.q), dims, strides, box,
              elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+      encode(&o_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.out, dims, strides, box, elem_strides,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  prefill_kernel<D, G><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(p, q_map);
+  prefill_kernel<D, G><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(p, q_map, o_map);
   return cudaGetLastError();
 }
 
