@@ -407,6 +407,9 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
     //                         or, past the last row, zeros.
     bool ok = true;
     int u = 0;  // query tiles so far
+    // query tiles are read and output tiles written once: first out of L2, ahead of the K/V
+    // rows that the other query tiles of the same request read again
+    const uint64_t once = tc::l2_evict_first_policy();
     // where each slot's tile goes (lane k holds slot k): first position, first head, rows
     int pend_pos = 0, pend_head = 0, pend_rows = 0;
     // write tile v's staged rows out: one TMA store per 64-column block when all BQ positions
@@ -419,7 +422,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
       const uint32_t src = q_slot(v);
       if (rows == C::M) {
         if (lane == 0) {
-          for (int cb = 0; cb < D / 64; ++cb) tc::tma_store_3d(&o_map, src + cb * (C::M * 128), cb * 64, head, pos);
+          for (int cb = 0; cb < D / 64; ++cb)
+            tc::tma_store_3d_hint(&o_map, src + cb * (C::M * 128), cb * 64, head, pos, once);
           tc::bulk_commit();
           tc::bulk_wait_read_all();  // the slot may be refilled once the stores have read it
         }
@@ -453,7 +457,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
         if (lane == 0) {
           tc::mbar_arrive_expect_tx(q_full(u), (uint32_t)C::Q_BYTES);
           for (int cb = 0; cb < D / 64; ++cb)
-            tc::tma_load_3d(q_slot(u) + cb * (C::M * 128), &q_map, cb * 64, it.kvh * G, it.q0 + qf, q_full(u));
+            tc::tma_load_3d_hint(q_slot(u) + cb * (C::M * 128), &q_map, cb * 64, it.kvh * G, it.q0 + qf, q_full(u),
+                                 once);
         }
         __syncwarp();
       }

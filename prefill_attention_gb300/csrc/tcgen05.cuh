@@ -66,23 +66,35 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 
 // ---------------------------------------------------------------- TMA (tensor copies)
 
-// 3-D tiled load of one box at coordinates (x innermost, y, z) into shared memory; the box's
-// bytes (including zeros filled in for coordinates outside the tensor) complete on `bar`.
-// x times the element size must be a multiple of 16 bytes.
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int x, int y, int z, uint32_t bar) {
+// L2 policy that marks lines as first to evict (for data read or written once).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// 3-D tiled load of one box at coordinates (x innermost, y, z) into shared memory with an L2
+// cache policy; the box's bytes (including zeros filled in for coordinates outside the tensor)
+// complete on `bar`.  x times the element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void* tmap, int x, int y, int z, uint32_t bar,
+                                                 uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
-      "[%5];" ::"r"(dst),
-      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar)
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
+      "{%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
       : "memory");
 }
 
 // 3-D tiled store of one box from shared memory (same box and swizzle as the tensor map's
-// loads), tracked by this thread's bulk async-group.  Coordinates must not be negative.
-__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int x, int y, int z) {
-  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(tmap),
-               "r"(src), "r"(x), "r"(y), "r"(z)
-               : "memory");
+// loads) with an L2 cache policy, tracked by this thread's bulk async-group.  Coordinates
+// must not be negative.
+__device__ __forceinline__ void tma_store_3d_hint(const void* tmap, uint32_t src, int x, int y, int z,
+                                                  uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%2, %3, %4}], [%1], %5;" ::"l"(
+          tmap),
+      "r"(src), "r"(x), "r"(y), "r"(z), "l"(policy)
+      : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until every committed bulk store of this thread has finished reading shared memory.
