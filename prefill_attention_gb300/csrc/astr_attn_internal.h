@@ -24,9 +24,10 @@ struct DecodeParams {
   int64_t r2t_stride;
   int64_t num_slots;             // rows of k_pool / v_pool (sizes the gather tensor maps)
   int batch, num_qo_heads, num_kv_heads, head_dim;
-  int num_splits;                // key chunks per KV head (kDecodeChunksPerCta per CTA)
+  int num_splits;                // chunks per KV head (kDecodeChunksPerCta per CTA)
   int part_pitch;                // partial slots per (b, h) row of o_part (= max_splits)
-  int min_chunk;                 // floor on the chunk length so no request needs > part_pitch slots
+  int min_chunk;                 // floor on the chunk length (32-key slots) so no request needs
+                                 // more than part_pitch partial slots
   float scale_log2;              // sm_scale * log2(e): logits are kept in base-2 units on chip
   int combine_all;               // combine even single-chunk requests (partials supplied by the caller)
   int indptr_before_wait;        // combine: kv_indptr may be read before the dependency wait (the

@@ -13,40 +13,38 @@
 //     step; here it drives the split schedule.
 //
 // GB300 design:
-//   * Token-balanced split schedule.  For each KV head the flat key space [0, T) of the
-//     whole batch (T = kv_indptr[B]) is cut into equal chunks of C keys, one CTA per chunk,
-//     so every CTA moves the same number of bytes however skewed seq_lens is.  A chunk may
-//     hold the tail of one request and the head of the next; each such piece produces one
-//     partial, indexed by (chunk - first chunk of the request), and a request that lies
-//     inside one chunk is written to the output directly.  C depends only on T, the grid
-//     and a host-supplied floor, so the combine recomputes it identically.
-//   * One persistent CTA per SM, warp specialised:
-//       warps 4-9 (producers) -- three groups of two warps, group g owning ring stage g
-//               (tiles g, g+3, ...): a group gathers the K and V rows of its 128-key tile
-//               slot by slot with 16-byte cp.async into a 128-byte-swizzled layout (16-byte
-//               chunk c of row r at c ^ (r & 7), so 8 consecutive rows of one chunk hit 8
-//               different bank groups).  Each 32-key quarter of a tile is its own cp.async
-//               group with its own full barrier, so a quarter is published as soon as it
-//               lands.  Three 64 KB tiles are in flight.
-//       warps 0-3 (consumers) -- warp w takes quarter (w + j) mod 4 of tile j and keeps its
-//               own online-softmax state.  The products are computed transposed, S^T = K Q^T
-//               and O^T += V^T P^T, as warp-level bf16 MMAs (m16n8k16, fp32 accumulators in
-//               registers, operands via ldmatrix from the swizzled tiles): the 16-row MMA
-//               side is keys or head_dim and the 8-wide side the G query heads of the KV
-//               head, so one K/V load serves all of them with little padding.  P goes from
-//               the S^T accumulator layout to the B-operand layout with movmatrix.  P is
-//               split into hi = bf16(p) and lo = bf16(p - hi) and both halves go through the
-//               MMA, which keeps p to ~2^-17 relative precision.  Softmax in base 2 (the
-//               scale carries log2 e) with a lazy rescale: a warp moves its reference max
-//               only when a score exceeds it by more than 2^8.  A quarter with no valid key
-//               (the ragged end of a piece) is skipped; rotating the quarters spreads those
-//               savings over the warps.  The four warps merge once per request piece
-//               through shared memory; there is no per-tile CTA synchronisation.
-//     Measured alternatives (see the profiles): a CUDA-core version was issue bound
-//     (~550 instructions per 4 KB of K/V); a tcgen05 version with S^T / O^T accumulators in
-//     tensor memory spent ~150 cycles per M=128 x N=16 x K=16 MMA, ~2400 cycles per 64 KB
-//     tile on the critical path; TMA tile::gather4 for the row gather delivered ~12 GB/s
-//     per SM.
+//   * Slot-balanced split schedule.  Each request's keys are cut into 32-key slots from its
+//     first key (the last one possibly short); for each KV head the batch's slots lie end to
+//     end (request b starts at slot SP_b) and are cut into equal chunks of C slots, one warp
+//     pair per chunk, so every pair runs the same number of ring slots however skewed
+//     seq_lens is.  (Slots, not keys: with every pair's slots in flight the memory system is
+//     saturated and a pair's pace is its slots in flight per round trip, so a short slot
+//     costs as much as a full one.)  A chunk may hold the tail of one request and the head
+//     of the next; each such piece produces one partial, indexed by (chunk - SP_b / C), and a
+//     request that lies inside one chunk is written to the output directly.  C depends only
+//     on kv_indptr, the grid and a host-supplied floor, so the combine recomputes it.
+//   * One CTA per SM with four independent (producer, consumer) warp pairs, each with its
+//     own chunk and its own ring of 32-key slots (K, V and the piece's query rows):
+//       producer -- lane k reads the slot id of key k (one slot ahead) and gathers the K and
+//               V rows with 16-byte cp.async into 128-byte-swizzled tiles (chunk c of row r
+//               at c ^ (r & 7)); cp.async.mbarrier.arrive publishes a slot when it lands, so
+//               the producer never waits for its own copies, only for a free slot.
+//       consumer -- S^T = K Q^T and O^T += V^T P^T as warp-level bf16 MMAs (m16n8k16, fp32
+//               accumulators in registers, operands by ldmatrix): the 16-row side is keys or
+//               head_dim and the 8-wide side the G query heads, so one K/V load serves all
+//               of them with little padding.  P goes to the B-operand layout by movmatrix,
+//               split into hi = bf16(p) and lo = bf16(p - hi), both through the MMA (p to
+//               ~2^-17 relative).  Base-2 softmax with a lazy rescale (the reference max moves
+//               only when a score exceeds it by more than 2^8); the exact max is kept for the
+//               partial.  At a piece end the result is staged through the slot just used and
+//               written with 16-byte stores.
+//   * Launched as a programmatic dependent: shared-memory set-up and an L2 warm-up of each
+//     pair's first slots (from tables read through L2 only; prefetch hints, nothing kept)
+//     run before griddepcontrol.wait, so the first misses overlap the previous kernel.
+//   * Measured alternatives: a CUDA-core version was issue bound (~550 instructions per
+//     4 KB of K/V); a tcgen05 version with S^T / O^T accumulators in tensor memory spent
+//     ~150 cycles per M=128 x N=16 x K=16 MMA on the critical path; TMA tile::gather4 for
+//     the row gather delivered ~12 GB/s per SM.
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
