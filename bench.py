@@ -79,6 +79,18 @@ def decode_bytes(w) -> dict:
 # ------------------------------------------------------------------ traffic record
 
 
+def source_digest(path: str) -> str:
+    """sha-256 (first 16 hex digits) of a CUDA source with comments and whitespace removed, so
+    that a counter record survives comment edits but not code changes."""
+    import re
+    with open(path, "r") as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    text = re.sub(r"\s+", "", text)
+    return hashlib.sha256(text.encode()).hexdigest()[:16]
+
+
 def recorded_traffic(kernel: str, source: str):
     """Per-launch DRAM bytes from the committed ncu summary, if it was taken on this source."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -88,9 +100,7 @@ def recorded_traffic(kernel: str, source: str):
         rec = json.load(f).get(kernel)
     if not rec:
         return None
-    with open(os.path.join(ROOT, "prefill_attention_gb300", "csrc", source), "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()[:16]
-    if rec.get("source_sha") != sha:
+    if rec.get("source_digest") != source_digest(os.path.join(ROOT, "prefill_attention_gb300", "csrc", source)):
         return None
     return rec.get("bytes_per_launch")
 
