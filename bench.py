@@ -48,6 +48,7 @@ DECODE_CFG = 2
 PREFILL_CFG = 5
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 POOL_COPIES = 4          # rotate KV-pool copies so each call's working set is cold in L2
+                         # (fewer when one pool alone is several times the L2)
 MAX_SPLITS = 64
 
 
@@ -203,7 +204,7 @@ def run_reference(args, rank: int, world: int):
         return
     import oracle
     oracle.build()
-    w = workload.config(DECODE_CFG)
+    w = workload.config(args.decode_workload)
     cores = os.cpu_count() or 1
     # each step: the whole B=32 batch (all 1024 (request, head) rows), fp64, all host cores
     for _ in range(args.warmup):
@@ -214,12 +215,14 @@ def run_reference(args, rank: int, world: int):
     dt = (time.perf_counter() - t0) / max(args.steps, 1)
     val = w.kv_bytes() / dt / 1e9
     line = {
-        "impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": "GB/s", "n_gpus": args.gpus,
+        "impl": "reference",
+        "metric": METRIC if args.decode_workload == DECODE_CFG else METRIC.split(", B=")[0] + f", {w.name}",
+        "value": round(val, 4), "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "seed": w.seed, "sample": "whole batch per step"},
         "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": "whole decode batch (32 requests x 32 heads) per step, fp64 C oracle"},
+                         "sample": f"whole decode batch ({w.batch} requests x {w.num_qo_heads} heads) per step, fp64 C oracle"},
         "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -237,6 +240,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--num-splits", type=int, default=0, help="force the decode split count (0 = planned)")
+    ap.add_argument("--decode-workload", type=int, default=DECODE_CFG, choices=[1, 2, 3, 4],
+                    help="decode workload of the step (default 2, the headline; 3 = long context, "
+                         "4 = large batch are extra measurements, not the headline)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -275,7 +281,7 @@ def main():
     peaks, peaks_src = load_peaks()
 
     # ---------------- decode inputs (replica per rank, same seed so every rank does equal work)
-    w = workload.config(DECODE_CFG)
+    w = workload.config(args.decode_workload)
     nbytes = decode_bytes(w)
 
     def bf(a):
@@ -285,7 +291,8 @@ def main():
         return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
 
     q = bf(w.q)
-    pools = [(bf(w.k_pool), bf(w.v_pool)) for _ in range(POOL_COPIES)]
+    n_copies = max(1, min(POOL_COPIES, -(-int(6e8) // max(int(nbytes["kv"]), 1))))
+    pools = [(bf(w.k_pool), bf(w.v_pool)) for _ in range(n_copies)]
     r2t, seq, kvi = i32(w.req_to_token), i32(w.seq_lens), i32(w.kv_indptr)
     dims = pa.make_dims(w.batch, w.num_qo_heads, w.num_kv_heads, w.head_dim, w.num_slots, w.r2t_stride,
                         w.max_seq_len, max_splits=MAX_SPLITS, num_splits=args.num_splits)
@@ -296,11 +303,11 @@ def main():
     sh = int(stream.cuda_stream)
 
     def decode(i):
-        k, v = pools[i % POOL_COPIES]
+        k, v = pools[i % n_copies]
         pa.astr_attn_paged_decode(q, k, v, r2t, seq, kvi, o_part, ml_part, out, dims, w.sm_scale, stream=sh)
 
     def split_only(i):
-        k, v = pools[i % POOL_COPIES]
+        k, v = pools[i % n_copies]
         pa.astr_attn_decode_split(q, k, v, r2t, seq, kvi, o_part, ml_part, dims, w.sm_scale, stream=sh)
 
     def timed(fn, n):
@@ -436,7 +443,7 @@ def main():
 
     traffic = recorded_traffic("decode_split", "decode.cu")
     line = {
-        "metric": METRIC,
+        "metric": METRIC if args.decode_workload == DECODE_CFG else METRIC.split(", B=")[0] + f", {w.name}",
         "value": round(value, 2),
         "unit": "GB/s",
         "n_gpus": world,
@@ -454,7 +461,7 @@ def main():
         "data": "synthetic",
         "config": {"workload": w.name, "seed": w.seed, "page_size": 1, "num_splits": S,
                    "kv_bytes_per_call": nbytes["kv"], "total_keys": int(w.seq_lens.sum()),
-                   "l2": f"rotating {POOL_COPIES} KV-pool copies ({POOL_COPIES * nbytes['kv'] / 1e6:.0f} MB > L2)",
+                   "l2": f"rotating {n_copies} KV-pool copies ({n_copies * nbytes['kv'] / 1e6:.0f} MB > L2)",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "kernel": "decode_split_kernel<128,4>", "achieved": round(split_gbs, 2),
                      "peak": peaks["hbm_gbs"], "peak_source": f"hbm_gbs ({peaks_src})", "unit": "GB/s",
