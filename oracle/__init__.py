@@ -22,7 +22,7 @@ _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lib = None
 
 __all__ = ["build", "lib_path", "decode", "prefill", "decode_split_partials", "decode_chunk_partials",
-           "chunk_split_counts", "combine", "load_variant"]
+           "chunk_split_counts", "combine", "kv_append", "load_variant"]
 
 
 def _compile(src: str, out: str, extra: Sequence[str] = ()) -> None:
@@ -54,9 +54,10 @@ def _declare(lib):
     lib.oracle_prefill_rows.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _P, _L, _P, _D, _L, _P, _P, _P, _I]
     lib.oracle_decode_split_partials.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _L, _P, _D, _I, _P, _P, _I]
     lib.oracle_combine.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P]
+    lib.oracle_kv_append.argtypes = [_I, _I, _I, _P, _P, _P, _L, _P, _P, _P, _P]
     lib.oracle_decode_chunk_partials.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _L, _P, _P, _D, _L, _L, _I, _P, _P]
     for f in ("oracle_decode_rows", "oracle_prefill_rows", "oracle_decode_split_partials", "oracle_combine",
-              "oracle_decode_chunk_partials"):
+              "oracle_decode_chunk_partials", "oracle_kv_append"):
         getattr(lib, f).restype = None
     return lib
 
@@ -181,3 +182,18 @@ def combine(o_part: np.ndarray, ml_part: np.ndarray, nsplit: Optional[np.ndarray
     out = np.zeros((B, Hq, D), dtype=np.float64)
     lib.oracle_combine(B, Hq, S, D, _ptr(o_part), _ptr(ml_part), _ptr(ns), _ptr(out))
     return out
+
+
+def kv_append(w, qo_indptr, k_new: np.ndarray, v_new: np.ndarray, lib=None):
+    """KV append: the pools of ``w`` after writing new token i of request b into slot
+    ``req_to_token[b, seq_len_b - q_len_b + i]``.  ``qo_indptr`` [B+1] gives the new rows of
+    each request in ``k_new`` / ``v_new`` [total_q, Hkv, d] (bf16 bits).  Returns new arrays
+    (k_pool, v_pool); ``w`` is not modified."""
+    lib = lib or _get()
+    B, Hkv, D = w.batch, w.num_kv_heads, w.head_dim
+    kp, vp = np.array(w.k_pool, dtype=np.uint16, order="C"), np.array(w.v_pool, dtype=np.uint16, order="C")
+    qo, sl, r2t = _c(qo_indptr, np.int32), _c(w.seq_lens, np.int32), _c(w.req_to_token, np.int32)
+    kn, vn = _c(k_new, np.uint16), _c(v_new, np.uint16)
+    lib.oracle_kv_append(B, Hkv, D, _ptr(qo), _ptr(sl), _ptr(r2t), r2t.shape[1], _ptr(kn), _ptr(vn), _ptr(kp),
+                         _ptr(vp))
+    return kp, vp

@@ -28,6 +28,13 @@
  *   an empty split stores m = -inf, l = 0, o = 0;
  *   combine:  M = max_s m_s,  w_s = exp(m_s - M),  out = (sum_s w_s o_s) / (sum_s w_s l_s).
  *
+ * The KV-append step (page "astrai/extension/attention_backend.py @47b3ed4",
+ * write-then-gather helper commit: the new tokens' K and V are written into the pool
+ * before attention gathers from it).  Reading: new token i of request b is the key at
+ * position c_b + i of that request, so it is stored at slot req_to_token[b][c_b + i]:
+ *   k_pool[slot, :, :] = k_new[qo_indptr[b] + i, :, :],  v_pool likewise;
+ * every other pool row keeps its contents.
+ *
  * Parallelism: independent output rows are spread over POSIX threads; each row is
  * computed start to finish by one thread in the order written above.
  */
@@ -324,6 +331,24 @@ void oracle_combine(int B, int Hq, int S, int D, const double *o_part, const dou
         for (int d = 0; d < D; ++d) o[d] += w * o_part[(base + s) * D + d];
       }
       for (int d = 0; d < D; ++d) o[d] /= L;
+    }
+  }
+}
+
+/* KV append: copy each new token's K and V rows (all KV heads) into its pool slot.
+ * k_new, v_new: [total_q, Hkv, D]; pools are modified in place. */
+void oracle_kv_append(int B, int Hkv, int D, const int32_t *qo_indptr, const int32_t *seq_lens,
+                      const int32_t *req_to_token, int64_t r2t_stride, const uint16_t *k_new,
+                      const uint16_t *v_new, uint16_t *k_pool, uint16_t *v_pool) {
+  const int64_t row = (int64_t)Hkv * D;  /* elements of one slot (all KV heads) */
+  for (int b = 0; b < B; ++b) {
+    const int64_t q_len = (int64_t)qo_indptr[b + 1] - qo_indptr[b];
+    const int64_t c = (int64_t)seq_lens[b] - q_len;
+    for (int64_t i = 0; i < q_len; ++i) {
+      const int64_t src = (int64_t)qo_indptr[b] + i;
+      const int32_t slot = req_to_token[(int64_t)b * r2t_stride + c + i];
+      memcpy(k_pool + (int64_t)slot * row, k_new + src * row, sizeof(uint16_t) * (size_t)row);
+      memcpy(v_pool + (int64_t)slot * row, v_new + src * row, sizeof(uint16_t) * (size_t)row);
     }
   }
 }

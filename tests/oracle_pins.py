@@ -7,8 +7,11 @@ mutation tests) and raises AssertionError when the oracle disagrees with:
   * closed forms (q = 0 gives the mean of the visible V rows; one key gives that V row;
     constant V gives the constant; hand-worked examples in tests/golden),
   * invariances (slot permutation, key shift, per-request markers),
-  * the split-KV identity (partials + log-sum-exp combine equals unsplit softmax).
+  * the split-KV identity (partials + log-sum-exp combine equals unsplit softmax),
+  * the KV-append step: attention over the pool after the append equals SDPA over each
+    request's cached keys followed by its new rows, laid out contiguously.
 """
+import dataclasses
 import json
 import math
 import os
@@ -340,9 +343,67 @@ def pin_prefill_row_is_decode(lib):
             assert np.array_equal(dec, got[r]), f"prefill row b={b} i={i} != decode"
 
 
+def _contiguous_after_append(w, qo, k_new, v_new):
+    """The workload whose request b holds keys (its first c_b cached keys, then its new rows)
+    in consecutive slots -- built by hand, without the append step."""
+    seq = w.seq_lens.astype(np.int64)
+    q_len = np.diff(qo.astype(np.int64))
+    base = np.concatenate([[0], np.cumsum(seq)])
+    T = int(base[-1])
+    kp = np.zeros((max(T, 1), w.num_kv_heads, w.head_dim), np.uint16)
+    vp = np.zeros_like(kp)
+    r2t = np.zeros((w.batch, max(int(seq.max()), 1)), np.int32)
+    for b in range(w.batch):
+        c = int(seq[b] - q_len[b])
+        cached = w.req_to_token[b, :c].astype(np.int64)
+        kp[base[b]:base[b] + c] = w.k_pool[cached]
+        vp[base[b]:base[b] + c] = w.v_pool[cached]
+        kp[base[b] + c:base[b + 1]] = k_new[qo[b]:qo[b + 1]]
+        vp[base[b] + c:base[b + 1]] = v_new[qo[b]:qo[b + 1]]
+        r2t[b, :seq[b]] = np.arange(base[b], base[b + 1], dtype=np.int32)
+    return dataclasses.replace(w, k_pool=kp, v_pool=vp, req_to_token=r2t)
+
+
+def pin_append_then_attend_is_sdpa_over_concatenation(lib):
+    """After the append, attention over the pool sees each request's cached keys followed by
+    its new rows (prefill: q_len_b new tokens at the causal offset; decode: the current token
+    as the last key), checked against fp64 SDPA on a hand-built contiguous layout."""
+    for w in (_small_prefill(seed=101, pmax=6), _small_decode(seed=103)):
+        w = dataclasses.replace(w, req_to_token=np.pad(w.req_to_token, ((0, 0), (0, 3))))
+        qo, kn, vn = workload.append_rows(w, seed=105)
+        kp, vp = oracle.kv_append(w, qo, kn, vn, lib=lib)
+        after = dataclasses.replace(w, k_pool=kp, v_pool=vp)
+        got = oracle.prefill(after, lib=lib) if w.kind == "prefill" else oracle.decode(after, lib=lib)
+        ref = sdpa_paged(_contiguous_after_append(w, qo, kn, vn))
+        err = np.abs(got - ref).max()
+        assert err <= 1e-12, f"{w.kind}: attention after append vs SDPA over concatenation: {err}"
+
+
+def pin_append_touches_only_new_slots(lib):
+    """Slots that hold no new token keep their bytes; each new token's slot holds exactly its
+    K and V rows (checked through the inverse of the slot table)."""
+    w = _small_prefill(seed=107, pmax=6)
+    w = dataclasses.replace(w, req_to_token=np.pad(w.req_to_token, ((0, 0), (0, 3))))
+    qo, kn, vn = workload.append_rows(w, seed=109)
+    kp, vp = oracle.kv_append(w, qo, kn, vn, lib=lib)
+    owner = {}  # slot -> flat new row
+    for b in range(w.batch):
+        for i in range(int(qo[b + 1] - qo[b])):
+            pos = int(w.seq_lens[b]) - int(qo[b + 1] - qo[b]) + i
+            owner[int(w.req_to_token[b, pos])] = int(qo[b]) + i
+    for slot in range(w.num_slots):
+        if slot in owner:
+            r = owner[slot]
+            assert np.array_equal(kp[slot], kn[r]) and np.array_equal(vp[slot], vn[r]), f"slot {slot}"
+        else:
+            assert np.array_equal(kp[slot], w.k_pool[slot]) and np.array_equal(vp[slot], w.v_pool[slot]), \
+                f"slot {slot} changed"
+
+
 ALL_PINS = [
     pin_sdpa_decode, pin_sdpa_prefill, pin_prefix0_is_textbook_causal, pin_golden,
     pin_q_zero_is_mean_of_visible_v, pin_single_key_returns_v, pin_per_request_marker, pin_dominant_key,
     pin_slot_permutation, pin_key_shift, pin_unreferenced_slots_unread, pin_split_combine, pin_chunk_partials_combine,
     pin_partial_is_softmax_piece, pin_prefill_row_is_decode,
+    pin_append_then_attend_is_sdpa_over_concatenation, pin_append_touches_only_new_slots,
 ]

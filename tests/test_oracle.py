@@ -36,6 +36,9 @@ MUTANTS = {
     "q_head_major": ("widen_row(J->q + ((int64_t)b * P->Hq + h) * D, D, qbuf);\n    attend",
                      "widen_row(J->q + ((int64_t)h * J->B + b) * D, D, qbuf);\n    attend"),
     "split_floor_chunk": ("int64_t chunk = (n + J->S - 1) / J->S;", "int64_t chunk = n / J->S > 0 ? n / J->S : 1;"),
+    "append_position_shift": ("r2t_stride + c + i];", "r2t_stride + c + i + 1];"),
+    "append_k_into_v": ("memcpy(v_pool + (int64_t)slot * row, v_new", "memcpy(v_pool + (int64_t)slot * row, k_new"),
+    "append_source_row_local": ("const int64_t src = (int64_t)qo_indptr[b] + i;", "const int64_t src = i;"),
     "key_index_transposed": ("k_pool + ((int64_t)slot * P->Hkv + kvh) * P->D", "k_pool + ((int64_t)kvh * P->Hkv + slot % P->Hkv) * P->D"),
 }
 

@@ -21,7 +21,7 @@ import numpy as np
 
 __all__ = [
     "Workload", "CONFIGS", "config", "make_decode", "make_prefill",
-    "fp32_to_bf16_bits", "bf16_bits_to_fp32", "make_from_lengths",
+    "fp32_to_bf16_bits", "bf16_bits_to_fp32", "make_from_lengths", "append_rows",
 ]
 
 
@@ -176,6 +176,26 @@ def make_prefill(B: int, Hq: int, Hkv: int, d: int, qlen: tuple, prefix: tuple, 
     return make_from_lengths(rng, kind="prefill", name=name, seq_lens=seq_lens, q_lens=q_lens, Hq=Hq, Hkv=Hkv,
                              d=d, stride=stride if stride is not None else qlen[1] + prefix[1],
                              extra_slots=extra_slots, seed=seed)
+
+
+def append_rows(w: Workload, seed: int):
+    """New K/V rows for the KV-append step over workload ``w``: (qo_indptr, k_new, v_new).
+
+    A prefill workload appends its q_len_b new tokens per request (its own qo_indptr); a
+    decode workload appends one token per request that has at least one key (the current
+    token, the last key of the request).  k_new and v_new are [total_new, Hkv, d] bf16 bits,
+    drawn K then V from ``default_rng(seed)`` as fp32 N(0,1) rounded to bf16.
+    """
+    rng = np.random.default_rng(seed)
+    if w.qo_indptr is not None:
+        qo = np.asarray(w.qo_indptr, dtype=np.int32)
+    else:
+        qo = np.zeros(w.batch + 1, dtype=np.int32)
+        qo[1:] = np.cumsum(np.minimum(w.seq_lens, 1))
+    n = int(qo[-1])
+    k_new = _normal_bf16(rng, (n, w.num_kv_heads, w.head_dim))
+    v_new = _normal_bf16(rng, (n, w.num_kv_heads, w.head_dim))
+    return qo, k_new, v_new
 
 
 def config(idx: int, seed: Optional[int] = None) -> Workload:
