@@ -13,6 +13,8 @@ Also reported in the same line:
                     on its stream: algorithmic K+V bytes per launch / mean duration.
   * prefill      -- the ragged prefill entry point on the 16-request extend workload,
                     FLOP/s against the measured dense bf16 tensor-core peak.
+  * kv_append    -- the KV-append step (the extend workload's new K/V rows written into their
+                    pool slots), bytes moved per second against the measured HBM copy peak.
   * e2e          -- the same decode metric with every input in pinned host memory, the
                     host->device copies and the device->host read of `out` inside the
                     timed region (and a variant where only q and the index arrays move).
@@ -428,6 +430,27 @@ def main():
     flops = prefill_flops(wp)
     pf_tflops = flops / t_pf / 1e12
 
+    # ---------------- KV-append step on the extend workload (rotating copies: cold in L2)
+    aqo_np, akn_np, avn_np = workload.append_rows(wp, seed=wp.seed + 1)
+    a_rows = int(aqo_np[-1])
+    a_bytes = 4 * a_rows * wp.num_kv_heads * wp.head_dim * 2  # read K and V rows, write them
+    a_copy_bytes = 2 * akn_np.nbytes + 2 * wp.k_pool.nbytes
+    n_app = max(2, min(8, -(-int(8e8) // a_copy_bytes)))
+    aqo = i32(aqo_np)
+    app_sets = [(bf(akn_np), bf(avn_np), bf(wp.k_pool), bf(wp.v_pool)) for _ in range(n_app)]
+    adims = pa.make_dims(wp.batch, wp.num_qo_heads, wp.num_kv_heads, wp.head_dim, wp.num_slots, wp.r2t_stride,
+                         wp.max_seq_len, total_q=a_rows)
+
+    def kv_append(i):
+        kn, vn, kp_, vp_ = app_sets[i % n_app]
+        pa.astr_attn_kv_append(kn, vn, aqo, pr, ps_, kp_, vp_, adims, stream=sh)
+
+    timed(kv_append, 3 * n_app)
+    n_a = max(40, min(args.steps // 10, 400))
+    t_app = timed(kv_append, n_a) / n_a
+    app_gbs = a_bytes / t_app / 1e9
+    del app_sets
+
     # ---------------- CPU baseline: the oracle on this host (rank 0 at N=1 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -473,6 +496,13 @@ def main():
                                  "peak_source": f"bf16_tflops burst ({peaks_src})", "unit": "TFLOP/s",
                                  "frac": round(pf_tflops / peaks["bf16_tflops"], 4),
                                  "traffic": recorded_traffic("prefill", "prefill.cu")}},
+        "kv_append": {"workload": wp.name, "rows": a_rows, "us_per_call": round(t_app * 1e6, 3),
+                      "bytes_per_call": a_bytes,
+                      "l2": f"rotating {n_app} input/pool copies ({n_app * a_copy_bytes / 1e6:.0f} MB)",
+                      "roofline": {"bound": "hbm", "achieved": round(app_gbs, 2), "peak": peaks["hbm_gbs"],
+                                   "peak_source": f"hbm_gbs ({peaks_src})", "unit": "GB/s",
+                                   "frac": round(app_gbs / peaks["hbm_gbs"], 4),
+                                   "traffic": recorded_traffic("kv_append", "append.cu")}},
         "e2e": {"value": round(sum_over_ranks(nbytes["kv"]) / t_e2e_full / 1e9, 3), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d_full, "d2h_bytes_per_step": d2h,
                 "resident_kv": {"value": round(sum_over_ranks(nbytes["kv"]) / t_e2e_res / 1e9, 3), "unit": "GB/s",

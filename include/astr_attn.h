@@ -194,6 +194,30 @@ int astr_attn_paged_decode_noalloc(const uint16_t* q, const uint16_t* k_pool, co
                                    const int32_t* req_to_token, const int32_t* seq_lens, const int32_t* kv_indptr,
                                    uint16_t* out, const astr_attn_dims* dims, float sm_scale, void* stream);
 
+/*
+ * KV append: write the new tokens' K and V into their pool slots (P5, write-then-gather
+ * helper commit: the new K/V go into the pool before attention gathers from it).  Request b
+ * has q_len_b = qo_indptr[b+1] - qo_indptr[b] new tokens, which are its key positions
+ * c_b .. seq_lens[b] - 1 (c_b = seq_lens[b] - q_len_b, the prefill's causal offset; seq_lens
+ * already counts them).  For flat row r = qo_indptr[b] + i:
+ *   slot = req_to_token[b * r2t_stride + c_b + i],
+ *   k_pool[slot, :, :] = k_new[r, :, :],  v_pool[slot, :, :] = v_new[r, :, :]   (bit copies).
+ * Decode appends one token per request: qo_indptr[b] = b, the current token being the last
+ * key (position seq_lens[b] - 1).  Call it before astr_attn_prefill_ragged /
+ * astr_attn_paged_decode on the same stream.
+ *   - k_new, v_new: [total_q, num_kv_heads, head_dim] bf16 (dims->total_q rows), device,
+ *     16-byte aligned, not overlapping the pools.  k_pool / v_pool are written in place.
+ *   - Only the new tokens' slots change.  Distinct new tokens must map to distinct slots
+ *     (else which write lands is undefined).  A slot id outside [0, num_slots), or a
+ *     position outside the table row, is skipped (nothing written for that token).
+ *   - Reads dims->batch, num_kv_heads, head_dim, num_slots, r2t_stride, total_q (and checks
+ *     the shape fields as the attention calls do); batch = 0 or total_q = 0 does nothing.
+ * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, LAUNCH_FAILED.
+ */
+int astr_attn_kv_append(const uint16_t* k_new, const uint16_t* v_new, const int32_t* qo_indptr,
+                        const int32_t* req_to_token, const int32_t* seq_lens, uint16_t* k_pool, uint16_t* v_pool,
+                        const astr_attn_dims* dims, void* stream);
+
 /* Static description of a status code (never NULL). */
 const char* astr_attn_status_string(int status);
 

@@ -18,7 +18,7 @@ from typing import Optional
 __all__ = [
     "Dims", "AstrAttnError", "load", "lib_path", "make_dims",
     "astr_attn_paged_decode", "astr_attn_decode_split", "astr_attn_decode_combine", "astr_attn_prefill_ragged",
-    "astr_attn_paged_decode_noalloc",
+    "astr_attn_paged_decode_noalloc", "astr_attn_kv_append",
     "astr_attn_decode_num_splits", "astr_attn_decode_workspace_bytes", "astr_attn_status_string",
     "astr_attn_version", "alloc_decode_workspace",
     "ASTR_OK", "ASTR_ERR_INVALID_ARG", "ASTR_ERR_UNSUPPORTED", "ASTR_ERR_MISALIGNED",
@@ -40,7 +40,7 @@ _lib = None
 EXPORTED_SYMBOLS = [
     "astr_attn_decode_num_splits", "astr_attn_decode_workspace_bytes", "astr_attn_paged_decode",
     "astr_attn_decode_combine", "astr_attn_prefill_ragged", "astr_attn_status_string", "astr_attn_version",
-    "astr_attn_decode_split", "astr_attn_paged_decode_noalloc",
+    "astr_attn_decode_split", "astr_attn_paged_decode_noalloc", "astr_attn_kv_append",
 ]
 
 
@@ -83,12 +83,13 @@ def load():
     lib.astr_attn_decode_combine.argtypes = [P, P, P, P, P, D, P]
     lib.astr_attn_paged_decode_noalloc.argtypes = [P, P, P, P, P, P, P, D, F, P]
     lib.astr_attn_prefill_ragged.argtypes = [P, P, P, P, P, P, P, P, D, F, P]
+    lib.astr_attn_kv_append.argtypes = [P, P, P, P, P, P, P, D, P]
     lib.astr_attn_status_string.argtypes = [I32]
     lib.astr_attn_status_string.restype = ctypes.c_char_p
     lib.astr_attn_version.argtypes = []
     for f in ("astr_attn_decode_num_splits", "astr_attn_decode_workspace_bytes", "astr_attn_paged_decode",
               "astr_attn_decode_split", "astr_attn_decode_combine", "astr_attn_prefill_ragged", "astr_attn_version",
-              "astr_attn_paged_decode_noalloc"):
+              "astr_attn_paged_decode_noalloc", "astr_attn_kv_append"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -189,6 +190,14 @@ def astr_attn_prefill_ragged(q, qo_indptr, k_pool, v_pool, req_to_token, seq_len
                                          _ptr(seq_lens), _ptr(kv_indptr), _ptr(out), ctypes.byref(dims),
                                          float(sm_scale), _stream(stream))
     return _check(st, "astr_attn_prefill_ragged", check)
+
+
+def astr_attn_kv_append(k_new, v_new, qo_indptr, req_to_token, seq_lens, k_pool, v_pool, dims: Dims, stream=None,
+                        check: bool = True) -> int:
+    """Write the new tokens' K/V rows ([total_q, Hkv, d]) into their pool slots in place."""
+    st = load().astr_attn_kv_append(_ptr(k_new), _ptr(v_new), _ptr(qo_indptr), _ptr(req_to_token), _ptr(seq_lens),
+                                    _ptr(k_pool), _ptr(v_pool), ctypes.byref(dims), _stream(stream))
+    return _check(st, "astr_attn_kv_append", check)
 
 
 def alloc_decode_workspace(dims: Dims, device="cuda"):

@@ -257,4 +257,28 @@ int astr_attn_prefill_ragged(const uint16_t* q, const int32_t* qo_indptr, const 
   return ASTR_OK;
 }
 
+int astr_attn_kv_append(const uint16_t* k_new, const uint16_t* v_new, const int32_t* qo_indptr,
+                        const int32_t* req_to_token, const int32_t* seq_lens, uint16_t* k_pool, uint16_t* v_pool,
+                        const astr_attn_dims* d, void* stream) {
+  if (!k_new || !v_new || !qo_indptr || !req_to_token || !seq_lens || !k_pool || !v_pool) return ASTR_ERR_INVALID_ARG;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
+      !aligned(qo_indptr, 4) || !aligned(req_to_token, 4) || !aligned(seq_lens, 4))
+    return ASTR_ERR_MISALIGNED;
+  int st = check_common(d);
+  if (st != ASTR_OK) return st;
+  if (d->total_q < 0) return ASTR_ERR_INVALID_ARG;
+  if (d->batch == 0 || d->total_q == 0) return ASTR_OK;
+  if (d->num_slots < 1) return ASTR_ERR_INVALID_ARG;
+  astr::AppendParams p{};
+  p.k_new = k_new; p.v_new = v_new; p.qo_indptr = qo_indptr; p.req_to_token = req_to_token;
+  p.seq_lens = seq_lens; p.k_pool = k_pool; p.v_pool = v_pool;
+  p.r2t_stride = d->r2t_stride;
+  p.num_slots = d->num_slots;
+  p.batch = d->batch;
+  p.total_q = d->total_q;
+  p.row_vecs = d->num_kv_heads * d->head_dim * 2 / 16;
+  if (astr::launch_kv_append(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ASTR_ERR_LAUNCH_FAILED;
+  return ASTR_OK;
+}
+
 }  // extern "C"

@@ -52,10 +52,26 @@ struct PrefillParams {
   float scale_log2;
 };
 
+// KV append: one launch, one warp per new token.
+struct AppendParams {
+  const uint16_t* k_new;         // [total_q, Hkv, D]
+  const uint16_t* v_new;
+  const int32_t* qo_indptr;      // [B + 1]
+  const int32_t* req_to_token;   // [B, r2t_stride]
+  const int32_t* seq_lens;       // [B]
+  uint16_t* k_pool;              // [num_slots, Hkv, D]
+  uint16_t* v_pool;
+  int64_t r2t_stride;
+  int64_t num_slots;             // slot ids outside [0, num_slots) are skipped
+  int batch, total_q;
+  int row_vecs;                  // 16-byte vectors per slot row (Hkv * D * 2 / 16)
+};
+
 // Launchers return cudaSuccess or the launch error; they never synchronise.
 cudaError_t launch_decode_split(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream);
+cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream);
 
 // Whether the kernels exist for this (head_dim, group size).
 bool decode_supported(int head_dim, int group);

@@ -168,3 +168,37 @@ def test_library_imports_no_device_allocator(lib):
     syms = subprocess.run([nm, "-D", "--undefined-only", pa.lib_path()], capture_output=True, text=True).stdout
     for bad in ("cudaMalloc", "cudaFree", "cudaMallocAsync", "cudaFreeAsync", "cudaMallocManaged"):
         assert f" {bad}" not in syms and f"U {bad}@" not in syms, bad
+
+
+def _app(d, **ptr):
+    p = dict(kn=A, vn=A, qo=A, r2t=A, seq=A, k=A, v=A)
+    p.update(ptr)
+    return pa.astr_attn_kv_append(p["kn"], p["vn"], p["qo"], p["r2t"], p["seq"], p["k"], p["v"], d, stream=0,
+                                  check=False)
+
+
+@pytest.mark.parametrize("name", ["kn", "vn", "qo", "r2t", "seq", "k", "v"])
+def test_append_null_pointer(lib, name):
+    assert _app(_dims(), **{name: 0}) == pa.ASTR_ERR_INVALID_ARG
+
+
+def test_append_misaligned(lib):
+    assert _app(_dims(), kn=A + 8) == pa.ASTR_ERR_MISALIGNED
+    assert _app(_dims(), v=A + 2) == pa.ASTR_ERR_MISALIGNED
+    assert _app(_dims(), r2t=A + 2) == pa.ASTR_ERR_MISALIGNED
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(head_dim=80), pa.ASTR_ERR_UNSUPPORTED),
+    (dict(total_q=-1), pa.ASTR_ERR_INVALID_ARG),
+    (dict(num_slots=0), pa.ASTR_ERR_INVALID_ARG),
+    (dict(r2t_stride=10), pa.ASTR_ERR_INVALID_ARG),   # below max_seq_len
+])
+def test_append_bad_dims(lib, kw, status):
+    assert _app(_dims(**kw)) == status
+
+
+def test_append_nothing_to_do_without_gpu(lib):
+    assert _app(_dims(batch=0)) == pa.ASTR_OK
+    assert _app(_dims(total_q=0)) == pa.ASTR_OK
+    assert lib.astr_attn_kv_append(A, A, A, A, A, A, A, None, None) == pa.ASTR_ERR_INVALID_ARG
