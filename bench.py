@@ -450,6 +450,16 @@ def main():
     t_app = timed(kv_append, n_a) / n_a
     app_gbs = a_bytes / t_app / 1e9
     del app_sets
+    # context for the fraction: a plain contiguous device-to-device copy of the same bytes
+    cp_src = [torch.empty(a_bytes // 2, dtype=torch.uint8, device=dev) for _ in range(n_app)]
+    cp_dst = [torch.empty_like(x) for x in cp_src]
+
+    def plain_copy(i):
+        cp_dst[i % n_app].copy_(cp_src[i % n_app])
+
+    timed(plain_copy, 3 * n_app)
+    t_copy = timed(plain_copy, n_a) / n_a
+    del cp_src, cp_dst
 
     # ---------------- CPU baseline: the oracle on this host (rank 0 at N=1 only)
     cpu = None
@@ -498,6 +508,7 @@ def main():
                                  "traffic": recorded_traffic("prefill", "prefill.cu")}},
         "kv_append": {"workload": wp.name, "rows": a_rows, "us_per_call": round(t_app * 1e6, 3),
                       "bytes_per_call": a_bytes,
+                      "same_bytes_device_copy_us": round(t_copy * 1e6, 3),
                       "l2": f"rotating {n_app} input/pool copies ({n_app * a_copy_bytes / 1e6:.0f} MB)",
                       "roofline": {"bound": "hbm", "achieved": round(app_gbs, 2), "peak": peaks["hbm_gbs"],
                                    "peak_source": f"hbm_gbs ({peaks_src})", "unit": "GB/s",
