@@ -22,7 +22,7 @@ _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lib = None
 
 __all__ = ["build", "lib_path", "decode", "prefill", "decode_split_partials", "decode_chunk_partials",
-           "chunk_split_counts", "combine", "kv_append", "load_variant"]
+           "chunk_split_counts", "combine", "kv_append", "masked", "load_variant"]
 
 
 def _compile(src: str, out: str, extra: Sequence[str] = ()) -> None:
@@ -55,9 +55,11 @@ def _declare(lib):
     lib.oracle_decode_split_partials.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _L, _P, _D, _I, _P, _P, _I]
     lib.oracle_combine.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P]
     lib.oracle_kv_append.argtypes = [_I, _I, _I, _P, _P, _P, _L, _P, _P, _P, _P]
+    lib.oracle_masked_rows.argtypes = [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _L, _P, _D, _P, _I, _L, _L, _I, _L,
+                                       _P, _P, _P, _I]
     lib.oracle_decode_chunk_partials.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _L, _P, _P, _D, _L, _L, _I, _P, _P]
     for f in ("oracle_decode_rows", "oracle_prefill_rows", "oracle_decode_split_partials", "oracle_combine",
-              "oracle_decode_chunk_partials", "oracle_kv_append"):
+              "oracle_decode_chunk_partials", "oracle_kv_append", "oracle_masked_rows"):
         getattr(lib, f).restype = None
     return lib
 
@@ -197,3 +199,33 @@ def kv_append(w, qo_indptr, k_new: np.ndarray, v_new: np.ndarray, lib=None):
     lib.oracle_kv_append(B, Hkv, D, _ptr(qo), _ptr(sl), _ptr(r2t), r2t.shape[1], _ptr(kn), _ptr(vn), _ptr(kp),
                          _ptr(vp))
     return kp, vp
+
+
+def masked(w, mask: np.ndarray, causal: bool = True, rows: Optional[np.ndarray] = None,
+           nthreads: Optional[int] = None, lib=None) -> np.ndarray:
+    """Attention of workload ``w`` with an explicit mask: ``mask`` is uint8/bool, 2-D
+    [B, kv_pitch] or 3-D [B, q_pitch, kv_pitch] (nonzero = visible).  Prefill workloads also
+    take ``causal`` (False: every row sees all seq_len keys the mask leaves).  ``rows`` as
+    for ``decode`` / ``prefill``; default every row, returned as [rows, Hq, d]."""
+    lib = lib or _get()
+    B, Hq, Hkv, D = w.batch, w.num_qo_heads, w.num_kv_heads, w.head_dim
+    is_decode = w.kind == "decode"
+    n_rows = B if is_decode else int(w.q.shape[0])
+    full = rows is None
+    if full:
+        rr, hh = np.meshgrid(np.arange(n_rows, dtype=np.int32), np.arange(Hq, dtype=np.int32), indexing="ij")
+        rows = np.stack([rr.ravel(), hh.ravel()], axis=1)
+    rows = _c(rows, np.int32)
+    ir, ih = _c(rows[:, 0], np.int32), _c(rows[:, 1], np.int32)
+    m = _c(np.asarray(mask).astype(np.uint8), np.uint8)
+    if m.ndim not in (2, 3) or m.shape[0] != B:
+        raise ValueError("mask must be [B, kv_pitch] or [B, q_pitch, kv_pitch]")
+    kv_pitch, q_pitch = m.shape[-1], (m.shape[1] if m.ndim == 3 else 0)
+    out = np.zeros((rows.shape[0], D), dtype=np.float64)
+    q, kp, vp = _c(w.q, np.uint16), _c(w.k_pool, np.uint16), _c(w.v_pool, np.uint16)
+    r2t, sl = _c(w.req_to_token, np.int32), _c(w.seq_lens, np.int32)
+    qo = None if is_decode else _c(w.qo_indptr, np.int32)
+    lib.oracle_masked_rows(int(is_decode), B, Hq, Hkv, D, _ptr(q), _ptr(qo), _ptr(kp), _ptr(vp), _ptr(r2t),
+                           r2t.shape[1], _ptr(sl), float(w.sm_scale), _ptr(m), int(m.ndim), kv_pitch, q_pitch,
+                           int(bool(causal)), rows.shape[0], _ptr(ir), _ptr(ih), _ptr(out), _threads(nthreads))
+    return out.reshape(n_rows, Hq, D) if full else out

@@ -28,6 +28,14 @@
  *   an empty split stores m = -inf, l = 0, o = 0;
  *   combine:  M = max_s m_s,  w_s = exp(m_s - M),  out = (sum_s w_s o_s) / (sum_s w_s l_s).
  *
+ * Explicit masks (page "astrai/extension @6f67ba8", prefill-mask commit: 2-D [batch, kv_len]
+ * and 3-D [batch, q_len, kv_len] masks, causal and mask able to coexist; unified causal
+ * offset, -1 = off): key j of request b is visible to local query row i iff j < seq_len_b,
+ * (causal off or j <= c_b + i), and the mask byte is nonzero -- mask[b][j] (2-D) or
+ * mask[b][i][j] (3-D), rows kv_pitch bytes apart (3-D: q_pitch rows per request).  The row
+ * attends over exactly its visible keys, in key order; no visible key gives a zero row.
+ * Decode is the case q_len = 1, i = 0.
+ *
  * The KV-append step (page "astrai/extension/attention_backend.py @47b3ed4",
  * write-then-gather helper commit: the new tokens' K and V are written into the pool
  * before attention gathers from it).  Reading: new token i of request b is the key at
@@ -123,7 +131,7 @@ static void widen_row(const uint16_t *src, int D, double *dst) {
 
 /* ---------------------------------------------------------------- work items */
 
-enum { JOB_DECODE = 0, JOB_PREFILL = 1, JOB_PARTIALS = 2 };
+enum { JOB_DECODE = 0, JOB_PREFILL = 1, JOB_PARTIALS = 2, JOB_MASKED = 3 };
 
 typedef struct {
   int kind;
@@ -141,6 +149,11 @@ typedef struct {
   /* partials */
   int S;
   double *o_part, *ml_part;
+  /* explicit mask (JOB_MASKED): kind 2 = [B, kv_pitch], 3 = [B, q_pitch, kv_pitch]; rows are
+   * decode (b, h) pairs when is_decode, else (flat row, h) */
+  const uint8_t *mask;
+  int mask_dims, is_decode, causal;
+  int64_t kv_pitch, q_pitch;
   int next_thread;
   int nthreads;
 } job_t;
@@ -179,6 +192,33 @@ static void run_item(job_t *J, int64_t it, double *qbuf) {
     int64_t c = (int64_t)J->seq_lens[b] - q_len;  /* causal offset */
     widen_row(J->q + (r * P->Hq + h) * D, D, qbuf);
     attend(P, qbuf, kvh, J->req_to_token + (int64_t)b * J->r2t_stride, c + i + 1, J->out + it * D);
+  } else if (J->kind == JOB_MASKED) {
+    int b;
+    int64_t i, c;
+    if (J->is_decode) {
+      b = J->item_row[it];
+      i = 0;
+      c = (int64_t)J->seq_lens[b] - 1;
+      widen_row(J->q + ((int64_t)b * P->Hq + h) * D, D, qbuf);
+    } else {
+      int64_t r = J->item_row[it];
+      b = request_of_row(J->qo_indptr, J->B, r);
+      i = r - J->qo_indptr[b];
+      c = (int64_t)J->seq_lens[b] - ((int64_t)J->qo_indptr[b + 1] - J->qo_indptr[b]);
+      widen_row(J->q + (r * P->Hq + h) * D, D, qbuf);
+    }
+    const int32_t *row_slots = J->req_to_token + (int64_t)b * J->r2t_stride;
+    const uint8_t *mrow = J->mask_dims == 2 ? J->mask + (int64_t)b * J->kv_pitch
+                                            : J->mask + ((int64_t)b * J->q_pitch + i) * J->kv_pitch;
+    const int64_t n = J->seq_lens[b];
+    int32_t *vis = (int32_t *)malloc(sizeof(int32_t) * (size_t)(n > 0 ? n : 1));
+    int64_t nv = 0;
+    for (int64_t j = 0; j < n; ++j) {
+      const int causal_ok = !J->causal || j <= c + i;
+      if (causal_ok && mrow[j] != 0) vis[nv++] = row_slots[j];
+    }
+    attend(P, qbuf, kvh, vis, nv, J->out + it * D);
+    free(vis);
   } else { /* JOB_PARTIALS: even split of request b's keys into S pieces */
     int b = J->item_row[it];
     widen_row(J->q + ((int64_t)b * P->Hq + h) * D, D, qbuf);
@@ -351,4 +391,22 @@ void oracle_kv_append(int B, int Hkv, int D, const int32_t *qo_indptr, const int
       memcpy(v_pool + (int64_t)slot * row, v_new + src * row, sizeof(uint16_t) * (size_t)row);
     }
   }
+}
+
+/* Attention with an explicit mask (and, for prefill, the causal flag) for the listed rows:
+ * decode rows are (b, h) pairs (is_decode = 1, qo_indptr unused), prefill rows (flat row, h). */
+void oracle_masked_rows(int is_decode, int B, int Hq, int Hkv, int D, const uint16_t *q, const int32_t *qo_indptr,
+                        const uint16_t *k_pool, const uint16_t *v_pool, const int32_t *req_to_token,
+                        int64_t r2t_stride, const int32_t *seq_lens, double sm_scale, const uint8_t *mask,
+                        int mask_dims, int64_t kv_pitch, int64_t q_pitch, int causal, int64_t n_items,
+                        const int32_t *item_row, const int32_t *item_h, double *out, int nthreads) {
+  job_t J;
+  memset(&J, 0, sizeof J);
+  J.kind = JOB_MASKED;
+  J.P.Hq = Hq; J.P.Hkv = Hkv; J.P.D = D; J.P.k_pool = k_pool; J.P.v_pool = v_pool; J.P.sm_scale = sm_scale;
+  J.B = B; J.q = q; J.qo_indptr = qo_indptr; J.req_to_token = req_to_token; J.r2t_stride = r2t_stride;
+  J.seq_lens = seq_lens; J.n_items = n_items; J.item_row = item_row; J.item_head = item_h; J.out = out;
+  J.mask = mask; J.mask_dims = mask_dims; J.kv_pitch = kv_pitch; J.q_pitch = q_pitch;
+  J.is_decode = is_decode; J.causal = causal;
+  run_job(&J, nthreads);
 }

@@ -9,7 +9,11 @@ mutation tests) and raises AssertionError when the oracle disagrees with:
   * invariances (slot permutation, key shift, per-request markers),
   * the split-KV identity (partials + log-sum-exp combine equals unsplit softmax),
   * the KV-append step: attention over the pool after the append equals SDPA over each
-    request's cached keys followed by its new rows, laid out contiguously.
+    request's cached keys followed by its new rows, laid out contiguously,
+  * explicit masks: SDPA with the mask AND-ed in (causal on or off), rows with no visible key
+    exactly zero (empty-sum reading); an all-ones mask, a 3-D causal pattern with causal off,
+    a 2-D mask repeated over rows and a decode mask turned into a shorter slot table all
+    reproduce the corresponding unmasked or 2-D results bit for bit.
 """
 import dataclasses
 import json
@@ -400,10 +404,83 @@ def pin_append_touches_only_new_slots(lib):
                 f"slot {slot} changed"
 
 
+def _masked_cases():
+    wp = _small_prefill(seed=121, qmax=9, pmax=12)
+    wd = _small_decode(seed=123)
+    out = []
+    for w in (wp, wd):
+        for dims in (2, 3):
+            m = workload.make_mask(w, dims, seed=125 + dims, keep=0.6)
+            if dims == 3:
+                m[0, 0, :] = 0  # a row with no visible key
+            else:
+                m[-1, :] = 0    # a request with no visible key
+            out.append((w, m))
+    return out
+
+
+def pin_masked_matches_sdpa(lib):
+    """Masked attention (2-D and 3-D, causal on and off) against fp64 SDPA with the mask
+    AND-ed into its boolean mask; rows that see no key are zero."""
+    for w, m in _masked_cases():
+        # the rows _masked_cases planted with no visible key (first row of request 0 for 3-D
+        # masks, every row of the last request for 2-D masks)
+        if w.kind == "decode":
+            planted = [0] if m.ndim == 3 else [w.batch - 1]
+        else:
+            b = 0 if m.ndim == 3 else w.batch - 1
+            planted = [0] if m.ndim == 3 else list(range(int(w.qo_indptr[b]), int(w.qo_indptr[b + 1])))
+        for causal in ((True, False) if w.kind == "prefill" else (True,)):
+            got = oracle.masked(w, m, causal=causal, lib=lib)
+            assert not got[planted].any(), "a row with no visible key is not zero"
+            with np.errstate(invalid="ignore"):
+                ref = sdpa_paged(w, extra_mask=m, causal=causal)
+            empty = np.isnan(ref).all(axis=(1, 2))  # SDPA gives NaN or 0 there, by version
+            ref[empty] = 0.0
+            err = np.abs(got - ref).max()
+            assert err <= 1e-12, f"{w.kind} dims={m.ndim} causal={causal}: masked vs SDPA {err}"
+
+
+def pin_mask_identities(lib):
+    """All-ones mask = no mask; 3-D lower-triangular causal pattern with causal off = causal;
+    2-D mask = the same mask repeated over every row as 3-D (all bit-exact)."""
+    wp = _small_prefill(seed=131)
+    kv = -(-wp.max_seq_len // 16) * 16
+    ones = np.ones((wp.batch, kv), np.uint8)
+    assert np.array_equal(oracle.masked(wp, ones, lib=lib), oracle.prefill(wp, lib=lib))
+    tri = np.zeros((wp.batch, wp.max_q_len, kv), np.uint8)
+    for b in range(wp.batch):
+        c = int(wp.seq_lens[b]) - int(wp.q_lens[b])
+        for i in range(int(wp.q_lens[b])):
+            tri[b, i, :c + i + 1] = 1
+    assert np.array_equal(oracle.masked(wp, tri, causal=False, lib=lib), oracle.prefill(wp, lib=lib))
+    m2 = workload.make_mask(wp, 2, seed=133, keep=0.5)
+    m3 = np.repeat(m2[:, None, :], wp.max_q_len, axis=1)
+    for causal in (True, False):
+        assert np.array_equal(oracle.masked(wp, m2, causal=causal, lib=lib),
+                              oracle.masked(wp, m3, causal=causal, lib=lib))
+
+
+def pin_decode_mask_is_shorter_table(lib):
+    """A decode mask equals decoding over a slot table that lists only the visible keys."""
+    w = _small_decode(seed=137)
+    m = workload.make_mask(w, 2, seed=139, keep=0.5)
+    r2t = np.zeros_like(w.req_to_token)
+    seq = np.zeros_like(w.seq_lens)
+    for b in range(w.batch):
+        keep = [int(w.req_to_token[b, j]) for j in range(int(w.seq_lens[b])) if m[b, j]]
+        r2t[b, :len(keep)] = keep
+        seq[b] = len(keep)
+    kvi = np.concatenate([[0], np.cumsum(seq)]).astype(np.int32)
+    short = dataclasses.replace(w, req_to_token=r2t, seq_lens=seq, kv_indptr=kvi)
+    assert np.array_equal(oracle.masked(w, m, lib=lib), oracle.decode(short, lib=lib))
+
+
 ALL_PINS = [
     pin_sdpa_decode, pin_sdpa_prefill, pin_prefix0_is_textbook_causal, pin_golden,
     pin_q_zero_is_mean_of_visible_v, pin_single_key_returns_v, pin_per_request_marker, pin_dominant_key,
     pin_slot_permutation, pin_key_shift, pin_unreferenced_slots_unread, pin_split_combine, pin_chunk_partials_combine,
     pin_partial_is_softmax_piece, pin_prefill_row_is_decode,
     pin_append_then_attend_is_sdpa_over_concatenation, pin_append_touches_only_new_slots,
+    pin_masked_matches_sdpa, pin_mask_identities, pin_decode_mask_is_shorter_table,
 ]

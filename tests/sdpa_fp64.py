@@ -19,8 +19,13 @@ def _f64(bits: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(bf16_bits_to_fp32(bits).astype(np.float64))
 
 
-def sdpa_paged(w) -> np.ndarray:
-    """Returns [rows, Hq, d] float64, rows = B (decode) or total_q (prefill)."""
+def sdpa_paged(w, extra_mask=None, causal: bool = True) -> np.ndarray:
+    """Returns [rows, Hq, d] float64, rows = B (decode) or total_q (prefill).
+
+    ``extra_mask`` (2-D [B, kv] or 3-D [B, q, kv], nonzero = visible) is AND-ed into the
+    boolean mask; ``causal=False`` drops the causal term (the prefill-mask commit of page
+    "astrai/extension @6f67ba8": causal and mask coexist, causal may be off).  Rows with no
+    visible key come back as NaN from SDPA; callers compare them separately."""
     B, Hq, Hkv, D = w.batch, w.num_qo_heads, w.num_kv_heads, w.head_dim
     G = Hq // Hkv
     seq = w.seq_lens.astype(np.int64)
@@ -46,7 +51,18 @@ def sdpa_paged(w) -> np.ndarray:
     Q = q_all[torch.from_numpy(qrows)].permute(0, 2, 1, 3)  # [B, Hq, max_q, D]
     # bottom-right causal: key j visible to local row i iff j <= (seq - qlen) + i, and j < seq
     offset = (seq - qlen)[:, None, None]
-    mask = (pos[:, None, :] <= offset + qi[:, :, None]) & kv_valid[:, None, :]
+    mask = kv_valid[:, None, :] & np.ones((B, max_q, 1), dtype=bool)
+    if causal:
+        mask = mask & (pos[:, None, :] <= offset + qi[:, :, None])
+    if extra_mask is not None:
+        em = np.asarray(extra_mask) != 0
+        if em.ndim == 2:
+            em = em[:, None, :max_kv]
+        else:
+            em = em[:, :max_q, :max_kv]
+            if em.shape[1] < max_q:  # rows past the mask's q extent are padding, dropped below
+                em = np.concatenate([em, np.zeros((B, max_q - em.shape[1], max_kv), dtype=bool)], axis=1)
+        mask = mask & em
     # fully masked padded rows would give NaN; they are dropped, so let them see key 0
     mask = mask | (~q_valid[:, :, None] & (pos[:, None, :] == 0))
     mask_t = torch.from_numpy(mask)[:, None, :, :]

@@ -39,6 +39,10 @@ MUTANTS = {
     "append_position_shift": ("r2t_stride + c + i];", "r2t_stride + c + i + 1];"),
     "append_k_into_v": ("memcpy(v_pool + (int64_t)slot * row, v_new", "memcpy(v_pool + (int64_t)slot * row, k_new"),
     "append_source_row_local": ("const int64_t src = (int64_t)qo_indptr[b] + i;", "const int64_t src = i;"),
+    "mask_ignored": ("if (causal_ok && mrow[j] != 0)", "if (causal_ok)"),
+    "mask_row_not_offset_by_query_row": ("((int64_t)b * J->q_pitch + i) * J->kv_pitch", "((int64_t)b * J->q_pitch) * J->kv_pitch"),
+    "causal_flag_ignored": ("const int causal_ok = !J->causal || j <= c + i;", "const int causal_ok = j <= c + i;"),
+    "mask_2d_row_pitch": ("J->mask + (int64_t)b * J->kv_pitch\n", "J->mask + (int64_t)b * J->q_pitch\n"),
     "key_index_transposed": ("k_pool + ((int64_t)slot * P->Hkv + kvh) * P->D", "k_pool + ((int64_t)kvh * P->Hkv + slot % P->Hkv) * P->D"),
 }
 

@@ -21,7 +21,7 @@ import numpy as np
 
 __all__ = [
     "Workload", "CONFIGS", "config", "make_decode", "make_prefill",
-    "fp32_to_bf16_bits", "bf16_bits_to_fp32", "make_from_lengths", "append_rows",
+    "fp32_to_bf16_bits", "bf16_bits_to_fp32", "make_from_lengths", "append_rows", "make_mask",
 ]
 
 
@@ -196,6 +196,20 @@ def append_rows(w: Workload, seed: int):
     k_new = _normal_bf16(rng, (n, w.num_kv_heads, w.head_dim))
     v_new = _normal_bf16(rng, (n, w.num_kv_heads, w.head_dim))
     return qo, k_new, v_new
+
+
+def make_mask(w: Workload, dims: int, seed: int, keep: float = 0.75) -> np.ndarray:
+    """An explicit attention mask for workload ``w``: uint8 (1 = visible, 0 = masked), each
+    byte 1 with probability ``keep`` (``default_rng(seed)``, one uniform per byte).
+
+    dims = 2: [B, kv_pitch]; dims = 3: [B, q_pitch, kv_pitch] with q_pitch = max_q_len (1 for
+    decode).  kv_pitch = max_seq_len rounded up to 16 bytes; bytes past a request's keys or
+    rows are drawn too and are never read.
+    """
+    rng = np.random.default_rng(seed)
+    kv_pitch = max(16, -(-w.max_seq_len // 16) * 16)
+    shape = (w.batch, kv_pitch) if dims == 2 else (w.batch, max(1, w.max_q_len), kv_pitch)
+    return (rng.random(shape) < keep).astype(np.uint8)
 
 
 def config(idx: int, seed: Optional[int] = None) -> Workload:
