@@ -13,6 +13,10 @@ Also reported in the same line:
                     on its stream: algorithmic K+V bytes per launch / mean duration.
   * prefill      -- the ragged prefill entry point on the 16-request extend workload,
                     FLOP/s against the measured dense bf16 tensor-core peak.
+  * masked       -- the explicit-mask entry points on the same workloads: prefill with a 3-D
+                    mask (causal on) and decode with a 2-D mask, each byte kept with
+                    probability 0.75; FLOP/s and GB/s count the same work as the unmasked calls
+                    (masked keys are still read and scored).
   * kv_append    -- the KV-append step (the extend workload's new K/V rows written into their
                     pool slots), bytes moved per second against the measured HBM copy peak.
   * e2e          -- the same decode metric with every input in pinned host memory, the
@@ -430,6 +434,26 @@ def main():
     flops = prefill_flops(wp)
     pf_tflops = flops / t_pf / 1e12
 
+    # ---------------- explicit-mask entry points (prefill: 3-D mask; decode: 2-D mask)
+    pmask = torch.from_numpy(workload.make_mask(wp, 3, seed=wp.seed + 7, keep=0.75)).to(dev)
+    pm = pa.make_mask(pmask, causal=True)
+
+    def prefill_masked(i):
+        pa.astr_attn_prefill_ragged_masked(pq, pqo, pk, pv, pr, ps_, pki, pm, pout, pdims, wp.sm_scale, stream=sh)
+
+    timed(prefill_masked, 5)
+    t_pfm = timed(prefill_masked, n_pf) / n_pf
+    dmask = torch.from_numpy(workload.make_mask(w, 2, seed=w.seed + 7, keep=0.75)).to(dev)
+    dm = pa.make_mask(dmask)
+
+    def decode_masked(i):
+        k, v = pools[i % n_copies]
+        pa.astr_attn_paged_decode_masked(q, k, v, r2t, seq, kvi, dm, o_part, ml_part, out, dims, w.sm_scale,
+                                         stream=sh)
+
+    timed(decode_masked, 20)
+    t_dm = timed(decode_masked, n_split) / n_split
+
     # ---------------- KV-append step on the extend workload (rotating copies: cold in L2)
     aqo_np, akn_np, avn_np = workload.append_rows(wp, seed=wp.seed + 1)
     a_rows = int(aqo_np[-1])
@@ -506,6 +530,14 @@ def main():
                                  "peak_source": f"bf16_tflops burst ({peaks_src})", "unit": "TFLOP/s",
                                  "frac": round(pf_tflops / peaks["bf16_tflops"], 4),
                                  "traffic": recorded_traffic("prefill", "prefill.cu")}},
+        "masked": {"prefill": {"workload": wp.name, "mask": "3-D [B, max_q_len, kv_pitch], keep 0.75, causal on",
+                               "us_per_call": round(t_pfm * 1e6, 3),
+                               "tflops": round(flops / t_pfm / 1e12, 2),
+                               "frac": round(flops / t_pfm / 1e12 / peaks["bf16_tflops"], 4)},
+                   "decode": {"workload": w.name, "mask": "2-D [B, kv_pitch], keep 0.75",
+                              "us_per_call": round(t_dm * 1e6, 3),
+                              "gbs": round(nbytes["kv"] / t_dm / 1e9, 2),
+                              "frac": round(nbytes["kv"] / t_dm / 1e9 / peaks["hbm_gbs"], 4)}},
         "kv_append": {"workload": wp.name, "rows": a_rows, "us_per_call": round(t_app * 1e6, 3),
                       "bytes_per_call": a_bytes,
                       "same_bytes_device_copy_us": round(t_copy * 1e6, 3),

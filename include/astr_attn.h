@@ -172,6 +172,50 @@ int astr_attn_prefill_ragged(const uint16_t* q, const int32_t* qo_indptr, const 
                              void* stream);
 
 /*
+ * Explicit attention mask (P3, prefill-mask commit: 2-D [batch, kv_len] and 3-D
+ * [batch, q_len, kv_len] masks, causal and mask may coexist; unified-causal-offset commit:
+ * the causal offset can be switched off).  Host struct read during the call only.  Key j of
+ * request b is visible to its local query row i iff j < seq_lens[b], the causal rule holds
+ * (causal = 1: j <= seq_lens[b] - q_len_b + i; causal = 0: always) and, when `mask` is not
+ * NULL, its byte for (b, i, j) is nonzero:
+ *   dims = 2:  mask[b * kv_pitch + j]                      (the same for every row i)
+ *   dims = 3:  mask[(b * q_pitch + i) * kv_pitch + j]
+ * A query row with no visible key is written as zeros.  Decode has one row per request
+ * (i = 0) and no causal rule (its row sees every key).
+ */
+typedef struct astr_attn_mask {
+  const uint8_t* mask;   /* DEVICE bytes, nonzero = visible, 16-byte aligned; NULL = no explicit mask */
+  int32_t dims;          /* 2 or 3 (read only when mask is not NULL) */
+  int32_t kv_pitch;      /* bytes per mask row: a multiple of 16, >= max_seq_len */
+  int32_t q_pitch;       /* dims = 3: rows per request, >= max_q_len for prefill, >= 1 for decode */
+  int32_t causal;        /* prefill: 1 = causal offset seq_len - q_len, 0 = off; decode ignores it */
+} astr_attn_mask;
+
+/*
+ * astr_attn_paged_decode with an explicit mask (struct above; mask->causal is not read).  The
+ * split kernel reads each 32-key slot's mask bytes next to its slot ids; masked keys get
+ * exactly zero weight.  Same arguments, rules and errors as astr_attn_paged_decode, plus
+ * INVALID_ARG for a NULL `mask` struct or bad dims / pitches and MISALIGNED for mask->mask.
+ */
+int astr_attn_paged_decode_masked(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
+                                  const int32_t* req_to_token, const int32_t* seq_lens, const int32_t* kv_indptr,
+                                  const astr_attn_mask* mask, float* o_part, float* ml_part, uint16_t* out,
+                                  const astr_attn_dims* dims, float sm_scale, void* stream);
+
+/*
+ * astr_attn_prefill_ragged with an explicit mask and/or the causal offset switched off
+ * (struct above).  mask->mask = NULL with causal = 1 is astr_attn_prefill_ragged itself; with
+ * causal = 0 every row attends over all seq_lens[b] keys of its request.  Each softmax thread
+ * reads its row's 64 mask bytes per key tile while the tile's scores are computed.  Same
+ * arguments, rules and errors as astr_attn_prefill_ragged, plus INVALID_ARG for a NULL `mask`
+ * struct, bad dims / pitches or causal not 0/1, and MISALIGNED for mask->mask.
+ */
+int astr_attn_prefill_ragged_masked(const uint16_t* q, const int32_t* qo_indptr, const uint16_t* k_pool,
+                                    const uint16_t* v_pool, const int32_t* req_to_token, const int32_t* seq_lens,
+                                    const int32_t* kv_indptr, const astr_attn_mask* mask, uint16_t* out,
+                                    const astr_attn_dims* dims, float sm_scale, void* stream);
+
+/*
  * Paged decode that allocates nothing (no counterpart in the source pages; this is a
  * service of this library).  Same computation, arguments, rules and errors as
  * astr_attn_paged_decode minus o_part / ml_part: the split-KV partials go to a 16 MiB

@@ -18,7 +18,8 @@ from typing import Optional
 __all__ = [
     "Dims", "AstrAttnError", "load", "lib_path", "make_dims",
     "astr_attn_paged_decode", "astr_attn_decode_split", "astr_attn_decode_combine", "astr_attn_prefill_ragged",
-    "astr_attn_paged_decode_noalloc", "astr_attn_kv_append",
+    "astr_attn_paged_decode_noalloc", "astr_attn_kv_append", "astr_attn_paged_decode_masked",
+    "astr_attn_prefill_ragged_masked", "Mask", "make_mask",
     "astr_attn_decode_num_splits", "astr_attn_decode_workspace_bytes", "astr_attn_status_string",
     "astr_attn_version", "alloc_decode_workspace",
     "ASTR_OK", "ASTR_ERR_INVALID_ARG", "ASTR_ERR_UNSUPPORTED", "ASTR_ERR_MISALIGNED",
@@ -41,6 +42,7 @@ EXPORTED_SYMBOLS = [
     "astr_attn_decode_num_splits", "astr_attn_decode_workspace_bytes", "astr_attn_paged_decode",
     "astr_attn_decode_combine", "astr_attn_prefill_ragged", "astr_attn_status_string", "astr_attn_version",
     "astr_attn_decode_split", "astr_attn_paged_decode_noalloc", "astr_attn_kv_append",
+    "astr_attn_paged_decode_masked", "astr_attn_prefill_ragged_masked",
 ]
 
 
@@ -58,6 +60,24 @@ class Dims(ctypes.Structure):
         ("max_seq_len", ctypes.c_int32), ("total_q", ctypes.c_int32), ("max_q_len", ctypes.c_int32),
         ("max_splits", ctypes.c_int32), ("num_splits", ctypes.c_int32),
     ]
+
+
+class Mask(ctypes.Structure):
+    """Mirror of ``astr_attn_mask`` (see include/astr_attn.h)."""
+    _fields_ = [("mask", ctypes.c_void_p), ("dims", ctypes.c_int32), ("kv_pitch", ctypes.c_int32),
+                ("q_pitch", ctypes.c_int32), ("causal", ctypes.c_int32)]
+
+
+def make_mask(mask=None, causal: bool = True) -> Mask:
+    """Mask struct for a device uint8/bool tensor of shape [B, kv_pitch] or [B, q_pitch, kv_pitch]
+    (or None: no explicit mask, only the causal flag)."""
+    if mask is None:
+        return Mask(None, 0, 0, 0, int(bool(causal)))
+    shape = tuple(mask.shape)
+    if len(shape) not in (2, 3):
+        raise ValueError("mask must be [B, kv_pitch] or [B, q_pitch, kv_pitch]")
+    return Mask(int(mask.data_ptr()), len(shape), int(shape[-1]), int(shape[1]) if len(shape) == 3 else 0,
+                int(bool(causal)))
 
 
 def lib_path() -> str:
@@ -84,12 +104,16 @@ def load():
     lib.astr_attn_paged_decode_noalloc.argtypes = [P, P, P, P, P, P, P, D, F, P]
     lib.astr_attn_prefill_ragged.argtypes = [P, P, P, P, P, P, P, P, D, F, P]
     lib.astr_attn_kv_append.argtypes = [P, P, P, P, P, P, P, D, P]
+    M = ctypes.POINTER(Mask)
+    lib.astr_attn_paged_decode_masked.argtypes = [P, P, P, P, P, P, M, P, P, P, D, F, P]
+    lib.astr_attn_prefill_ragged_masked.argtypes = [P, P, P, P, P, P, P, M, P, D, F, P]
     lib.astr_attn_status_string.argtypes = [I32]
     lib.astr_attn_status_string.restype = ctypes.c_char_p
     lib.astr_attn_version.argtypes = []
     for f in ("astr_attn_decode_num_splits", "astr_attn_decode_workspace_bytes", "astr_attn_paged_decode",
               "astr_attn_decode_split", "astr_attn_decode_combine", "astr_attn_prefill_ragged", "astr_attn_version",
-              "astr_attn_paged_decode_noalloc", "astr_attn_kv_append"):
+              "astr_attn_paged_decode_noalloc", "astr_attn_kv_append", "astr_attn_paged_decode_masked",
+              "astr_attn_prefill_ragged_masked"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -198,6 +222,27 @@ def astr_attn_kv_append(k_new, v_new, qo_indptr, req_to_token, seq_lens, k_pool,
     st = load().astr_attn_kv_append(_ptr(k_new), _ptr(v_new), _ptr(qo_indptr), _ptr(req_to_token), _ptr(seq_lens),
                                     _ptr(k_pool), _ptr(v_pool), ctypes.byref(dims), _stream(stream))
     return _check(st, "astr_attn_kv_append", check)
+
+
+def astr_attn_paged_decode_masked(q, k_pool, v_pool, req_to_token, seq_lens, kv_indptr, mask: Mask, o_part, ml_part,
+                                  out, dims: Dims, sm_scale: float, stream=None, check: bool = True) -> int:
+    """Paged decode with an explicit mask (``make_mask``)."""
+    st = load().astr_attn_paged_decode_masked(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(req_to_token),
+                                              _ptr(seq_lens), _ptr(kv_indptr),
+                                              None if mask is None else ctypes.byref(mask), _ptr(o_part),
+                                              _ptr(ml_part), _ptr(out), ctypes.byref(dims), float(sm_scale),
+                                              _stream(stream))
+    return _check(st, "astr_attn_paged_decode_masked", check)
+
+
+def astr_attn_prefill_ragged_masked(q, qo_indptr, k_pool, v_pool, req_to_token, seq_lens, kv_indptr, mask: Mask,
+                                    out, dims: Dims, sm_scale: float, stream=None, check: bool = True) -> int:
+    """Ragged prefill with an explicit mask and/or the causal offset off (``make_mask``)."""
+    st = load().astr_attn_prefill_ragged_masked(_ptr(q), _ptr(qo_indptr), _ptr(k_pool), _ptr(v_pool),
+                                                _ptr(req_to_token), _ptr(seq_lens), _ptr(kv_indptr),
+                                                None if mask is None else ctypes.byref(mask), _ptr(out),
+                                                ctypes.byref(dims), float(sm_scale), _stream(stream))
+    return _check(st, "astr_attn_prefill_ragged_masked", check)
 
 
 def alloc_decode_workspace(dims: Dims, device="cuda"):

@@ -149,27 +149,65 @@ static int decode_prepare(const astr_attn_dims* d, float sm_scale, astr::DecodeP
   return ASTR_OK;
 }
 
-int astr_attn_paged_decode(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
-                           const int32_t* req_to_token, const int32_t* seq_lens, const int32_t* kv_indptr,
-                           float* o_part, float* ml_part, uint16_t* out, const astr_attn_dims* dims, float sm_scale,
-                           void* stream) {
+// Explicit-mask arguments: shape rules, then the pitches of request b's bytes (and of its rows).
+static int check_mask(const astr_attn_mask* m, const astr_attn_dims* d, bool decode, int64_t* req_pitch,
+                      int64_t* row_pitch) {
+  if (m == nullptr || d == nullptr) return ASTR_ERR_INVALID_ARG;
+  if (m->causal != 0 && m->causal != 1) return ASTR_ERR_INVALID_ARG;
+  *req_pitch = *row_pitch = 0;
+  if (m->mask == nullptr) return ASTR_OK;
+  if (!aligned(m->mask, 16)) return ASTR_ERR_MISALIGNED;
+  if (m->dims != 2 && m->dims != 3) return ASTR_ERR_INVALID_ARG;
+  if (m->kv_pitch < 16 || m->kv_pitch % 16 != 0 || m->kv_pitch < d->max_seq_len) return ASTR_ERR_INVALID_ARG;
+  if (m->dims == 3 && (m->q_pitch < 1 || (!decode && m->q_pitch < d->max_q_len))) return ASTR_ERR_INVALID_ARG;
+  *req_pitch = (m->dims == 3) ? (int64_t)m->q_pitch * m->kv_pitch : (int64_t)m->kv_pitch;
+  *row_pitch = (m->dims == 3) ? (int64_t)m->kv_pitch : 0;
+  return ASTR_OK;
+}
+
+static int paged_decode_impl(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
+                             const int32_t* req_to_token, const int32_t* seq_lens, const int32_t* kv_indptr,
+                             const astr_attn_mask* mask, float* o_part, float* ml_part, uint16_t* out,
+                             const astr_attn_dims* dims, float sm_scale, void* stream) {
   if (!q || !k_pool || !v_pool || !req_to_token || !seq_lens || !kv_indptr || !o_part || !ml_part || !out)
     return ASTR_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(o_part, 16) ||
       !aligned(ml_part, 16) || !aligned(out, 16) || !aligned(req_to_token, 4) || !aligned(seq_lens, 4) ||
       !aligned(kv_indptr, 4))
     return ASTR_ERR_MISALIGNED;
+  int64_t mask_req_pitch = 0, mask_row_pitch = 0;
+  int st = ASTR_OK;
+  if (mask != nullptr && (st = check_mask(mask, dims, true, &mask_req_pitch, &mask_row_pitch)) != ASTR_OK) return st;
   astr::DecodeParams p{};
   bool nothing = false;
-  int st = decode_prepare(dims, sm_scale, &p, &nothing);
+  st = decode_prepare(dims, sm_scale, &p, &nothing);
   if (st != ASTR_OK || nothing) return st;
+  astr::DecodeMask dm{nullptr, 0, 0};
+  if (mask != nullptr && mask->mask != nullptr) dm = astr::DecodeMask{mask->mask, mask_req_pitch, mask->kv_pitch};
   p.q = q; p.k_pool = k_pool; p.v_pool = v_pool; p.req_to_token = req_to_token; p.seq_lens = seq_lens;
   p.kv_indptr = kv_indptr; p.o_part = o_part; p.ml_part = ml_part; p.out = out;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (astr::launch_decode_split(p, s) != cudaSuccess) return ASTR_ERR_LAUNCH_FAILED;
+  if (astr::launch_decode_split(p, dm.mask != nullptr ? &dm : nullptr, s) != cudaSuccess) return ASTR_ERR_LAUNCH_FAILED;
   p.indptr_before_wait = 1;  // the combine follows this call's split kernel directly
   if (astr::launch_decode_combine(p, s) != cudaSuccess) return ASTR_ERR_LAUNCH_FAILED;
   return ASTR_OK;
+}
+
+int astr_attn_paged_decode(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
+                           const int32_t* req_to_token, const int32_t* seq_lens, const int32_t* kv_indptr,
+                           float* o_part, float* ml_part, uint16_t* out, const astr_attn_dims* dims, float sm_scale,
+                           void* stream) {
+  return paged_decode_impl(q, k_pool, v_pool, req_to_token, seq_lens, kv_indptr, nullptr, o_part, ml_part, out, dims,
+                           sm_scale, stream);
+}
+
+int astr_attn_paged_decode_masked(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
+                                  const int32_t* req_to_token, const int32_t* seq_lens, const int32_t* kv_indptr,
+                                  const astr_attn_mask* mask, float* o_part, float* ml_part, uint16_t* out,
+                                  const astr_attn_dims* dims, float sm_scale, void* stream) {
+  if (mask == nullptr) return ASTR_ERR_INVALID_ARG;
+  return paged_decode_impl(q, k_pool, v_pool, req_to_token, seq_lens, kv_indptr, mask, o_part, ml_part, out, dims,
+                           sm_scale, stream);
 }
 
 int astr_attn_decode_split(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
@@ -186,7 +224,8 @@ int astr_attn_decode_split(const uint16_t* q, const uint16_t* k_pool, const uint
   if (st != ASTR_OK || nothing) return st;
   p.q = q; p.k_pool = k_pool; p.v_pool = v_pool; p.req_to_token = req_to_token; p.seq_lens = seq_lens;
   p.kv_indptr = kv_indptr; p.o_part = o_part; p.ml_part = ml_part;
-  if (astr::launch_decode_split(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ASTR_ERR_LAUNCH_FAILED;
+  if (astr::launch_decode_split(p, nullptr, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return ASTR_ERR_LAUNCH_FAILED;
   return ASTR_OK;
 }
 
@@ -214,10 +253,10 @@ int astr_attn_decode_combine(const float* o_part, const float* ml_part, const in
   return ASTR_OK;
 }
 
-int astr_attn_prefill_ragged(const uint16_t* q, const int32_t* qo_indptr, const uint16_t* k_pool,
-                             const uint16_t* v_pool, const int32_t* req_to_token, const int32_t* seq_lens,
-                             const int32_t* kv_indptr, uint16_t* out, const astr_attn_dims* d, float sm_scale,
-                             void* stream) {
+static int prefill_impl(const uint16_t* q, const int32_t* qo_indptr, const uint16_t* k_pool, const uint16_t* v_pool,
+                        const int32_t* req_to_token, const int32_t* seq_lens, const int32_t* kv_indptr,
+                        const astr_attn_mask* mask, uint16_t* out, const astr_attn_dims* d, float sm_scale,
+                        void* stream) {
   (void)kv_indptr;
   if (!q || !qo_indptr || !k_pool || !v_pool || !req_to_token || !seq_lens || !out) return ASTR_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16) ||
@@ -230,6 +269,8 @@ int astr_attn_prefill_ragged(const uint16_t* q, const int32_t* qo_indptr, const 
   if (!std::isfinite(sm_scale)) return ASTR_ERR_INVALID_ARG;
   const int G = d->num_qo_heads / d->num_kv_heads;
   if (!astr::prefill_supported(d->head_dim, G)) return ASTR_ERR_UNSUPPORTED;
+  int64_t mask_req_pitch = 0, mask_row_pitch = 0;
+  if (mask != nullptr && (st = check_mask(mask, d, false, &mask_req_pitch, &mask_row_pitch)) != ASTR_OK) return st;
   if (d->batch == 0 || d->total_q == 0 || d->max_q_len == 0) return ASTR_OK;
   int dev = 0;
   if ((st = current_device(&dev)) != ASTR_OK) return st;
@@ -253,8 +294,32 @@ int astr_attn_prefill_ragged(const uint16_t* q, const int32_t* qo_indptr, const 
   if ((st = sm_count(dev, &sms)) != ASTR_OK) return st;
   p.num_ctas = sms;
   p.scale_log2 = sm_scale * 1.4426950408889634f;
+  p.causal = (mask == nullptr) ? 1 : mask->causal;
+  if (mask != nullptr && mask->mask != nullptr) {
+    p.mask = mask->mask;
+    p.mask_req_pitch = mask_req_pitch;
+    p.mask_row_pitch = mask_row_pitch;
+    p.mask_kv_pitch = mask->kv_pitch;
+  }
   if (astr::launch_prefill(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ASTR_ERR_LAUNCH_FAILED;
   return ASTR_OK;
+}
+
+int astr_attn_prefill_ragged(const uint16_t* q, const int32_t* qo_indptr, const uint16_t* k_pool,
+                             const uint16_t* v_pool, const int32_t* req_to_token, const int32_t* seq_lens,
+                             const int32_t* kv_indptr, uint16_t* out, const astr_attn_dims* d, float sm_scale,
+                             void* stream) {
+  return prefill_impl(q, qo_indptr, k_pool, v_pool, req_to_token, seq_lens, kv_indptr, nullptr, out, d, sm_scale,
+                      stream);
+}
+
+int astr_attn_prefill_ragged_masked(const uint16_t* q, const int32_t* qo_indptr, const uint16_t* k_pool,
+                                    const uint16_t* v_pool, const int32_t* req_to_token, const int32_t* seq_lens,
+                                    const int32_t* kv_indptr, const astr_attn_mask* mask, uint16_t* out,
+                                    const astr_attn_dims* d, float sm_scale, void* stream) {
+  if (mask == nullptr) return ASTR_ERR_INVALID_ARG;
+  return prefill_impl(q, qo_indptr, k_pool, v_pool, req_to_token, seq_lens, kv_indptr, mask, out, d, sm_scale,
+                      stream);
 }
 
 int astr_attn_kv_append(const uint16_t* k_new, const uint16_t* v_new, const int32_t* qo_indptr,

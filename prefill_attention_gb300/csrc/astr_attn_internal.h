@@ -34,6 +34,14 @@ struct DecodeParams {
                                  // previous kernel is this call's split kernel, which does not write it)
 };
 
+// Decode with an explicit mask: request b's bytes start at mask + b * req_pitch, one byte per
+// key position.  Kept out of DecodeParams so the unmasked kernels' parameter block is unchanged.
+struct DecodeMask {
+  const uint8_t* mask;
+  int64_t req_pitch;
+  int kv_pitch;                  // bytes in a mask row (a multiple of 16)
+};
+
 // Prefill/extend: one launch of the tensor-core kernel.
 struct PrefillParams {
   const uint16_t* q;             // [total_q, Hq, D]
@@ -50,6 +58,11 @@ struct PrefillParams {
   int num_q_tiles;               // upper bound on (request, query-tile pair) work items per KV head
   int num_ctas;                  // persistent CTAs to launch (one per SM)
   float scale_log2;
+  int causal;                    // 1: key j visible to local row i iff j <= seq_len - q_len + i; 0: off
+  const uint8_t* mask;           // explicit mask or nullptr: row i of request b at
+                                 // mask + b * mask_req_pitch + i * mask_row_pitch (0 for 2-D masks)
+  int64_t mask_req_pitch, mask_row_pitch;
+  int mask_kv_pitch;             // bytes in a mask row (a multiple of 16)
 };
 
 // KV append: one launch, one warp per new token.
@@ -68,9 +81,10 @@ struct AppendParams {
 };
 
 // Launchers return cudaSuccess or the launch error; they never synchronise.
-cudaError_t launch_decode_split(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_decode_split(const DecodeParams& p, const DecodeMask* mask, cudaStream_t stream);  // mask may be null
 cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream);
-cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream);
+cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream);         // dispatches on p.mask
+cudaError_t launch_prefill_masked(const PrefillParams& p, cudaStream_t stream);  // the explicit-mask kernels
 cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream);
 
 // Whether the kernels exist for this (head_dim, group size).

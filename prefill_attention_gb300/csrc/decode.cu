@@ -114,7 +114,10 @@ struct DecCfg {
   static constexpr int RING = STAGES * SLOT;
   static constexpr int BAR_OFF = NPAIR * RING;
   static constexpr int NBAR = NPAIR * 2 * STAGES;  // full[pair][slot], empty[pair][slot]
-  static constexpr int SMEM_BYTES = BAR_OFF + NBAR * 8 + 16 * 4;  // + per-pair error flags
+  static constexpr int MASK_OFF = BAR_OFF + NBAR * 8 + 16 * 4;  // after the per-pair error flags
+  static constexpr int MASK_BYTES = BK;                           // explicit-mask bytes of a ring slot
+  static constexpr int SMEM_BYTES = MASK_OFF;                     // without an explicit mask
+  static constexpr int SMEM_BYTES_MASKED = MASK_OFF + NPAIR * STAGES * MASK_BYTES;
   static constexpr int KSTEPS = D / 16;            // MMA k-steps over head_dim (S^T = K Q^T)
   static constexpr int MT_D = D / 16;              // 16-row m-tiles over head_dim (O^T = V^T P^T)
   static constexpr int STG_PITCH = D + 4;          // fp32 staging row pitch (conflict-free writes)
@@ -122,8 +125,15 @@ struct DecCfg {
   static_assert(STAGES >= 2, "a ring needs two slots");
   static_assert(SLOT % 1024 == 0 && KV_BYTES % 1024 == 0, "swizzle atoms");
   static_assert((QROWS * STG_PITCH + 2 * QROWS) * 4 <= 2 * KV_BYTES, "piece staging fits in K | V");
-  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+  static_assert(SMEM_BYTES_MASKED <= 227 * 1024, "shared memory budget");
+  static_assert(MASK_OFF % 16 == 0 && MASK_BYTES % 16 == 0, "16-byte cp.async of mask bytes");
 };
+
+__device__ __forceinline__ uint32_t lds_u8(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
 
 __device__ __forceinline__ void sts128_zero(uint32_t addr) {
   asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(addr), "r"(0) : "memory");
@@ -327,9 +337,23 @@ __device__ __forceinline__ bool wait_or_fail(uint32_t bar, uint32_t parity, vola
   return false;
 }
 
-template <int D, int G>
-__global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(const DecodeParams p) {
+// The split kernel's parameter block: DecodeParams, followed by the mask for the masked kernels.
+struct DecodeParamsMasked {
+  DecodeParams p;
+  DecodeMask m;
+};
+template <bool MASK> struct SplitArg { using type = DecodeParams; };
+template <> struct SplitArg<true> { using type = DecodeParamsMasked; };
+// (host and device: the launcher reads the grid shape through params_of too)
+__host__ __device__ __forceinline__ const DecodeParams& params_of(const DecodeParams& a) { return a; }
+__host__ __device__ __forceinline__ const DecodeParams& params_of(const DecodeParamsMasked& a) { return a.p; }
+__host__ __device__ __forceinline__ DecodeMask mask_of(const DecodeParams&) { return DecodeMask{nullptr, 0, 0}; }
+__host__ __device__ __forceinline__ DecodeMask mask_of(const DecodeParamsMasked& a) { return a.m; }
+
+template <int D, int G, bool MASK>
+__global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(const typename SplitArg<MASK>::type arg) {
   using C = DecCfg<D, G>;
+  const DecodeParams& p = params_of(arg);
   constexpr int NH = C::NH;
   extern __shared__ __align__(1024) unsigned char smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -345,6 +369,7 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(
   const uint32_t bars = sbase + C::BAR_OFF + 8u * (pair * 2 * C::STAGES);
   auto full = [&](int s) { return bars + 8u * s; };
   auto empty = [&](int s) { return bars + 8u * (C::STAGES + s); };
+  const uint32_t mask_ring = sbase + C::MASK_OFF + pair * C::STAGES * C::MASK_BYTES;  // explicit-mask bytes
   volatile int* err = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 8 * C::NBAR) + pair;
 
   // ---- set-up (shared memory only): barriers; Q rows of absent heads stay zero throughout
@@ -415,6 +440,16 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(
         cp_async16(kst + o, p.k_pool + off, valid);
         cp_async16(vst + o, p.v_pool + off, valid);
       }
+      if (MASK && lane < C::MASK_BYTES / 16) {
+        // the slot's explicit-mask bytes: request-local positions start at a multiple of 32, and
+        // a 16-byte chunk that begins inside the row (pitch a multiple of 16) ends inside it;
+        // chunks past the row are zero-filled (those keys are past max_seq_len anyway)
+        const int pos = it.start - it.ind_b + 16 * lane;
+        const DecodeMask mk = mask_of(arg);
+        const bool in_row = pos < mk.kv_pitch;
+        const uint8_t* src = mk.mask + (in_row ? (int64_t)it.b * mk.req_pitch + pos : 0);
+        cp_async16(mask_ring + s * C::MASK_BYTES + 16 * lane, src, in_row);
+      }
       cp_async_arrive_noinc(full(s));  // completes once this lane's copies (and older ones) land
       it.next(ind, B, hs);
       my_id = slot_id(it);
@@ -439,6 +474,13 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(
       const int nkeys = it.end - it.start;  // valid keys of the slot; the rest are masked
       if (!wait_or_fail(full(s), (uint32_t)((i / C::STAGES) & 1), err)) break;
       const uint32_t kst = ring + s * C::SLOT, vst = kst + C::KV_BYTES, qst = vst + C::KV_BYTES;
+      // visibility of this lane's keys 16 mt + g4 + 8 hh, bit 2 mt + hh (explicit mask)
+      uint32_t kvis = 0u;
+      if constexpr (MASK) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          kvis |= (lds_u8(mask_ring + s * C::MASK_BYTES + 16 * (k >> 1) + g4 + 8 * (k & 1)) != 0u ? 1u : 0u) << k;
+      }
 
       if (opens) {  // new request piece: its query rows, fresh softmax state
 #pragma unroll
@@ -496,7 +538,9 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int key = mt * 16 + g4 + (e >> 1) * 8;
-            const float x = (key < nkeys) ? (sc[mt][nh][e] + s2[mt][nh][e]) * scale : -CUDART_INF_F;
+            bool vis = key < nkeys;
+            if constexpr (MASK) vis = vis && ((kvis >> (2 * mt + (e >> 1))) & 1u);
+            const float x = vis ? (sc[mt][nh][e] + s2[mt][nh][e]) * scale : -CUDART_INF_F;
             sc[mt][nh][e] = x;
             rmax[nh][e & 1] = fmaxf(rmax[nh][e & 1], x);
           }
@@ -769,27 +813,29 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
   }
 }
 
-template <int D, int G>
-cudaError_t launch_split_t(const DecodeParams& p, cudaStream_t stream) {
+template <int D, int G, bool MASK>
+cudaError_t launch_split_t(const typename SplitArg<MASK>::type& arg, cudaStream_t stream) {
+  const DecodeParams& p = params_of(arg);
   using C = DecCfg<D, G>;
+  constexpr int smem = MASK ? C::SMEM_BYTES_MASKED : C::SMEM_BYTES;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e =
-        cudaFuncSetAttribute(decode_split_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        cudaFuncSetAttribute(decode_split_kernel<D, G, MASK>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((p.num_splits + C::NPAIR - 1) / C::NPAIR, p.num_kv_heads);  // NPAIR chunks per CTA
   cfg.blockDim = dim3(C::THREADS);
-  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // set-up overlaps the previous kernel
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, decode_split_kernel<D, G>, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, decode_split_kernel<D, G, MASK>, arg);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -801,10 +847,13 @@ bool decode_supported(int head_dim, int group) {
          (group == 1 || group == 2 || group == 4 || group == 8 || group == 16);
 }
 
-cudaError_t launch_decode_split(const DecodeParams& p, cudaStream_t stream) {
+cudaError_t launch_decode_split(const DecodeParams& p, const DecodeMask* mask, cudaStream_t stream) {
   const int G = p.num_qo_heads / p.num_kv_heads;
-#define ASTR_DEC_CASE(DD, GG) \
-  if (p.head_dim == DD && G == GG) return launch_split_t<DD, GG>(p, stream);
+  // the kernels with an explicit mask are a separate instantiation with a longer parameter block
+  const DecodeParamsMasked pm{p, mask != nullptr ? *mask : DecodeMask{nullptr, 0, 0}};
+#define ASTR_DEC_CASE(DD, GG)                                                                            \
+  if (p.head_dim == DD && G == GG)                                                                       \
+    return mask != nullptr ? launch_split_t<DD, GG, true>(pm, stream) : launch_split_t<DD, GG, false>(p, stream);
   ASTR_DEC_CASE(128, 4) ASTR_DEC_CASE(128, 1) ASTR_DEC_CASE(128, 2) ASTR_DEC_CASE(128, 8) ASTR_DEC_CASE(128, 16)
   ASTR_DEC_CASE(64, 4) ASTR_DEC_CASE(64, 1) ASTR_DEC_CASE(64, 2) ASTR_DEC_CASE(64, 8) ASTR_DEC_CASE(64, 16)
 #undef ASTR_DEC_CASE

@@ -144,6 +144,32 @@ __device__ __forceinline__ void mma_ts_h(uint32_t d, uint32_t a_tmem, uint32_t b
       : "memory");
 }
 // Keeps the values in registers at this point (they are computed before it, not between MMAs).
+// 16 mask bytes, read through L1 (the rows of one query position are shared by its G heads).
+__device__ __forceinline__ uint4 ldg_nc_v4(const uint8_t* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+// 64 mask bytes -> 64 bits (bit k = byte k nonzero).  Per 32-bit word: __vcmpne4 turns each
+// nonzero byte into 0xff; keeping bit 0 of every byte and multiplying by 0x01020408 moves
+// byte k's bit to bit 24 + k (the four partial products land on distinct bits, no carries).
+__device__ __forceinline__ uint64_t mask_bits64(const uint4 (&w)[4]) {
+  uint32_t lo = 0, hi = 0;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint32_t v[4] = {w[c].x, w[c].y, w[c].z, w[c].w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t nib = (((__vcmpne4(v[k], 0u) & 0x01010101u) * 0x01020408u) >> 24) & 0xfu;
+      const int sh = 16 * c + 4 * k;  // bit position of this word's first byte
+      if (sh < 32) lo |= nib << sh;
+      else hi |= nib << (sh - 32);
+    }
+  }
+  return ((uint64_t)hi << 32) | lo;
+}
+
 template <int N>
 __device__ __forceinline__ void keep_regs(uint32_t (&v)[N]) {
 #pragma unroll
@@ -152,8 +178,10 @@ __device__ __forceinline__ void keep_regs(uint32_t (&v)[N]) {
 
 // One work item: KV head kvh, request b, query-tile pair pr (tiles 2 pr and 2 pr + 1 of the
 // request, the second possibly absent).  Items are numbered pair-major, KV-head-minor.
+// cb is the causal offset seq_len - q_len (with the causal offset off: seq_len - 1, so that
+// every row's key window, clipped at kvn = seq_len, is all of the request's keys).
 struct PrefillItem {
-  int b, kvh, q0, q_len, cb, first0, nq, n_tiles;
+  int b, kvh, q0, q_len, cb, kvn, first0, nq, n_tiles;
 };
 
 // Fills the item's fields once its request b and pair pr are known.
@@ -163,11 +191,12 @@ __device__ __forceinline__ void fill_item(const PrefillParams& p, int b, int pr,
   it.kvh = kvh;
   it.q0 = __ldg(p.qo_indptr + b);
   it.q_len = __ldg(p.qo_indptr + b + 1) - it.q0;
-  it.cb = __ldg(p.seq_lens + b) - it.q_len;
+  it.kvn = __ldg(p.seq_lens + b);
+  it.cb = p.causal ? it.kvn - it.q_len : it.kvn - 1;
   it.first0 = pr * BQ2;
   it.nq = min(BQ2 / BQ, (it.q_len - it.first0 + BQ - 1) / BQ);
   const int last = min(it.q_len, it.first0 + it.nq * BQ) - 1;
-  it.n_tiles = (it.cb + last + 1 + BN - 1) / BN;
+  it.n_tiles = (min(it.cb + last + 1, it.kvn) + BN - 1) / BN;
 }
 
 // Decodes item w of the natural order by a warp-parallel prefix scan of the per-request pair
@@ -209,7 +238,7 @@ __device__ __forceinline__ int upper_index(const int* pst, int n, int x) {
   return l;
 }
 
-template <int D, int G>
+template <int D, int G, bool MASK>
 __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(const PrefillParams p,
                                                                                 const __grid_constant__ CUtensorMap q_map,
                                                                                 const __grid_constant__ CUtensorMap o_map) {
@@ -315,7 +344,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
       PrefillItem it;
       fill_item<BQ2, C::BQ, C::BN>(p, b, w - pst[b], 0, it);
       int units = 0;
-      for (int t = 0; t < it.nq; ++t) units += (it.cb + min(it.q_len, it.first0 + (t + 1) * C::BQ) + C::BN - 1) / C::BN;
+      for (int t = 0; t < it.nq; ++t)
+        units += (min(it.cb + min(it.q_len, it.first0 + (t + 1) * C::BQ), it.kvn) + C::BN - 1) / C::BN;
       const int c = 2 * it.n_tiles + (units + 2) / 4 + 9 - (it.nq == 1 ? 3 : 0);
       key[w] = (uint16_t)(C::SORT_BUCKETS - 1 - min(max(c, 0), C::SORT_BUCKETS - 1));  // ascending key = descending cost
     }
@@ -480,7 +510,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
       if (!get_item(n_item, it)) break;
       const int kvh = it.kvh;
       const int32_t* r2t = p.req_to_token + (size_t)it.b * p.r2t_stride;
-      const int kv_end = min(it.cb + min(it.q_len, it.first0 + BQ2), it.cb + it.q_len);
+      const int kv_end = min(it.cb + min(it.q_len, it.first0 + BQ2), it.kvn);
       const int j_first = (st - g_base % C::STAGES + C::STAGES) % C::STAGES;
       auto ids_of = [&](int j, int half) {  // slot id of key 32 half + lane of item tile j, or -1
         const int key = j * C::BN + half * 32 + lane;
@@ -547,7 +577,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
     for (int n_item = 0; ok; ++n_item) {
       if (!get_item(n_item, it)) break;
       if (lane == 0) {
-        const int nk = (t < it.nq) ? (it.cb + min(it.q_len, it.first0 + (t + 1) * C::BQ) + C::BN - 1) / C::BN : 0;
+        const int nk =
+            (t < it.nq) ? (min(it.cb + min(it.q_len, it.first0 + (t + 1) * C::BQ), it.kvn) + C::BN - 1) / C::BN : 0;
         const int n = it.n_tiles;
         const uint32_t q_lo = (uint32_t)qd0 + (uint32_t)((((u0 + t) % C::Q_SLOTS) * C::Q_BYTES) >> 4);
         auto wait_one = [&](uint32_t bar, uint32_t parity, bool ready) {  // blocking only if not pre-tested ready
@@ -656,6 +687,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
     const uint32_t o_col = tmem + lane_base + t * C::TMEM_TILE;
     const float scale = p.scale_log2;
     const bool pos_scale = scale >= 0.f;
+    constexpr bool has_mask = MASK;
     int gs = 0, n_used = 0;  // same counters as the MMA thread, for this query tile
     int g_base = 0;          // global index of the item's KV tile 0
     int u0 = 0;              // query tiles of the items before this one
@@ -670,14 +702,25 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
         continue;
       }
       const int qf = it.first0 + t * C::BQ, ql = min(it.q_len, qf + C::BQ) - 1;
-      const int n_keys = (it.cb + ql + 1 + C::BN - 1) / C::BN;
-      const int qi = qf + row / G;                       // this thread's query position
-      const int limit = it.cb + min(qi, ql);             // last key this row attends
-      const int mask_from = (it.cb + qf + 1) / C::BN;    // tiles >= this one hold a masked key for some row
+      const int n_keys = (min(it.cb + ql + 1, it.kvn) + C::BN - 1) / C::BN;
+      const int qi = qf + row / G;                              // this thread's query position
+      const int limit = min(it.cb + min(qi, ql), it.kvn - 1);   // last key this row attends
+      const int mask_from = min(it.cb + qf + 1, it.kvn) / C::BN;  // tiles >= this one hold a masked key for some row
+      // explicit mask: this row's bytes (padded rows past the tile's last position reuse it)
+      const uint8_t* mrow = has_mask ? p.mask + (int64_t)it.b * p.mask_req_pitch + (int64_t)min(qi, ql) * p.mask_row_pitch
+                                     : nullptr;
       float m_run = -CUDART_INF_F, l_run = 0.f;
       for (int j = 0; j < n_keys; ++j) {
         const int gb = gs + j;
         const uint32_t sb = o_col + D + (gb & 1) * C::BN;  // S_t(j), then P_t(j)
+        // the tile's 64 mask bytes load while S is computed; a 16-byte chunk that starts inside
+        // the row (pitch a multiple of 16) lies inside it, later ones read as masked
+        uint4 mw[4];
+        if (has_mask) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            mw[c] = (j * C::BN + 16 * c < p.mask_kv_pitch) ? ldg_nc_v4(mrow + j * C::BN + 16 * c) : make_uint4(0, 0, 0, 0);
+        }
         if (!(ok = wait_or_fail(s_full(t, gb & 1), (uint32_t)((gb >> 1) & 1)))) break;
         tc::fence_after_sync();
         float s[C::BN];
@@ -694,10 +737,18 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
         // row max of sm_scale * s in base-2 units: max (or min for a negative scale) of the raw
         // scores times the scale; on tiles that cross the causal edge, keys past this row's
         // limit are set to the extreme that the max / min ignores, and get p = 0 below
-        const bool masked = j >= mask_from;
+        const bool masked = has_mask || j >= mask_from;
         const int j0 = j * C::BN;
         const float skip = pos_scale ? -CUDART_INF_F : CUDART_INF_F;
-        if (masked) {
+        // explicit mask: bit c of vb = key j0 + c visible (mask byte nonzero, key <= limit)
+        uint64_t vb = 0;
+        if (has_mask) {
+          vb = mask_bits64(mw);
+          const int n_in = limit - j0 + 1;  // keys of the tile within the row's window
+          vb = (n_in >= 64) ? vb : (n_in <= 0 ? 0ull : vb & ((1ull << n_in) - 1ull));
+#pragma unroll
+          for (int c = 0; c < C::BN; ++c) s[c] = ((vb >> c) & 1ull) ? s[c] : skip;
+        } else if (masked) {
 #pragma unroll
           for (int c = 0; c < C::BN; ++c) s[c] = (j0 + c <= limit) ? s[c] : skip;
         }
@@ -712,7 +763,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
         }
         const float ext = pos_scale ? max3(max3(e4[0], e4[1], e4[2]), e4[3], skip)
                                     : min3(min3(e4[0], e4[1], e4[2]), e4[3], skip);
-        const float m_tile = (j0 > limit) ? -CUDART_INF_F : ext * scale;  // -inf: no visible key
+        const bool none = has_mask ? vb == 0ull : j0 > limit;
+        const float m_tile = none ? -CUDART_INF_F : ext * scale;  // -inf: no visible key
         const bool need = m_tile > m_run + C::kRescaleThreshold;  // true on the first visible tile
         if (__any_sync(kFullMask, need)) {
           const float alpha = need ? fast_exp2(m_run - m_tile) : 1.f;  // 0 while m_run = -inf
@@ -752,7 +804,10 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
             float x0, x1;
             upk2(fma2(pk2(s[c0], s[c0 + 1]), sc2, nm2), x0, x1);
             float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-            if (masked) {
+            if (has_mask) {
+              p0 = ((vb >> c0) & 1ull) ? p0 : 0.f;
+              p1 = ((vb >> (c0 + 1)) & 1ull) ? p1 : 0.f;
+            } else if (masked) {
               p0 = (j0 + c0 <= limit) ? p0 : 0.f;
               p1 = (j0 + c0 + 1 <= limit) ? p1 : 0.f;
             }
@@ -783,7 +838,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
       ok = wait_or_fail(o_done(t), (uint32_t)(n_used & 1));
       tc::fence_after_sync();
       tc::fence_proxy_async_smem();  // the tensor core's reads of this buffer precede the writes below
-      const float inv = (ok && !*err) ? 1.f / l_run : CUDART_NAN_F;   // a timed-out wait poisons the tile
+      // a timed-out wait poisons the tile; a row with no visible key (explicit mask) is zero
+      const float inv = (ok && !*err) ? (l_run > 0.f ? 1.f / l_run : 0.f) : CUDART_NAN_F;
       const uint32_t stg = q_slot(u);
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
@@ -833,13 +889,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
   return fn;
 }
 
-template <int D, int G>
+template <int D, int G, bool MASK>
 cudaError_t launch_prefill_t(const PrefillParams& p, cudaStream_t stream) {
   using C = PrefillCfg<D, G>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e =
-        cudaFuncSetAttribute(prefill_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        cudaFuncSetAttribute(prefill_kernel<D, G, MASK>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -863,12 +919,27 @@ cudaError_t launch_prefill_t(const PrefillParams& p, cudaStream_t stream) {
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  prefill_kernel<D, G><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(p, q_map, o_map);
+  prefill_kernel<D, G, MASK><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(p, q_map, o_map);
   return cudaGetLastError();
+}
+
+template <bool MASK>
+cudaError_t dispatch_prefill(const PrefillParams& p, cudaStream_t stream) {
+  const int G = p.num_qo_heads / p.num_kv_heads;
+#define ASTR_PF_CASE(DD, GG) \
+  if (p.head_dim == DD && G == GG) return launch_prefill_t<DD, GG, MASK>(p, stream);
+  ASTR_PF_CASE(128, 4) ASTR_PF_CASE(128, 1) ASTR_PF_CASE(128, 2) ASTR_PF_CASE(128, 8) ASTR_PF_CASE(128, 16)
+  ASTR_PF_CASE(64, 4) ASTR_PF_CASE(64, 1) ASTR_PF_CASE(64, 2) ASTR_PF_CASE(64, 8) ASTR_PF_CASE(64, 16)
+#undef ASTR_PF_CASE
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
+// The kernels with an explicit mask are a second instantiation of the same template, compiled
+// in their own translation unit (prefill_masked.cu includes this file with
+// ASTR_PREFILL_MASKED_TU defined) so the two sets build in parallel.
+#ifndef ASTR_PREFILL_MASKED_TU
 int prefill_rows_per_cta() { return 256; }
 
 bool prefill_supported(int head_dim, int group) {
@@ -876,13 +947,11 @@ bool prefill_supported(int head_dim, int group) {
 }
 
 cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream) {
-  const int G = p.num_qo_heads / p.num_kv_heads;
-#define ASTR_PF_CASE(DD, GG) \
-  if (p.head_dim == DD && G == GG) return launch_prefill_t<DD, GG>(p, stream);
-  ASTR_PF_CASE(128, 4) ASTR_PF_CASE(128, 1) ASTR_PF_CASE(128, 2) ASTR_PF_CASE(128, 8) ASTR_PF_CASE(128, 16)
-  ASTR_PF_CASE(64, 4) ASTR_PF_CASE(64, 1) ASTR_PF_CASE(64, 2) ASTR_PF_CASE(64, 8) ASTR_PF_CASE(64, 16)
-#undef ASTR_PF_CASE
-  return cudaErrorInvalidValue;
+  if (p.mask != nullptr) return launch_prefill_masked(p, stream);
+  return dispatch_prefill<false>(p, stream);
 }
+#else
+cudaError_t launch_prefill_masked(const PrefillParams& p, cudaStream_t stream) { return dispatch_prefill<true>(p, stream); }
+#endif
 
 }  // namespace astr

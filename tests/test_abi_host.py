@@ -202,3 +202,52 @@ def test_append_nothing_to_do_without_gpu(lib):
     assert _app(_dims(batch=0)) == pa.ASTR_OK
     assert _app(_dims(total_q=0)) == pa.ASTR_OK
     assert lib.astr_attn_kv_append(A, A, A, A, A, A, A, None, None) == pa.ASTR_ERR_INVALID_ARG
+
+
+def _mask(ptr=A, dims=3, kv_pitch=2000, q_pitch=16, causal=1):
+    return pa.Mask(ptr, dims, kv_pitch, q_pitch, causal)
+
+
+def _pfm(d, m, **ptr):
+    p = dict(q=A, qo=A, k=A, v=A, r2t=A, seq=A, kvi=A, out=A)
+    p.update(ptr)
+    return pa.astr_attn_prefill_ragged_masked(p["q"], p["qo"], p["k"], p["v"], p["r2t"], p["seq"], p["kvi"], m,
+                                              p["out"], d, 0.1, stream=0, check=False)
+
+
+def _decm(d, m):
+    return pa.astr_attn_paged_decode_masked(A, A, A, A, A, A, m, A, A, A, d, 0.1, stream=0, check=False)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dims=4), pa.ASTR_ERR_INVALID_ARG),
+    (dict(kv_pitch=2008), pa.ASTR_ERR_INVALID_ARG),      # not a multiple of 16
+    (dict(kv_pitch=1984), pa.ASTR_ERR_INVALID_ARG),      # below max_seq_len
+    (dict(q_pitch=15), pa.ASTR_ERR_INVALID_ARG),         # below max_q_len
+    (dict(causal=2), pa.ASTR_ERR_INVALID_ARG),
+    (dict(ptr=A + 8), pa.ASTR_ERR_MISALIGNED),
+])
+def test_prefill_masked_bad_mask(lib, kw, status):
+    assert _pfm(_dims(batch=0), _mask(**kw)) == status   # checked before the empty-batch early return
+
+
+def test_prefill_masked_accepts_valid_masks_and_null_struct_is_rejected(lib):
+    assert _pfm(_dims(batch=0), _mask()) == pa.ASTR_OK
+    assert _pfm(_dims(batch=0), _mask(dims=2, q_pitch=0)) == pa.ASTR_OK
+    assert _pfm(_dims(batch=0), _mask(ptr=None, dims=0, kv_pitch=0, q_pitch=0, causal=0)) == pa.ASTR_OK
+    assert _pfm(_dims(batch=0), None) == pa.ASTR_ERR_INVALID_ARG
+    assert _pfm(_dims(batch=0), _mask(), q=0) == pa.ASTR_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dims=1), pa.ASTR_ERR_INVALID_ARG),
+    (dict(kv_pitch=0), pa.ASTR_ERR_INVALID_ARG),
+    (dict(q_pitch=0), pa.ASTR_ERR_INVALID_ARG),          # 3-D needs at least one row per request
+    (dict(ptr=A + 4), pa.ASTR_ERR_MISALIGNED),
+])
+def test_decode_masked_bad_mask(lib, kw, status):
+    assert _decm(_dims(batch=0), _mask(**kw)) == status
+
+
+def test_decode_masked_null_struct(lib):
+    assert _decm(_dims(batch=0), None) == pa.ASTR_ERR_INVALID_ARG
