@@ -17,6 +17,8 @@ Also reported in the same line:
                     mask (causal on) and decode with a 2-D mask, each byte kept with
                     probability 0.75; FLOP/s and GB/s count the same work as the unmasked calls
                     (masked keys are still read and scored).
+  * contiguous   -- decode over a contiguous "bhld" K/V cache (stride addressing, no slot
+                    table; 2 rotating copies) and prefill over a "blhd" cache, same workloads.
   * kv_append    -- the KV-append step (the extend workload's new K/V rows written into their
                     pool slots), bytes moved per second against the measured HBM copy peak.
   * e2e          -- the same decode metric with every input in pinned host memory, the
@@ -454,6 +456,41 @@ def main():
     timed(decode_masked, 20)
     t_dm = timed(decode_masked, n_split) / n_split
 
+    # ---------------- contiguous K/V caches (stride addressing instead of the slot table)
+    def contiguous(wl, head_major):
+        """The workload's K and V rows by request position: [B, L, Hkv, d] views ("bhld" storage
+        when head_major)."""
+        L = wl.max_seq_len
+        kc = np.zeros((wl.batch, L, wl.num_kv_heads, wl.head_dim), np.uint16)
+        vc = np.zeros_like(kc)
+        for b in range(wl.batch):
+            n = int(wl.seq_lens[b])
+            sl_ = wl.req_to_token[b, :n].astype(np.int64)
+            kc[b, :n], vc[b, :n] = wl.k_pool[sl_], wl.v_pool[sl_]
+        if head_major:
+            return [bf(a.transpose(0, 2, 1, 3)).transpose(1, 2) for a in (kc, vc)]
+        return [bf(a) for a in (kc, vc)]
+
+    dcaches = [contiguous(w, True) for _ in range(2)]
+    dlay = pa.make_kv_layout(dcaches[0][0])
+
+    def decode_contig(i):
+        kc, vc = dcaches[i % 2]
+        pa.astr_attn_decode_contiguous(q, kc, vc, dlay, seq, kvi, o_part, ml_part, out, dims, w.sm_scale, stream=sh)
+
+    timed(decode_contig, 20)
+    t_dc = timed(decode_contig, n_split) / n_split
+    del dcaches
+    pkc, pvc = contiguous(wp, False)
+    play = pa.make_kv_layout(pkc)
+
+    def prefill_contig(i):
+        pa.astr_attn_prefill_contiguous(pq, pqo, pkc, pvc, play, ps_, pki, pout, pdims, wp.sm_scale, stream=sh)
+
+    timed(prefill_contig, 5)
+    t_pc = timed(prefill_contig, n_pf) / n_pf
+    del pkc, pvc
+
     # ---------------- KV-append step on the extend workload (rotating copies: cold in L2)
     aqo_np, akn_np, avn_np = workload.append_rows(wp, seed=wp.seed + 1)
     a_rows = int(aqo_np[-1])
@@ -538,6 +575,12 @@ def main():
                               "us_per_call": round(t_dm * 1e6, 3),
                               "gbs": round(nbytes["kv"] / t_dm / 1e9, 2),
                               "frac": round(nbytes["kv"] / t_dm / 1e9 / peaks["hbm_gbs"], 4)}},
+        "contiguous": {"decode": {"workload": w.name, "layout": "bhld", "us_per_call": round(t_dc * 1e6, 3),
+                                  "gbs": round(nbytes["kv"] / t_dc / 1e9, 2),
+                                  "frac": round(nbytes["kv"] / t_dc / 1e9 / peaks["hbm_gbs"], 4)},
+                       "prefill": {"workload": wp.name, "layout": "blhd", "us_per_call": round(t_pc * 1e6, 3),
+                                   "tflops": round(flops / t_pc / 1e12, 2),
+                                   "frac": round(flops / t_pc / 1e12 / peaks["bf16_tflops"], 4)}},
         "kv_append": {"workload": wp.name, "rows": a_rows, "us_per_call": round(t_app * 1e6, 3),
                       "bytes_per_call": a_bytes,
                       "same_bytes_device_copy_us": round(t_copy * 1e6, 3),

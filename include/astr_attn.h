@@ -216,6 +216,47 @@ int astr_attn_prefill_ragged_masked(const uint16_t* q, const int32_t* qo_indptr,
                                     const astr_attn_dims* dims, float sm_scale, void* stream);
 
 /*
+ * Contiguous K/V cache layout (P3, stride-addressing and layout commits: Q/KV/O addressed
+ * through strides so "bhld" and "blhd" caches work without copies).  Host struct read during
+ * the call only.  Element e of key position j, KV head h, request b of a contiguous cache sits
+ * at cache[b * batch_stride + j * token_stride + h * head_stride + e]; all strides are in
+ * elements, non-negative and multiples of 8 (16-byte rows).  For a cache of L positions:
+ *   bhld  [batch, Hkv, L, head_dim]:  batch_stride = Hkv*L*d, head_stride = L*d, token_stride = d
+ *   blhd  [batch, L, Hkv, head_dim]:  batch_stride = L*Hkv*d, token_stride = Hkv*d, head_stride = d
+ * Positions 0 .. dims->max_seq_len - 1 of every request must lie inside the cache.
+ */
+typedef struct astr_attn_kv_layout {
+  int64_t batch_stride;
+  int64_t token_stride;
+  int64_t head_stride;
+} astr_attn_kv_layout;
+
+/*
+ * Decode over a contiguous K/V cache: astr_attn_paged_decode (and, with `mask` not NULL,
+ * astr_attn_paged_decode_masked) with key j of request b read from the cache rows of layout
+ * `layout` instead of pool[req_to_token[b][j]].  dims->r2t_stride and num_slots are not read;
+ * dims->max_seq_len bounds the positions read (a key at or past it reads as zeros).  Same
+ * schedule, partial layout, rules and errors otherwise, plus INVALID_ARG for a NULL layout or
+ * negative strides and MISALIGNED for strides that are not multiples of 8.
+ */
+int astr_attn_decode_contiguous(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                                const astr_attn_kv_layout* layout, const int32_t* seq_lens, const int32_t* kv_indptr,
+                                const astr_attn_mask* mask, float* o_part, float* ml_part, uint16_t* out,
+                                const astr_attn_dims* dims, float sm_scale, void* stream);
+
+/*
+ * Ragged prefill over a contiguous K/V cache: astr_attn_prefill_ragged (with `mask` not NULL,
+ * astr_attn_prefill_ragged_masked, causal switch included) with key j of request b read from
+ * the cache rows of `layout`.  Query rows and outputs keep the packed [total_q, Hq, head_dim]
+ * layout.  dims->r2t_stride and num_slots are not read; dims->max_seq_len bounds the positions
+ * read.  Errors as astr_attn_decode_contiguous.
+ */
+int astr_attn_prefill_contiguous(const uint16_t* q, const int32_t* qo_indptr, const uint16_t* k_cache,
+                                 const uint16_t* v_cache, const astr_attn_kv_layout* layout, const int32_t* seq_lens,
+                                 const int32_t* kv_indptr, const astr_attn_mask* mask, uint16_t* out,
+                                 const astr_attn_dims* dims, float sm_scale, void* stream);
+
+/*
  * Paged decode that allocates nothing (no counterpart in the source pages; this is a
  * service of this library).  Same computation, arguments, rules and errors as
  * astr_attn_paged_decode minus o_part / ml_part: the split-KV partials go to a 16 MiB

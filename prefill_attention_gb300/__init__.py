@@ -19,7 +19,8 @@ __all__ = [
     "Dims", "AstrAttnError", "load", "lib_path", "make_dims",
     "astr_attn_paged_decode", "astr_attn_decode_split", "astr_attn_decode_combine", "astr_attn_prefill_ragged",
     "astr_attn_paged_decode_noalloc", "astr_attn_kv_append", "astr_attn_paged_decode_masked",
-    "astr_attn_prefill_ragged_masked", "Mask", "make_mask",
+    "astr_attn_prefill_ragged_masked", "Mask", "make_mask", "KvLayout", "make_kv_layout",
+    "astr_attn_decode_contiguous", "astr_attn_prefill_contiguous",
     "astr_attn_decode_num_splits", "astr_attn_decode_workspace_bytes", "astr_attn_status_string",
     "astr_attn_version", "alloc_decode_workspace",
     "ASTR_OK", "ASTR_ERR_INVALID_ARG", "ASTR_ERR_UNSUPPORTED", "ASTR_ERR_MISALIGNED",
@@ -42,7 +43,8 @@ EXPORTED_SYMBOLS = [
     "astr_attn_decode_num_splits", "astr_attn_decode_workspace_bytes", "astr_attn_paged_decode",
     "astr_attn_decode_combine", "astr_attn_prefill_ragged", "astr_attn_status_string", "astr_attn_version",
     "astr_attn_decode_split", "astr_attn_paged_decode_noalloc", "astr_attn_kv_append",
-    "astr_attn_paged_decode_masked", "astr_attn_prefill_ragged_masked",
+    "astr_attn_paged_decode_masked", "astr_attn_prefill_ragged_masked", "astr_attn_decode_contiguous",
+    "astr_attn_prefill_contiguous",
 ]
 
 
@@ -80,6 +82,21 @@ def make_mask(mask=None, causal: bool = True) -> Mask:
                 int(bool(causal)))
 
 
+class KvLayout(ctypes.Structure):
+    """Mirror of ``astr_attn_kv_layout`` (strides in elements; see include/astr_attn.h)."""
+    _fields_ = [("batch_stride", ctypes.c_int64), ("token_stride", ctypes.c_int64), ("head_stride", ctypes.c_int64)]
+
+
+def make_kv_layout(cache) -> KvLayout:
+    """Layout of a contiguous K/V cache tensor given with its logical dims ordered
+    [batch, position, kv_head, head_dim] (a "blhd" tensor as is, a "bhld" one as
+    ``cache.transpose(1, 2)``): the strides are read from the tensor, no copy is made."""
+    sb, sl, sh, se = (int(x) for x in cache.stride())
+    if se != 1:
+        raise ValueError("head_dim must be the contiguous dimension")
+    return KvLayout(sb, sl, sh)
+
+
 def lib_path() -> str:
     return _LIB_PATH
 
@@ -107,13 +124,16 @@ def load():
     M = ctypes.POINTER(Mask)
     lib.astr_attn_paged_decode_masked.argtypes = [P, P, P, P, P, P, M, P, P, P, D, F, P]
     lib.astr_attn_prefill_ragged_masked.argtypes = [P, P, P, P, P, P, P, M, P, D, F, P]
+    LY = ctypes.POINTER(KvLayout)
+    lib.astr_attn_decode_contiguous.argtypes = [P, P, P, LY, P, P, M, P, P, P, D, F, P]
+    lib.astr_attn_prefill_contiguous.argtypes = [P, P, P, P, LY, P, P, M, P, D, F, P]
     lib.astr_attn_status_string.argtypes = [I32]
     lib.astr_attn_status_string.restype = ctypes.c_char_p
     lib.astr_attn_version.argtypes = []
     for f in ("astr_attn_decode_num_splits", "astr_attn_decode_workspace_bytes", "astr_attn_paged_decode",
               "astr_attn_decode_split", "astr_attn_decode_combine", "astr_attn_prefill_ragged", "astr_attn_version",
               "astr_attn_paged_decode_noalloc", "astr_attn_kv_append", "astr_attn_paged_decode_masked",
-              "astr_attn_prefill_ragged_masked"):
+              "astr_attn_prefill_ragged_masked", "astr_attn_decode_contiguous", "astr_attn_prefill_contiguous"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -243,6 +263,29 @@ def astr_attn_prefill_ragged_masked(q, qo_indptr, k_pool, v_pool, req_to_token, 
                                                 None if mask is None else ctypes.byref(mask), _ptr(out),
                                                 ctypes.byref(dims), float(sm_scale), _stream(stream))
     return _check(st, "astr_attn_prefill_ragged_masked", check)
+
+
+def astr_attn_decode_contiguous(q, k_cache, v_cache, layout: KvLayout, seq_lens, kv_indptr, o_part, ml_part, out,
+                                dims: Dims, sm_scale: float, mask: Optional[Mask] = None, stream=None,
+                                check: bool = True) -> int:
+    """Split-KV decode over a contiguous K/V cache (``make_kv_layout``); optional explicit mask."""
+    st = load().astr_attn_decode_contiguous(_ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                            None if layout is None else ctypes.byref(layout), _ptr(seq_lens),
+                                            _ptr(kv_indptr), None if mask is None else ctypes.byref(mask),
+                                            _ptr(o_part), _ptr(ml_part), _ptr(out), ctypes.byref(dims),
+                                            float(sm_scale), _stream(stream))
+    return _check(st, "astr_attn_decode_contiguous", check)
+
+
+def astr_attn_prefill_contiguous(q, qo_indptr, k_cache, v_cache, layout: KvLayout, seq_lens, kv_indptr, out,
+                                 dims: Dims, sm_scale: float, mask: Optional[Mask] = None, stream=None,
+                                 check: bool = True) -> int:
+    """Ragged prefill over a contiguous K/V cache; optional mask / causal switch (``make_mask``)."""
+    st = load().astr_attn_prefill_contiguous(_ptr(q), _ptr(qo_indptr), _ptr(k_cache), _ptr(v_cache),
+                                             None if layout is None else ctypes.byref(layout), _ptr(seq_lens),
+                                             _ptr(kv_indptr), None if mask is None else ctypes.byref(mask),
+                                             _ptr(out), ctypes.byref(dims), float(sm_scale), _stream(stream))
+    return _check(st, "astr_attn_prefill_contiguous", check)
 
 
 def alloc_decode_workspace(dims: Dims, device="cuda"):

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG, "libastr_attn.so")
-SOURCES = ["api.cu", "decode.cu", "prefill.cu", "prefill_masked.cu", "noalloc.cu", "append.cu"]
+SOURCES = ["api.cu", "decode.cu", "prefill.cu", "prefill_masked.cu", "prefill_contig.cu", "noalloc.cu", "append.cu"]
 HEADERS = ["common.cuh", "tcgen05.cuh", "astr_attn_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -149,6 +149,24 @@ static int decode_prepare(const astr_attn_dims* d, float sm_scale, astr::DecodeP
   return ASTR_OK;
 }
 
+// Contiguous-cache layout: strides non-negative multiples of 8 elements (16-byte rows).
+static int check_layout(const astr_attn_kv_layout* l, const astr_attn_dims* d, astr::KvStrides* ks) {
+  if (l == nullptr || d == nullptr) return ASTR_ERR_INVALID_ARG;
+  if (l->batch_stride < 0 || l->token_stride < 0 || l->head_stride < 0) return ASTR_ERR_INVALID_ARG;
+  if (l->batch_stride % 8 != 0 || l->token_stride % 8 != 0 || l->head_stride % 8 != 0) return ASTR_ERR_MISALIGNED;
+  *ks = astr::KvStrides{l->batch_stride, l->token_stride, l->head_stride, d->max_seq_len};
+  return ASTR_OK;
+}
+
+// The dims as the shared checks expect them when K/V come from a contiguous cache: no slot
+// table (its pitch taken as max_seq_len) and no pool (one nominal slot).
+static astr_attn_dims contiguous_dims(const astr_attn_dims* d) {
+  astr_attn_dims c = *d;
+  c.r2t_stride = d->max_seq_len;
+  c.num_slots = 1;
+  return c;
+}
+
 // Explicit-mask arguments: shape rules, then the pitches of request b's bytes (and of its rows).
 static int check_mask(const astr_attn_mask* m, const astr_attn_dims* d, bool decode, int64_t* req_pitch,
                       int64_t* row_pitch) {
@@ -167,27 +185,33 @@ static int check_mask(const astr_attn_mask* m, const astr_attn_dims* d, bool dec
 
 static int paged_decode_impl(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
                              const int32_t* req_to_token, const int32_t* seq_lens, const int32_t* kv_indptr,
-                             const astr_attn_mask* mask, float* o_part, float* ml_part, uint16_t* out,
-                             const astr_attn_dims* dims, float sm_scale, void* stream) {
-  if (!q || !k_pool || !v_pool || !req_to_token || !seq_lens || !kv_indptr || !o_part || !ml_part || !out)
+                             const astr_attn_mask* mask, const astr_attn_kv_layout* layout, float* o_part,
+                             float* ml_part, uint16_t* out, const astr_attn_dims* dims, float sm_scale, void* stream) {
+  const bool contig = layout != nullptr;  // K/V from a contiguous cache: no slot table
+  if (!q || !k_pool || !v_pool || (!contig && !req_to_token) || !seq_lens || !kv_indptr || !o_part || !ml_part || !out)
     return ASTR_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(o_part, 16) ||
       !aligned(ml_part, 16) || !aligned(out, 16) || !aligned(req_to_token, 4) || !aligned(seq_lens, 4) ||
       !aligned(kv_indptr, 4))
     return ASTR_ERR_MISALIGNED;
+  if (dims == nullptr) return ASTR_ERR_INVALID_ARG;
   int64_t mask_req_pitch = 0, mask_row_pitch = 0;
   int st = ASTR_OK;
   if (mask != nullptr && (st = check_mask(mask, dims, true, &mask_req_pitch, &mask_row_pitch)) != ASTR_OK) return st;
+  astr::KvStrides ks{0, 0, 0, 0};
+  if (contig && (st = check_layout(layout, dims, &ks)) != ASTR_OK) return st;
+  const astr_attn_dims cdims = contig ? contiguous_dims(dims) : *dims;
   astr::DecodeParams p{};
   bool nothing = false;
-  st = decode_prepare(dims, sm_scale, &p, &nothing);
+  st = decode_prepare(&cdims, sm_scale, &p, &nothing);
   if (st != ASTR_OK || nothing) return st;
   astr::DecodeMask dm{nullptr, 0, 0};
   if (mask != nullptr && mask->mask != nullptr) dm = astr::DecodeMask{mask->mask, mask_req_pitch, mask->kv_pitch};
   p.q = q; p.k_pool = k_pool; p.v_pool = v_pool; p.req_to_token = req_to_token; p.seq_lens = seq_lens;
   p.kv_indptr = kv_indptr; p.o_part = o_part; p.ml_part = ml_part; p.out = out;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (astr::launch_decode_split(p, dm.mask != nullptr ? &dm : nullptr, s) != cudaSuccess) return ASTR_ERR_LAUNCH_FAILED;
+  if (astr::launch_decode_split(p, dm.mask != nullptr ? &dm : nullptr, contig ? &ks : nullptr, s) != cudaSuccess)
+    return ASTR_ERR_LAUNCH_FAILED;
   p.indptr_before_wait = 1;  // the combine follows this call's split kernel directly
   if (astr::launch_decode_combine(p, s) != cudaSuccess) return ASTR_ERR_LAUNCH_FAILED;
   return ASTR_OK;
@@ -197,8 +221,8 @@ int astr_attn_paged_decode(const uint16_t* q, const uint16_t* k_pool, const uint
                            const int32_t* req_to_token, const int32_t* seq_lens, const int32_t* kv_indptr,
                            float* o_part, float* ml_part, uint16_t* out, const astr_attn_dims* dims, float sm_scale,
                            void* stream) {
-  return paged_decode_impl(q, k_pool, v_pool, req_to_token, seq_lens, kv_indptr, nullptr, o_part, ml_part, out, dims,
-                           sm_scale, stream);
+  return paged_decode_impl(q, k_pool, v_pool, req_to_token, seq_lens, kv_indptr, nullptr, nullptr, o_part, ml_part,
+                           out, dims, sm_scale, stream);
 }
 
 int astr_attn_paged_decode_masked(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
@@ -206,8 +230,17 @@ int astr_attn_paged_decode_masked(const uint16_t* q, const uint16_t* k_pool, con
                                   const astr_attn_mask* mask, float* o_part, float* ml_part, uint16_t* out,
                                   const astr_attn_dims* dims, float sm_scale, void* stream) {
   if (mask == nullptr) return ASTR_ERR_INVALID_ARG;
-  return paged_decode_impl(q, k_pool, v_pool, req_to_token, seq_lens, kv_indptr, mask, o_part, ml_part, out, dims,
-                           sm_scale, stream);
+  return paged_decode_impl(q, k_pool, v_pool, req_to_token, seq_lens, kv_indptr, mask, nullptr, o_part, ml_part, out,
+                           dims, sm_scale, stream);
+}
+
+int astr_attn_decode_contiguous(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                                const astr_attn_kv_layout* layout, const int32_t* seq_lens, const int32_t* kv_indptr,
+                                const astr_attn_mask* mask, float* o_part, float* ml_part, uint16_t* out,
+                                const astr_attn_dims* dims, float sm_scale, void* stream) {
+  if (layout == nullptr) return ASTR_ERR_INVALID_ARG;
+  return paged_decode_impl(q, k_cache, v_cache, nullptr, seq_lens, kv_indptr, mask, layout, o_part, ml_part, out,
+                           dims, sm_scale, stream);
 }
 
 int astr_attn_decode_split(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
@@ -224,7 +257,7 @@ int astr_attn_decode_split(const uint16_t* q, const uint16_t* k_pool, const uint
   if (st != ASTR_OK || nothing) return st;
   p.q = q; p.k_pool = k_pool; p.v_pool = v_pool; p.req_to_token = req_to_token; p.seq_lens = seq_lens;
   p.kv_indptr = kv_indptr; p.o_part = o_part; p.ml_part = ml_part;
-  if (astr::launch_decode_split(p, nullptr, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+  if (astr::launch_decode_split(p, nullptr, nullptr, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return ASTR_ERR_LAUNCH_FAILED;
   return ASTR_OK;
 }
@@ -255,10 +288,19 @@ int astr_attn_decode_combine(const float* o_part, const float* ml_part, const in
 
 static int prefill_impl(const uint16_t* q, const int32_t* qo_indptr, const uint16_t* k_pool, const uint16_t* v_pool,
                         const int32_t* req_to_token, const int32_t* seq_lens, const int32_t* kv_indptr,
-                        const astr_attn_mask* mask, uint16_t* out, const astr_attn_dims* d, float sm_scale,
-                        void* stream) {
+                        const astr_attn_mask* mask, const astr_attn_kv_layout* layout, uint16_t* out,
+                        const astr_attn_dims* dims, float sm_scale, void* stream) {
   (void)kv_indptr;
-  if (!q || !qo_indptr || !k_pool || !v_pool || !req_to_token || !seq_lens || !out) return ASTR_ERR_INVALID_ARG;
+  const bool contig = layout != nullptr;  // K/V from a contiguous cache: no slot table
+  if (!q || !qo_indptr || !k_pool || !v_pool || (!contig && !req_to_token) || !seq_lens || !out || !dims)
+    return ASTR_ERR_INVALID_ARG;
+  astr::KvStrides ks{0, 0, 0, 0};
+  if (contig) {
+    const int lst = check_layout(layout, dims, &ks);
+    if (lst != ASTR_OK) return lst;
+  }
+  const astr_attn_dims cdims = contig ? contiguous_dims(dims) : *dims;
+  const astr_attn_dims* d = &cdims;
   if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16) ||
       !aligned(qo_indptr, 4) || !aligned(req_to_token, 4) || !aligned(seq_lens, 4) ||
       (kv_indptr != nullptr && !aligned(kv_indptr, 4)))
@@ -301,6 +343,8 @@ static int prefill_impl(const uint16_t* q, const int32_t* qo_indptr, const uint1
     p.mask_row_pitch = mask_row_pitch;
     p.mask_kv_pitch = mask->kv_pitch;
   }
+  p.contig = contig ? 1 : 0;
+  p.kv = ks;
   if (astr::launch_prefill(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ASTR_ERR_LAUNCH_FAILED;
   return ASTR_OK;
 }
@@ -309,8 +353,8 @@ int astr_attn_prefill_ragged(const uint16_t* q, const int32_t* qo_indptr, const 
                              const uint16_t* v_pool, const int32_t* req_to_token, const int32_t* seq_lens,
                              const int32_t* kv_indptr, uint16_t* out, const astr_attn_dims* d, float sm_scale,
                              void* stream) {
-  return prefill_impl(q, qo_indptr, k_pool, v_pool, req_to_token, seq_lens, kv_indptr, nullptr, out, d, sm_scale,
-                      stream);
+  return prefill_impl(q, qo_indptr, k_pool, v_pool, req_to_token, seq_lens, kv_indptr, nullptr, nullptr, out, d,
+                      sm_scale, stream);
 }
 
 int astr_attn_prefill_ragged_masked(const uint16_t* q, const int32_t* qo_indptr, const uint16_t* k_pool,
@@ -318,7 +362,16 @@ int astr_attn_prefill_ragged_masked(const uint16_t* q, const int32_t* qo_indptr,
                                     const int32_t* kv_indptr, const astr_attn_mask* mask, uint16_t* out,
                                     const astr_attn_dims* d, float sm_scale, void* stream) {
   if (mask == nullptr) return ASTR_ERR_INVALID_ARG;
-  return prefill_impl(q, qo_indptr, k_pool, v_pool, req_to_token, seq_lens, kv_indptr, mask, out, d, sm_scale,
+  return prefill_impl(q, qo_indptr, k_pool, v_pool, req_to_token, seq_lens, kv_indptr, mask, nullptr, out, d,
+                      sm_scale, stream);
+}
+
+int astr_attn_prefill_contiguous(const uint16_t* q, const int32_t* qo_indptr, const uint16_t* k_cache,
+                                 const uint16_t* v_cache, const astr_attn_kv_layout* layout, const int32_t* seq_lens,
+                                 const int32_t* kv_indptr, const astr_attn_mask* mask, uint16_t* out,
+                                 const astr_attn_dims* d, float sm_scale, void* stream) {
+  if (layout == nullptr) return ASTR_ERR_INVALID_ARG;
+  return prefill_impl(q, qo_indptr, k_cache, v_cache, nullptr, seq_lens, kv_indptr, mask, layout, out, d, sm_scale,
                       stream);
 }
 

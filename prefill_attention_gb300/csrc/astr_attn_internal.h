@@ -10,6 +10,14 @@ namespace astr {
 // Decode split kernel: a CTA runs this many independent warp pairs, one key chunk each.
 constexpr int kDecodeChunksPerCta = 4;
 
+// Contiguous (stride-addressed) K/V cache instead of pool + slot table: element e of key
+// position j, KV head h, request b sits at b * batch + j * token + h * head + e (elements; all
+// three strides multiples of 8, i.e. 16 bytes).  Positions up to max_len - 1 exist.
+struct KvStrides {
+  int64_t batch, token, head;
+  int max_len;
+};
+
 // Decode: one launch of the split kernel followed by one launch of the combine kernel.
 struct DecodeParams {
   const uint16_t* q;             // [B, Hq, D]
@@ -63,6 +71,8 @@ struct PrefillParams {
                                  // mask + b * mask_req_pitch + i * mask_row_pitch (0 for 2-D masks)
   int64_t mask_req_pitch, mask_row_pitch;
   int mask_kv_pitch;             // bytes in a mask row (a multiple of 16)
+  int contig;                    // 1: K/V rows come from a contiguous cache addressed by kv
+  KvStrides kv;
 };
 
 // KV append: one launch, one warp per new token.
@@ -81,10 +91,13 @@ struct AppendParams {
 };
 
 // Launchers return cudaSuccess or the launch error; they never synchronise.
-cudaError_t launch_decode_split(const DecodeParams& p, const DecodeMask* mask, cudaStream_t stream);  // mask may be null
+// mask / strides may be null (no explicit mask / the paged pool through req_to_token)
+cudaError_t launch_decode_split(const DecodeParams& p, const DecodeMask* mask, const KvStrides* strides,
+                                cudaStream_t stream);
 cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream);         // dispatches on p.mask
 cudaError_t launch_prefill_masked(const PrefillParams& p, cudaStream_t stream);  // the explicit-mask kernels
+cudaError_t launch_prefill_contig(const PrefillParams& p, cudaStream_t stream);  // the contiguous-cache kernels
 cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream);
 
 // Whether the kernels exist for this (head_dim, group size).

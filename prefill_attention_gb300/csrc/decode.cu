@@ -261,8 +261,9 @@ struct TileIter {
 // requests, one coalesced load and one broadcast per round, all rounds issued together (R is
 // picked from the batch size: the unrolled rounds cost latency even when idle); batches of
 // more than 256 requests skip the warm-up.
-template <int D, int G, int BK, int R>
-__device__ __forceinline__ void warm_first_slots(const DecodeParams& p, int vc, int kvh, int n_slots, int lane) {
+template <int D, int G, int BK, int R, bool CONTIG>
+__device__ __forceinline__ void warm_first_slots(const DecodeParams& p, const KvStrides& ks, int vc, int kvh,
+                                                 int n_slots, int lane) {
   const int B = p.batch;
   const int32_t* ind = p.kv_indptr;
   int x[R], y[R];
@@ -316,11 +317,18 @@ __device__ __forceinline__ void warm_first_slots(const DecodeParams& p, int vc, 
   const size_t head_stride = (size_t)p.num_kv_heads * D;
   for (int k = lane; k < n_slots * BK; k += 32) {
     const int key = k0 + k;
-    if (key < 0 || key >= ib1 - ib || (int64_t)key >= p.r2t_stride) continue;
-    const int id = ldcg_i32(p.req_to_token + (int64_t)b * p.r2t_stride + key);
-    if ((uint64_t)(uint32_t)id >= (uint64_t)p.num_slots) continue;  // negative ids wrap past num_slots
-    const uint16_t* kr = p.k_pool + (size_t)id * head_stride + (size_t)kvh * D;
-    const uint16_t* vr = p.v_pool + (size_t)id * head_stride + (size_t)kvh * D;
+    size_t row;
+    if constexpr (CONTIG) {
+      if (key < 0 || key >= ib1 - ib || key >= ks.max_len) continue;
+      row = (size_t)b * ks.batch + (size_t)key * ks.token + (size_t)kvh * ks.head;
+    } else {
+      if (key < 0 || key >= ib1 - ib || (int64_t)key >= p.r2t_stride) continue;
+      const int id = ldcg_i32(p.req_to_token + (int64_t)b * p.r2t_stride + key);
+      if ((uint64_t)(uint32_t)id >= (uint64_t)p.num_slots) continue;  // negative ids wrap past num_slots
+      row = (size_t)id * head_stride + (size_t)kvh * D;
+    }
+    const uint16_t* kr = p.k_pool + row;
+    const uint16_t* vr = p.v_pool + row;
 #pragma unroll
     for (int off = 0; off < D; off += 64) {  // 128-byte lines
       prefetch_l2(kr + off);
@@ -337,22 +345,29 @@ __device__ __forceinline__ bool wait_or_fail(uint32_t bar, uint32_t parity, vola
   return false;
 }
 
-// The split kernel's parameter block: DecodeParams, followed by the mask for the masked kernels.
-struct DecodeParamsMasked {
+// Kernel variants: MODE bit 0 = explicit mask, bit 1 = contiguous (stride-addressed) K/V cache
+// instead of the slot table.  MODE 0 takes DecodeParams alone; the others take the longer block
+// below, so the plain kernel's parameter block (and code) stays as it is.
+constexpr int kModeMask = 1, kModeContig = 2;
+struct DecodeParamsExt {
   DecodeParams p;
   DecodeMask m;
+  KvStrides s;
 };
-template <bool MASK> struct SplitArg { using type = DecodeParams; };
-template <> struct SplitArg<true> { using type = DecodeParamsMasked; };
+template <int MODE> struct SplitArg { using type = DecodeParamsExt; };
+template <> struct SplitArg<0> { using type = DecodeParams; };
 // (host and device: the launcher reads the grid shape through params_of too)
 __host__ __device__ __forceinline__ const DecodeParams& params_of(const DecodeParams& a) { return a; }
-__host__ __device__ __forceinline__ const DecodeParams& params_of(const DecodeParamsMasked& a) { return a.p; }
+__host__ __device__ __forceinline__ const DecodeParams& params_of(const DecodeParamsExt& a) { return a.p; }
 __host__ __device__ __forceinline__ DecodeMask mask_of(const DecodeParams&) { return DecodeMask{nullptr, 0, 0}; }
-__host__ __device__ __forceinline__ DecodeMask mask_of(const DecodeParamsMasked& a) { return a.m; }
+__host__ __device__ __forceinline__ DecodeMask mask_of(const DecodeParamsExt& a) { return a.m; }
+__host__ __device__ __forceinline__ KvStrides strides_of(const DecodeParams&) { return KvStrides{0, 0, 0, 0}; }
+__host__ __device__ __forceinline__ KvStrides strides_of(const DecodeParamsExt& a) { return a.s; }
 
-template <int D, int G, bool MASK>
-__global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(const typename SplitArg<MASK>::type arg) {
+template <int D, int G, int MODE>
+__global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(const typename SplitArg<MODE>::type arg) {
   using C = DecCfg<D, G>;
+  constexpr bool MASK = (MODE & kModeMask) != 0, CONTIG = (MODE & kModeContig) != 0;
   const DecodeParams& p = params_of(arg);
   constexpr int NH = C::NH;
   extern __shared__ __align__(1024) unsigned char smem[];
@@ -385,8 +400,10 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(
   __syncthreads();
   // Before the wait: warm L2 with this pair's first ring slots (prefetch hints only, from
   // tables read through L2 that may still be changing; see warm_first_slots).
-  if (is_producer && B <= 32) warm_first_slots<D, G, C::BK, 1>(p, blockIdx.x * C::NPAIR + pair, kvh, C::STAGES, lane);
-  else if (is_producer && B <= 256) warm_first_slots<D, G, C::BK, 8>(p, blockIdx.x * C::NPAIR + pair, kvh, C::STAGES, lane);
+  if (is_producer && B <= 32)
+    warm_first_slots<D, G, C::BK, 1, CONTIG>(p, strides_of(arg), blockIdx.x * C::NPAIR + pair, kvh, C::STAGES, lane);
+  else if (is_producer && B <= 256)
+    warm_first_slots<D, G, C::BK, 8, CONTIG>(p, strides_of(arg), blockIdx.x * C::NPAIR + pair, kvh, C::STAGES, lane);
   // Launched as a programmatic dependent of the previous kernel in the stream: the set-up
   // above overlapped its tail; from here on its writes are visible and its reads are done,
   // so nothing read before this point is used.  (A no-op for an ordinary launch.)
@@ -411,6 +428,7 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(
     const size_t head_stride = (size_t)p.num_kv_heads * D;
     const unsigned nslots = (unsigned)p.num_slots;
     auto slot_id = [&](const TileIter<C::BK>& t) {  // lane k: slot id of key k of the slot, or -1
+      if constexpr (CONTIG) return 0;  // contiguous cache: rows are addressed by position
       const int flat = t.start + lane;
       return (t.valid(hs) && flat < t.end)
                  ? ldg_nc_i32(p.req_to_token + (int64_t)t.b * p.r2t_stride + (flat - t.ind_b))
@@ -433,9 +451,21 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(
       for (int r = 0; r < C::KV_IT; ++r) {
         const int flat = r * 32 + lane;
         const int key = flat / C::CPR, c = flat % C::CPR;
-        const int id = __shfl_sync(kFullMask, my_id, key);
-        const bool valid = (unsigned)id < nslots;  // padding and out-of-range ids read as zeros
-        const size_t off = valid ? (size_t)id * head_stride + (size_t)kvh * D + c * 8 : 0;
+        bool valid;
+        size_t off;
+        if constexpr (CONTIG) {
+          // key `key` of the slot is position (start - ind_b) + key of request b; keys past the
+          // request's end read as zeros
+          const KvStrides ks = strides_of(arg);
+          valid = key < it.end - it.start && it.start - it.ind_b + key < ks.max_len;
+          off = valid ? (size_t)it.b * ks.batch + (size_t)(it.start - it.ind_b + key) * ks.token +
+                            (size_t)kvh * ks.head + c * 8
+                      : 0;
+        } else {
+          const int id = __shfl_sync(kFullMask, my_id, key);
+          valid = (unsigned)id < nslots;  // padding and out-of-range ids read as zeros
+          off = valid ? (size_t)id * head_stride + (size_t)kvh * D + c * 8 : 0;
+        }
         const uint32_t o = sw128(key, c, C::BK);
         cp_async16(kst + o, p.k_pool + off, valid);
         cp_async16(vst + o, p.v_pool + off, valid);
@@ -813,15 +843,15 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
   }
 }
 
-template <int D, int G, bool MASK>
-cudaError_t launch_split_t(const typename SplitArg<MASK>::type& arg, cudaStream_t stream) {
+template <int D, int G, int MODE>
+cudaError_t launch_split_t(const typename SplitArg<MODE>::type& arg, cudaStream_t stream) {
   const DecodeParams& p = params_of(arg);
   using C = DecCfg<D, G>;
-  constexpr int smem = MASK ? C::SMEM_BYTES_MASKED : C::SMEM_BYTES;
+  constexpr int smem = (MODE & kModeMask) ? C::SMEM_BYTES_MASKED : C::SMEM_BYTES;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e =
-        cudaFuncSetAttribute(decode_split_kernel<D, G, MASK>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaFuncSetAttribute(decode_split_kernel<D, G, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -835,7 +865,7 @@ cudaError_t launch_split_t(const typename SplitArg<MASK>::type& arg, cudaStream_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, decode_split_kernel<D, G, MASK>, arg);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, decode_split_kernel<D, G, MODE>, arg);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -847,13 +877,23 @@ bool decode_supported(int head_dim, int group) {
          (group == 1 || group == 2 || group == 4 || group == 8 || group == 16);
 }
 
-cudaError_t launch_decode_split(const DecodeParams& p, const DecodeMask* mask, cudaStream_t stream) {
+cudaError_t launch_decode_split(const DecodeParams& p, const DecodeMask* mask, const KvStrides* strides,
+                                cudaStream_t stream) {
   const int G = p.num_qo_heads / p.num_kv_heads;
-  // the kernels with an explicit mask are a separate instantiation with a longer parameter block
-  const DecodeParamsMasked pm{p, mask != nullptr ? *mask : DecodeMask{nullptr, 0, 0}};
-#define ASTR_DEC_CASE(DD, GG)                                                                            \
-  if (p.head_dim == DD && G == GG)                                                                       \
-    return mask != nullptr ? launch_split_t<DD, GG, true>(pm, stream) : launch_split_t<DD, GG, false>(p, stream);
+  // the kernels with a mask or a contiguous cache are separate instantiations with a longer
+  // parameter block
+  const DecodeParamsExt pe{p, mask != nullptr ? *mask : DecodeMask{nullptr, 0, 0},
+                           strides != nullptr ? *strides : KvStrides{0, 0, 0, 0}};
+  const int mode = (mask != nullptr ? kModeMask : 0) | (strides != nullptr ? kModeContig : 0);
+#define ASTR_DEC_CASE(DD, GG)                                                     \
+  if (p.head_dim == DD && G == GG) {                                              \
+    switch (mode) {                                                               \
+      case 0: return launch_split_t<DD, GG, 0>(p, stream);                        \
+      case kModeMask: return launch_split_t<DD, GG, kModeMask>(pe, stream);       \
+      case kModeContig: return launch_split_t<DD, GG, kModeContig>(pe, stream);   \
+      default: return launch_split_t<DD, GG, kModeMask | kModeContig>(pe, stream); \
+    }                                                                             \
+  }
   ASTR_DEC_CASE(128, 4) ASTR_DEC_CASE(128, 1) ASTR_DEC_CASE(128, 2) ASTR_DEC_CASE(128, 8) ASTR_DEC_CASE(128, 16)
   ASTR_DEC_CASE(64, 4) ASTR_DEC_CASE(64, 1) ASTR_DEC_CASE(64, 2) ASTR_DEC_CASE(64, 8) ASTR_DEC_CASE(64, 16)
 #undef ASTR_DEC_CASE

@@ -238,7 +238,7 @@ __device__ __forceinline__ int upper_index(const int* pst, int n, int x) {
   return l;
 }
 
-template <int D, int G, bool MASK>
+template <int D, int G, bool MASK, bool CONTIG>
 __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(const PrefillParams p,
                                                                                 const __grid_constant__ CUtensorMap q_map,
                                                                                 const __grid_constant__ CUtensorMap o_map) {
@@ -514,6 +514,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
       const int j_first = (st - g_base % C::STAGES + C::STAGES) % C::STAGES;
       auto ids_of = [&](int j, int half) {  // slot id of key 32 half + lane of item tile j, or -1
         const int key = j * C::BN + half * 32 + lane;
+        if constexpr (CONTIG) return (j < it.n_tiles && key < kv_end) ? key : -1;  // rows addressed by position
         return (j < it.n_tiles && key < kv_end) ? ldg_nc_i32(r2t + key) : -1;
       };
       // one K/V tile: row `key` comes from the slot id held by lane key % 32 of id0 (keys
@@ -526,8 +527,15 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
           const int flat = i * 32 + lane;
           const int key = flat / C::CPR, c = flat % C::CPR;  // key < 32 exactly for the first half of `i`
           const int id = __shfl_sync(kFullMask, (i < C::KV_IT / 2) ? id0 : id1, key & 31);
-          const bool valid = (unsigned)id < nslots;
-          const size_t off = valid ? (size_t)id * head_stride + (size_t)kvh * D + c * 8 : 0;
+          bool valid;
+          size_t off;
+          if constexpr (CONTIG) {  // id = key position in request b's contiguous rows
+            valid = (unsigned)id < (unsigned)p.kv.max_len;
+            off = valid ? (size_t)it.b * p.kv.batch + (size_t)id * p.kv.token + (size_t)kvh * p.kv.head + c * 8 : 0;
+          } else {
+            valid = (unsigned)id < nslots;
+            off = valid ? (size_t)id * head_stride + (size_t)kvh * D + c * 8 : 0;
+          }
           const uint32_t o = sw128(key, c, C::BN);
           cp_async16(kdst + o, p.k_pool + off, valid);
           cp_async16(vdst + o, p.v_pool + off, valid);
@@ -889,13 +897,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
   return fn;
 }
 
-template <int D, int G, bool MASK>
+template <int D, int G, bool MASK, bool CONTIG>
 cudaError_t launch_prefill_t(const PrefillParams& p, cudaStream_t stream) {
   using C = PrefillCfg<D, G>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e =
-        cudaFuncSetAttribute(prefill_kernel<D, G, MASK>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        cudaFuncSetAttribute(prefill_kernel<D, G, MASK, CONTIG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -919,15 +928,15 @@ cudaError_t launch_prefill_t(const PrefillParams& p, cudaStream_t stream) {
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  prefill_kernel<D, G, MASK><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(p, q_map, o_map);
+  prefill_kernel<D, G, MASK, CONTIG><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(p, q_map, o_map);
   return cudaGetLastError();
 }
 
-template <bool MASK>
+template <bool MASK, bool CONTIG>
 cudaError_t dispatch_prefill(const PrefillParams& p, cudaStream_t stream) {
   const int G = p.num_qo_heads / p.num_kv_heads;
 #define ASTR_PF_CASE(DD, GG) \
-  if (p.head_dim == DD && G == GG) return launch_prefill_t<DD, GG, MASK>(p, stream);
+  if (p.head_dim == DD && G == GG) return launch_prefill_t<DD, GG, MASK, CONTIG>(p, stream);
   ASTR_PF_CASE(128, 4) ASTR_PF_CASE(128, 1) ASTR_PF_CASE(128, 2) ASTR_PF_CASE(128, 8) ASTR_PF_CASE(128, 16)
   ASTR_PF_CASE(64, 4) ASTR_PF_CASE(64, 1) ASTR_PF_CASE(64, 2) ASTR_PF_CASE(64, 8) ASTR_PF_CASE(64, 16)
 #undef ASTR_PF_CASE
@@ -936,10 +945,19 @@ cudaError_t dispatch_prefill(const PrefillParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-// The kernels with an explicit mask are a second instantiation of the same template, compiled
-// in their own translation unit (prefill_masked.cu includes this file with
-// ASTR_PREFILL_MASKED_TU defined) so the two sets build in parallel.
-#ifndef ASTR_PREFILL_MASKED_TU
+// The kernels with an explicit mask and those over a contiguous K/V cache are further
+// instantiations of the same template, compiled in translation units of their own
+// (prefill_masked.cu and prefill_contig.cu include this file with ASTR_PREFILL_MASKED_TU or
+// ASTR_PREFILL_CONTIG_TU defined) so the sets build in parallel.
+#if defined(ASTR_PREFILL_MASKED_TU)
+cudaError_t launch_prefill_masked(const PrefillParams& p, cudaStream_t stream) {
+  return dispatch_prefill<true, false>(p, stream);
+}
+#elif defined(ASTR_PREFILL_CONTIG_TU)
+cudaError_t launch_prefill_contig(const PrefillParams& p, cudaStream_t stream) {
+  return p.mask != nullptr ? dispatch_prefill<true, true>(p, stream) : dispatch_prefill<false, true>(p, stream);
+}
+#else
 int prefill_rows_per_cta() { return 256; }
 
 bool prefill_supported(int head_dim, int group) {
@@ -947,11 +965,10 @@ bool prefill_supported(int head_dim, int group) {
 }
 
 cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream) {
+  if (p.contig) return launch_prefill_contig(p, stream);
   if (p.mask != nullptr) return launch_prefill_masked(p, stream);
-  return dispatch_prefill<false>(p, stream);
+  return dispatch_prefill<false, false>(p, stream);
 }
-#else
-cudaError_t launch_prefill_masked(const PrefillParams& p, cudaStream_t stream) { return dispatch_prefill<true>(p, stream); }
 #endif
 
 }  // namespace astr

@@ -251,3 +251,34 @@ def test_decode_masked_bad_mask(lib, kw, status):
 
 def test_decode_masked_null_struct(lib):
     assert _decm(_dims(batch=0), None) == pa.ASTR_ERR_INVALID_ARG
+
+
+def _lay(b=2000 * 8 * 128, t=8 * 128, h=128):
+    return pa.KvLayout(b, t, h)
+
+
+def _pfc(d, layout, **ptr):
+    p = dict(q=A, qo=A, k=A, v=A, seq=A, kvi=A, out=A)
+    p.update(ptr)
+    return pa.astr_attn_prefill_contiguous(p["q"], p["qo"], p["k"], p["v"], layout, p["seq"], p["kvi"], p["out"], d,
+                                           0.1, stream=0, check=False)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(t=-8), pa.ASTR_ERR_INVALID_ARG),
+    (dict(h=100), pa.ASTR_ERR_MISALIGNED),     # not a multiple of 8 elements
+    (dict(b=12), pa.ASTR_ERR_MISALIGNED),
+])
+def test_contiguous_bad_layout(lib, kw, status):
+    assert _pfc(_dims(batch=0), _lay(**kw)) == status
+
+
+def test_contiguous_null_layout_and_table_not_needed(lib):
+    assert lib.astr_attn_prefill_contiguous(A, A, A, A, None, A, A, None, A, ctypes.byref(_dims(batch=0)),
+                                            ctypes.c_float(0.1), None) == pa.ASTR_ERR_INVALID_ARG
+    # no slot table: r2t_stride and num_slots are not read
+    assert _pfc(_dims(batch=0, r2t_stride=0, num_slots=0), _lay()) == pa.ASTR_OK
+    assert _pfc(_dims(batch=0), _lay(), k=A + 2) == pa.ASTR_ERR_MISALIGNED
+    st = lib.astr_attn_decode_contiguous(A, A, A, None, A, A, None, A, A, A, ctypes.byref(_dims(batch=0)),
+                                         ctypes.c_float(0.1), None)
+    assert st == pa.ASTR_ERR_INVALID_ARG
