@@ -41,6 +41,12 @@
 //   * Launched as a programmatic dependent: shared-memory set-up and an L2 warm-up of each
 //     pair's first slots (from tables read through L2 only; prefetch hints, nothing kept)
 //     run before griddepcontrol.wait, so the first misses overlap the previous kernel.
+//   * Variants of the same kernel (template MODE): an explicit mask (page "astrai/extension
+//     @6f67ba8", prefill-mask commit) -- the producer copies each slot's 32 mask bytes next to
+//     its K/V and the consumer gives masked keys exactly zero weight; and a contiguous K/V
+//     cache (stride-addressing and layout commits) -- rows are addressed from the request, the
+//     position and the KV head, with no slot-id load.  The plain kernel keeps its own
+//     parameter block and code.
 //   * Measured alternatives: a CUDA-core version was issue bound (~550 instructions per
 //     4 KB of K/V); a tcgen05 version with S^T / O^T accumulators in tensor memory spent
 //     ~150 cycles per M=128 x N=16 x K=16 MMA on the critical path; TMA tile::gather4 for

@@ -31,6 +31,13 @@
 //   * P stays in tensor memory as two bf16 planes, hi (p truncated to bf16) and lo =
 //     bf16(p - hi); O accumulates P_hi V + P_lo V, which carries p to ~2^-17 relative
 //     instead of bf16's 2^-9, so the only bf16 rounding left is the output's.
+//   * Variants of the same template: the causal rule can be switched off (unified-causal-
+//     offset commit, offset -1) -- each row's key window then ends at seq_len; MASK adds an
+//     explicit 2-D / 3-D mask (prefill-mask commit: causal and mask coexist), read by each
+//     softmax thread as 64 bytes per key tile while the tile's scores are computed; CONTIG
+//     reads K/V from a contiguous cache by strides (stride-addressing and layout commits)
+//     instead of through req_to_token.  The masked and contiguous sets are compiled in
+//     prefill_masked.cu and prefill_contig.cu.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
