@@ -160,6 +160,10 @@ class ClockSampler:
 
     def stop(self):
         if self.proc is None:
+            try:
+                os.remove(self.path)
+            except OSError:
+                pass
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
         self.proc.terminate()
         try:
