@@ -160,6 +160,8 @@ class ClockSampler:
 
     def stop(self):
         if self.proc is None:
+            if getattr(self, "fh", None) is not None:
+                self.fh.close()
             try:
                 os.remove(self.path)
             except OSError:
