@@ -282,3 +282,19 @@ def test_contiguous_null_layout_and_table_not_needed(lib):
     st = lib.astr_attn_decode_contiguous(A, A, A, None, A, A, None, A, A, A, ctypes.byref(_dims(batch=0)),
                                          ctypes.c_float(0.1), None)
     assert st == pa.ASTR_ERR_INVALID_ARG
+
+
+def test_header_is_plain_c(tmp_path):
+    """The ABI header compiles as C99 with warnings as errors (no C++ in the interface)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "astr_attn.h"\n'
+                   "int main(void) { astr_attn_dims d = {0}; astr_attn_mask m = {0}; astr_attn_kv_layout l = {0};\n"
+                   "  int (*v)(void) = astr_attn_version; (void)d; (void)m; (void)l; (void)v; return 0; }\n")
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.dirname(HEADER),
+                        "-c", str(src), "-o", str(tmp_path / "use_header.o")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
