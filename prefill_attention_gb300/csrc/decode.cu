@@ -434,11 +434,14 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(
     const size_t head_stride = (size_t)p.num_kv_heads * D;
     const unsigned nslots = (unsigned)p.num_slots;
     auto slot_id = [&](const TileIter<C::BK>& t) {  // lane k: slot id of key k of the slot, or -1
-      if constexpr (CONTIG) return 0;  // contiguous cache: rows are addressed by position
-      const int flat = t.start + lane;
-      return (t.valid(hs) && flat < t.end)
-                 ? ldg_nc_i32(p.req_to_token + (int64_t)t.b * p.r2t_stride + (flat - t.ind_b))
-                 : -1;
+      if constexpr (CONTIG) {
+        return 0;  // contiguous cache: rows are addressed by position, no ids
+      } else {
+        const int flat = t.start + lane;
+        return (t.valid(hs) && flat < t.end)
+                   ? ldg_nc_i32(p.req_to_token + (int64_t)t.b * p.r2t_stride + (flat - t.ind_b))
+                   : -1;
+      }
     };
     int my_id = slot_id(it);
     for (int i = 0; it.valid(hs); ++i) {

@@ -521,8 +521,11 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
       const int j_first = (st - g_base % C::STAGES + C::STAGES) % C::STAGES;
       auto ids_of = [&](int j, int half) {  // slot id of key 32 half + lane of item tile j, or -1
         const int key = j * C::BN + half * 32 + lane;
-        if constexpr (CONTIG) return (j < it.n_tiles && key < kv_end) ? key : -1;  // rows addressed by position
-        return (j < it.n_tiles && key < kv_end) ? ldg_nc_i32(r2t + key) : -1;
+        if constexpr (CONTIG) {
+          return (j < it.n_tiles && key < kv_end) ? key : -1;  // contiguous cache: the position itself
+        } else {
+          return (j < it.n_tiles && key < kv_end) ? ldg_nc_i32(r2t + key) : -1;
+        }
       };
       // one K/V tile: row `key` comes from the slot id held by lane key % 32 of id0 (keys
       // 0-31) or id1 (keys 32-63); padding and out-of-range ids read as zeros.  K and V share
