@@ -476,11 +476,18 @@ def pin_decode_mask_is_shorter_table(lib):
     assert np.array_equal(oracle.masked(w, m, lib=lib), oracle.decode(short, lib=lib))
 
 
+def pin_sdpa_head_dim_32(lib):
+    """Head dim 32 (the size the pages' dispatch-switch commit adds) against fp64 SDPA, decode
+    and prefill."""
+    pin_sdpa_decode(lib, w=_small_decode(seed=141, Hq=8, Hkv=2, d=32))
+    pin_sdpa_prefill(lib, w=_small_prefill(seed=143, Hq=8, Hkv=4, d=32))
+
+
 ALL_PINS = [
     pin_sdpa_decode, pin_sdpa_prefill, pin_prefix0_is_textbook_causal, pin_golden,
     pin_q_zero_is_mean_of_visible_v, pin_single_key_returns_v, pin_per_request_marker, pin_dominant_key,
     pin_slot_permutation, pin_key_shift, pin_unreferenced_slots_unread, pin_split_combine, pin_chunk_partials_combine,
     pin_partial_is_softmax_piece, pin_prefill_row_is_decode,
     pin_append_then_attend_is_sdpa_over_concatenation, pin_append_touches_only_new_slots,
-    pin_masked_matches_sdpa, pin_mask_identities, pin_decode_mask_is_shorter_table,
+    pin_masked_matches_sdpa, pin_mask_identities, pin_decode_mask_is_shorter_table, pin_sdpa_head_dim_32,
 ]
