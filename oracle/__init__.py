@@ -21,8 +21,8 @@ _SRC = os.path.join(_HERE, "attn_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lib = None
 
-__all__ = ["build", "lib_path", "decode", "prefill", "decode_split_partials", "decode_chunk_partials",
-           "chunk_split_counts", "combine", "kv_append", "masked", "load_variant"]
+__all__ = ["build", "lib_path", "decode", "prefill", "decode_split_partials", "partial_ranges", "combine",
+           "kv_append", "masked", "load_variant"]
 
 
 def _compile(src: str, out: str, extra: Sequence[str] = ()) -> None:
@@ -57,9 +57,9 @@ def _declare(lib):
     lib.oracle_kv_append.argtypes = [_I, _I, _I, _P, _P, _P, _L, _P, _P, _P, _P]
     lib.oracle_masked_rows.argtypes = [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _L, _P, _D, _P, _I, _L, _L, _I, _L,
                                        _P, _P, _P, _I]
-    lib.oracle_decode_chunk_partials.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _L, _P, _P, _D, _L, _L, _I, _P, _P]
+    lib.oracle_partial_ranges.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _L, _D, _L, _P, _P, _P, _P, _P, _P, _I]
     for f in ("oracle_decode_rows", "oracle_prefill_rows", "oracle_decode_split_partials", "oracle_combine",
-              "oracle_decode_chunk_partials", "oracle_kv_append", "oracle_masked_rows"):
+              "oracle_partial_ranges", "oracle_kv_append", "oracle_masked_rows"):
         getattr(lib, f).restype = None
     return lib
 
@@ -147,31 +147,27 @@ def decode_split_partials(w, S: int, nthreads: Optional[int] = None, lib=None):
     return o, ml
 
 
-def decode_chunk_partials(w, C: int, pitch: int, W: int = 1, lib=None):
-    """Chunk partials: each request's keys in slots of W keys from its first key, the
-    batch's slots end to end in request order, chunks of C slots (W = 1: chunks of C keys
-    of the flat key space).
+def partial_ranges(w, items, nthreads: Optional[int] = None, lib=None):
+    """Split partials over explicit key ranges: ``items`` is an int array [n, 4] of
+    (b, h, lo, hi) -- query head h of request b over its keys lo .. hi-1.
 
-    Returns (o_part [B,Hq,pitch,d], ml_part [B,Hq,pitch,2], nsplit [B]); unused slots hold NaN.
+    Returns (o [n, d], ml [n, 2]) in fp64: o unnormalised, ml = (max logit, sum of exp);
+    an empty range gives (0, -inf, 0).
     """
     lib = lib or _get()
     B, Hq, Hkv, D = w.batch, w.num_qo_heads, w.num_kv_heads, w.head_dim
-    o = np.full((B, Hq, pitch, D), np.nan, dtype=np.float64)
-    ml = np.full((B, Hq, pitch, 2), np.nan, dtype=np.float64)
+    items = np.asarray(items, dtype=np.int64).reshape(-1, 4)
+    ib, ih = _c(items[:, 0], np.int32), _c(items[:, 1], np.int32)
+    lo, hi = _c(items[:, 2], np.int64), _c(items[:, 3], np.int64)
+    n = items.shape[0]
+    o = np.zeros((n, D), dtype=np.float64)
+    ml = np.zeros((n, 2), dtype=np.float64)
     q, kp, vp = _c(w.q, np.uint16), _c(w.k_pool, np.uint16), _c(w.v_pool, np.uint16)
-    r2t, sl, ki = _c(w.req_to_token, np.int32), _c(w.seq_lens, np.int32), _c(w.kv_indptr, np.int32)
-    lib.oracle_decode_chunk_partials(B, Hq, Hkv, D, _ptr(q), _ptr(kp), _ptr(vp), _ptr(r2t), r2t.shape[1], _ptr(sl),
-                                     _ptr(ki), float(w.sm_scale), int(C), int(W), int(pitch), _ptr(o), _ptr(ml))
-    return o, ml, chunk_split_counts(w.seq_lens, C, W)
-
-
-def chunk_split_counts(seq_lens, C: int, W: int = 1) -> np.ndarray:
-    """Number of C-slot chunks that overlap each request (slots of W keys from its first key)."""
-    n = np.maximum(np.asarray(seq_lens, dtype=np.int64), 0)
-    ns = (n + W - 1) // W
-    a = np.concatenate([[0], np.cumsum(ns)[:-1]])
-    e = a + ns
-    return np.where(e > a, (e - 1) // C - a // C + 1, 0).astype(np.int32)
+    r2t = _c(w.req_to_token, np.int32)
+    lib.oracle_partial_ranges(B, Hq, Hkv, D, _ptr(q), _ptr(kp), _ptr(vp), _ptr(r2t), r2t.shape[1],
+                              float(w.sm_scale), n, _ptr(ib), _ptr(ih), _ptr(lo), _ptr(hi), _ptr(o), _ptr(ml),
+                              _threads(nthreads))
+    return o, ml
 
 
 def combine(o_part: np.ndarray, ml_part: np.ndarray, nsplit: Optional[np.ndarray] = None, lib=None) -> np.ndarray:

@@ -131,7 +131,7 @@ static void widen_row(const uint16_t *src, int D, double *dst) {
 
 /* ---------------------------------------------------------------- work items */
 
-enum { JOB_DECODE = 0, JOB_PREFILL = 1, JOB_PARTIALS = 2, JOB_MASKED = 3 };
+enum { JOB_DECODE = 0, JOB_PREFILL = 1, JOB_PARTIALS = 2, JOB_MASKED = 3, JOB_RANGES = 4 };
 
 typedef struct {
   int kind;
@@ -149,6 +149,8 @@ typedef struct {
   /* partials */
   int S;
   double *o_part, *ml_part;
+  /* key ranges (JOB_RANGES): item n covers keys [item_lo[n], item_hi[n]) of its request */
+  const int64_t *item_lo, *item_hi;
   /* explicit mask (JOB_MASKED): kind 2 = [B, kv_pitch], 3 = [B, q_pitch, kv_pitch]; rows are
    * decode (b, h) pairs when is_decode, else (flat row, h) */
   const uint8_t *mask;
@@ -219,6 +221,11 @@ static void run_item(job_t *J, int64_t it, double *qbuf) {
     }
     attend(P, qbuf, kvh, vis, nv, J->out + it * D);
     free(vis);
+  } else if (J->kind == JOB_RANGES) {
+    int b = J->item_row[it];
+    widen_row(J->q + ((int64_t)b * P->Hq + h) * D, D, qbuf);
+    partial(P, qbuf, kvh, J->req_to_token + (int64_t)b * J->r2t_stride, J->item_lo[it], J->item_hi[it],
+            J->o_part + it * D, &J->ml_part[2 * it], &J->ml_part[2 * it + 1]);
   } else { /* JOB_PARTIALS: even split of request b's keys into S pieces */
     int b = J->item_row[it];
     widen_row(J->q + ((int64_t)b * P->Hq + h) * D, D, qbuf);
@@ -311,43 +318,24 @@ void oracle_decode_split_partials(int B, int Hq, int Hkv, int D, const uint16_t 
   free(ih);
 }
 
-/* Chunk partials over the batch's slots.  Request b's keys are cut into slots of W keys
- * starting at its first key (ceil(seq_len_b / W) slots, the last one possibly short); the
- * slots of all requests are laid end to end in request order (request b's first slot is
- * SP_b = sum over b' < b of ceil(seq_len_b' / W)) and cut into chunks of C slots.  For every
- * request b and every chunk c that overlaps it, the partial over the keys of the overlapping
- * slots is stored in slot c - SP_b / C of o_part [B,Hq,pitch,D] / ml_part [B,Hq,pitch,2].
- * Slots no chunk maps to are not written.  With W = 1 a slot is a key, so chunks are C
- * consecutive keys of the flat key space (kv_indptr order).  This is the split-KV
- * decomposition of the kernel-rename commit with the split boundaries placed over the whole
- * batch (kv_indptr commit) instead of per request. */
-void oracle_decode_chunk_partials(int B, int Hq, int Hkv, int D, const uint16_t *q, const uint16_t *k_pool,
-                                  const uint16_t *v_pool, const int32_t *req_to_token, int64_t r2t_stride,
-                                  const int32_t *seq_lens, const int32_t *kv_indptr, double sm_scale, int64_t C,
-                                  int64_t W, int pitch, double *o_part, double *ml_part) {
-  (void)kv_indptr;
-  pool_t P;
-  P.Hq = Hq; P.Hkv = Hkv; P.D = D; P.k_pool = k_pool; P.v_pool = v_pool; P.sm_scale = sm_scale;
-  const int G = Hq / Hkv;
-  double *qbuf = (double *)malloc(sizeof(double) * (size_t)D);
-  int64_t sp = 0;  /* first slot of request b */
-  for (int b = 0; b < B; ++b) {
-    const int64_t n = seq_lens[b] > 0 ? seq_lens[b] : 0;
-    const int64_t ns = (n + W - 1) / W;  /* slots of request b */
-    const int32_t *slots = req_to_token + (int64_t)b * r2t_stride;
-    for (int64_t c = sp / C; ns > 0 && c * C < sp + ns; ++c) {
-      const int64_t g0 = c * C > sp ? c * C : sp, g1 = (c + 1) * C < sp + ns ? (c + 1) * C : sp + ns;
-      const int64_t lo = (g0 - sp) * W, hi = (g1 - sp) * W < n ? (g1 - sp) * W : n;  /* keys of the overlap */
-      const int64_t s = c - sp / C;
-      for (int h = 0; h < Hq; ++h) {
-        widen_row(q + ((int64_t)b * Hq + h) * D, D, qbuf);
-        const int64_t base = ((int64_t)b * Hq + h) * pitch + s;
-        partial(&P, qbuf, h / G, slots, lo, hi, o_part + base * D, &ml_part[2 * base], &ml_part[2 * base + 1]);
-      }
-    }
-    sp += ns;
-  }
-  free(qbuf);
+/* Partials over explicit key ranges: item n is (request b, query head h, keys [lo, hi) of
+ * request b, i.e. positions lo .. hi-1 of its req_to_token row); it stores the split's
+ * (o, m, l) as described in the header into o_out [n_items, D] and ml_out [n_items, 2].
+ * Where the split boundaries lie is the caller's choice: this is the per-split piece of the
+ * kernel-rename commit for any one split. */
+void oracle_partial_ranges(int B, int Hq, int Hkv, int D, const uint16_t *q, const uint16_t *k_pool,
+                           const uint16_t *v_pool, const int32_t *req_to_token, int64_t r2t_stride,
+                           double sm_scale, int64_t n_items, const int32_t *item_b, const int32_t *item_h,
+                           const int64_t *item_lo, const int64_t *item_hi, double *o_out, double *ml_out,
+                           int nthreads) {
+  job_t J;
+  memset(&J, 0, sizeof J);
+  J.kind = JOB_RANGES;
+  J.P.Hq = Hq; J.P.Hkv = Hkv; J.P.D = D; J.P.k_pool = k_pool; J.P.v_pool = v_pool; J.P.sm_scale = sm_scale;
+  J.B = B; J.q = q; J.req_to_token = req_to_token; J.r2t_stride = r2t_stride;
+  J.n_items = n_items; J.item_row = item_b; J.item_head = item_h; J.item_lo = item_lo; J.item_hi = item_hi;
+  J.o_part = o_out; J.ml_part = ml_out;
+  run_job(&J, nthreads);
 }
 
 /* Log-sum-exp combine of the first nsplit[b] partials of each (b, h); out [B,Hq,D]. */

@@ -2,6 +2,8 @@
 import numpy as np
 
 import prefill_attention_gb300 as pa
+import split_schedule
+from split_schedule import SLOT_KEYS  # noqa: F401
 
 TOL = 1e-2  # max abs error of bf16 outputs against the fp64 oracle
 
@@ -43,19 +45,10 @@ def prefill_dims(w):
                         w.max_seq_len, total_q=w.total_q, max_q_len=w.max_q_len)
 
 
-SLOT_KEYS = 32  # keys per slot of the decode split schedule
-
-
 def decode_chunk_slots(w, n_chunks, max_splits):
     """Chunk length in 32-key slots of the decode split schedule, as documented for
     astr_attn_paged_decode."""
-    n_slots = int(sum(-(-int(n) // SLOT_KEYS) for n in w.seq_lens if n > 0))
-    if max_splits <= 1:
-        return max(n_slots, 1)
-    c = -(-n_slots // n_chunks)
-    m = -(-w.max_seq_len // SLOT_KEYS)
-    floor = max(1, -(-m // (max_splits - 1)))
-    return max(c, floor)
+    return split_schedule.chunk_slots(w.seq_lens, w.max_seq_len, n_chunks, max_splits)
 
 
 def run_decode(w, t=None, max_splits=32, num_splits=0, stream=None, return_parts=False):

@@ -26,6 +26,7 @@ import oracle
 import workload
 from workload import bf16_bits_to_fp32, fp32_to_bf16_bits, make_from_lengths
 
+import split_schedule
 from sdpa_fp64 import sdpa_paged
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "worked_examples.json")
@@ -273,9 +274,9 @@ def pin_split_combine(lib):
 
 
 def pin_chunk_partials_combine(lib):
-    """Chunks over the batch's slots (boundaries anywhere in the end-to-end slot sequence, so
-    chunks straddle requests): chunk partials + combine == unsplit attention, for several
-    chunk lengths and slot widths (W = 1: chunks of the flat key space)."""
+    """Partials over key ranges that straddle the batch's request boundaries anywhere (the
+    library's slot/chunk schedule, with several chunk lengths and slot widths; W = 1: chunks
+    of the flat key space) + combine == unsplit attention."""
     w = _small_decode(seed=73, B=6, lo=0, hi=45)
     w.seq_lens[2] = 0   # an empty request owns no chunk
     w.kv_indptr[1:] = np.cumsum(w.seq_lens)
@@ -284,23 +285,36 @@ def pin_chunk_partials_combine(lib):
     for W in (1, 5, 32):
         n_slots = int(sum(-(-int(n) // W) for n in w.seq_lens))
         for C in (1, 2, 7, 16, 33, n_slots, n_slots + 5, T):
-            ns = oracle.chunk_split_counts(w.seq_lens, C, W)
+            ns = split_schedule.split_counts(w.seq_lens, C, W)
             pitch = max(1, int(ns.max()))
-            o, ml, ns2 = oracle.decode_chunk_partials(w, C, pitch, W, lib=lib)
-            assert np.array_equal(ns, ns2)
-            # brute force: count (request, chunk) overlaps key by key, through each key's slot
-            overlaps, sp = set(), 0
-            for b in range(w.batch):
-                n = int(w.seq_lens[b])
-                overlaps |= {(b, (sp + j // W) // C) for j in range(n)}
-                sp += -(-n // W)
-            assert int(ns.sum()) == len(overlaps)
+            o, ml, _ = split_schedule.chunk_partials(w, C, pitch, W, lib=lib)
             got = oracle.combine(np.nan_to_num(o), np.where(np.isnan(ml), -np.inf, ml), nsplit=ns, lib=lib)
             err = np.abs(got - ref).max()
             assert err <= 1e-12, f"chunk combine W={W} C={C}: {err}"
             # every written slot is a proper partial: finite m, positive l
             for b in range(w.batch):
                 assert np.all(np.isfinite(ml[b, :, :ns[b], 0])) and np.all(ml[b, :, :ns[b], 1] > 0)
+
+
+def pin_partial_ranges_match_even_split(lib):
+    """A partial over an explicit key range equals the even-split partial over the same keys
+    (two entry points of the oracle, the same definition)."""
+    w = _small_decode(seed=75, B=3, lo=5, hi=30)
+    S = 3
+    o, ml = oracle.decode_split_partials(w, S, lib=lib)
+    items = []
+    for b in range(w.batch):
+        n = int(w.seq_lens[b]); c = -(-n // S)
+        for s in range(S):
+            for h in range(w.num_qo_heads):
+                items.append((b, h, min(s * c, n), min((s + 1) * c, n)))
+    po, pml = oracle.partial_ranges(w, np.array(items), lib=lib)
+    k = 0
+    for b in range(w.batch):
+        for s in range(S):
+            for h in range(w.num_qo_heads):
+                assert np.array_equal(po[k], o[b, h, s]) and np.array_equal(pml[k], ml[b, h, s])
+                k += 1
 
 
 def pin_partial_is_softmax_piece(lib):
@@ -487,6 +501,7 @@ ALL_PINS = [
     pin_sdpa_decode, pin_sdpa_prefill, pin_prefix0_is_textbook_causal, pin_golden,
     pin_q_zero_is_mean_of_visible_v, pin_single_key_returns_v, pin_per_request_marker, pin_dominant_key,
     pin_slot_permutation, pin_key_shift, pin_unreferenced_slots_unread, pin_split_combine, pin_chunk_partials_combine,
+    pin_partial_ranges_match_even_split,
     pin_partial_is_softmax_piece, pin_prefill_row_is_decode,
     pin_append_then_attend_is_sdpa_over_concatenation, pin_append_touches_only_new_slots,
     pin_masked_matches_sdpa, pin_mask_identities, pin_decode_mask_is_shorter_table, pin_sdpa_head_dim_32,

@@ -16,6 +16,7 @@ if not torch.cuda.is_available():
     pytest.skip("no CUDA device", allow_module_level=True)
 
 import prefill_attention_gb300 as pa  # noqa: E402
+import split_schedule  # noqa: E402
 from gpu_util import SLOT_KEYS, TOL, decode_chunk_slots, decode_dims, run_decode, sample_rows, to_f64, upload  # noqa: E402
 
 
@@ -73,7 +74,7 @@ def test_partials_match_oracle_chunks():
     out, o, ml, n_used = run_decode(w, max_splits=max_splits, num_splits=n, return_parts=True)
     assert n_used == n
     C = decode_chunk_slots(w, n, max_splits)
-    o_ref, ml_ref, ns = oracle.decode_chunk_partials(w, C, max_splits, SLOT_KEYS)
+    o_ref, ml_ref, ns = split_schedule.chunk_partials(w, C, max_splits, SLOT_KEYS)
     assert ns.max() <= max_splits
     assert (ns >= 2).any()
     for b in range(w.batch):
@@ -94,7 +95,7 @@ def test_combine_alone_on_oracle_chunk_partials():
     max_splits, n = 8, 7
     dims = decode_dims(w, max_splits=max_splits, num_splits=n)
     C = decode_chunk_slots(w, n, max_splits)
-    o_ref, ml_ref, ns = oracle.decode_chunk_partials(w, C, max_splits, SLOT_KEYS)
+    o_ref, ml_ref, ns = split_schedule.chunk_partials(w, C, max_splits, SLOT_KEYS)
     o_part = torch.from_numpy(np.nan_to_num(o_ref).astype(np.float32)).cuda().contiguous()
     ml_part = torch.from_numpy(np.nan_to_num(ml_ref).astype(np.float32)).cuda().contiguous()
     out = torch.empty((w.batch, w.num_qo_heads, w.head_dim), dtype=torch.bfloat16, device="cuda")

@@ -35,6 +35,7 @@ MUTANTS = {
     "combine_sign": ("exp(m - M);", "exp(M - m);"),
     "q_head_major": ("widen_row(J->q + ((int64_t)b * P->Hq + h) * D, D, qbuf);\n    attend",
                      "widen_row(J->q + ((int64_t)h * J->B + b) * D, D, qbuf);\n    attend"),
+    "range_start_shifted": ("J->item_lo[it], J->item_hi[it],", "J->item_lo[it] + 1, J->item_hi[it],"),
     "split_floor_chunk": ("int64_t chunk = (n + J->S - 1) / J->S;", "int64_t chunk = n / J->S > 0 ? n / J->S : 1;"),
     "append_position_shift": ("r2t_stride + c + i];", "r2t_stride + c + i + 1];"),
     "append_k_into_v": ("memcpy(v_pool + (int64_t)slot * row, v_new", "memcpy(v_pool + (int64_t)slot * row, k_new"),
