@@ -6,13 +6,18 @@ page_size=1 random slot table, bf16 -- reported as K+V bytes read per second (GB
 microseconds per call and the fraction of the measured HBM copy bandwidth.  A step is
 one decode call (split kernel + combine kernel) through the C ABI on inputs already in
 HBM.  L2 is defeated by rotating through several copies of the KV pools (working set
-well above the 126 MB L2), so every call reads its keys from DRAM.
+well above the 126 MB L2), so every call reads its keys from DRAM.  The timed region of
+`--steps` calls runs `--repeats` times (each between a barrier and a synchronize); the
+line reports the median region and the spread of all of them.
 
 Also reported in the same line:
   * roofline     -- the split kernel alone (the dominant kernel), timed with CUDA events
                     on its stream: algorithmic K+V bytes per launch / mean duration.
   * prefill      -- the ragged prefill entry point on the 16-request extend workload,
-                    FLOP/s against the measured dense bf16 tensor-core peak.
+                    FLOP/s against the measured dense bf16 tensor-core peak (rotating
+                    query / pool / output copies, so each call is cold in L2).
+  * decode_workloads -- the other decode workloads (B=4 d=64 tiny, B=8 long context, B=256
+                    large batch): us per call, K+V GB/s and the fraction of the copy peak.
   * masked       -- the explicit-mask entry points on the same workloads: prefill with a 3-D
                     mask (causal on) and decode with a 2-D mask, each byte kept with
                     probability 0.75; FLOP/s and GB/s count the same work as the unmasked calls
@@ -24,7 +29,8 @@ Also reported in the same line:
   * e2e          -- the same decode metric with every input in pinned host memory, the
                     host->device copies and the device->host read of `out` inside the
                     timed region (and a variant where only q and the index arrays move).
-  * cpu_baseline -- the fp64 CPU oracle timed on this host on a bounded sample.
+  * cpu_baseline -- the fp64 CPU oracle timed on this host on a bounded sample (decode: whole
+                    batches; prefill_cpu_baseline: a sample of (query row, head) rows).
 
 --impl reference times the fp64 oracle (the only reference implementation this build
 has) on the same workload and prints the same line with "impl": "reference".
@@ -214,6 +220,31 @@ def oracle_gbs(w, seconds: float, nthreads: int):
     return w.kv_bytes() / dt / 1e9, dt, reps
 
 
+def oracle_prefill_tflops(wp, seconds: float, nthreads: int, seed: int = 1):
+    """Time the fp64 oracle on a random sample of (flat query row, head) rows of prefill workload
+    ``wp`` for ~`seconds`; TFLOP/s counted as for the GPU (4 d per attended (query, key) pair)."""
+    import oracle
+    oracle.build()
+    rng = np.random.default_rng(seed)
+    qo = np.asarray(wp.qo_indptr, dtype=np.int64)
+    req = np.searchsorted(qo, np.arange(wp.total_q), side="right") - 1
+    vis = (wp.seq_lens[req].astype(np.int64) - (qo[req + 1] - qo[req])) + (np.arange(wp.total_q) - qo[req]) + 1
+
+    def sample(n):
+        rows = np.stack([rng.integers(0, wp.total_q, n), rng.integers(0, wp.num_qo_heads, n)], 1).astype(np.int32)
+        return rows, 4.0 * wp.head_dim * float(vis[rows[:, 0]].sum())
+
+    rows, fl = sample(256)
+    t0 = time.perf_counter()
+    oracle.prefill(wp, rows=rows, nthreads=nthreads)
+    one = max(time.perf_counter() - t0, 1e-4)
+    rows, fl = sample(max(256, min(int(256 * seconds / one), 4_000_000)))
+    t0 = time.perf_counter()
+    oracle.prefill(wp, rows=rows, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return fl / dt / 1e12, rows.shape[0], dt
+
+
 def run_reference(args, rank: int, world: int):
     if rank != 0:
         return
@@ -251,6 +282,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=4000)
     ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--repeats", type=int, default=7, help="timed regions of --steps calls (median reported)")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -346,12 +378,16 @@ def main():
     while time.perf_counter() < t_end:
         timed(decode, 200)
 
-    # ---------------- timed region: K decode steps
-    barrier()
-    elapsed = timed(decode, args.steps)
-    barrier()
+    # ---------------- timed regions: K decode steps each, repeated; the median region counts
+    regions = []
+    for _ in range(max(1, args.repeats)):
+        barrier()
+        elapsed = timed(decode, args.steps)
+        barrier()
+        regions.append(aggregate_weak(dist, elapsed, float(nbytes["kv"]) * args.steps, dev))
     clk = clocks.stop()
-    elapsed_max, total_kv, bytes_per_s = aggregate_weak(dist, elapsed, float(nbytes["kv"]) * args.steps, dev)
+    region_us = sorted(r[0] / args.steps * 1e6 for r in regions)
+    elapsed_max, total_kv, bytes_per_s = sorted(regions)[len(regions) // 2]
     value = bytes_per_s / 1e9
     us_per_call = elapsed_max / args.steps * 1e6
 
@@ -426,29 +462,88 @@ def main():
     h2d_res = sum(t.numel() * t.element_size() for t in (hq, hr, hs, hi))
     d2h = hout.numel() * hout.element_size()
 
-    # ---------------- prefill entry point on the extend workload
+    # ---------------- the other decode workloads, each timed on its own (one pool copy when it
+    # is several times the L2 already)
+    decode_workloads = {}
+    for cfg in (1, 3, 4):
+        if cfg == args.decode_workload:
+            continue
+        wx = workload.config(cfg)
+        bx = decode_bytes(wx)
+        nx = max(1, min(POOL_COPIES, -(-int(6e8) // max(int(bx["kv"]), 1))))
+        xpools = [(bf(wx.k_pool), bf(wx.v_pool)) for _ in range(nx)]
+        xq, xr, xs, xi = bf(wx.q), i32(wx.req_to_token), i32(wx.seq_lens), i32(wx.kv_indptr)
+        xdims = pa.make_dims(wx.batch, wx.num_qo_heads, wx.num_kv_heads, wx.head_dim, wx.num_slots, wx.r2t_stride,
+                             wx.max_seq_len, max_splits=MAX_SPLITS)
+        xo, xm = pa.alloc_decode_workspace(xdims, device=dev)
+        xout = torch.empty_like(xq)
+
+        def decode_x(i, xpools=xpools, xq=xq, xr=xr, xs=xs, xi=xi, xdims=xdims, xo=xo, xm=xm, xout=xout, wx=wx,
+                     nx=nx):
+            k, v = xpools[i % nx]
+            pa.astr_attn_paged_decode(xq, k, v, xr, xs, xi, xo, xm, xout, xdims, wx.sm_scale, stream=sh)
+
+        n_x = max(20, min(args.steps, int(0.3 / max(bx["kv"] / 5e12, 2e-6))))
+        timed(decode_x, 10)
+        t_x = statistics.median(timed(decode_x, n_x) / n_x for _ in range(3))
+        rec = {"workload": wx.name, "seed": wx.seed, "us_per_call": round(t_x * 1e6, 3),
+               "kv_bytes_per_call": bx["kv"], "gbs": round(bx["kv"] / t_x / 1e9, 2),
+               "frac_of_hbm": round(bx["kv"] / t_x / 1e9 / peaks["hbm_gbs"], 4),
+               "l2": f"{nx} KV-pool copies ({nx * bx['kv'] / 1e6:.0f} MB)"}
+        if cfg == 1:  # launch-bound: the CUDA-graph replay time is the meaningful one
+            try:
+                gx = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gx, stream=stream):
+                    for i in range(64):
+                        decode_x(i)
+                gx.replay()
+                torch.cuda.synchronize()
+                ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(stream):
+                    ev0.record(stream)
+                    for _ in range(10):
+                        gx.replay()
+                    ev1.record(stream)
+                ev1.synchronize()
+                rec["us_per_call_graph"] = round(ev0.elapsed_time(ev1) * 1e3 / 640, 3)
+                del gx
+            except Exception as e:
+                rec["us_per_call_graph"] = f"capture failed: {e}"
+        decode_workloads[f"workload_{cfg}"] = rec
+        del xpools, xo, xm
+    torch.cuda.empty_cache()
+
+    # ---------------- prefill entry point on the extend workload (rotating query / pool /
+    # output copies: one copy, ~135 MB, is about the L2's size)
     wp = workload.config(PREFILL_CFG)
-    pq, pk, pv = bf(wp.q), bf(wp.k_pool), bf(wp.v_pool)
+    n_pcp = 3
+    pcopies = [(bf(wp.q), bf(wp.k_pool), bf(wp.v_pool)) for _ in range(n_pcp)]
+    pq, pk, pv = pcopies[0]
     pqo, pr, ps_, pki = i32(wp.qo_indptr), i32(wp.req_to_token), i32(wp.seq_lens), i32(wp.kv_indptr)
     pdims = pa.make_dims(wp.batch, wp.num_qo_heads, wp.num_kv_heads, wp.head_dim, wp.num_slots, wp.r2t_stride,
                          wp.max_seq_len, total_q=wp.total_q, max_q_len=wp.max_q_len)
-    pout = torch.empty_like(pq)
+    pouts = [torch.empty_like(pq) for _ in range(n_pcp)]
+    pout = pouts[0]
 
     def prefill(i):
-        pa.astr_attn_prefill_ragged(pq, pqo, pk, pv, pr, ps_, pki, pout, pdims, wp.sm_scale, stream=sh)
+        q_, k_, v_ = pcopies[i % n_pcp]
+        pa.astr_attn_prefill_ragged(q_, pqo, k_, v_, pr, ps_, pki, pouts[i % n_pcp], pdims, wp.sm_scale, stream=sh)
 
-    timed(prefill, 5)
-    n_pf = max(20, min(args.steps // 10, 400))
-    t_pf = timed(prefill, n_pf) / n_pf
+    timed(prefill, 6)
+    n_pf = max(21, min(args.steps // 10, 399))
+    t_pf = statistics.median(timed(prefill, n_pf) / n_pf for _ in range(3))
     flops = prefill_flops(wp)
     pf_tflops = flops / t_pf / 1e12
+    pf_copy_mb = (wp.q.nbytes * 2 + wp.k_pool.nbytes * 2) / 1e6
 
     # ---------------- explicit-mask entry points (prefill: 3-D mask; decode: 2-D mask)
     pmask = torch.from_numpy(workload.make_mask(wp, 3, seed=wp.seed + 7, keep=0.75)).to(dev)
     pm = pa.make_mask(pmask, causal=True)
 
     def prefill_masked(i):
-        pa.astr_attn_prefill_ragged_masked(pq, pqo, pk, pv, pr, ps_, pki, pm, pout, pdims, wp.sm_scale, stream=sh)
+        q_, k_, v_ = pcopies[i % n_pcp]
+        pa.astr_attn_prefill_ragged_masked(q_, pqo, k_, v_, pr, ps_, pki, pm, pouts[i % n_pcp], pdims, wp.sm_scale,
+                                           stream=sh)
 
     timed(prefill_masked, 5)
     t_pfm = timed(prefill_masked, n_pf) / n_pf
@@ -530,12 +625,16 @@ def main():
     del cp_src, cp_dst
 
     # ---------------- CPU baseline: the oracle on this host (rank 0 at N=1 only)
-    cpu = None
+    cpu = cpu_pf = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cores = os.cpu_count() or 1
         gbs, dt, reps = oracle_gbs(w, args.cpu_seconds, cores)
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                "sample": f"whole B=32 decode batch, fp64 C oracle, {reps} calls of {dt:.3f} s"}
+        tf, n_rows, dtp = oracle_prefill_tflops(wp, args.cpu_seconds / 2, cores)
+        cpu_pf = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                  "sample": f"{n_rows} random (query row, head) rows of the extend workload, fp64 C oracle, "
+                            f"{dtp:.2f} s"}
 
     if rank != 0:
         if dist is not None:
@@ -552,6 +651,8 @@ def main():
         "warmup": args.warmup,
         "ms_per_step": round(elapsed_max / args.steps * 1e3, 6),
         "us_per_call": round(us_per_call, 3),
+        "repeats": {"regions": len(region_us), "steps_each": args.steps, "us_per_call_min": round(region_us[0], 3),
+                    "us_per_call_median": round(us_per_call, 3), "us_per_call_max": round(region_us[-1], 3)},
         "us_per_call_graph": round(graph_us, 3) if isinstance(graph_us, float) else graph_us,
         "frac_of_hbm": round(value / world / peaks["hbm_gbs"], 4),
         "frac_of_nominal_8tbs": round(value / world / 7900.0, 4),
@@ -570,6 +671,7 @@ def main():
                      "traffic": traffic},
         "prefill": {"workload": wp.name, "seed": wp.seed, "us_per_call": round(t_pf * 1e6, 3),
                     "flops_per_call": flops,
+                    "l2": f"rotating {n_pcp} query/pool/output copies ({n_pcp * pf_copy_mb:.0f} MB)",
                     "roofline": {"bound": "tensor", "achieved": round(pf_tflops, 2), "peak": peaks["bf16_tflops"],
                                  "peak_source": f"bf16_tflops burst ({peaks_src})", "unit": "TFLOP/s",
                                  "frac": round(pf_tflops / peaks["bf16_tflops"], 4),
@@ -600,8 +702,10 @@ def main():
                 "h2d_bytes_per_step": h2d_full, "d2h_bytes_per_step": d2h,
                 "resident_kv": {"value": round(sum_over_ranks(nbytes["kv"]) / t_e2e_res / 1e9, 3), "unit": "GB/s",
                                 "h2d_bytes_per_step": h2d_res, "d2h_bytes_per_step": d2h}},
-        "gpu_launches": 2 * args.steps,
+        "decode_workloads": decode_workloads,
+        "gpu_launches": 2 * args.steps * len(region_us),
         "cpu_baseline": cpu,
+        "prefill_cpu_baseline": cpu_pf,
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                    "samples": clk["samples"]},
     }

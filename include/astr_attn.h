@@ -5,6 +5,7 @@
  * over a KV-cache pool addressed through a req_to_token slot table at page_size = 1.
  * Sources (AstrAI commit log pages; "P3" = page "astrai/extension @6f67ba8",
  * "P1" = page "astrai/extension/backend/attention.py @c9ceca1",
+ * "P2" = page "astrai/extension/backend @c9ceca1",
  * "P5" = page "astrai/extension/attention_backend.py @47b3ed4"):
  *   - P3, CUDA-backend commit: decode goes through attn_paged_decode and prefill through
  *     attn_prefill; req_to_token serves as the page table with one token per page.
@@ -43,11 +44,21 @@
  *       o_part            [batch, num_qo_heads, max_splits, head_dim] fp32
  *       ml_part           [batch, num_qo_heads, max_splits, 2]       fp32 (m, l)
  *   - Query head h reads KV head h / (num_qo_heads / num_kv_heads) (consecutive groups).
- *   - Caller preconditions (not checked, as that would need device reads): every slot id
- *     in row b's first seq_lens[b] entries is in [0, num_slots); 0 <= seq_lens[b] <=
+ *   - Caller preconditions (not checked on the host, as that would need device reads): every
+ *     slot id in row b's first seq_lens[b] entries is in [0, num_slots); 0 <= seq_lens[b] <=
  *     max_seq_len <= r2t_stride; kv_indptr is the exclusive prefix sum of seq_lens;
  *     for prefill 0 <= qo_indptr[b+1] - qo_indptr[b] <= seq_lens[b], qo_indptr[0] = 0 and
- *     qo_indptr[batch] = total_q.  Violations give undefined results.
+ *     qo_indptr[batch] = total_q.  Violations give wrong results but no out-of-bounds access:
+ *     a slot id outside the pool, or a key position past the table row, reads as a zero row
+ *     (the KV append skips that token) and raises ASTR_KSTATUS_BAD_INPUT in the status word.
+ *   - Errors found on the GPU (P1, input-validation bullet; P2, misaligned-input bullet: bad
+ *     inputs are rejected with a clear error) cannot be returned by an asynchronous call.  When
+ *     dims->status points to a device int32, the kernels OR the ASTR_KSTATUS_* bits below into
+ *     it; the caller zeroes it before the call and reads it after synchronising the stream.
+ *     Every wait of a kernel's pipeline is bounded (dims->wait_limit polls); a wait that runs
+ *     out makes the kernel give up, write the outputs it still owns as NaN (prefill: the tiles
+ *     it has not finished stay unwritten), raise ASTR_KSTATUS_TIMEOUT and return, leaving the
+ *     CUDA context usable.  Outputs are valid only when the status word stays 0.
  */
 #ifndef ASTR_ATTN_H
 #define ASTR_ATTN_H
@@ -69,7 +80,13 @@ typedef enum astr_status {
   ASTR_ERR_DEVICE = -6                /* querying the current device failed */
 } astr_status;
 
-/* Shapes and capacities; host struct read during the call only. */
+/* Status-word bits set by the kernels (see the conventions above). */
+#define ASTR_KSTATUS_TIMEOUT 1    /* a pipeline wait ran out: the call's outputs are invalid */
+#define ASTR_KSTATUS_BAD_INPUT 2  /* an out-of-pool slot id or a key position past r2t_stride was met */
+#define ASTR_KSTATUS_SMEM 4       /* the shared-memory window was not 1024-byte aligned: no work done */
+
+/* Shapes and capacities; host struct read during the call only.  Zero-initialise it: the
+ * trailing fields then take their defaults. */
 typedef struct astr_attn_dims {
   int32_t batch;         /* requests in the batch (0 = nothing to do) */
   int32_t num_qo_heads;  /* Hq */
@@ -82,6 +99,9 @@ typedef struct astr_attn_dims {
   int32_t max_q_len;     /* prefill: upper bound of q_len (sizes the grid); ignored by decode */
   int32_t max_splits;    /* decode: partial slots per (request, head) in o_part / ml_part (>= 1) */
   int32_t num_splits;    /* decode: key chunks per KV head; 0 = plan automatically (one wave) */
+  int32_t* status;       /* optional DEVICE int32, 4-byte aligned: kernels OR ASTR_KSTATUS_* bits
+                            into it (NULL = not reported); owned by the caller */
+  uint32_t wait_limit;   /* polls per pipeline wait before a kernel gives up; 0 = default (2^20) */
 } astr_attn_dims;
 
 /*

@@ -25,6 +25,7 @@ __all__ = [
     "astr_attn_version", "alloc_decode_workspace",
     "ASTR_OK", "ASTR_ERR_INVALID_ARG", "ASTR_ERR_UNSUPPORTED", "ASTR_ERR_MISALIGNED",
     "ASTR_ERR_WORKSPACE_TOO_SMALL", "ASTR_ERR_LAUNCH_FAILED", "ASTR_ERR_DEVICE", "EXPORTED_SYMBOLS",
+    "ASTR_KSTATUS_TIMEOUT", "ASTR_KSTATUS_BAD_INPUT", "ASTR_KSTATUS_SMEM",
 ]
 
 ASTR_OK = 0
@@ -34,6 +35,11 @@ ASTR_ERR_MISALIGNED = -3
 ASTR_ERR_WORKSPACE_TOO_SMALL = -4
 ASTR_ERR_LAUNCH_FAILED = -5
 ASTR_ERR_DEVICE = -6
+
+# bits of the status word (dims.status)
+ASTR_KSTATUS_TIMEOUT = 1
+ASTR_KSTATUS_BAD_INPUT = 2
+ASTR_KSTATUS_SMEM = 4
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libastr_attn.so")
@@ -61,6 +67,7 @@ class Dims(ctypes.Structure):
         ("head_dim", ctypes.c_int32), ("num_slots", ctypes.c_int64), ("r2t_stride", ctypes.c_int32),
         ("max_seq_len", ctypes.c_int32), ("total_q", ctypes.c_int32), ("max_q_len", ctypes.c_int32),
         ("max_splits", ctypes.c_int32), ("num_splits", ctypes.c_int32),
+        ("status", ctypes.c_void_p), ("wait_limit", ctypes.c_uint32),
     ]
 
 
@@ -140,9 +147,12 @@ def load():
 
 
 def make_dims(batch, num_qo_heads, num_kv_heads, head_dim, num_slots, r2t_stride, max_seq_len, total_q=0,
-              max_q_len=0, max_splits=1, num_splits=0) -> Dims:
+              max_q_len=0, max_splits=1, num_splits=0, status=None, wait_limit=0) -> Dims:
+    """``status``: optional device int32 tensor (or pointer) the kernels OR their ASTR_KSTATUS_*
+    bits into; ``wait_limit``: polls per pipeline wait before a kernel gives up (0 = default)."""
     return Dims(int(batch), int(num_qo_heads), int(num_kv_heads), int(head_dim), int(num_slots), int(r2t_stride),
-                int(max_seq_len), int(total_q), int(max_q_len), int(max_splits), int(num_splits))
+                int(max_seq_len), int(total_q), int(max_q_len), int(max_splits), int(num_splits), _ptr(status),
+                int(wait_limit))
 
 
 def _ptr(t) -> Optional[int]:

@@ -10,10 +10,30 @@
 #include "astr_attn.h"
 #include "astr_attn_internal.h"
 
+namespace astr {
+
+cudaError_t set_smem_limit_once(const void* func, int bytes, std::atomic<bool> (&done)[kMaxDevices]) {
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  std::lock_guard<std::mutex> lk(mu);
+  if (done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  done[dev].store(true, std::memory_order_release);
+  return cudaSuccess;
+}
+
+}  // namespace astr
+
 namespace {
 
-constexpr int kMaxDevices = 64;
+using astr::kMaxDevices;
 constexpr int kDecodeCtasPerSm = 1;     // the split kernel is persistent: one CTA per SM
+constexpr uint32_t kDefaultWaitLimit = 1u << 20;  // polls per pipeline wait (dims->wait_limit = 0)
 
 std::mutex g_mu;
 int g_sm_count[kMaxDevices] = {0};
@@ -51,8 +71,11 @@ int check_common(const astr_attn_dims* d) {
   if (d->r2t_stride < d->max_seq_len) return ASTR_ERR_INVALID_ARG;
   if (d->batch > 0 && d->max_seq_len > 0 && d->num_slots < 1) return ASTR_ERR_INVALID_ARG;
   if (d->num_kv_heads > 65535 || d->batch > 65535) return ASTR_ERR_INVALID_ARG;  // grid y / z limits
+  if (d->status != nullptr && !aligned(d->status, 4)) return ASTR_ERR_MISALIGNED;
   return ASTR_OK;
 }
+
+uint32_t wait_limit_of(const astr_attn_dims* d) { return d->wait_limit != 0 ? d->wait_limit : kDefaultWaitLimit; }
 
 // Key chunks per KV head: one wave of persistent CTAs (kv heads x CTAs = SMs), each CTA
 // running kDecodeChunksPerCta chunks.
@@ -100,7 +123,7 @@ const char* astr_attn_status_string(int status) {
   }
 }
 
-int astr_attn_version(void) { return 100; }
+int astr_attn_version(void) { return 20000; }
 
 int astr_attn_decode_workspace_bytes(const astr_attn_dims* d, size_t* o_bytes, size_t* ml_bytes) {
   if (d == nullptr || o_bytes == nullptr || ml_bytes == nullptr) return ASTR_ERR_INVALID_ARG;
@@ -145,6 +168,8 @@ static int decode_prepare(const astr_attn_dims* d, float sm_scale, astr::DecodeP
   p->part_pitch = d->max_splits;
   p->min_chunk = plan_min_chunk(d);
   p->scale_log2 = sm_scale * 1.4426950408889634f;
+  p->status = d->status;
+  p->wait_limit = wait_limit_of(d);
   if (p->num_splits > 0x7fffffff / 2) return ASTR_ERR_INVALID_ARG;
   return ASTR_OK;
 }
@@ -345,6 +370,8 @@ static int prefill_impl(const uint16_t* q, const int32_t* qo_indptr, const uint1
   }
   p.contig = contig ? 1 : 0;
   p.kv = ks;
+  p.status = d->status;
+  p.wait_limit = wait_limit_of(d);
   if (astr::launch_prefill(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ASTR_ERR_LAUNCH_FAILED;
   return ASTR_OK;
 }
@@ -395,6 +422,7 @@ int astr_attn_kv_append(const uint16_t* k_new, const uint16_t* v_new, const int3
   p.batch = d->batch;
   p.total_q = d->total_q;
   p.row_vecs = d->num_kv_heads * d->head_dim * 2 / 16;
+  p.status = d->status;
   if (astr::launch_kv_append(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ASTR_ERR_LAUNCH_FAILED;
   return ASTR_OK;
 }

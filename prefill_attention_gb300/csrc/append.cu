@@ -88,7 +88,10 @@ __global__ void __launch_bounds__(kAppendWarps * 32) kv_append_kernel(const Appe
   const int64_t pos = (int64_t)__ldg(p.seq_lens + b) - ((int64_t)q1 - q0) + ((int64_t)r - q0);
   int64_t slot = -1;
   if (pos >= 0 && pos < p.r2t_stride) slot = __ldg(p.req_to_token + (size_t)b * p.r2t_stride + pos);
-  if (slot < 0 || slot >= p.num_slots) return;  // warp-uniform: ids outside the pool are skipped
+  if (slot < 0 || slot >= p.num_slots) {  // warp-uniform: ids outside the pool are skipped and reported
+    if (lane == 0 && p.status != nullptr) atomicOr(p.status, kStatusBadInput);
+    return;
+  }
   uint4* kd = reinterpret_cast<uint4*>(p.k_pool) + (size_t)slot * nvec;
   uint4* vd = reinterpret_cast<uint4*>(p.v_pool) + (size_t)slot * nvec;
 #pragma unroll

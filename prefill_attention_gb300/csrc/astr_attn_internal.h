@@ -5,7 +5,19 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace astr {
+
+constexpr int kMaxDevices = 64;
+
+// Raises func's dynamic shared-memory limit to `bytes` on the current device, once per device
+// (the attribute belongs to the device that is current when it is set).  `done` is the
+// caller's table for this kernel.  Thread-safe.
+cudaError_t set_smem_limit_once(const void* func, int bytes, std::atomic<bool> (&done)[kMaxDevices]);
+
+// Status-word bits (the ASTR_KSTATUS_* values of the C header).
+constexpr int kStatusTimeout = 1, kStatusBadInput = 2, kStatusSmem = 4;
 
 // Decode split kernel: a CTA runs this many independent warp pairs, one key chunk each.
 constexpr int kDecodeChunksPerCta = 4;
@@ -40,6 +52,8 @@ struct DecodeParams {
   int combine_all;               // combine even single-chunk requests (partials supplied by the caller)
   int indptr_before_wait;        // combine: kv_indptr may be read before the dependency wait (the
                                  // previous kernel is this call's split kernel, which does not write it)
+  int32_t* status;               // optional status word (kStatus* bits, OR-ed in); may be null
+  uint32_t wait_limit;           // polls per pipeline wait before giving up
 };
 
 // Decode with an explicit mask: request b's bytes start at mask + b * req_pitch, one byte per
@@ -73,6 +87,8 @@ struct PrefillParams {
   int mask_kv_pitch;             // bytes in a mask row (a multiple of 16)
   int contig;                    // 1: K/V rows come from a contiguous cache addressed by kv
   KvStrides kv;
+  int32_t* status;               // optional status word (kStatus* bits, OR-ed in); may be null
+  uint32_t wait_limit;           // polls per pipeline wait before giving up
 };
 
 // KV append: one launch, one warp per new token.
@@ -88,6 +104,7 @@ struct AppendParams {
   int64_t num_slots;             // slot ids outside [0, num_slots) are skipped
   int batch, total_q;
   int row_vecs;                  // 16-byte vectors per slot row (Hkv * D * 2 / 16)
+  int32_t* status;               // optional status word (kStatus* bits, OR-ed in); may be null
 };
 
 // Launchers return cudaSuccess or the launch error; they never synchronise.

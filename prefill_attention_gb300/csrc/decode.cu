@@ -343,12 +343,12 @@ __device__ __forceinline__ void warm_first_slots(const DecodeParams& p, const Kv
   }
 }
 
-// Bounded wait that gives up (and raises the pair's error flag) on timeout or once the flag is up.
-__device__ __forceinline__ bool wait_or_fail(uint32_t bar, uint32_t parity, volatile int* err) {
-  if (*err) return false;
-  if (tc::mbar_wait(bar, parity)) return true;
-  *err = 1;
-  return false;
+// Bounded wait, agreed by the whole warp, that gives up (and raises the pair's error flag) on
+// timeout or once the flag is up.
+__device__ __forceinline__ bool wait_or_fail(uint32_t bar, uint32_t parity, volatile int* err, uint32_t limit) {
+  const bool ok = __all_sync(kFullMask, *err == 0 && tc::mbar_wait(bar, parity, limit));
+  if (!ok) *err = 1;
+  return ok;
 }
 
 // Kernel variants: MODE bit 0 = explicit mask, bit 1 = contiguous (stride-addressed) K/V cache
@@ -384,7 +384,9 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(
   const int kvh = blockIdx.y;
   const int B = p.batch;
   const int32_t* ind = p.kv_indptr;
-  if ((sbase & 1023u) != 0) return;  // swizzle atoms need a 1024-byte aligned window
+  // swizzle atoms need a 1024-byte aligned window; without one the pairs do no work and
+  // poison their outputs (the error flags start raised)
+  const bool smem_ok = (sbase & 1023u) == 0;
 
   const uint32_t ring = sbase + pair * C::RING;
   const uint32_t bars = sbase + C::BAR_OFF + 8u * (pair * 2 * C::STAGES);
@@ -396,7 +398,7 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(
   // ---- set-up (shared memory only): barriers; Q rows of absent heads stay zero throughout
   if (tid == 0) {
     for (int i = 0; i < C::NPAIR * 2 * C::STAGES; ++i) tc::mbar_init(sbase + C::BAR_OFF + 8u * i, 32);
-    for (int i = 0; i < C::NPAIR; ++i) reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 8 * C::NBAR)[i] = 0;
+    for (int i = 0; i < C::NPAIR; ++i) reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 8 * C::NBAR)[i] = smem_ok ? 0 : 1;
     tc::fence_mbarrier_init();
   }
   for (int i = tid; i < C::NPAIR * C::STAGES * (C::Q_BYTES / 16); i += C::THREADS) {
@@ -427,26 +429,36 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(
   SlotBracket first{0, 0, 0, 0};
   if (ls < hs) first = locate_slot(ind, B, ls, lane);
 
-  if (ls < hs && is_producer) {
+  if (ls < hs && smem_ok && is_producer) {
     // ======================= producer warp: gathers the chunk's K / V rows slot by slot
     TileIter<C::BK> it;
     it.start_at(first, ls);
     const size_t head_stride = (size_t)p.num_kv_heads * D;
     const unsigned nslots = (unsigned)p.num_slots;
-    auto slot_id = [&](const TileIter<C::BK>& t) {  // lane k: slot id of key k of the slot, or -1
+    // lane k: slot id of key k of the slot (-1 past the request's keys); `real` = the key is one
+    // of the request's.  A real key whose position is past the table row, or whose id (checked
+    // when it is used, one slot later) lies outside the pool, reads as zeros and is reported.
+    bool bad_input = false, my_real = false;
+    auto slot_id = [&](const TileIter<C::BK>& t, bool& real) {
       if constexpr (CONTIG) {
+        real = false;
         return 0;  // contiguous cache: rows are addressed by position, no ids
       } else {
         const int flat = t.start + lane;
-        return (t.valid(hs) && flat < t.end)
-                   ? ldg_nc_i32(p.req_to_token + (int64_t)t.b * p.r2t_stride + (flat - t.ind_b))
-                   : -1;
+        real = t.valid(hs) && flat < t.end;
+        if (real && flat - t.ind_b >= p.r2t_stride) {
+          bad_input = true;
+          real = false;
+        }
+        return real ? ldg_nc_i32(p.req_to_token + (int64_t)t.b * p.r2t_stride + (flat - t.ind_b)) : -1;
       }
     };
-    int my_id = slot_id(it);
-    for (int i = 0; it.valid(hs); ++i) {
+    int my_id = slot_id(it, my_real);
+    int i = 0;  // ring slots published so far
+    for (; it.valid(hs); ++i) {
       const int s = i % C::STAGES;
-      if (i >= C::STAGES && !wait_or_fail(empty(s), (uint32_t)((i / C::STAGES - 1) & 1), err)) break;
+      if (i >= C::STAGES && !wait_or_fail(empty(s), (uint32_t)((i / C::STAGES - 1) & 1), err, p.wait_limit)) break;
+      if constexpr (!CONTIG) bad_input |= my_real && (unsigned)my_id >= nslots;
       const uint32_t kst = ring + s * C::SLOT, vst = kst + C::KV_BYTES, qst = vst + C::KV_BYTES;
       if (it.opens_piece(ls)) {  // first slot of a piece: its G query rows
         const uint16_t* qsrc = p.q + ((size_t)it.b * p.num_qo_heads + (size_t)kvh * G) * D;
@@ -491,10 +503,17 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(
       }
       cp_async_arrive_noinc(full(s));  // completes once this lane's copies (and older ones) land
       it.next(ind, B, hs);
-      my_id = slot_id(it);
+      my_id = slot_id(it, my_real);
     }
     cp_async_wait<0>();
-  } else if (ls < hs) {
+    if (*err) {
+      // the consumer gave up: let the arrivals of the slots published last land (each slot's
+      // newest phase; its 32 arrivals are this warp's) before the CTA's shared memory goes away
+      for (int k = max(0, i - C::STAGES); k < i; ++k)
+        tc::mbar_wait(full(k % C::STAGES), (uint32_t)((k / C::STAGES) & 1), tc::kWaitLimit);
+    }
+    if (p.status != nullptr && __any_sync(kFullMask, bad_input) && lane == 0) atomicOr(p.status, kStatusBadInput);
+  } else if (ls < hs && smem_ok) {
     // ======================= consumer warp: online softmax over the chunk's slots
     // Transposed products so the 16-row MMA side is keys / head_dim, not the few heads:
     //   S^T (32 keys x 8 heads) = K Q^T,   O^T (D x 8 heads) += V^T P^T.
@@ -511,7 +530,7 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(
       const int s = i % C::STAGES;
       const bool opens = it.opens_piece(ls), closes = it.closes_piece(hs);
       const int nkeys = it.end - it.start;  // valid keys of the slot; the rest are masked
-      if (!wait_or_fail(full(s), (uint32_t)((i / C::STAGES) & 1), err)) break;
+      if (!wait_or_fail(full(s), (uint32_t)((i / C::STAGES) & 1), err, p.wait_limit)) break;
       const uint32_t kst = ring + s * C::SLOT, vst = kst + C::KV_BYTES, qst = vst + C::KV_BYTES;
       // visibility of this lane's keys 16 mt + g4 + 8 hh, bit 2 mt + hh (explicit mask)
       uint32_t kvis = 0u;
@@ -733,7 +752,9 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(
   }
   __syncthreads();
   if (*err && ls < hs && !is_producer) {
-    // a wait timed out: poison every output this pair owns so the call reads as failed
+    // a wait timed out (or the window was misaligned): report it and poison every output this
+    // pair owns so the call reads as failed
+    if (p.status != nullptr && lane == 0) atomicOr(p.status, smem_ok ? kStatusTimeout : kStatusSmem);
     TileIter<C::BK> it;
     it.start_at(first, ls);
     for (; it.valid(hs); it.next(ind, B, hs)) {
@@ -857,13 +878,9 @@ cudaError_t launch_split_t(const typename SplitArg<MODE>::type& arg, cudaStream_
   const DecodeParams& p = params_of(arg);
   using C = DecCfg<D, G>;
   constexpr int smem = (MODE & kModeMask) ? C::SMEM_BYTES_MASKED : C::SMEM_BYTES;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(decode_split_kernel<D, G, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<bool> attr_done[kMaxDevices];
+  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(decode_split_kernel<D, G, MODE>), smem, attr_done);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((p.num_splits + C::NPAIR - 1) / C::NPAIR, p.num_kv_heads);  // NPAIR chunks per CTA
   cfg.blockDim = dim3(C::THREADS);
@@ -874,7 +891,7 @@ cudaError_t launch_split_t(const typename SplitArg<MODE>::type& arg, cudaStream_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, decode_split_kernel<D, G, MODE>, arg);
+  e = cudaLaunchKernelEx(&cfg, decode_split_kernel<D, G, MODE>, arg);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -16,18 +16,20 @@
 //   * All calls share the one array, so calls that overlap on the GPU (different streams,
 //     or different host threads without ordering) race on it; serialise them.
 //   * The array keeps the previous call's contents; nothing in it needs to start at zero
-//     because every partial the combine reads is written by the same call.
+//     because every partial the combine reads is written by the same call (a split kernel
+//     that gives up writes its partials as NaN, and reports it in the status word).
 #include <cstdint>
 #include <mutex>
 
 #include <cuda_runtime.h>
 
 #include "astr_attn.h"
+#include "astr_attn_internal.h"
 
 namespace {
 
 constexpr size_t kScratchBytes = size_t(16) << 20;  // 16 MiB of partials per process and device
-constexpr int kMaxDevices = 64;
+using astr::kMaxDevices;
 
 __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 
@@ -62,13 +64,19 @@ extern "C" {
 int astr_attn_paged_decode_noalloc(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
                                    const int32_t* req_to_token, const int32_t* seq_lens, const int32_t* kv_indptr,
                                    uint16_t* out, const astr_attn_dims* dims, float sm_scale, void* stream) {
+  // the argument checks of astr_attn_paged_decode, in its order, come first, so both entry
+  // points return the same status for the same arguments (an empty batch included)
+  if (!q || !k_pool || !v_pool || !req_to_token || !seq_lens || !kv_indptr || !out) return ASTR_ERR_INVALID_ARG;
+  const auto misaligned = [](const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a != 0; };
+  if (misaligned(q, 16) || misaligned(k_pool, 16) || misaligned(v_pool, 16) || misaligned(out, 16) ||
+      misaligned(req_to_token, 4) || misaligned(seq_lens, 4) || misaligned(kv_indptr, 4))
+    return ASTR_ERR_MISALIGNED;
   if (dims == nullptr) return ASTR_ERR_INVALID_ARG;
   size_t o_bytes = 0, ml_bytes = 0;
   int st = astr_attn_decode_workspace_bytes(dims, &o_bytes, &ml_bytes);
   if (st != ASTR_OK) return st;
   const size_t ml_off = (o_bytes + 255) & ~size_t(255);
   if (ml_off + ml_bytes > kScratchBytes) return ASTR_ERR_WORKSPACE_TOO_SMALL;
-  if (dims->batch == 0) return ASTR_OK;
   void* base = nullptr;
   if ((st = scratch_for_current_device(&base)) != ASTR_OK) return st;
   float* o_part = static_cast<float*>(base);

@@ -82,7 +82,6 @@ struct PrefillCfg {
   static constexpr uint32_t TMEM_TILE = 256;           // tile t: O at 256 t, S buffers at 256 t + D + {0, BN}
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr int KV_IT = BN * CPR / 32;          // cp.async per producer lane per K (or V) tile
-  static constexpr int RPI = 32 / CPR;                 // output rows per coalesced warp store
   static constexpr uint32_t IDESC_S = tc::idesc_bf16_f32(M, BN, false, false);   // K-major A and B
   static constexpr uint32_t IDESC_PV = tc::idesc_bf16_f32(M, D, false, true);    // B (V) MN-major
   static constexpr float kRescaleThreshold = 8.f;     // log2 units
@@ -254,7 +253,10 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
   extern __shared__ __align__(1024) unsigned char smem[];
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if ((sbase & 1023u) != 0) return;   // swizzle atoms need a 1024-byte aligned window
+  if ((sbase & 1023u) != 0) {  // swizzle atoms need a 1024-byte aligned window: report, do nothing
+    if (tid == 0 && p.status != nullptr) atomicOr(p.status, kStatusSmem);
+    return;
+  }
 
   const uint32_t bars = sbase + C::BAR_OFF;
   auto kv_full = [&](int s) { return bars + 8u * s; };
@@ -429,7 +431,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
   // Bounded wait, agreed by the whole warp (so warp-collective tcgen05 ops after it stay
   // converged); a timeout, or an error raised elsewhere, makes every later wait fail.
   auto wait_or_fail = [&](uint32_t bar, uint32_t parity) -> bool {
-    bool ok = (*err == 0) && tc::mbar_wait(bar, parity);
+    bool ok = (*err == 0) && tc::mbar_wait(bar, parity, p.wait_limit);
     ok = __all_sync(kFullMask, ok);
     if (!ok) *err = 1;
     return ok;
@@ -502,6 +504,11 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
     }
     for (int v = max(0, u - C::Q_SLOTS); ok && v < u; ++v) write_out(v);  // the last tiles
     if (lane == 0) tc::bulk_wait_all();
+    if (!ok) {
+      // a wait gave up: let the query loads still in flight (the last tiles issued, one phase
+      // per slot) land before the CTA's shared memory goes away
+      for (int v = max(0, u - C::Q_SLOTS); v < u; ++v) tc::mbar_wait(q_full(v), q_par(v), tc::kWaitLimit);
+    }
     __syncwarp();
   } else if (warp >= C::KV_WARP0) {
     // ======================= K/V gathers: warp KV_WARP0 + s fills stage s with every KV tile
@@ -511,7 +518,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
     const unsigned nslots = (unsigned)p.num_slots;
     const uint32_t kdst = sbase + C::K_OFF + st * C::KV_BYTES, vdst = sbase + C::V_OFF + st * C::KV_BYTES;
     int g_base = 0;  // global index of the current item's KV tile 0
-    bool ok = true;
+    bool ok = true, bad_input = false;
     PrefillItem it;
     for (int n_item = 0; ok; ++n_item) {
       if (!get_item(n_item, it)) break;
@@ -519,12 +526,22 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
       const int32_t* r2t = p.req_to_token + (size_t)it.b * p.r2t_stride;
       const int kv_end = min(it.cb + min(it.q_len, it.first0 + BQ2), it.kvn);
       const int j_first = (st - g_base % C::STAGES + C::STAGES) % C::STAGES;
-      auto ids_of = [&](int j, int half) {  // slot id of key 32 half + lane of item tile j, or -1
+      // slot id of key 32 half + lane of item tile j, or -1 past the keys the item reads;
+      // `real`: a key of the request whose id is checked against the pool when it is used (a
+      // position past the table row is not read and is reported at once)
+      auto ids_of = [&](int j, int half, bool& real) {
         const int key = j * C::BN + half * 32 + lane;
+        real = j < it.n_tiles && key < kv_end;
         if constexpr (CONTIG) {
-          return (j < it.n_tiles && key < kv_end) ? key : -1;  // contiguous cache: the position itself
+          const int pos = real ? key : -1;  // contiguous cache: the position itself
+          real = false;
+          return pos;
         } else {
-          return (j < it.n_tiles && key < kv_end) ? ldg_nc_i32(r2t + key) : -1;
+          if (real && key >= p.r2t_stride) {
+            bad_input = true;
+            real = false;
+          }
+          return real ? ldg_nc_i32(r2t + key) : -1;
         }
       };
       // one K/V tile: row `key` comes from the slot id held by lane key % 32 of id0 (keys
@@ -552,14 +569,16 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
         }
         cp_async_commit();
       };
-      int id0 = ids_of(j_first, 0), id1 = ids_of(j_first, 1);
+      bool real0, real1;
+      int id0 = ids_of(j_first, 0, real0), id1 = ids_of(j_first, 1, real1);
       for (int j = j_first; j < it.n_tiles; j += C::STAGES) {
         const int g = g_base + j;
         const uint32_t par = (uint32_t)(((g / C::STAGES) - 1) & 1);  // phase of tile g - STAGES
         if (g >= C::STAGES && !(ok = wait_or_fail(kv_empty(st), par))) break;
+        if constexpr (!CONTIG) bad_input |= (real0 && (unsigned)id0 >= nslots) || (real1 && (unsigned)id1 >= nslots);
         gather(id0, id1);
-        id0 = ids_of(j + C::STAGES, 0);  // next tile of this stage: its slot ids load meanwhile
-        id1 = ids_of(j + C::STAGES, 1);
+        id0 = ids_of(j + C::STAGES, 0, real0);  // next tile of this stage: its slot ids load meanwhile
+        id1 = ids_of(j + C::STAGES, 1, real1);
         cp_async_wait<0>();
         tc::fence_proxy_async_smem();  // the tensor core reads the tiles through the async proxy
         tc::mbar_arrive(kv_full(st));
@@ -567,6 +586,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
       g_base += it.n_tiles;
     }
     cp_async_wait<0>();
+    if (p.status != nullptr && __any_sync(kFullMask, bad_input) && lane == 0) atomicOr(p.status, kStatusBadInput);
   } else if (warp >= C::MMA_WARP) {
     // ======================= MMA issue: warp MMA_WARP + t, lane 0 alone, for query tile t.
     // tcgen05.mma issue runs nearly in step with execution, so whatever the issuing thread
@@ -599,8 +619,10 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
             (t < it.nq) ? (min(it.cb + min(it.q_len, it.first0 + (t + 1) * C::BQ), it.kvn) + C::BN - 1) / C::BN : 0;
         const int n = it.n_tiles;
         const uint32_t q_lo = (uint32_t)qd0 + (uint32_t)((((u0 + t) % C::Q_SLOTS) * C::Q_BYTES) >> 4);
-        auto wait_one = [&](uint32_t bar, uint32_t parity, bool ready) {  // blocking only if not pre-tested ready
-          if (ok && !ready && !tc::mbar_wait(bar, parity)) {
+        // blocking only if not pre-tested ready; gives up (and stops this thread's issue) on a
+        // timeout or once another warp has given up
+        auto wait_one = [&](uint32_t bar, uint32_t parity, bool ready) {
+          if (ok && (*err != 0 || (!ready && !tc::mbar_wait(bar, parity, p.wait_limit)))) {
             *err = 1;
             ok = false;
           }
@@ -613,6 +635,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
         // issue S_t(j); while it runs, test barrier `nb` (parity `np`); returns that test.
         // Descriptors are formed before the first MMA so the MMAs issue back to back.
         auto issue_s = [&](int j, uint32_t nb, uint32_t np) -> bool {
+          if (!ok) return false;  // a wait gave up: issue nothing more
           const uint32_t sd = od + D + sbuf(j) * C::BN;
           const uint32_t klo = k_lo + (uint32_t)((stage(j) * C::KV_BYTES) >> 4);
           uint32_t al[D / 16], bl[D / 16];
@@ -633,6 +656,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
           return r;
         };
         auto issue_pv = [&](int j, uint32_t nb, uint32_t np) -> bool {
+          if (!ok) return false;  // a wait gave up: issue nothing more
           const uint32_t pa = od + D + sbuf(j) * C::BN;  // P hi in [0, 32), lo in [32, 64)
           const uint32_t vlo = v_lo + (uint32_t)((stage(j) * C::KV_BYTES) >> 4);
           uint32_t bl[C::BN / 16];
@@ -693,8 +717,9 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
     }
     if (lane == 0) {
       // every MMA this thread issued has completed before the CTA may release tensor memory
+      // (MMAs always complete, so this wait takes the default limit whatever the caller's)
       tc::mma_commit(fin);
-      if (!tc::mbar_wait(fin, 0)) *err = 1;
+      if (!tc::mbar_wait(fin, 0, tc::kWaitLimit)) *err = 1;
     }
     __syncwarp();
   } else {
@@ -890,6 +915,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
   if (warp == 0) {
     tc::fence_after_sync();
     tc::tmem_dealloc<C::TMEM_COLS>(tmem);
+    if (lane == 0 && *err != 0 && p.status != nullptr) atomicOr(p.status, kStatusTimeout);
   }
 }
 
@@ -910,14 +936,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
 template <int D, int G, bool MASK, bool CONTIG>
 cudaError_t launch_prefill_t(const PrefillParams& p, cudaStream_t stream) {
   using C = PrefillCfg<D, G>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(prefill_kernel<D, G, MASK, CONTIG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<bool> attr_done[kMaxDevices];
+  const cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(prefill_kernel<D, G, MASK, CONTIG>),
+                                            C::SMEM_BYTES, attr_done);
+  if (e != cudaSuccess) return e;
   // persistent CTAs, one per SM, each walking its share of the items
   const int64_t items = (int64_t)p.num_q_tiles * p.num_kv_heads;
   const int grid = (int)(items < p.num_ctas ? items : p.num_ctas);

@@ -14,7 +14,7 @@
 namespace astr {
 namespace tc {
 
-constexpr uint32_t kWaitLimit = 1u << 20;  // try_wait polls; each poll may suspend briefly
+constexpr uint32_t kWaitLimit = 1u << 20;  // default try_wait polls per wait; each poll may suspend briefly
 
 // ---------------------------------------------------------------- mbarrier
 
@@ -26,9 +26,10 @@ __device__ __forceinline__ void fence_mbarrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
-// Wait until the phase with parity `parity` has completed.  Returns false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+// Wait until the phase with parity `parity` has completed, polling at most `limit` times.
+// Returns false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit = kWaitLimit) {
+  for (uint32_t i = 0; i < limit; ++i) {
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"

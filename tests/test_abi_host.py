@@ -30,11 +30,24 @@ def test_header_declares_and_library_exports_every_entry_point(lib):
         assert hasattr(lib, n), f"missing export {n}"
 
 
-def test_dims_struct_layout_matches_header():
-    # int32 x4, int64, int32 x6 -> 48 bytes (int64 at offset 16, tail padded to 8)
-    assert ctypes.sizeof(pa.Dims) == 48
-    assert pa.Dims.num_slots.offset == 16
-    assert pa.Dims.num_splits.offset == 44
+def test_dims_struct_layout_matches_header(tmp_path):
+    """The ctypes mirror has the C struct's size and field offsets (compiled from the header)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    fields = [f for f, _ in pa.Dims._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "astr_attn.h"\nint main(void) {\n'
+                   '  printf("%zu\\n", sizeof(astr_attn_dims));\n'
+                   + "".join(f'  printf("%zu\\n", offsetof(astr_attn_dims, {f}));\n' for f in fields)
+                   + "  return 0; }\n")
+    exe = tmp_path / "layout"
+    subprocess.run([gcc, "-std=c99", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    assert got[0] == ctypes.sizeof(pa.Dims)
+    assert got[1:] == [getattr(pa.Dims, f).offset for f in fields]
 
 
 def test_status_strings(lib):
@@ -147,6 +160,32 @@ def test_prefill_kv_indptr_may_be_null_and_empty_batch_is_noop(lib):
 def test_workspace_bytes(lib):
     ob, mb = pa.astr_attn_decode_workspace_bytes(_dims(batch=32, max_splits=5))
     assert ob == 32 * 32 * 5 * 128 * 4 and mb == 32 * 32 * 5 * 2 * 4
+
+
+def test_status_word_must_be_4_byte_aligned(lib):
+    assert _dec(_dims(status=A + 2)) == pa.ASTR_ERR_MISALIGNED
+    assert _pf(_dims(status=A + 1)) == pa.ASTR_ERR_MISALIGNED
+    assert _app(_dims(status=A + 3)) == pa.ASTR_ERR_MISALIGNED
+    # a 4-byte aligned word passes and the call fails later, on the bad head_dim
+    assert _dec(_dims(status=A + 4, head_dim=96)) == pa.ASTR_ERR_UNSUPPORTED
+
+
+def _noalloc(d, **ptr):
+    p = dict(q=A, k=A, v=A, r2t=A, seq=A, kvi=A, out=A)
+    p.update(ptr)
+    return pa.astr_attn_paged_decode_noalloc(p["q"], p["k"], p["v"], p["r2t"], p["seq"], p["kvi"], p["out"], d, 0.1,
+                                             stream=0, check=False)
+
+
+@pytest.mark.parametrize("name,addr", [("q", 0), ("k", 0), ("v", 0), ("r2t", 0), ("seq", 0), ("kvi", 0), ("out", 0),
+                                       ("q", A + 8), ("out", A + 2), ("r2t", A + 2), ("kvi", A + 1)])
+@pytest.mark.parametrize("batch", [0, 4])
+def test_noalloc_checks_arguments_like_the_workspace_entry_point(lib, name, addr, batch):
+    """Same status as astr_attn_paged_decode for the same bad pointer, an empty batch included."""
+    d = _dims(batch=batch)
+    expect = pa.ASTR_ERR_INVALID_ARG if addr == 0 else pa.ASTR_ERR_MISALIGNED
+    assert _dec(d, **{name: addr}) == expect
+    assert _noalloc(d, **{name: addr}) == expect
 
 
 def test_noalloc_rejects_oversize_and_null_dims_without_gpu(lib):

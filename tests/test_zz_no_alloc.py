@@ -11,6 +11,7 @@ import pytest
 
 import oracle
 import workload
+from workload import make_from_lengths
 
 pytestmark = pytest.mark.gpu
 
@@ -38,3 +39,31 @@ def test_noalloc_matches_workspace_entry_point_twice(cfg):
         assert np.isfinite(got).all(), f"call {call}"
         assert np.abs(got - ref).max() <= TOL, f"call {call}: differs from the workspace entry point"
         assert np.abs(got - oracle.decode(w)).max() <= TOL, f"call {call}: differs from the oracle"
+
+
+def test_partials_left_by_a_larger_call_are_never_read():
+    """A large call fills much of the shared array; smaller calls with other split layouts
+    (requests inside one chunk next to requests over several) must read only the partials
+    they wrote themselves, whatever the array held before."""
+    big = workload.config(2)
+    tb = upload(big)
+    out_b = torch.empty_like(tb["q"])
+    pa.astr_attn_paged_decode_noalloc(tb["q"], tb["k"], tb["v"], tb["r2t"], tb["seq"], tb["kvi"], out_b,
+                                      decode_dims(big, max_splits=16), big.sm_scale)
+    rng = np.random.default_rng(4242)
+    small = make_from_lengths(rng, kind="decode", name="after-big", seq_lens=[3, 200, 31, 33, 500, 1, 64, 0],
+                              q_lens=None, Hq=8, Hkv=2, d=64)
+    ts = upload(small)
+    ref_small = oracle.decode(small)
+    for n_chunks in (0, 5, 37, 3):
+        dims = decode_dims(small, max_splits=8, num_splits=n_chunks)
+        out = torch.full_like(ts["q"], float("nan"))
+        pa.astr_attn_paged_decode_noalloc(ts["q"], ts["k"], ts["v"], ts["r2t"], ts["seq"], ts["kvi"], out, dims,
+                                          small.sm_scale)
+        torch.cuda.synchronize()
+        got = to_f64(out)
+        ref = to_f64(run_decode(small, ts, max_splits=8, num_splits=n_chunks))
+        assert np.isfinite(got).all(), f"n_chunks={n_chunks}"
+        assert np.abs(got - ref).max() <= TOL, f"n_chunks={n_chunks}: differs from the workspace entry point"
+        assert np.abs(got - ref_small).max() <= TOL, f"n_chunks={n_chunks}: differs from the oracle"
+    assert np.abs(to_f64(out_b) - oracle.decode(big)).max() <= TOL
