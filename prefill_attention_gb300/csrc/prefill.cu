@@ -682,7 +682,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
         // o_done wait
         for (; ok && uw < u0 + min(t + 1, it.nq); ++uw) {
           wait_one(q_full(uw), q_par(uw), false);
-          tc::mbar_arrive(q_free(uw));
+          if (ok) tc::mbar_arrive(q_free(uw));  // (a tile not seen landing is never released)
         }
         bool ready = false;  // pre-test result for the next wait
         if (nk > 0) {
@@ -705,7 +705,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
             // only once it has landed: otherwise the release could run ahead and count toward
             // an earlier phase of the stage's empty barrier
             wait_one(kv_full(stage(j)), kv_par(j), false);
-            tc::mma_commit(kv_empty(stage(j)));
+            if (ok) tc::mma_commit(kv_empty(stage(j)));
           }
         }
         gs += nk;
