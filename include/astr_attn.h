@@ -73,7 +73,7 @@ extern "C" {
 typedef enum astr_status {
   ASTR_OK = 0,
   ASTR_ERR_INVALID_ARG = -1,          /* null pointer, negative or inconsistent dims, non-finite sm_scale */
-  ASTR_ERR_UNSUPPORTED = -2,          /* head_dim not 64/128, Hq % Hkv != 0, group size not supported */
+  ASTR_ERR_UNSUPPORTED = -2,          /* head_dim not 32/64/128, Hq % Hkv != 0, group size not supported */
   ASTR_ERR_MISALIGNED = -3,           /* a pointer breaks the alignment rule above */
   ASTR_ERR_WORKSPACE_TOO_SMALL = -4,  /* explicit combine layout: num_splits above max_splits */
   ASTR_ERR_LAUNCH_FAILED = -5,        /* a CUDA launch or attribute call failed (cudaGetLastError) */
@@ -84,6 +84,8 @@ typedef enum astr_status {
 #define ASTR_KSTATUS_TIMEOUT 1    /* a pipeline wait ran out: the call's outputs are invalid */
 #define ASTR_KSTATUS_BAD_INPUT 2  /* an out-of-pool slot id or a key position past r2t_stride was met */
 #define ASTR_KSTATUS_SMEM 4       /* the shared-memory window was not 1024-byte aligned: no work done */
+#define ASTR_KSTATUS_RANGE 8      /* prefill: an output row came out non-finite -- P V runs in fp16, so a
+                                     V element beyond 65504 (or a non-finite input) makes it so */
 
 /* Shapes and capacities; host struct read during the call only.  Zero-initialise it: the
  * trailing fields then take their defaults. */
@@ -91,7 +93,7 @@ typedef struct astr_attn_dims {
   int32_t batch;         /* requests in the batch (0 = nothing to do) */
   int32_t num_qo_heads;  /* Hq */
   int32_t num_kv_heads;  /* Hkv; Hq % Hkv == 0; group size Hq/Hkv in {1,2,4,8,16} */
-  int32_t head_dim;      /* 64 or 128 */
+  int32_t head_dim;      /* 32, 64 or 128 */
   int64_t num_slots;     /* rows of k_pool / v_pool */
   int32_t r2t_stride;    /* elements between consecutive req_to_token rows */
   int32_t max_seq_len;   /* host-known upper bound of seq_lens (bounds the partials per request) */
@@ -101,7 +103,8 @@ typedef struct astr_attn_dims {
   int32_t num_splits;    /* decode: key chunks per KV head; 0 = plan automatically (one wave) */
   int32_t* status;       /* optional DEVICE int32, 4-byte aligned: kernels OR ASTR_KSTATUS_* bits
                             into it (NULL = not reported); owned by the caller */
-  uint32_t wait_limit;   /* polls per pipeline wait before a kernel gives up; 0 = default (2^20) */
+  uint32_t wait_limit;   /* polls per pipeline wait before a kernel gives up (the first poll does not
+                            block, later ones may suspend the thread briefly); 0 = default (2^20) */
 } astr_attn_dims;
 
 /*

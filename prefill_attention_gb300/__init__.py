@@ -25,7 +25,7 @@ __all__ = [
     "astr_attn_version", "alloc_decode_workspace",
     "ASTR_OK", "ASTR_ERR_INVALID_ARG", "ASTR_ERR_UNSUPPORTED", "ASTR_ERR_MISALIGNED",
     "ASTR_ERR_WORKSPACE_TOO_SMALL", "ASTR_ERR_LAUNCH_FAILED", "ASTR_ERR_DEVICE", "EXPORTED_SYMBOLS",
-    "ASTR_KSTATUS_TIMEOUT", "ASTR_KSTATUS_BAD_INPUT", "ASTR_KSTATUS_SMEM",
+    "ASTR_KSTATUS_TIMEOUT", "ASTR_KSTATUS_BAD_INPUT", "ASTR_KSTATUS_SMEM", "ASTR_KSTATUS_RANGE",
 ]
 
 ASTR_OK = 0
@@ -40,6 +40,7 @@ ASTR_ERR_DEVICE = -6
 ASTR_KSTATUS_TIMEOUT = 1
 ASTR_KSTATUS_BAD_INPUT = 2
 ASTR_KSTATUS_SMEM = 4
+ASTR_KSTATUS_RANGE = 8
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libastr_attn.so")

@@ -67,7 +67,7 @@ int check_common(const astr_attn_dims* d) {
       d->r2t_stride < 0 || d->max_seq_len < 0)
     return ASTR_ERR_INVALID_ARG;
   if (d->num_qo_heads % d->num_kv_heads != 0) return ASTR_ERR_UNSUPPORTED;
-  if (d->head_dim != 64 && d->head_dim != 128) return ASTR_ERR_UNSUPPORTED;
+  if (d->head_dim != 32 && d->head_dim != 64 && d->head_dim != 128) return ASTR_ERR_UNSUPPORTED;
   if (d->r2t_stride < d->max_seq_len) return ASTR_ERR_INVALID_ARG;
   if (d->batch > 0 && d->max_seq_len > 0 && d->num_slots < 1) return ASTR_ERR_INVALID_ARG;
   if (d->num_kv_heads > 65535 || d->batch > 65535) return ASTR_ERR_INVALID_ARG;  // grid y / z limits
@@ -114,7 +114,7 @@ const char* astr_attn_status_string(int status) {
   switch (status) {
     case ASTR_OK: return "ok";
     case ASTR_ERR_INVALID_ARG: return "invalid argument (null pointer, negative or inconsistent dims, non-finite scale)";
-    case ASTR_ERR_UNSUPPORTED: return "unsupported shape (head_dim must be 64 or 128; Hq % Hkv == 0; supported group size)";
+    case ASTR_ERR_UNSUPPORTED: return "unsupported shape (head_dim must be 32, 64 or 128; Hq % Hkv == 0; supported group size)";
     case ASTR_ERR_MISALIGNED: return "misaligned pointer (bf16/fp32 arrays need 16-byte, int32 arrays 4-byte alignment)";
     case ASTR_ERR_WORKSPACE_TOO_SMALL: return "workspace too small (num_splits above max_splits)";
     case ASTR_ERR_LAUNCH_FAILED: return "CUDA launch failed";

@@ -17,7 +17,7 @@ constexpr int kMaxDevices = 64;
 cudaError_t set_smem_limit_once(const void* func, int bytes, std::atomic<bool> (&done)[kMaxDevices]);
 
 // Status-word bits (the ASTR_KSTATUS_* values of the C header).
-constexpr int kStatusTimeout = 1, kStatusBadInput = 2, kStatusSmem = 4;
+constexpr int kStatusTimeout = 1, kStatusBadInput = 2, kStatusSmem = 4, kStatusRange = 8;
 
 // Decode split kernel: a CTA runs this many independent warp pairs, one key chunk each.
 constexpr int kDecodeChunksPerCta = 4;

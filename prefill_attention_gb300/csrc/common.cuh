@@ -6,6 +6,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -26,6 +27,12 @@ __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
 
 __device__ __forceinline__ uint32_t float2_to_bf16x2_rn(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Two fp32 values to packed fp16 (round to nearest even; |x| > 65504 gives inf), lo in bits 0-15.
+__device__ __forceinline__ uint32_t float2_to_f16x2_rn(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
 }
 

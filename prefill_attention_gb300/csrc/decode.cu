@@ -112,8 +112,11 @@ struct DecCfg {
   static constexpr int KV_IT = BK * CPR / 32;      // cp.async per producer lane per K slot
   static constexpr int NH = (G + 7) / 8;           // 8-wide MMA n-tiles over the query heads
   static constexpr int QROWS = 8 * NH;             // query rows in a slot, zero padded
-  static constexpr int KV_BYTES = BK * D * 2;      // K (or V) part of a slot
-  static constexpr int Q_BYTES = QROWS * D * 2;
+  // rows live in 128-byte-swizzled column blocks of 64 elements; a 32-element row (d = 32)
+  // takes the first half of a block's 128-byte row
+  static constexpr int NCB = (D + 63) / 64;        // column blocks per row
+  static constexpr int KV_BYTES = BK * NCB * 128;  // K (or V) part of a slot
+  static constexpr int Q_BYTES = QROWS * NCB * 128;
   static constexpr int SLOT = 2 * KV_BYTES + Q_BYTES;   // K | V | Q
   static constexpr int STAGES_FIT = (220 * 1024) / (NPAIR * SLOT);
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;  // ring slots per pair
@@ -128,6 +131,7 @@ struct DecCfg {
   static constexpr int MT_D = D / 16;              // 16-row m-tiles over head_dim (O^T = V^T P^T)
   static constexpr int STG_PITCH = D + 4;          // fp32 staging row pitch (conflict-free writes)
   static_assert(G <= 16, "at most 16 query heads per KV head");
+  static_assert(D == 32 || D % 64 == 0, "head_dim 32 or a multiple of 64");
   static_assert(STAGES >= 2, "a ring needs two slots");
   static_assert(SLOT % 1024 == 0 && KV_BYTES % 1024 == 0, "swizzle atoms");
   static_assert((QROWS * STG_PITCH + 2 * QROWS) * 4 <= 2 * KV_BYTES, "piece staging fits in K | V");
@@ -458,7 +462,6 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(
     for (; it.valid(hs); ++i) {
       const int s = i % C::STAGES;
       if (i >= C::STAGES && !wait_or_fail(empty(s), (uint32_t)((i / C::STAGES - 1) & 1), err, p.wait_limit)) break;
-      if constexpr (!CONTIG) bad_input |= my_real && (unsigned)my_id >= nslots;
       const uint32_t kst = ring + s * C::SLOT, vst = kst + C::KV_BYTES, qst = vst + C::KV_BYTES;
       if (it.opens_piece(ls)) {  // first slot of a piece: its G query rows
         const uint16_t* qsrc = p.q + ((size_t)it.b * p.num_qo_heads + (size_t)kvh * G) * D;
@@ -502,6 +505,8 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(
         cp_async16(mask_ring + s * C::MASK_BYTES + 16 * lane, src, in_row);
       }
       cp_async_arrive_noinc(full(s));  // completes once this lane's copies (and older ones) land
+      // (checked here, after the copies are issued: a check before them costs the gather ~0.2 us)
+      if constexpr (!CONTIG) bad_input |= my_real && (unsigned)my_id >= nslots;
       it.next(ind, B, hs);
       my_id = slot_id(it, my_real);
     }
@@ -799,13 +804,15 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
   if (p.kv_indptr != nullptr && S == 1 && !p.combine_all) return;  // written directly by the split kernel
   const size_t base = (size_t)wid * p.part_pitch;
   const float* ml = p.ml_part + base * 2;
-  using VecT = typename std::conditional<VPL == 4, float4, float2>::type;
+  using VecT = typename std::conditional<VPL == 4, float4, typename std::conditional<VPL == 2, float2, float>::type>::type;
   const VecT* o = reinterpret_cast<const VecT*>(p.o_part + base * D) + lane;  // slot s at o[s * 32]
   auto fma_vec = [](float (&a)[VPL], float w, const VecT& v) {
     if constexpr (VPL == 4) {
       a[0] += w * v.x; a[1] += w * v.y; a[2] += w * v.z; a[3] += w * v.w;
-    } else {
+    } else if constexpr (VPL == 2) {
       a[0] += w * v.x; a[1] += w * v.y;
+    } else {
+      a[0] += w * v;
     }
   };
   float acc[VPL];
@@ -868,8 +875,10 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
     pk.x = float2_to_bf16x2_rn(acc[0] * inv, acc[1] * inv);
     pk.y = float2_to_bf16x2_rn(acc[2] * inv, acc[3] * inv);
     *reinterpret_cast<uint2*>(dst) = pk;
-  } else {
+  } else if constexpr (VPL == 2) {
     *reinterpret_cast<uint32_t*>(dst) = float2_to_bf16x2_rn(acc[0] * inv, acc[1] * inv);
+  } else {
+    *dst = (uint16_t)(float2_to_bf16x2_rn(acc[0] * inv, 0.f) & 0xffffu);
   }
 }
 
@@ -899,7 +908,7 @@ cudaError_t launch_split_t(const typename SplitArg<MODE>::type& arg, cudaStream_
 }  // namespace
 
 bool decode_supported(int head_dim, int group) {
-  return (head_dim == 64 || head_dim == 128) &&
+  return (head_dim == 32 || head_dim == 64 || head_dim == 128) &&
          (group == 1 || group == 2 || group == 4 || group == 8 || group == 16);
 }
 
@@ -922,6 +931,7 @@ cudaError_t launch_decode_split(const DecodeParams& p, const DecodeMask* mask, c
   }
   ASTR_DEC_CASE(128, 4) ASTR_DEC_CASE(128, 1) ASTR_DEC_CASE(128, 2) ASTR_DEC_CASE(128, 8) ASTR_DEC_CASE(128, 16)
   ASTR_DEC_CASE(64, 4) ASTR_DEC_CASE(64, 1) ASTR_DEC_CASE(64, 2) ASTR_DEC_CASE(64, 8) ASTR_DEC_CASE(64, 16)
+  ASTR_DEC_CASE(32, 4) ASTR_DEC_CASE(32, 1) ASTR_DEC_CASE(32, 2) ASTR_DEC_CASE(32, 8) ASTR_DEC_CASE(32, 16)
 #undef ASTR_DEC_CASE
   return cudaErrorInvalidValue;
 }
@@ -943,6 +953,7 @@ cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream) {
   cudaError_t e;
   if (p.head_dim == 128) e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<128>, p);
   else if (p.head_dim == 64) e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<64>, p);
+  else if (p.head_dim == 32) e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<32>, p);
   else return cudaErrorInvalidValue;
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -17,8 +17,8 @@
 //     prologue and takes its share in snake order.
 //   * Warp roles (15 warps): 0-7 softmax and epilogue, four per query tile, thread = row =
 //     TMEM lane; 8-9 issue the MMAs, one thread per query tile; 10-13 gather K/V, one warp
-//     per ring stage; 14 loads the query tiles by TMA (a box of BQ positions x G heads x 64
-//     columns is exactly 128 rows of the swizzled operand layout).
+//     per ring stage; 14 loads the query tiles by TMA (a box of BQ positions x G heads x one
+//     column block is exactly 128 rows of the swizzled operand layout).
 //   * S = Q K^T and O += P V run as tcgen05.mma (bf16 in, fp32 accumulate); S is double
 //     buffered and O stays in tensor memory.  A K/V ring stage is refilled once the P V that
 //     read its V (and so the S that read its K) has completed.
@@ -26,11 +26,18 @@
 //     while the current item runs (its second once the current item's first tile is done).
 //     A finished tile's slot then stages its output rows, which leave as 512-byte coalesced
 //     stores; O in tensor memory is released as soon as it is read.
-//   * Softmax: base-2 online softmax with a lazy rescale (O and l rescaled only when a row's
-//     max grows by more than 8), exact because P, l and O share one reference max.
-//   * P stays in tensor memory as two bf16 planes, hi (p truncated to bf16) and lo =
-//     bf16(p - hi); O accumulates P_hi V + P_lo V, which carries p to ~2^-17 relative
-//     instead of bf16's 2^-9, so the only bf16 rounding left is the output's.
+//   * Softmax: base-2 online softmax with a lazy reference max (O and l rescaled only when a
+//     row's max grows by more than 7), exact because P, l and O share one reference.  The row
+//     max is taken only on a row's first visible tile and when the tile's row sum shows that
+//     some p may approach the fp16 limit; otherwise a tile costs one packed FMA, two
+//     exponentials, one packed add and one fp16 pack per pair of scores.
+//   * P V runs in fp16 (P written over S in tensor memory as fp16 pairs; the gather warps turn
+//     each V tile into fp16 in shared memory once it lands): fp16 carries p to 2^-11 relative
+//     against bf16's 2^-8, which keeps P's rounding well inside the output's (a bf16 P pushed
+//     some outputs past a 1e-2 tolerance).  The K/V landing (kv_full) lets S start; the V
+//     conversion completes on its own barrier (v_full) that only P V waits for.  V must lie
+//     within the fp16 range (|v| <= 65504): a value beyond it makes the rows that read it
+//     non-finite, which the epilogue reports in the status word.
 //   * Variants of the same template: the causal rule can be switched off (unified-causal-
 //     offset commit, offset -1) -- each row's key window then ends at seq_len; MASK adds an
 //     explicit 2-D / 3-D mask (prefill-mask commit: causal and mask coexist), read by each
@@ -62,6 +69,14 @@ struct PrefillCfg {
   static constexpr int Q_WARP = KV_WARP0 + STAGES;     // query-tile loads
   static constexpr int THREADS = (Q_WARP + 1) * 32;
   static constexpr int CPR = D / 8;                    // 16-byte chunks per row
+  // operand tiles are K-major rows in swizzled column blocks: 64 elements (128-byte swizzle)
+  // for D >= 64, one block of 32 elements (64-byte swizzle) for D = 32
+  static constexpr int SW_BYTES = D * 2 < 128 ? D * 2 : 128;   // bytes of a row in one column block
+  static constexpr int CB_ELEMS = SW_BYTES / 2;                 // elements per column block
+  static constexpr int NCB = D / CB_ELEMS;                      // column blocks per row
+  static constexpr uint32_t ATOM = 8 * SW_BYTES;                // bytes of one 8-row swizzle atom
+  static constexpr uint32_t SW_MODE = SW_BYTES == 128 ? 2u : 4u;  // descriptor swizzle field
+  static constexpr int KPB = CB_ELEMS / 16;                     // MMA k-steps per column block
   static constexpr int Q_BYTES = M * D * 2;            // one query tile
   static constexpr int KV_BYTES = BN * D * 2;          // one K (or V) tile
   static constexpr int Q_OFF = 0;                      // Q_SLOTS query tiles
@@ -69,8 +84,8 @@ struct PrefillCfg {
   static constexpr int V_OFF = K_OFF + STAGES * KV_BYTES;
   static constexpr int BAR_OFF = V_OFF + STAGES * KV_BYTES;
   // barriers: kv_full, kv_empty [STAGES]; q_full, q_free, o_staged [Q_SLOTS]; s_full, p_full
-  // [NQ][2]; o_done, o_free [NQ]; fin.  Then the error flag and TMEM address.
-  static constexpr int NBAR = 2 * STAGES + 3 * Q_SLOTS + 6 * NQ + 1;
+  // [NQ][2]; o_done, o_free [NQ]; fin; v_full [STAGES].  Then the error flag and TMEM address.
+  static constexpr int NBAR = 2 * STAGES + 3 * Q_SLOTS + 6 * NQ + 1 + STAGES;  // + v_full [STAGES]
   static constexpr int LIST_OFF = (BAR_OFF + NBAR * 8 + 8 + 15) & ~15;
   // this CTA's items in order, as (request, pair within the request, KV head)
   static constexpr int MAX_CTA_ITEMS = 128;
@@ -83,19 +98,33 @@ struct PrefillCfg {
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr int KV_IT = BN * CPR / 32;          // cp.async per producer lane per K (or V) tile
   static constexpr uint32_t IDESC_S = tc::idesc_bf16_f32(M, BN, false, false);   // K-major A and B
-  static constexpr uint32_t IDESC_PV = tc::idesc_bf16_f32(M, D, false, true);    // B (V) MN-major
-  static constexpr float kRescaleThreshold = 8.f;     // log2 units
+  static constexpr uint32_t IDESC_PV = tc::idesc_f16_f32(M, D, false, true);     // fp16 P and V, V MN-major
+  // P = 2^(sm_scale s - m + kPOffset) in fp16: the running reference m moves up when a row's
+  // tile max exceeds it by more than kRescaleThreshold, so p <= 2^15 (< 65504) after a max pass;
+  // without one, a tile row sum of at most kPSumLimit bounds every p the same way
+  static constexpr float kPOffset = 8.f;               // log2 units
+  static constexpr float kRescaleThreshold = 7.f;      // log2 units
+  static constexpr float kPSumLimit = 32768.f;
   static_assert((Q_OFF | K_OFF | V_OFF | Q_BYTES | KV_BYTES) % 1024 == 0, "swizzle atoms must be 1024-byte aligned");
   static_assert(D + 2 * BN <= (int)TMEM_TILE, "tensor-memory budget per tile");
-  static_assert(KV_IT * 32 == BN * CPR && D % 64 == 0, "whole warp iterations, whole 128-byte column blocks");
-  static_assert((MAX_SORT_REQS + 1 + SORT_BUCKETS) * 4 + MAX_SORT_PAIRS * 4 <= 2 * STAGES * KV_BYTES, "prologue scratch");
+  static_assert(KV_IT * 32 == BN * CPR && (D == 32 || D % 64 == 0), "whole warp iterations, whole column blocks");
+  static_assert((MAX_SORT_REQS + 1 + SORT_BUCKETS) * 4 + MAX_SORT_PAIRS * 4 <= Q_SLOTS * Q_BYTES + 2 * STAGES * KV_BYTES,
+                "prologue scratch");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
-// Byte offset of 16-byte chunk c of row r in a 128-byte-swizzled K-major tile whose
-// 64-element column blocks each hold `rows` rows.
-__device__ __forceinline__ uint32_t sw128(int r, int c, int rows) {
-  return (uint32_t)((c >> 3) * rows * 128 + (r >> 3) * 1024 + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4));
+// Byte offset of 16-byte chunk c of row r in a swizzled K-major tile whose column blocks each
+// hold `rows` rows: 128-byte swizzle (SWB = 128: 64-element blocks, chunk c & 7 of a 128-byte
+// row at (c ^ r) & 7) or 64-byte swizzle (SWB = 64: one 32-element block, chunk c of a 64-byte
+// row at c ^ ((r >> 1) & 3)), the layouts the TMA boxes and the MMA descriptors use.
+template <int SWB>
+__device__ __forceinline__ uint32_t swz(int r, int c, int rows) {
+  if constexpr (SWB == 128) {
+    return (uint32_t)((c >> 3) * rows * 128 + (r >> 3) * 1024 + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4));
+  } else {
+    static_assert(SWB == 64, "64- or 128-byte swizzle");
+    return (uint32_t)((r >> 3) * 512 + (r & 7) * 64 + (((c & 3) ^ ((r >> 1) & 3)) << 4));
+  }
 }
 
 // Packed fp32 pairs (f32x2 arithmetic on sm_100-family SMs) and three-input max / min.
@@ -276,6 +305,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
   auto o_done = [&](int t) { return tb + 8u * (4 * C::NQ + t); };
   auto o_free = [&](int t) { return tb + 8u * (5 * C::NQ + t); };
   const uint32_t fin = tb + 8u * (6 * C::NQ);
+  // V of stage s turned into fp16 (the K/V landing itself is kv_full)
+  auto v_full = [&](int s) { return fin + 8u + 8u * s; };
   volatile int* err = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 8 * C::NBAR);
   const uint32_t slot = sbase + C::BAR_OFF + 8 * C::NBAR + 4;
   if (tid == 0) {
@@ -297,6 +328,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
       tc::mbar_init(o_free(t), 128);
     }
     tc::mbar_init(fin, C::NQ);
+    for (int s = 0; s < C::STAGES; ++s) tc::mbar_init(v_full(s), 32);
     *err = 0;
     tc::fence_mbarrier_init();
   }
@@ -316,7 +348,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
   // cost the same and have consecutive indices, so the pairs are sorted and then expanded.
   // Each CTA keeps only its own list; problems too large for it use the natural order.
   int* list = reinterpret_cast<int*>(smem + C::LIST_OFF);
-  int* pst = reinterpret_cast<int*>(smem + C::K_OFF);  // scratch: the K/V ring is not in use yet
+  int* pst = reinterpret_cast<int*>(smem + C::Q_OFF);  // scratch: the query and K/V rings are not in use yet
   int* cnt = pst + C::MAX_SORT_REQS + 1;
   uint16_t* key = reinterpret_cast<uint16_t*>(cnt + C::SORT_BUCKETS);
   uint16_t* order = key + C::MAX_SORT_PAIRS;
@@ -451,7 +483,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
     const uint64_t once = tc::l2_evict_first_policy();
     // where each slot's tile goes (lane k holds slot k): first position, first head, rows
     int pend_pos = 0, pend_head = 0, pend_rows = 0;
-    // write tile v's staged rows out: one TMA store per 64-column block when all BQ positions
+    // write tile v's staged rows out: one TMA store per column block when all BQ positions
     // are the request's, else the valid rows with coalesced stores (never past the request)
     auto write_out = [&](int v) {
       if (!(ok = wait_or_fail(o_staged(v), q_par(v)))) return;
@@ -461,8 +493,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
       const uint32_t src = q_slot(v);
       if (rows == C::M) {
         if (lane == 0) {
-          for (int cb = 0; cb < D / 64; ++cb)
-            tc::tma_store_3d_hint(&o_map, src + cb * (C::M * 128), cb * 64, head, pos, once);
+          for (int cb = 0; cb < C::NCB; ++cb)
+            tc::tma_store_3d_hint(&o_map, src + cb * (C::M * C::SW_BYTES), cb * C::CB_ELEMS, head, pos, once);
           tc::bulk_commit();
           tc::bulk_wait_read_all();  // the slot may be refilled once the stores have read it
         }
@@ -471,7 +503,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
         for (int i = 0; i < C::M * C::CPR / 32; ++i) {
           const int flat = i * 32 + lane, r = flat / C::CPR, c = flat % C::CPR;
           if (r < rows) {
-            const uint4 x = lds128(src + sw128(r, c, C::M));
+            const uint4 x = lds128(src + swz<C::SW_BYTES>(r, c, C::M));
             *reinterpret_cast<uint4*>(obase + ((size_t)(r / G) * p.num_qo_heads + r % G) * D + c * 8) = x;
           }
         }
@@ -495,9 +527,9 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
         }
         if (lane == 0) {
           tc::mbar_arrive_expect_tx(q_full(u), (uint32_t)C::Q_BYTES);
-          for (int cb = 0; cb < D / 64; ++cb)
-            tc::tma_load_3d_hint(q_slot(u) + cb * (C::M * 128), &q_map, cb * 64, it.kvh * G, it.q0 + qf, q_full(u),
-                                 once);
+          for (int cb = 0; cb < C::NCB; ++cb)
+            tc::tma_load_3d_hint(q_slot(u) + cb * (C::M * C::SW_BYTES), &q_map, cb * C::CB_ELEMS, it.kvh * G,
+                                 it.q0 + qf, q_full(u), once);
         }
         __syncwarp();
       }
@@ -563,7 +595,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
             valid = (unsigned)id < nslots;
             off = valid ? (size_t)id * head_stride + (size_t)kvh * D + c * 8 : 0;
           }
-          const uint32_t o = sw128(key, c, C::BN);
+          const uint32_t o = swz<C::SW_BYTES>(key, c, C::BN);
           cp_async16(kdst + o, p.k_pool + off, valid);
           cp_async16(vdst + o, p.v_pool + off, valid);
         }
@@ -581,12 +613,28 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
         id1 = ids_of(j + C::STAGES, 1, real1);
         cp_async_wait<0>();
         tc::fence_proxy_async_smem();  // the tensor core reads the tiles through the async proxy
-        tc::mbar_arrive(kv_full(st));
+        tc::mbar_arrive(kv_full(st));  // K landed: S may start
+        // P V runs in fp16: each lane turns the V chunks it copied into fp16 in place, same layout
+#pragma unroll 4
+        for (int i = 0; i < C::KV_IT; ++i) {
+          const int flat = i * 32 + lane;
+          const uint32_t a = vdst + swz<C::SW_BYTES>(flat / C::CPR, flat % C::CPR, C::BN);
+          uint4 x = lds128(a);
+          float2 f;
+          f = bf16x2_to_float2(x.x); x.x = float2_to_f16x2_rn(f.x, f.y);
+          f = bf16x2_to_float2(x.y); x.y = float2_to_f16x2_rn(f.x, f.y);
+          f = bf16x2_to_float2(x.z); x.z = float2_to_f16x2_rn(f.x, f.y);
+          f = bf16x2_to_float2(x.w); x.w = float2_to_f16x2_rn(f.x, f.y);
+          sts128(a, x);
+        }
+        tc::fence_proxy_async_smem();
+        tc::mbar_arrive(v_full(st));
       }
       g_base += it.n_tiles;
     }
     cp_async_wait<0>();
     if (p.status != nullptr && __any_sync(kFullMask, bad_input) && lane == 0) atomicOr(p.status, kStatusBadInput);
+
   } else if (warp >= C::MMA_WARP) {
     // ======================= MMA issue: warp MMA_WARP + t, lane 0 alone, for query tile t.
     // tcgen05.mma issue runs nearly in step with execution, so whatever the issuing thread
@@ -599,9 +647,9 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
     // count two arrivals per phase.
     const int t = warp - C::MMA_WARP;
     // descriptor halves of query slot 0, K stage 0 (K-major) and V stage 0 (MN-major)
-    const uint64_t qd0 = tc::smem_desc_sw128(sbase + C::Q_OFF, 16, 1024);
-    const uint64_t kd0 = tc::smem_desc_sw128(sbase + C::K_OFF, 16, 1024);
-    const uint64_t vd0 = tc::smem_desc_sw128(sbase + C::V_OFF, C::BN * 128, 1024);
+    const uint64_t qd0 = tc::smem_desc_swz(sbase + C::Q_OFF, 16, C::ATOM, C::SW_MODE);
+    const uint64_t kd0 = tc::smem_desc_swz(sbase + C::K_OFF, 16, C::ATOM, C::SW_MODE);
+    const uint64_t vd0 = tc::smem_desc_swz(sbase + C::V_OFF, C::BN * C::SW_BYTES, C::ATOM, C::SW_MODE);
     const uint32_t q_hi = (uint32_t)(qd0 >> 32), k_hi = (uint32_t)(kd0 >> 32), v_hi = (uint32_t)(vd0 >> 32);
     const uint32_t k_lo = (uint32_t)kd0, v_lo = (uint32_t)vd0;
     const uint32_t od = tmem + t * C::TMEM_TILE;  // O of tile t; S / P buffers at od + D + {0, BN}
@@ -641,8 +689,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
           uint32_t al[D / 16], bl[D / 16];
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            al[kk] = q_lo + (uint32_t)(((kk >> 2) * (C::M * 128) + (kk & 3) * 32) >> 4);
-            bl[kk] = klo + (uint32_t)(((kk >> 2) * (C::BN * 128) + (kk & 3) * 32) >> 4);
+            al[kk] = q_lo + (uint32_t)(((kk / C::KPB) * (C::M * C::SW_BYTES) + (kk % C::KPB) * 32) >> 4);
+            bl[kk] = klo + (uint32_t)(((kk / C::KPB) * (C::BN * C::SW_BYTES) + (kk % C::KPB) * 32) >> 4);
           }
           keep_regs(al);
           keep_regs(bl);
@@ -657,18 +705,17 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
         };
         auto issue_pv = [&](int j, uint32_t nb, uint32_t np) -> bool {
           if (!ok) return false;  // a wait gave up: issue nothing more
-          const uint32_t pa = od + D + sbuf(j) * C::BN;  // P hi in [0, 32), lo in [32, 64)
+          const uint32_t pa = od + D + sbuf(j) * C::BN;  // P (fp16 pairs) in columns [0, 32)
           const uint32_t vlo = v_lo + (uint32_t)((stage(j) * C::KV_BYTES) >> 4);
           uint32_t bl[C::BN / 16];
 #pragma unroll
-          for (int kk = 0; kk < C::BN / 16; ++kk) bl[kk] = vlo + (uint32_t)((kk * 16 * 128) >> 4);
+          for (int kk = 0; kk < C::BN / 16; ++kk) bl[kk] = vlo + (uint32_t)((kk * 16 * C::SW_BYTES) >> 4);
           keep_regs(bl);
           const uint32_t acc0 = j > 0 ? 1u : 0u;
           bool r = false;
 #pragma unroll
           for (int kk = 0; kk < C::BN / 16; ++kk) {
             mma_ts_h(od, pa + kk * 8, bl[kk], v_hi, C::IDESC_PV, kk > 0 ? 1u : acc0);
-            mma_ts_h(od, pa + C::BN / 2 + kk * 8, bl[kk], v_hi, C::IDESC_PV, 1u);
             if (kk == 1) r = nb != 0u && tc::mbar_test(nb, np);
           }
           tc::mma_commit(kv_empty(stage(j)));  // the stage may be refilled once P V_j is done
@@ -698,6 +745,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
             // O_t += P_t(j) V_j (the item's first P V overwrites O once the epilogue of the
             // item before has read it)
             if (j == 0 && n_used > 0) wait_one(o_free(t), (uint32_t)((n_used - 1) & 1), false);
+            wait_one(v_full(stage(j)), kv_par(j), false);
             wait_one(p_full(t, sbuf(j)), s_par(j), ready);
             ready = issue_pv(j, j + 2 < nk ? kv_full(stage(j + 2)) : 0u, kv_par(j + 2));
           } else {
@@ -777,9 +825,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
             for (int c = 0; c < 32; ++c) s[half * 32 + c] = __uint_as_float(raw[c]);
           }
         }
-        // row max of sm_scale * s in base-2 units: max (or min for a negative scale) of the raw
-        // scores times the scale; on tiles that cross the causal edge, keys past this row's
-        // limit are set to the extreme that the max / min ignores, and get p = 0 below
+        // Keys past this row's limit (tiles that cross the causal edge) or hidden by the explicit
+        // mask are set to the extreme that the row max / min ignores, and get p = 0 below.
         const bool masked = has_mask || j >= mask_from;
         const int j0 = j * C::BN;
         const float skip = pos_scale ? -CUDART_INF_F : CUDART_INF_F;
@@ -795,55 +842,60 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
 #pragma unroll
           for (int c = 0; c < C::BN; ++c) s[c] = (j0 + c <= limit) ? s[c] : skip;
         }
-        float e4[4];
+        // P = 2^(sm_scale s - m_run + kPOffset) as fp16 pairs (P V runs in fp16: 11 significant
+        // bits, so the only rounding that matters is the output's).  The row max (min for a
+        // negative scale) is taken only on a row's first visible tile and when the tile's row
+        // sum exceeds kPSumLimit (then some p may be near the fp16 limit): the reference moves
+        // up, O and l are rescaled, and P is recomputed.
+        bool do_max = __any_sync(kFullMask, m_run == -CUDART_INF_F);
+        uint32_t ph[C::BN / 2];
+        float lsum = 0.f;
+        for (;;) {
+          if (do_max) {
+            float e4[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {  // four independent 3-input chains over 16 scores each
-          float e = skip;
+            for (int q = 0; q < 4; ++q) {  // four independent 3-input chains over 16 scores each
+              float e = skip;
 #pragma unroll
-          for (int c = q * 16; c < q * 16 + 16; c += 2)
-            e = pos_scale ? max3(e, s[c], s[c + 1]) : min3(e, s[c], s[c + 1]);
-          e4[q] = e;
-        }
-        const float ext = pos_scale ? max3(max3(e4[0], e4[1], e4[2]), e4[3], skip)
-                                    : min3(min3(e4[0], e4[1], e4[2]), e4[3], skip);
-        const bool none = has_mask ? vb == 0ull : j0 > limit;
-        const float m_tile = none ? -CUDART_INF_F : ext * scale;  // -inf: no visible key
-        const bool need = m_tile > m_run + C::kRescaleThreshold;  // true on the first visible tile
-        if (__any_sync(kFullMask, need)) {
-          const float alpha = need ? fast_exp2(m_run - m_tile) : 1.f;  // 0 while m_run = -inf
-          if (j > 0) {
-            // O holds P V of KV tiles < j once P V_{j-1} completes; the issuing thread commits
-            // that KV tile's empty barrier right after it, so wait for that phase (rare: only
-            // when the row max grows by more than the threshold)
-            const int gp = g_base + j - 1;
-            if (!(ok = wait_or_fail(kv_empty(gp % C::STAGES), (uint32_t)((gp / C::STAGES) & 1)))) break;
-            tc::fence_after_sync();
+              for (int c = q * 16; c < q * 16 + 16; c += 2)
+                e = pos_scale ? max3(e, s[c], s[c + 1]) : min3(e, s[c], s[c + 1]);
+              e4[q] = e;
+            }
+            const float ext = pos_scale ? max3(max3(e4[0], e4[1], e4[2]), e4[3], skip)
+                                        : min3(min3(e4[0], e4[1], e4[2]), e4[3], skip);
+            const bool none = has_mask ? vb == 0ull : j0 > limit;
+            const float m_tile = none ? -CUDART_INF_F : ext * scale;  // -inf: no visible key
+            const bool need = m_tile > m_run + C::kRescaleThreshold;  // true on the first visible tile
+            if (__any_sync(kFullMask, need)) {
+              const float alpha = need ? fast_exp2(m_run - m_tile) : 1.f;  // 0 while m_run = -inf
+              if (j > 0) {
+                // O holds P V of KV tiles < j once P V_{j-1} completes; the issuing thread commits
+                // that KV tile's empty barrier right after it, so wait for that phase (rare: only
+                // when the row max grows past the threshold)
+                const int gp = g_base + j - 1;
+                if (!(ok = wait_or_fail(kv_empty(gp % C::STAGES), (uint32_t)((gp / C::STAGES) & 1)))) break;
+                tc::fence_after_sync();
 #pragma unroll 1
-            for (int cc = 0; cc < D / 16; ++cc) {
-              uint32_t o[16];
-              tc::tmem_ld16(o_col + cc * 16, o);
-              tc::tmem_ld_wait();
+                for (int cc = 0; cc < D / 16; ++cc) {
+                  uint32_t o[16];
+                  tc::tmem_ld16(o_col + cc * 16, o);
+                  tc::tmem_ld_wait();
 #pragma unroll
-              for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-              tc::tmem_st16(o_col + cc * 16, o);
+                  for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                  tc::tmem_st16(o_col + cc * 16, o);
+                }
+              }
+              l_run *= alpha;
+              if (need) m_run = m_tile;
             }
           }
-          l_run *= alpha;
-          if (need) m_run = m_tile;
-        }
-        // P = 2^(scale s - m) as bf16 hi / lo planes in the S columns just read: hi = p with its
-        // low 16 bits cleared (exactly a bf16), lo = bf16(p - hi), so p = hi + lo to ~2^-17
-        // relative; P V then runs as two MMAs and P is not rounded to bf16.  Pairs of scores
-        // go through packed fp32x2 arithmetic.
-        const float neg_m = (m_run == -CUDART_INF_F) ? 0.f : -m_run;
-        const uint64_t sc2 = pk2(scale, scale), nm2 = pk2(neg_m, neg_m), minus1 = pk2(-1.f, -1.f);
-        uint64_t lsum2 = pk2(0.f, 0.f);
+          // pairs of scores through packed fp32x2 arithmetic
+          const float neg_m = (m_run == -CUDART_INF_F) ? 0.f : C::kPOffset - m_run;
+          const uint64_t sc2 = pk2(scale, scale), nm2 = pk2(neg_m, neg_m);
+          uint64_t lsum2 = pk2(0.f, 0.f);
 #pragma unroll
-        for (int half = 0; half < C::BN / 32; ++half) {
-          uint32_t ph[16], pl[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int c0 = half * 32 + 2 * e;
+          for (int e = 0; e < C::BN / 2; ++e) {
+            const int c0 = 2 * e;
             float x0, x1;
             upk2(fma2(pk2(s[c0], s[c0 + 1]), sc2, nm2), x0, x1);
             float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
@@ -854,21 +906,18 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
               p0 = (j0 + c0 <= limit) ? p0 : 0.f;
               p1 = (j0 + c0 + 1 <= limit) ? p1 : 0.f;
             }
-            const uint64_t p2 = pk2(p0, p1);
-            lsum2 = add2(lsum2, p2);
-            const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
-            ph[e] = __byte_perm(b0, b1, 0x7632);  // upper halves: truncated bf16 of p0 (low), p1 (high)
-            float l0, l1;
-            upk2(fma2(pk2(__uint_as_float(b0 & 0xffff0000u), __uint_as_float(b1 & 0xffff0000u)), minus1, p2), l0, l1);
-            pl[e] = float2_to_bf16x2_rn(l0, l1);
+            lsum2 = add2(lsum2, pk2(p0, p1));
+            ph[e] = float2_to_f16x2_rn(p0, p1);
           }
-          tc::tmem_st16(sb + half * 16, ph);
-          tc::tmem_st16(sb + C::BN / 2 + half * 16, pl);
+          float ls0, ls1;
+          upk2(lsum2, ls0, ls1);
+          lsum = ls0 + ls1;
+          if (do_max || !__any_sync(kFullMask, lsum > C::kPSumLimit)) break;
+          do_max = true;
         }
-        float ls0, ls1;
-        upk2(lsum2, ls0, ls1);
-        const float lsum = ls0 + ls1;
+        if (!ok) break;
         l_run += lsum;
+        tc::tmem_st32(sb, ph);  // P over the S columns just read (fp16 pairs: 32 columns)
         tc::tmem_st_wait();
         tc::fence_before_sync();
         tc::mbar_arrive(p_full(t, gb & 1));
@@ -884,11 +933,14 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
       // a timed-out wait poisons the tile; a row with no visible key (explicit mask) is zero
       const float inv = (ok && !*err) ? (l_run > 0.f ? 1.f / l_run : 0.f) : CUDART_NAN_F;
       const uint32_t stg = q_slot(u);
+      bool nonfinite = false;
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
         tc::tmem_ld32(o_col + cc * 32, o);
         tc::tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) nonfinite |= !(fabsf(__uint_as_float(o[c])) <= 3.4e38f);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           uint4 v;
@@ -896,9 +948,11 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
           v.y = float2_to_bf16x2_rn(__uint_as_float(o[q4 * 8 + 2]) * inv, __uint_as_float(o[q4 * 8 + 3]) * inv);
           v.z = float2_to_bf16x2_rn(__uint_as_float(o[q4 * 8 + 4]) * inv, __uint_as_float(o[q4 * 8 + 5]) * inv);
           v.w = float2_to_bf16x2_rn(__uint_as_float(o[q4 * 8 + 6]) * inv, __uint_as_float(o[q4 * 8 + 7]) * inv);
-          sts128(stg + sw128(row, cc * 4 + q4, C::M), v);
+          sts128(stg + swz<C::SW_BYTES>(row, cc * 4 + q4, C::M), v);
         }
       }
+      if (ok && !*err && p.status != nullptr && __any_sync(kFullMask, nonfinite) && lane == 0)
+        atomicOr(p.status, kStatusRange);
       tc::fence_before_sync();
       tc::mbar_arrive(o_free(t));    // O of this tile may be overwritten by the next item
       tc::fence_proxy_async_smem();  // the staged rows are read by TMA stores (async proxy)
@@ -944,20 +998,22 @@ cudaError_t launch_prefill_t(const PrefillParams& p, cudaStream_t stream) {
   const int64_t items = (int64_t)p.num_q_tiles * p.num_kv_heads;
   const int grid = (int)(items < p.num_ctas ? items : p.num_ctas);
   if (grid <= 0) return cudaSuccess;
-  // q as [total_q][Hq][D] bf16; one box = BQ positions x the G heads of a KV head x 64 columns
+  // q as [total_q][Hq][D] bf16; one box = BQ positions x the G heads of a KV head x one column
+  // block (64 columns with 128-byte swizzle; 32 with 64-byte swizzle for D = 32)
   const PFN_cuTensorMapEncodeTiled_v12000 encode = encode_tiled();
   if (encode == nullptr) return cudaErrorNotSupported;
   // (out has the same layout; its map writes whole tiles of one request)
   CUtensorMap q_map, o_map;
   const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.num_qo_heads, (cuuint64_t)p.total_q};
   const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)p.num_qo_heads * D * 2};
-  const cuuint32_t box[3] = {64u, (cuuint32_t)G, (cuuint32_t)C::BQ};
+  const cuuint32_t box[3] = {(cuuint32_t)C::CB_ELEMS, (cuuint32_t)G, (cuuint32_t)C::BQ};
+  const CUtensorMapSwizzle swz_mode = C::SW_BYTES == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   const cuuint32_t elem_strides[3] = {1u, 1u, 1u};
   if (encode(&q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(p.q), dims, strides, box,
-             elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, swz_mode,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
       encode(&o_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.out, dims, strides, box, elem_strides,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swz_mode, CU_TENSOR_MAP_L2_PROMOTION_NONE,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   prefill_kernel<D, G, MASK, CONTIG><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(p, q_map, o_map);
@@ -971,6 +1027,7 @@ cudaError_t dispatch_prefill(const PrefillParams& p, cudaStream_t stream) {
   if (p.head_dim == DD && G == GG) return launch_prefill_t<DD, GG, MASK, CONTIG>(p, stream);
   ASTR_PF_CASE(128, 4) ASTR_PF_CASE(128, 1) ASTR_PF_CASE(128, 2) ASTR_PF_CASE(128, 8) ASTR_PF_CASE(128, 16)
   ASTR_PF_CASE(64, 4) ASTR_PF_CASE(64, 1) ASTR_PF_CASE(64, 2) ASTR_PF_CASE(64, 8) ASTR_PF_CASE(64, 16)
+  ASTR_PF_CASE(32, 4) ASTR_PF_CASE(32, 1) ASTR_PF_CASE(32, 2) ASTR_PF_CASE(32, 8) ASTR_PF_CASE(32, 16)
 #undef ASTR_PF_CASE
   return cudaErrorInvalidValue;
 }
@@ -993,7 +1050,8 @@ cudaError_t launch_prefill_contig(const PrefillParams& p, cudaStream_t stream) {
 int prefill_rows_per_cta() { return 256; }
 
 bool prefill_supported(int head_dim, int group) {
-  return (head_dim == 64 || head_dim == 128) && (group == 1 || group == 2 || group == 4 || group == 8 || group == 16);
+  return (head_dim == 32 || head_dim == 64 || head_dim == 128) &&
+         (group == 1 || group == 2 || group == 4 || group == 8 || group == 16);
 }
 
 cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream) {

@@ -78,11 +78,3 @@ def run_prefill(w, t=None, stream=None):
                                 w.sm_scale, stream=stream)
     torch.cuda.synchronize()
     return out
-
-
-def sample_rows(rng, n_rows, n_heads, k):
-    """k distinct (row, head) pairs plus the first and last row, for oracle sampling."""
-    rows = rng.integers(0, n_rows, size=k)
-    heads = rng.integers(0, n_heads, size=k)
-    extra = np.array([[0, 0], [n_rows - 1, n_heads - 1]])
-    return np.concatenate([np.stack([rows, heads], 1), extra]).astype(np.int32)
