@@ -6,7 +6,9 @@ page_size=1 random slot table, bf16 -- reported as K+V bytes read per second (GB
 microseconds per call and the fraction of the measured HBM copy bandwidth.  A step is
 one decode call (split kernel + combine kernel) through the C ABI on inputs already in
 HBM.  L2 is defeated by rotating through several copies of the KV pools (working set
-well above the 126 MB L2), so every call reads its keys from DRAM.  The timed region of
+well above the 126 MB L2), so every call reads its keys from DRAM.  Each timed region
+starts with the GPU busy (a short spin kernel queued before the start event), so the host's
+latency to launch the first call is not counted; the e2e object counts everything.  The timed region of
 `--steps` calls runs `--repeats` times (each between a barrier and a synchronize); the
 line reports the median region and the spread of all of them.
 
@@ -64,6 +66,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 POOL_COPIES = 4          # rotate KV-pool copies so each call's working set is cold in L2
                          # (fewer when one pool alone is several times the L2)
 MAX_SPLITS = 64
+SPIN_CYCLES = 1_000_000  # GPU clock cycles of the pre-region spin (~0.5 ms at 2 GHz)
 
 
 def load_peaks():
@@ -360,6 +363,11 @@ def main():
     def timed(fn, n):
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
+            # a ~0.5 ms spin before the start event keeps the GPU busy while the host queues the
+            # first calls, so the region times the calls back to back rather than the host's
+            # launch of the first one (outside the region; not one of this library's kernels)
+            if hasattr(torch.cuda, "_sleep"):
+                torch.cuda._sleep(SPIN_CYCLES)
             ev0.record(stream)
             for i in range(n):
                 fn(i)
