@@ -280,6 +280,53 @@ int astr_attn_prefill_contiguous(const uint16_t* q, const int32_t* qo_indptr, co
                                  const astr_attn_dims* dims, float sm_scale, void* stream);
 
 /*
+ * Query and output addressed by strides (P3, stride-addressing and layout commits: Q, KV and O
+ * addressed through strides, so "bhld" / "blhd" tensors work without copies).  Host struct
+ * read during the call only.  Strides are in elements, non-negative multiples of 8 (16-byte
+ * rows); head_dim is contiguous.  Element e of query head h in request-local query row i of
+ * request b sits at
+ *   q_batch_stride == 0 (rows packed flat):  q[(r0_b + i) * q_token_stride + h * q_head_stride + e],
+ *                                            r0_b = qo_indptr[b] for prefill, b for decode;
+ *   q_batch_stride  > 0 (rows padded per request):
+ *                                            q[b * q_batch_stride + i * q_token_stride + h * q_head_stride + e],
+ * and the output element likewise with the o_* strides.  Decode has one row per request (i = 0).
+ *   packed [rows, Hq, d]:        {0, Hq*d, d} (the layout of the entry points above)
+ *   padded bhld [B, Hq, L, d]:   {Hq*L*d, d, L*d}        padded blhd [B, L, Hq, d]: {L*Hq*d, Hq*d, d}
+ * A padded prefill tensor holds at least dims->max_q_len positions per request.
+ */
+typedef struct astr_attn_qo_layout {
+  int64_t q_batch_stride, q_token_stride, q_head_stride;
+  int64_t o_batch_stride, o_token_stride, o_head_stride;
+} astr_attn_qo_layout;
+
+/*
+ * Decode with every layout choice at once: K/V from the paged pool through req_to_token
+ * (kv_layout NULL) or from a contiguous cache (kv_layout given; req_to_token not read), query
+ * and output by the strides of qo_layout (NULL: packed [B, Hq, d]), an optional explicit mask
+ * (NULL: none).  The same computation, schedule, partial layout, rules and errors as
+ * astr_attn_paged_decode / _masked / astr_attn_decode_contiguous, plus INVALID_ARG for
+ * negative strides and MISALIGNED for strides that are not multiples of 8.
+ */
+int astr_attn_decode_strided(const uint16_t* q, const uint16_t* k, const uint16_t* v, const int32_t* req_to_token,
+                             const astr_attn_kv_layout* kv_layout, const astr_attn_qo_layout* qo_layout,
+                             const int32_t* seq_lens, const int32_t* kv_indptr, const astr_attn_mask* mask,
+                             float* o_part, float* ml_part, uint16_t* out, const astr_attn_dims* dims, float sm_scale,
+                             void* stream);
+
+/*
+ * Ragged prefill with every layout choice at once (as astr_attn_decode_strided): K/V paged or
+ * contiguous, query rows and outputs by the strides of qo_layout (NULL: packed [total_q, Hq, d];
+ * padded tensors are addressed by (request, local row), packed ones by qo_indptr[b] + row),
+ * optional mask and causal switch.  qo_indptr always gives each request's q_len.  Only the rows
+ * of each request's q_len are written.  Errors as astr_attn_decode_strided.
+ */
+int astr_attn_prefill_strided(const uint16_t* q, const int32_t* qo_indptr, const uint16_t* k, const uint16_t* v,
+                              const int32_t* req_to_token, const astr_attn_kv_layout* kv_layout,
+                              const astr_attn_qo_layout* qo_layout, const int32_t* seq_lens, const int32_t* kv_indptr,
+                              const astr_attn_mask* mask, uint16_t* out, const astr_attn_dims* dims, float sm_scale,
+                              void* stream);
+
+/*
  * Paged decode that allocates nothing (no counterpart in the source pages; this is a
  * service of this library).  Same computation, arguments, rules and errors as
  * astr_attn_paged_decode minus o_part / ml_part: the split-KV partials go to a 16 MiB

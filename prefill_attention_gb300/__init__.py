@@ -20,8 +20,8 @@ __all__ = [
     "astr_attn_paged_decode", "astr_attn_decode_split", "astr_attn_decode_combine", "astr_attn_prefill_ragged",
     "astr_attn_paged_decode_noalloc", "astr_attn_kv_append", "astr_attn_paged_decode_masked",
     "astr_attn_prefill_ragged_masked", "Mask", "make_mask", "KvLayout", "make_kv_layout",
-    "astr_attn_decode_contiguous", "astr_attn_prefill_contiguous",
-    "astr_attn_decode_num_splits", "astr_attn_decode_workspace_bytes", "astr_attn_status_string",
+    "astr_attn_decode_contiguous", "astr_attn_prefill_contiguous", "QoLayout", "make_qo_layout",
+    "astr_attn_decode_strided", "astr_attn_prefill_strided", "astr_attn_decode_num_splits", "astr_attn_decode_workspace_bytes", "astr_attn_status_string",
     "astr_attn_version", "alloc_decode_workspace",
     "ASTR_OK", "ASTR_ERR_INVALID_ARG", "ASTR_ERR_UNSUPPORTED", "ASTR_ERR_MISALIGNED",
     "ASTR_ERR_WORKSPACE_TOO_SMALL", "ASTR_ERR_LAUNCH_FAILED", "ASTR_ERR_DEVICE", "EXPORTED_SYMBOLS",
@@ -51,7 +51,7 @@ EXPORTED_SYMBOLS = [
     "astr_attn_decode_combine", "astr_attn_prefill_ragged", "astr_attn_status_string", "astr_attn_version",
     "astr_attn_decode_split", "astr_attn_paged_decode_noalloc", "astr_attn_kv_append",
     "astr_attn_paged_decode_masked", "astr_attn_prefill_ragged_masked", "astr_attn_decode_contiguous",
-    "astr_attn_prefill_contiguous",
+    "astr_attn_prefill_contiguous", "astr_attn_decode_strided", "astr_attn_prefill_strided",
 ]
 
 
@@ -105,6 +105,25 @@ def make_kv_layout(cache) -> KvLayout:
     return KvLayout(sb, sl, sh)
 
 
+class QoLayout(ctypes.Structure):
+    """Mirror of ``astr_attn_qo_layout`` (strides in elements; see include/astr_attn.h)."""
+    _fields_ = [("q_batch_stride", ctypes.c_int64), ("q_token_stride", ctypes.c_int64),
+                ("q_head_stride", ctypes.c_int64), ("o_batch_stride", ctypes.c_int64),
+                ("o_token_stride", ctypes.c_int64), ("o_head_stride", ctypes.c_int64)]
+
+
+def make_qo_layout(q, out, padded: bool) -> QoLayout:
+    """Strides of query / output tensors given with logical dims [rows, Hq, d] (packed; padded
+    = False) or [B, L, Hq, d] (padded per request; a "bhld" tensor as ``t.transpose(1, 2)``),
+    read from the tensors themselves (no copy)."""
+    def strides(t):
+        st = [int(x) for x in t.stride()]
+        if st[-1] != 1:
+            raise ValueError("head_dim must be the contiguous dimension")
+        return (st[0], st[1], st[2]) if padded else (0, st[0], st[1])
+    return QoLayout(*strides(q), *strides(out))
+
+
 def lib_path() -> str:
     return _LIB_PATH
 
@@ -135,13 +154,17 @@ def load():
     LY = ctypes.POINTER(KvLayout)
     lib.astr_attn_decode_contiguous.argtypes = [P, P, P, LY, P, P, M, P, P, P, D, F, P]
     lib.astr_attn_prefill_contiguous.argtypes = [P, P, P, P, LY, P, P, M, P, D, F, P]
+    QL = ctypes.POINTER(QoLayout)
+    lib.astr_attn_decode_strided.argtypes = [P, P, P, P, LY, QL, P, P, M, P, P, P, D, F, P]
+    lib.astr_attn_prefill_strided.argtypes = [P, P, P, P, P, LY, QL, P, P, M, P, D, F, P]
     lib.astr_attn_status_string.argtypes = [I32]
     lib.astr_attn_status_string.restype = ctypes.c_char_p
     lib.astr_attn_version.argtypes = []
     for f in ("astr_attn_decode_num_splits", "astr_attn_decode_workspace_bytes", "astr_attn_paged_decode",
               "astr_attn_decode_split", "astr_attn_decode_combine", "astr_attn_prefill_ragged", "astr_attn_version",
               "astr_attn_paged_decode_noalloc", "astr_attn_kv_append", "astr_attn_paged_decode_masked",
-              "astr_attn_prefill_ragged_masked", "astr_attn_decode_contiguous", "astr_attn_prefill_contiguous"):
+              "astr_attn_prefill_ragged_masked", "astr_attn_decode_contiguous", "astr_attn_prefill_contiguous",
+              "astr_attn_decode_strided", "astr_attn_prefill_strided"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -297,6 +320,35 @@ def astr_attn_prefill_contiguous(q, qo_indptr, k_cache, v_cache, layout: KvLayou
                                              _ptr(kv_indptr), None if mask is None else ctypes.byref(mask),
                                              _ptr(out), ctypes.byref(dims), float(sm_scale), _stream(stream))
     return _check(st, "astr_attn_prefill_contiguous", check)
+
+
+def _ref(x):
+    return None if x is None else ctypes.byref(x)
+
+
+def astr_attn_decode_strided(q, k, v, req_to_token, seq_lens, kv_indptr, o_part, ml_part, out, dims: Dims,
+                             sm_scale: float, kv_layout: Optional[KvLayout] = None,
+                             qo_layout: Optional[QoLayout] = None, mask: Optional[Mask] = None, stream=None,
+                             check: bool = True) -> int:
+    """Decode with K/V paged (kv_layout None) or contiguous, query / output by strides (qo_layout;
+    None = packed), optional mask."""
+    st = load().astr_attn_decode_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(req_to_token), _ref(kv_layout),
+                                         _ref(qo_layout), _ptr(seq_lens), _ptr(kv_indptr), _ref(mask), _ptr(o_part),
+                                         _ptr(ml_part), _ptr(out), ctypes.byref(dims), float(sm_scale),
+                                         _stream(stream))
+    return _check(st, "astr_attn_decode_strided", check)
+
+
+def astr_attn_prefill_strided(q, qo_indptr, k, v, req_to_token, seq_lens, kv_indptr, out, dims: Dims,
+                              sm_scale: float, kv_layout: Optional[KvLayout] = None,
+                              qo_layout: Optional[QoLayout] = None, mask: Optional[Mask] = None, stream=None,
+                              check: bool = True) -> int:
+    """Ragged prefill with K/V paged or contiguous, query / output by strides, optional mask."""
+    st = load().astr_attn_prefill_strided(_ptr(q), _ptr(qo_indptr), _ptr(k), _ptr(v), _ptr(req_to_token),
+                                          _ref(kv_layout), _ref(qo_layout), _ptr(seq_lens), _ptr(kv_indptr),
+                                          _ref(mask), _ptr(out), ctypes.byref(dims), float(sm_scale),
+                                          _stream(stream))
+    return _check(st, "astr_attn_prefill_strided", check)
 
 
 def alloc_decode_workspace(dims: Dims, device="cuda"):

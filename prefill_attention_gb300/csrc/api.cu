@@ -174,6 +174,21 @@ static int decode_prepare(const astr_attn_dims* d, float sm_scale, astr::DecodeP
   return ASTR_OK;
 }
 
+// Query / output strides: non-negative multiples of 8 elements (16-byte rows); NULL = packed.
+static int check_qo_layout(const astr_attn_qo_layout* l, const astr_attn_dims* d, astr_attn_qo_layout* out) {
+  const int64_t row = (int64_t)d->num_qo_heads * d->head_dim;
+  *out = astr_attn_qo_layout{0, row, d->head_dim, 0, row, d->head_dim};
+  if (l == nullptr) return ASTR_OK;
+  const int64_t v[6] = {l->q_batch_stride, l->q_token_stride, l->q_head_stride,
+                        l->o_batch_stride, l->o_token_stride, l->o_head_stride};
+  for (int64_t x : v)
+    if (x < 0) return ASTR_ERR_INVALID_ARG;
+  for (int64_t x : v)
+    if (x % 8 != 0) return ASTR_ERR_MISALIGNED;
+  *out = *l;
+  return ASTR_OK;
+}
+
 // Contiguous-cache layout: strides non-negative multiples of 8 elements (16-byte rows).
 static int check_layout(const astr_attn_kv_layout* l, const astr_attn_dims* d, astr::KvStrides* ks) {
   if (l == nullptr || d == nullptr) return ASTR_ERR_INVALID_ARG;
@@ -210,8 +225,9 @@ static int check_mask(const astr_attn_mask* m, const astr_attn_dims* d, bool dec
 
 static int paged_decode_impl(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
                              const int32_t* req_to_token, const int32_t* seq_lens, const int32_t* kv_indptr,
-                             const astr_attn_mask* mask, const astr_attn_kv_layout* layout, float* o_part,
-                             float* ml_part, uint16_t* out, const astr_attn_dims* dims, float sm_scale, void* stream) {
+                             const astr_attn_mask* mask, const astr_attn_kv_layout* layout,
+                             const astr_attn_qo_layout* qo_layout, float* o_part, float* ml_part, uint16_t* out,
+                             const astr_attn_dims* dims, float sm_scale, void* stream) {
   const bool contig = layout != nullptr;  // K/V from a contiguous cache: no slot table
   if (!q || !k_pool || !v_pool || (!contig && !req_to_token) || !seq_lens || !kv_indptr || !o_part || !ml_part || !out)
     return ASTR_ERR_INVALID_ARG;
@@ -225,11 +241,18 @@ static int paged_decode_impl(const uint16_t* q, const uint16_t* k_pool, const ui
   if (mask != nullptr && (st = check_mask(mask, dims, true, &mask_req_pitch, &mask_row_pitch)) != ASTR_OK) return st;
   astr::KvStrides ks{0, 0, 0, 0};
   if (contig && (st = check_layout(layout, dims, &ks)) != ASTR_OK) return st;
+  astr_attn_qo_layout qo{};
+  if ((st = check_qo_layout(qo_layout, dims, &qo)) != ASTR_OK) return st;
   const astr_attn_dims cdims = contig ? contiguous_dims(dims) : *dims;
   astr::DecodeParams p{};
   bool nothing = false;
   st = decode_prepare(&cdims, sm_scale, &p, &nothing);
   if (st != ASTR_OK || nothing) return st;
+  // one row per request: a packed tensor steps by its row stride, a padded one by its batch stride
+  p.q_req = qo.q_batch_stride > 0 ? qo.q_batch_stride : qo.q_token_stride;
+  p.q_head = qo.q_head_stride;
+  p.o_req = qo.o_batch_stride > 0 ? qo.o_batch_stride : qo.o_token_stride;
+  p.o_head = qo.o_head_stride;
   astr::DecodeMask dm{nullptr, 0, 0};
   if (mask != nullptr && mask->mask != nullptr) dm = astr::DecodeMask{mask->mask, mask_req_pitch, mask->kv_pitch};
   p.q = q; p.k_pool = k_pool; p.v_pool = v_pool; p.req_to_token = req_to_token; p.seq_lens = seq_lens;
@@ -246,8 +269,8 @@ int astr_attn_paged_decode(const uint16_t* q, const uint16_t* k_pool, const uint
                            const int32_t* req_to_token, const int32_t* seq_lens, const int32_t* kv_indptr,
                            float* o_part, float* ml_part, uint16_t* out, const astr_attn_dims* dims, float sm_scale,
                            void* stream) {
-  return paged_decode_impl(q, k_pool, v_pool, req_to_token, seq_lens, kv_indptr, nullptr, nullptr, o_part, ml_part,
-                           out, dims, sm_scale, stream);
+  return paged_decode_impl(q, k_pool, v_pool, req_to_token, seq_lens, kv_indptr, nullptr, nullptr, nullptr, o_part,
+                           ml_part, out, dims, sm_scale, stream);
 }
 
 int astr_attn_paged_decode_masked(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
@@ -255,8 +278,8 @@ int astr_attn_paged_decode_masked(const uint16_t* q, const uint16_t* k_pool, con
                                   const astr_attn_mask* mask, float* o_part, float* ml_part, uint16_t* out,
                                   const astr_attn_dims* dims, float sm_scale, void* stream) {
   if (mask == nullptr) return ASTR_ERR_INVALID_ARG;
-  return paged_decode_impl(q, k_pool, v_pool, req_to_token, seq_lens, kv_indptr, mask, nullptr, o_part, ml_part, out,
-                           dims, sm_scale, stream);
+  return paged_decode_impl(q, k_pool, v_pool, req_to_token, seq_lens, kv_indptr, mask, nullptr, nullptr, o_part,
+                           ml_part, out, dims, sm_scale, stream);
 }
 
 int astr_attn_decode_contiguous(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
@@ -264,8 +287,17 @@ int astr_attn_decode_contiguous(const uint16_t* q, const uint16_t* k_cache, cons
                                 const astr_attn_mask* mask, float* o_part, float* ml_part, uint16_t* out,
                                 const astr_attn_dims* dims, float sm_scale, void* stream) {
   if (layout == nullptr) return ASTR_ERR_INVALID_ARG;
-  return paged_decode_impl(q, k_cache, v_cache, nullptr, seq_lens, kv_indptr, mask, layout, o_part, ml_part, out,
-                           dims, sm_scale, stream);
+  return paged_decode_impl(q, k_cache, v_cache, nullptr, seq_lens, kv_indptr, mask, layout, nullptr, o_part, ml_part,
+                           out, dims, sm_scale, stream);
+}
+
+int astr_attn_decode_strided(const uint16_t* q, const uint16_t* k, const uint16_t* v, const int32_t* req_to_token,
+                             const astr_attn_kv_layout* kv_layout, const astr_attn_qo_layout* qo_layout,
+                             const int32_t* seq_lens, const int32_t* kv_indptr, const astr_attn_mask* mask,
+                             float* o_part, float* ml_part, uint16_t* out, const astr_attn_dims* dims, float sm_scale,
+                             void* stream) {
+  return paged_decode_impl(q, k, v, kv_layout != nullptr ? nullptr : req_to_token, seq_lens, kv_indptr, mask,
+                           kv_layout, qo_layout, o_part, ml_part, out, dims, sm_scale, stream);
 }
 
 int astr_attn_decode_split(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
@@ -282,6 +314,8 @@ int astr_attn_decode_split(const uint16_t* q, const uint16_t* k_pool, const uint
   if (st != ASTR_OK || nothing) return st;
   p.q = q; p.k_pool = k_pool; p.v_pool = v_pool; p.req_to_token = req_to_token; p.seq_lens = seq_lens;
   p.kv_indptr = kv_indptr; p.o_part = o_part; p.ml_part = ml_part;
+  p.q_req = p.o_req = (int64_t)dims->num_qo_heads * dims->head_dim;
+  p.q_head = p.o_head = dims->head_dim;
   if (astr::launch_decode_split(p, nullptr, nullptr, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return ASTR_ERR_LAUNCH_FAILED;
   return ASTR_OK;
@@ -307,14 +341,17 @@ int astr_attn_decode_combine(const float* o_part, const float* ml_part, const in
   p.o_part = const_cast<float*>(o_part);
   p.ml_part = const_cast<float*>(ml_part);
   p.out = out;
+  p.q_req = p.o_req = (int64_t)dims->num_qo_heads * dims->head_dim;
+  p.q_head = p.o_head = dims->head_dim;
   if (astr::launch_decode_combine(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ASTR_ERR_LAUNCH_FAILED;
   return ASTR_OK;
 }
 
 static int prefill_impl(const uint16_t* q, const int32_t* qo_indptr, const uint16_t* k_pool, const uint16_t* v_pool,
                         const int32_t* req_to_token, const int32_t* seq_lens, const int32_t* kv_indptr,
-                        const astr_attn_mask* mask, const astr_attn_kv_layout* layout, uint16_t* out,
-                        const astr_attn_dims* dims, float sm_scale, void* stream) {
+                        const astr_attn_mask* mask, const astr_attn_kv_layout* layout,
+                        const astr_attn_qo_layout* qo_layout, uint16_t* out, const astr_attn_dims* dims,
+                        float sm_scale, void* stream) {
   (void)kv_indptr;
   const bool contig = layout != nullptr;  // K/V from a contiguous cache: no slot table
   if (!q || !qo_indptr || !k_pool || !v_pool || (!contig && !req_to_token) || !seq_lens || !out || !dims)
@@ -338,6 +375,8 @@ static int prefill_impl(const uint16_t* q, const int32_t* qo_indptr, const uint1
   if (!astr::prefill_supported(d->head_dim, G)) return ASTR_ERR_UNSUPPORTED;
   int64_t mask_req_pitch = 0, mask_row_pitch = 0;
   if (mask != nullptr && (st = check_mask(mask, d, false, &mask_req_pitch, &mask_row_pitch)) != ASTR_OK) return st;
+  astr_attn_qo_layout qo{};
+  if ((st = check_qo_layout(qo_layout, d, &qo)) != ASTR_OK) return st;
   if (d->batch == 0 || d->total_q == 0 || d->max_q_len == 0) return ASTR_OK;
   int dev = 0;
   if ((st = current_device(&dev)) != ASTR_OK) return st;
@@ -370,6 +409,9 @@ static int prefill_impl(const uint16_t* q, const int32_t* qo_indptr, const uint1
   }
   p.contig = contig ? 1 : 0;
   p.kv = ks;
+  p.q_batch = qo.q_batch_stride; p.q_token = qo.q_token_stride; p.q_head = qo.q_head_stride;
+  p.o_batch = qo.o_batch_stride; p.o_token = qo.o_token_stride; p.o_head = qo.o_head_stride;
+  p.q_rows = d->max_q_len;
   p.status = d->status;
   p.wait_limit = wait_limit_of(d);
   if (astr::launch_prefill(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ASTR_ERR_LAUNCH_FAILED;
@@ -380,8 +422,8 @@ int astr_attn_prefill_ragged(const uint16_t* q, const int32_t* qo_indptr, const 
                              const uint16_t* v_pool, const int32_t* req_to_token, const int32_t* seq_lens,
                              const int32_t* kv_indptr, uint16_t* out, const astr_attn_dims* d, float sm_scale,
                              void* stream) {
-  return prefill_impl(q, qo_indptr, k_pool, v_pool, req_to_token, seq_lens, kv_indptr, nullptr, nullptr, out, d,
-                      sm_scale, stream);
+  return prefill_impl(q, qo_indptr, k_pool, v_pool, req_to_token, seq_lens, kv_indptr, nullptr, nullptr, nullptr,
+                      out, d, sm_scale, stream);
 }
 
 int astr_attn_prefill_ragged_masked(const uint16_t* q, const int32_t* qo_indptr, const uint16_t* k_pool,
@@ -389,8 +431,8 @@ int astr_attn_prefill_ragged_masked(const uint16_t* q, const int32_t* qo_indptr,
                                     const int32_t* kv_indptr, const astr_attn_mask* mask, uint16_t* out,
                                     const astr_attn_dims* d, float sm_scale, void* stream) {
   if (mask == nullptr) return ASTR_ERR_INVALID_ARG;
-  return prefill_impl(q, qo_indptr, k_pool, v_pool, req_to_token, seq_lens, kv_indptr, mask, nullptr, out, d,
-                      sm_scale, stream);
+  return prefill_impl(q, qo_indptr, k_pool, v_pool, req_to_token, seq_lens, kv_indptr, mask, nullptr, nullptr, out,
+                      d, sm_scale, stream);
 }
 
 int astr_attn_prefill_contiguous(const uint16_t* q, const int32_t* qo_indptr, const uint16_t* k_cache,
@@ -398,8 +440,17 @@ int astr_attn_prefill_contiguous(const uint16_t* q, const int32_t* qo_indptr, co
                                  const int32_t* kv_indptr, const astr_attn_mask* mask, uint16_t* out,
                                  const astr_attn_dims* d, float sm_scale, void* stream) {
   if (layout == nullptr) return ASTR_ERR_INVALID_ARG;
-  return prefill_impl(q, qo_indptr, k_cache, v_cache, nullptr, seq_lens, kv_indptr, mask, layout, out, d, sm_scale,
-                      stream);
+  return prefill_impl(q, qo_indptr, k_cache, v_cache, nullptr, seq_lens, kv_indptr, mask, layout, nullptr, out, d,
+                      sm_scale, stream);
+}
+
+int astr_attn_prefill_strided(const uint16_t* q, const int32_t* qo_indptr, const uint16_t* k, const uint16_t* v,
+                              const int32_t* req_to_token, const astr_attn_kv_layout* kv_layout,
+                              const astr_attn_qo_layout* qo_layout, const int32_t* seq_lens, const int32_t* kv_indptr,
+                              const astr_attn_mask* mask, uint16_t* out, const astr_attn_dims* d, float sm_scale,
+                              void* stream) {
+  return prefill_impl(q, qo_indptr, k, v, kv_layout != nullptr ? nullptr : req_to_token, seq_lens, kv_indptr, mask,
+                      kv_layout, qo_layout, out, d, sm_scale, stream);
 }
 
 int astr_attn_kv_append(const uint16_t* k_new, const uint16_t* v_new, const int32_t* qo_indptr,

@@ -54,6 +54,9 @@ struct DecodeParams {
                                  // previous kernel is this call's split kernel, which does not write it)
   int32_t* status;               // optional status word (kStatus* bits, OR-ed in); may be null
   uint32_t wait_limit;           // polls per pipeline wait before giving up
+  // query row / output row of request b, head h at q + b * q_req + h * q_head (elements; the
+  // packed [B, Hq, D] layout is q_req = Hq * D, q_head = D), the same for out
+  int64_t q_req, q_head, o_req, o_head;
 };
 
 // Decode with an explicit mask: request b's bytes start at mask + b * req_pitch, one byte per
@@ -89,6 +92,11 @@ struct PrefillParams {
   KvStrides kv;
   int32_t* status;               // optional status word (kStatus* bits, OR-ed in); may be null
   uint32_t wait_limit;           // polls per pipeline wait before giving up
+  // query row i of request b, head h (elements): q_batch == 0 -> (qo_indptr[b] + i) * q_token +
+  // h * q_head (packed; [total_q, Hq, D] is q_token = Hq * D, q_head = D); q_batch > 0 ->
+  // b * q_batch + i * q_token + h * q_head (padded, q_rows positions per request).  Same for out.
+  int64_t q_batch, q_token, q_head, o_batch, o_token, o_head;
+  int q_rows;
 };
 
 // KV append: one launch, one warp per new token.

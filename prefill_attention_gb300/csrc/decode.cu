@@ -464,10 +464,10 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(
       if (i >= C::STAGES && !wait_or_fail(empty(s), (uint32_t)((i / C::STAGES - 1) & 1), err, p.wait_limit)) break;
       const uint32_t kst = ring + s * C::SLOT, vst = kst + C::KV_BYTES, qst = vst + C::KV_BYTES;
       if (it.opens_piece(ls)) {  // first slot of a piece: its G query rows
-        const uint16_t* qsrc = p.q + ((size_t)it.b * p.num_qo_heads + (size_t)kvh * G) * D;
+        const uint16_t* qsrc = p.q + (size_t)it.b * p.q_req + (size_t)kvh * G * p.q_head;
         for (int j = lane; j < G * C::CPR; j += 32) {
           const int g = j / C::CPR, c = j % C::CPR;
-          cp_async16(qst + sw128(g, c, C::QROWS), qsrc + (size_t)g * D + c * 8, true);
+          cp_async16(qst + sw128(g, c, C::QROWS), qsrc + (size_t)g * p.q_head + c * 8, true);
         }
       }
       // lane -> chunk (lane % CPR) of keys (r * 32 + lane) / CPR, r = 0 .. KV_IT-1
@@ -719,6 +719,7 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(
         const int b = it.b;
         const bool direct = (p.out != nullptr) && it.spb >= ls && it.spb + it.nslots() <= hs;  // whole request here
         const size_t qh0 = (size_t)b * p.num_qo_heads + (size_t)kvh * G;
+        uint16_t* const orow = p.out + (size_t)b * p.o_req + (size_t)kvh * G * p.o_head;  // head kvh * G of b
         if (direct) {
           // lane -> 8 consecutive d of one head: bf16(O / l), 16-byte stores
           for (int j = lane; j < G * (D / 8); j += 32) {
@@ -731,7 +732,7 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(
             v.y = float2_to_bf16x2_rn(src[2] * inv, src[3] * inv);
             v.z = float2_to_bf16x2_rn(src[4] * inv, src[5] * inv);
             v.w = float2_to_bf16x2_rn(src[6] * inv, src[7] * inv);
-            *reinterpret_cast<uint4*>(p.out + (qh0 + h) * D + d0) = v;
+            *reinterpret_cast<uint4*>(orow + (size_t)h * p.o_head + d0) = v;
           }
         } else if (vc - it.spb / CS < p.part_pitch) {  // (a request past max_seq_len keys is not written)
           const int slot = vc - it.spb / CS;
@@ -768,7 +769,8 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(
       for (int i = lane; i < G * D; i += 32) {
         const size_t qh = (size_t)it.b * p.num_qo_heads + (size_t)kvh * G + i / D;
         if (s < p.part_pitch) p.o_part[(qh * p.part_pitch + s) * D + i % D] = CUDART_NAN_F;
-        if (p.out != nullptr) p.out[qh * D + i % D] = 0x7fc0;
+        if (p.out != nullptr)
+          p.out[(size_t)it.b * p.o_req + ((size_t)kvh * G + i / D) * p.o_head + i % D] = 0x7fc0;
       }
     }
   }
@@ -869,7 +871,7 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(kFullMask, L, off);
   const float inv = (L > 0.f) ? 1.f / L : 0.f;
-  uint16_t* dst = p.out + (size_t)wid * D + lane * VPL;
+  uint16_t* dst = p.out + (size_t)b * p.o_req + (size_t)(wid - b * p.num_qo_heads) * p.o_head + lane * VPL;
   if constexpr (VPL == 4) {
     uint2 pk;
     pk.x = float2_to_bf16x2_rn(acc[0] * inv, acc[1] * inv);

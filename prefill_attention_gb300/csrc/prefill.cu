@@ -481,30 +481,38 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
     // query tiles are read and output tiles written once: first out of L2, ahead of the K/V
     // rows that the other query tiles of the same request read again
     const uint64_t once = tc::l2_evict_first_policy();
-    // where each slot's tile goes (lane k holds slot k): first position, first head, rows
-    int pend_pos = 0, pend_head = 0, pend_rows = 0;
+    // where each slot's tile goes (lane k holds slot k): request, first position (request-local
+    // for a padded output, flat for a packed one), first head, rows
+    int pend_b = 0, pend_pos = 0, pend_head = 0, pend_rows = 0;
+    const bool q_padded = p.q_batch > 0, o_padded = p.o_batch > 0;
     // write tile v's staged rows out: one TMA store per column block when all BQ positions
     // are the request's, else the valid rows with coalesced stores (never past the request)
     auto write_out = [&](int v) {
       if (!(ok = wait_or_fail(o_staged(v), q_par(v)))) return;
       const int k = v % C::Q_SLOTS;
-      const int pos = __shfl_sync(kFullMask, pend_pos, k), head = __shfl_sync(kFullMask, pend_head, k);
-      const int rows = __shfl_sync(kFullMask, pend_rows, k);
+      const int ob = __shfl_sync(kFullMask, pend_b, k), pos = __shfl_sync(kFullMask, pend_pos, k);
+      const int head = __shfl_sync(kFullMask, pend_head, k), rows = __shfl_sync(kFullMask, pend_rows, k);
       const uint32_t src = q_slot(v);
       if (rows == C::M) {
         if (lane == 0) {
-          for (int cb = 0; cb < C::NCB; ++cb)
-            tc::tma_store_3d_hint(&o_map, src + cb * (C::M * C::SW_BYTES), cb * C::CB_ELEMS, head, pos, once);
+          for (int cb = 0; cb < C::NCB; ++cb) {
+            if (o_padded)
+              tc::tma_store_4d_hint(&o_map, src + cb * (C::M * C::SW_BYTES), cb * C::CB_ELEMS, head, pos, ob, once);
+            else
+              tc::tma_store_3d_hint(&o_map, src + cb * (C::M * C::SW_BYTES), cb * C::CB_ELEMS, head, pos, once);
+          }
           tc::bulk_commit();
           tc::bulk_wait_read_all();  // the slot may be refilled once the stores have read it
         }
       } else {
-        uint16_t* obase = p.out + ((size_t)pos * p.num_qo_heads + (size_t)head) * D;
+        // row r of the tile is position pos + r / G, head head + r % G
+        const int64_t orow0 = (o_padded ? (int64_t)ob * p.o_batch : 0) + (int64_t)pos * p.o_token;
+        uint16_t* obase = p.out + orow0 + (int64_t)head * p.o_head;
         for (int i = 0; i < C::M * C::CPR / 32; ++i) {
           const int flat = i * 32 + lane, r = flat / C::CPR, c = flat % C::CPR;
           if (r < rows) {
             const uint4 x = lds128(src + swz<C::SW_BYTES>(r, c, C::M));
-            *reinterpret_cast<uint4*>(obase + ((size_t)(r / G) * p.num_qo_heads + r % G) * D + c * 8) = x;
+            *reinterpret_cast<uint4*>(obase + (int64_t)(r / G) * p.o_token + (int64_t)(r % G) * p.o_head + c * 8) = x;
           }
         }
         tc::fence_proxy_async_smem();  // the next TMA write of this slot follows these reads
@@ -521,15 +529,20 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
         }
         const int qf = it.first0 + t * C::BQ;
         if (lane == u % C::Q_SLOTS) {
-          pend_pos = it.q0 + qf;
+          pend_b = it.b;
+          pend_pos = o_padded ? qf : it.q0 + qf;
           pend_head = it.kvh * G;
           pend_rows = (min(it.q_len, qf + C::BQ) - qf) * G;
         }
         if (lane == 0) {
           tc::mbar_arrive_expect_tx(q_full(u), (uint32_t)C::Q_BYTES);
-          for (int cb = 0; cb < C::NCB; ++cb)
-            tc::tma_load_3d_hint(q_slot(u) + cb * (C::M * C::SW_BYTES), &q_map, cb * C::CB_ELEMS, it.kvh * G,
-                                 it.q0 + qf, q_full(u), once);
+          for (int cb = 0; cb < C::NCB; ++cb) {
+            const uint32_t dst = q_slot(u) + cb * (C::M * C::SW_BYTES);
+            if (q_padded)
+              tc::tma_load_4d_hint(dst, &q_map, cb * C::CB_ELEMS, it.kvh * G, qf, it.b, q_full(u), once);
+            else
+              tc::tma_load_3d_hint(dst, &q_map, cb * C::CB_ELEMS, it.kvh * G, it.q0 + qf, q_full(u), once);
+          }
         }
         __syncwarp();
       }
@@ -1003,18 +1016,24 @@ cudaError_t launch_prefill_t(const PrefillParams& p, cudaStream_t stream) {
   const PFN_cuTensorMapEncodeTiled_v12000 encode = encode_tiled();
   if (encode == nullptr) return cudaErrorNotSupported;
   // (out has the same layout; its map writes whole tiles of one request)
+  // packed rows: [total_q rows][Hq][D] by (row stride, head stride); padded: [B][q_rows][Hq][D]
+  // by (batch, row, head strides) -- a 4-D map addressed by (column, head, local row, request)
   CUtensorMap q_map, o_map;
-  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.num_qo_heads, (cuuint64_t)p.total_q};
-  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)p.num_qo_heads * D * 2};
-  const cuuint32_t box[3] = {(cuuint32_t)C::CB_ELEMS, (cuuint32_t)G, (cuuint32_t)C::BQ};
   const CUtensorMapSwizzle swz_mode = C::SW_BYTES == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-  const cuuint32_t elem_strides[3] = {1u, 1u, 1u};
-  if (encode(&q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(p.q), dims, strides, box,
-             elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, swz_mode,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
-      encode(&o_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.out, dims, strides, box, elem_strides,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, swz_mode, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+  const cuuint32_t box[4] = {(cuuint32_t)C::CB_ELEMS, (cuuint32_t)G, (cuuint32_t)C::BQ, 1u};
+  const cuuint32_t elem_strides[4] = {1u, 1u, 1u, 1u};
+  auto make_map = [&](CUtensorMap* map, const uint16_t* base, int64_t bstride, int64_t tstride, int64_t hstride,
+                      CUtensorMapL2promotion promo) {
+    const bool padded = bstride > 0;
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)p.num_qo_heads,
+                                (cuuint64_t)(padded ? p.q_rows : p.total_q), (cuuint64_t)p.batch};
+    const cuuint64_t strides[3] = {(cuuint64_t)hstride * 2, (cuuint64_t)tstride * 2, (cuuint64_t)bstride * 2};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, padded ? 4 : 3, const_cast<uint16_t*>(base), dims, strides,
+                  box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, swz_mode, promo,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  if (!make_map(&q_map, p.q, p.q_batch, p.q_token, p.q_head, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
+      !make_map(&o_map, p.out, p.o_batch, p.o_token, p.o_head, CU_TENSOR_MAP_L2_PROMOTION_NONE))
     return cudaErrorInvalidValue;
   prefill_kernel<D, G, MASK, CONTIG><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(p, q_map, o_map);
   return cudaGetLastError();

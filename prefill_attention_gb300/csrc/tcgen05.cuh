@@ -99,6 +99,23 @@ __device__ __forceinline__ void tma_store_3d_hint(const void* tmap, uint32_t src
       "r"(src), "r"(x), "r"(y), "r"(z), "l"(policy)
       : "memory");
 }
+// 4-D variants (x innermost, y, z, w) of the tiled load and store above.
+__device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const void* tmap, int x, int y, int z, int w,
+                                                 uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
+      "{%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_4d_hint(const void* tmap, uint32_t src, int x, int y, int z, int w,
+                                                  uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%2, %3, %4, %5}], [%1], %6;" ::"l"(
+          tmap),
+      "r"(src), "r"(x), "r"(y), "r"(z), "r"(w), "l"(policy)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until every committed bulk store of this thread has finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }

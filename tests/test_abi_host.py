@@ -337,3 +337,38 @@ def test_header_is_plain_c(tmp_path):
     r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.dirname(HEADER),
                         "-c", str(src), "-o", str(tmp_path / "use_header.o")], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def _qo(qb=0, qt=32 * 128, qh=128, ob=0, ot=32 * 128, oh=128):
+    return pa.QoLayout(qb, qt, qh, ob, ot, oh)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(qh=-8), pa.ASTR_ERR_INVALID_ARG),
+    (dict(ob=-128), pa.ASTR_ERR_INVALID_ARG),
+    (dict(qt=100), pa.ASTR_ERR_MISALIGNED),       # not a multiple of 8 elements
+    (dict(oh=4), pa.ASTR_ERR_MISALIGNED),
+])
+def test_strided_bad_qo_layout(lib, kw, status):
+    d = _dims(batch=0)
+    assert pa.astr_attn_prefill_strided(A, A, A, A, A, A, A, A, d, 0.1, qo_layout=_qo(**kw), stream=0,
+                                        check=False) == status
+    assert pa.astr_attn_decode_strided(A, A, A, A, A, A, A, A, A, d, 0.1, qo_layout=_qo(**kw), stream=0,
+                                       check=False) == status
+
+
+def test_strided_null_layouts_and_table_rules(lib):
+    d = _dims(batch=0)
+    # no layouts: the paged pool, packed rows -- the table is required then
+    assert pa.astr_attn_prefill_strided(A, A, A, A, A, A, A, A, d, 0.1, stream=0, check=False) == pa.ASTR_OK
+    assert pa.astr_attn_prefill_strided(A, A, A, A, 0, A, A, A, d, 0.1, stream=0,
+                                        check=False) == pa.ASTR_ERR_INVALID_ARG
+    # a contiguous cache: the table is not read (may be NULL)
+    assert pa.astr_attn_prefill_strided(A, A, A, A, 0, A, A, A, _dims(batch=0, r2t_stride=0, num_slots=0), 0.1,
+                                        kv_layout=_lay(), stream=0, check=False) == pa.ASTR_OK
+    # (decode asks for the device's SM count after its argument checks: DEVICE where no GPU is present)
+    st = pa.astr_attn_decode_strided(A, A, A, 0, A, A, A, A, A, d, 0.1, kv_layout=_lay(), qo_layout=_qo(), stream=0,
+                                     check=False)
+    assert st in (pa.ASTR_OK, pa.ASTR_ERR_DEVICE)
+    assert pa.astr_attn_decode_strided(A, A, A, 0, A, A, A, A, A, d, 0.1, qo_layout=_qo(), stream=0,
+                                       check=False) == pa.ASTR_ERR_INVALID_ARG   # paged pool needs the table
