@@ -249,19 +249,20 @@ static int paged_decode_impl(const uint16_t* q, const uint16_t* k_pool, const ui
   st = decode_prepare(&cdims, sm_scale, &p, &nothing);
   if (st != ASTR_OK || nothing) return st;
   // one row per request: a packed tensor steps by its row stride, a padded one by its batch stride
-  p.q_req = qo.q_batch_stride > 0 ? qo.q_batch_stride : qo.q_token_stride;
-  p.q_head = qo.q_head_stride;
-  p.o_req = qo.o_batch_stride > 0 ? qo.o_batch_stride : qo.o_token_stride;
-  p.o_head = qo.o_head_stride;
+  const astr::QoStrides qs{qo.q_batch_stride > 0 ? qo.q_batch_stride : qo.q_token_stride, qo.q_head_stride,
+                           qo.o_batch_stride > 0 ? qo.o_batch_stride : qo.o_token_stride, qo.o_head_stride};
+  const int64_t row = (int64_t)dims->num_qo_heads * dims->head_dim;
+  const bool packed = qs.q_req == row && qs.q_head == dims->head_dim && qs.o_req == row && qs.o_head == dims->head_dim;
   astr::DecodeMask dm{nullptr, 0, 0};
   if (mask != nullptr && mask->mask != nullptr) dm = astr::DecodeMask{mask->mask, mask_req_pitch, mask->kv_pitch};
   p.q = q; p.k_pool = k_pool; p.v_pool = v_pool; p.req_to_token = req_to_token; p.seq_lens = seq_lens;
   p.kv_indptr = kv_indptr; p.o_part = o_part; p.ml_part = ml_part; p.out = out;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (astr::launch_decode_split(p, dm.mask != nullptr ? &dm : nullptr, contig ? &ks : nullptr, s) != cudaSuccess)
+  if (astr::launch_decode_split(p, dm.mask != nullptr ? &dm : nullptr, contig ? &ks : nullptr, packed ? nullptr : &qs,
+                                s) != cudaSuccess)
     return ASTR_ERR_LAUNCH_FAILED;
   p.indptr_before_wait = 1;  // the combine follows this call's split kernel directly
-  if (astr::launch_decode_combine(p, s) != cudaSuccess) return ASTR_ERR_LAUNCH_FAILED;
+  if (astr::launch_decode_combine(p, packed ? nullptr : &qs, s) != cudaSuccess) return ASTR_ERR_LAUNCH_FAILED;
   return ASTR_OK;
 }
 
@@ -314,9 +315,7 @@ int astr_attn_decode_split(const uint16_t* q, const uint16_t* k_pool, const uint
   if (st != ASTR_OK || nothing) return st;
   p.q = q; p.k_pool = k_pool; p.v_pool = v_pool; p.req_to_token = req_to_token; p.seq_lens = seq_lens;
   p.kv_indptr = kv_indptr; p.o_part = o_part; p.ml_part = ml_part;
-  p.q_req = p.o_req = (int64_t)dims->num_qo_heads * dims->head_dim;
-  p.q_head = p.o_head = dims->head_dim;
-  if (astr::launch_decode_split(p, nullptr, nullptr, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+  if (astr::launch_decode_split(p, nullptr, nullptr, nullptr, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return ASTR_ERR_LAUNCH_FAILED;
   return ASTR_OK;
 }
@@ -341,9 +340,8 @@ int astr_attn_decode_combine(const float* o_part, const float* ml_part, const in
   p.o_part = const_cast<float*>(o_part);
   p.ml_part = const_cast<float*>(ml_part);
   p.out = out;
-  p.q_req = p.o_req = (int64_t)dims->num_qo_heads * dims->head_dim;
-  p.q_head = p.o_head = dims->head_dim;
-  if (astr::launch_decode_combine(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ASTR_ERR_LAUNCH_FAILED;
+  if (astr::launch_decode_combine(p, nullptr, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return ASTR_ERR_LAUNCH_FAILED;
   return ASTR_OK;
 }
 

@@ -54,8 +54,12 @@ struct DecodeParams {
                                  // previous kernel is this call's split kernel, which does not write it)
   int32_t* status;               // optional status word (kStatus* bits, OR-ed in); may be null
   uint32_t wait_limit;           // polls per pipeline wait before giving up
-  // query row / output row of request b, head h at q + b * q_req + h * q_head (elements; the
-  // packed [B, Hq, D] layout is q_req = Hq * D, q_head = D), the same for out
+};
+
+// Decode query / output rows by strides: request b, head h at q + b * q_req + h * q_head
+// (elements), the same for out.  The packed [B, Hq, D] layout is q_req = Hq * D, q_head = D;
+// the kernels take it at compile time when no strides are given.
+struct QoStrides {
   int64_t q_req, q_head, o_req, o_head;
 };
 
@@ -117,9 +121,10 @@ struct AppendParams {
 
 // Launchers return cudaSuccess or the launch error; they never synchronise.
 // mask / strides may be null (no explicit mask / the paged pool through req_to_token)
+// qo may be null as well (the packed query / output layout)
 cudaError_t launch_decode_split(const DecodeParams& p, const DecodeMask* mask, const KvStrides* strides,
-                                cudaStream_t stream);
-cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream);
+                                const QoStrides* qo, cudaStream_t stream);
+cudaError_t launch_decode_combine(const DecodeParams& p, const QoStrides* qo, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream);         // dispatches on p.mask
 cudaError_t launch_prefill_masked(const PrefillParams& p, cudaStream_t stream);  // the explicit-mask kernels
 cudaError_t launch_prefill_contig(const PrefillParams& p, cudaStream_t stream);  // the contiguous-cache kernels

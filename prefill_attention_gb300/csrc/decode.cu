@@ -356,13 +356,17 @@ __device__ __forceinline__ bool wait_or_fail(uint32_t bar, uint32_t parity, vola
 }
 
 // Kernel variants: MODE bit 0 = explicit mask, bit 1 = contiguous (stride-addressed) K/V cache
-// instead of the slot table.  MODE 0 takes DecodeParams alone; the others take the longer block
-// below, so the plain kernel's parameter block (and code) stays as it is.
-constexpr int kModeMask = 1, kModeContig = 2;
+// instead of the slot table, bit 2 = query / output by strides alone (the mask and contiguous
+// variants always take strides).  MODE 0 takes DecodeParams alone and the packed query /
+// output layout at compile time; the others take the longer block below, so the plain
+// kernel's parameter block and code stay as they are (a runtime row pitch there measurably
+// slows the split step).
+constexpr int kModeMask = 1, kModeContig = 2, kModeStrided = 4;
 struct DecodeParamsExt {
   DecodeParams p;
   DecodeMask m;
   KvStrides s;
+  QoStrides qo;
 };
 template <int MODE> struct SplitArg { using type = DecodeParamsExt; };
 template <> struct SplitArg<0> { using type = DecodeParams; };
@@ -373,11 +377,13 @@ __host__ __device__ __forceinline__ DecodeMask mask_of(const DecodeParams&) { re
 __host__ __device__ __forceinline__ DecodeMask mask_of(const DecodeParamsExt& a) { return a.m; }
 __host__ __device__ __forceinline__ KvStrides strides_of(const DecodeParams&) { return KvStrides{0, 0, 0, 0}; }
 __host__ __device__ __forceinline__ KvStrides strides_of(const DecodeParamsExt& a) { return a.s; }
+__host__ __device__ __forceinline__ QoStrides qo_of(const DecodeParams&) { return QoStrides{0, 0, 0, 0}; }
+__host__ __device__ __forceinline__ QoStrides qo_of(const DecodeParamsExt& a) { return a.qo; }
 
 template <int D, int G, int MODE>
 __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(const typename SplitArg<MODE>::type arg) {
   using C = DecCfg<D, G>;
-  constexpr bool MASK = (MODE & kModeMask) != 0, CONTIG = (MODE & kModeContig) != 0;
+  constexpr bool MASK = (MODE & kModeMask) != 0, CONTIG = (MODE & kModeContig) != 0, STRIDED = MODE != 0;
   const DecodeParams& p = params_of(arg);
   constexpr int NH = C::NH;
   extern __shared__ __align__(1024) unsigned char smem[];
@@ -464,10 +470,19 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(
       if (i >= C::STAGES && !wait_or_fail(empty(s), (uint32_t)((i / C::STAGES - 1) & 1), err, p.wait_limit)) break;
       const uint32_t kst = ring + s * C::SLOT, vst = kst + C::KV_BYTES, qst = vst + C::KV_BYTES;
       if (it.opens_piece(ls)) {  // first slot of a piece: its G query rows
-        const uint16_t* qsrc = p.q + (size_t)it.b * p.q_req + (size_t)kvh * G * p.q_head;
+        const uint16_t* qsrc;
+        size_t qpitch;  // elements between the query rows of consecutive heads
+        if constexpr (STRIDED) {
+          const QoStrides qo = qo_of(arg);
+          qsrc = p.q + (size_t)it.b * qo.q_req + (size_t)kvh * G * qo.q_head;
+          qpitch = (size_t)qo.q_head;
+        } else {
+          qsrc = p.q + ((size_t)it.b * p.num_qo_heads + (size_t)kvh * G) * D;
+          qpitch = D;
+        }
         for (int j = lane; j < G * C::CPR; j += 32) {
           const int g = j / C::CPR, c = j % C::CPR;
-          cp_async16(qst + sw128(g, c, C::QROWS), qsrc + (size_t)g * p.q_head + c * 8, true);
+          cp_async16(qst + sw128(g, c, C::QROWS), qsrc + (size_t)g * qpitch + c * 8, true);
         }
       }
       // lane -> chunk (lane % CPR) of keys (r * 32 + lane) / CPR, r = 0 .. KV_IT-1
@@ -719,8 +734,17 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(
         const int b = it.b;
         const bool direct = (p.out != nullptr) && it.spb >= ls && it.spb + it.nslots() <= hs;  // whole request here
         const size_t qh0 = (size_t)b * p.num_qo_heads + (size_t)kvh * G;
-        uint16_t* const orow = p.out + (size_t)b * p.o_req + (size_t)kvh * G * p.o_head;  // head kvh * G of b
         if (direct) {
+          uint16_t* orow;  // output row of head kvh * G of request b
+          size_t opitch;   // elements between the output rows of consecutive heads
+          if constexpr (STRIDED) {
+            const QoStrides qo = qo_of(arg);
+            orow = p.out + (size_t)b * qo.o_req + (size_t)kvh * G * qo.o_head;
+            opitch = (size_t)qo.o_head;
+          } else {
+            orow = p.out + qh0 * D;
+            opitch = D;
+          }
           // lane -> 8 consecutive d of one head: bf16(O / l), 16-byte stores
           for (int j = lane; j < G * (D / 8); j += 32) {
             const int h = j / (D / 8), d0 = (j % (D / 8)) * 8;
@@ -732,7 +756,7 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(
             v.y = float2_to_bf16x2_rn(src[2] * inv, src[3] * inv);
             v.z = float2_to_bf16x2_rn(src[4] * inv, src[5] * inv);
             v.w = float2_to_bf16x2_rn(src[6] * inv, src[7] * inv);
-            *reinterpret_cast<uint4*>(orow + (size_t)h * p.o_head + d0) = v;
+            *reinterpret_cast<uint4*>(orow + (size_t)h * opitch + d0) = v;
           }
         } else if (vc - it.spb / CS < p.part_pitch) {  // (a request past max_seq_len keys is not written)
           const int slot = vc - it.spb / CS;
@@ -769,16 +793,20 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(
       for (int i = lane; i < G * D; i += 32) {
         const size_t qh = (size_t)it.b * p.num_qo_heads + (size_t)kvh * G + i / D;
         if (s < p.part_pitch) p.o_part[(qh * p.part_pitch + s) * D + i % D] = CUDART_NAN_F;
-        if (p.out != nullptr)
-          p.out[(size_t)it.b * p.o_req + ((size_t)kvh * G + i / D) * p.o_head + i % D] = 0x7fc0;
+        if (p.out != nullptr) {
+          const QoStrides qo = qo_of(arg);
+          p.out[STRIDED ? (size_t)it.b * qo.o_req + ((size_t)kvh * G + i / D) * qo.o_head + i % D
+                        : qh * D + i % D] = 0x7fc0;
+        }
       }
     }
   }
 }
 
-// One warp per (request, query head): merge the request's partials and write bf16.
-template <int D>
-__global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams p) {
+// One warp per (request, query head): merge the request's partials and write bf16 (the output
+// row at the strides qo when STRIDED, else packed [B, Hq, D]).
+template <int D, bool STRIDED>
+__global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams p, const QoStrides qo) {
   constexpr int VPL = D / 32;  // output elements per lane
   const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -871,7 +899,9 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(kFullMask, L, off);
   const float inv = (L > 0.f) ? 1.f / L : 0.f;
-  uint16_t* dst = p.out + (size_t)b * p.o_req + (size_t)(wid - b * p.num_qo_heads) * p.o_head + lane * VPL;
+  uint16_t* dst = (STRIDED ? p.out + (size_t)b * qo.o_req + (size_t)(wid - b * p.num_qo_heads) * qo.o_head
+                           : p.out + (size_t)wid * D) +
+                  lane * VPL;
   if constexpr (VPL == 4) {
     uint2 pk;
     pk.x = float2_to_bf16x2_rn(acc[0] * inv, acc[1] * inv);
@@ -915,17 +945,21 @@ bool decode_supported(int head_dim, int group) {
 }
 
 cudaError_t launch_decode_split(const DecodeParams& p, const DecodeMask* mask, const KvStrides* strides,
-                                cudaStream_t stream) {
+                                const QoStrides* qo, cudaStream_t stream) {
   const int G = p.num_qo_heads / p.num_kv_heads;
-  // the kernels with a mask or a contiguous cache are separate instantiations with a longer
-  // parameter block
+  // the kernels with a mask, a contiguous cache or strided query / output rows are separate
+  // instantiations with a longer parameter block
+  const int64_t row = (int64_t)p.num_qo_heads * p.head_dim;
   const DecodeParamsExt pe{p, mask != nullptr ? *mask : DecodeMask{nullptr, 0, 0},
-                           strides != nullptr ? *strides : KvStrides{0, 0, 0, 0}};
-  const int mode = (mask != nullptr ? kModeMask : 0) | (strides != nullptr ? kModeContig : 0);
+                           strides != nullptr ? *strides : KvStrides{0, 0, 0, 0},
+                           qo != nullptr ? *qo : QoStrides{row, p.head_dim, row, p.head_dim}};
+  int mode = (mask != nullptr ? kModeMask : 0) | (strides != nullptr ? kModeContig : 0);
+  if (mode == 0 && qo != nullptr) mode = kModeStrided;
 #define ASTR_DEC_CASE(DD, GG)                                                     \
   if (p.head_dim == DD && G == GG) {                                              \
     switch (mode) {                                                               \
       case 0: return launch_split_t<DD, GG, 0>(p, stream);                        \
+      case kModeStrided: return launch_split_t<DD, GG, kModeStrided>(pe, stream); \
       case kModeMask: return launch_split_t<DD, GG, kModeMask>(pe, stream);       \
       case kModeContig: return launch_split_t<DD, GG, kModeContig>(pe, stream);   \
       default: return launch_split_t<DD, GG, kModeMask | kModeContig>(pe, stream); \
@@ -938,7 +972,7 @@ cudaError_t launch_decode_split(const DecodeParams& p, const DecodeMask* mask, c
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream) {
+cudaError_t launch_decode_combine(const DecodeParams& p, const QoStrides* qo, cudaStream_t stream) {
   const int rows = p.batch * p.num_qo_heads;
   const int warps_per_block = 8;
   dim3 grid((rows + warps_per_block - 1) / warps_per_block);
@@ -953,10 +987,13 @@ cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e;
-  if (p.head_dim == 128) e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<128>, p);
-  else if (p.head_dim == 64) e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<64>, p);
-  else if (p.head_dim == 32) e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<32>, p);
-  else return cudaErrorInvalidValue;
+  const QoStrides q = qo != nullptr ? *qo : QoStrides{0, 0, 0, 0};
+#define ASTR_COMB_CASE(DD)                                                                         \
+  if (p.head_dim == DD)                                                                           \
+    e = qo != nullptr ? cudaLaunchKernelEx(&cfg, decode_combine_kernel<DD, true>, p, q)             \
+                      : cudaLaunchKernelEx(&cfg, decode_combine_kernel<DD, false>, p, q);
+  ASTR_COMB_CASE(128) else ASTR_COMB_CASE(64) else ASTR_COMB_CASE(32) else return cudaErrorInvalidValue;
+#undef ASTR_COMB_CASE
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
