@@ -178,6 +178,37 @@ __device__ __forceinline__ void mma_ts_h(uint32_t d, uint32_t a_tmem, uint32_t b
       "r"(a_tmem), "r"(blo), "r"(bhi), "r"(idesc), "r"(acc)
       : "memory");
 }
+// The same MMAs and the tensor-core commit issued by one elected lane of a converged warp: every
+// lane computes the (warp-uniform) descriptors, so they stay in the uniform datapath that the
+// tensor-core instructions read, and only the issue itself is single-threaded.  (The leader of
+// a fully converged warp is the same lane every time, so the commit tracks its MMAs.)
+__device__ __forceinline__ void mma_ss_e(uint32_t d, uint32_t alo, uint32_t ahi, uint32_t blo, uint32_t bhi,
+                                         uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b64 a, b;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\tmov.b64 a, {%1, %2};\n\tmov.b64 b, {%3, %4};\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, p;\n\t}" ::"r"(d),
+      "r"(alo), "r"(ahi), "r"(blo), "r"(bhi), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_e(uint32_t d, uint32_t a_tmem, uint32_t blo, uint32_t bhi, uint32_t idesc,
+                                         uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b64 b;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\tmov.b64 b, {%2, %3};\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b, %4, p;\n\t}" ::"r"(d),
+      "r"(a_tmem), "r"(blo), "r"(bhi), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_e(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+      : "memory");
+}
+
 // Keeps the values in registers at this point (they are computed before it, not between MMAs).
 // 16 mask bytes, read through L1 (the rows of one query position are shared by its G heads).
 __device__ __forceinline__ uint4 ldg_nc_v4(const uint8_t* p) {
@@ -649,15 +680,15 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
     if (p.status != nullptr && __any_sync(kFullMask, bad_input) && lane == 0) atomicOr(p.status, kStatusBadInput);
 
   } else if (warp >= C::MMA_WARP) {
-    // ======================= MMA issue: warp MMA_WARP + t, lane 0 alone, for query tile t.
-    // tcgen05.mma issue runs nearly in step with execution, so whatever the issuing thread
-    // does between MMAs (waits, fences, commits) idles the tensor core unless another thread
-    // has MMAs queued: the two query tiles therefore have their own issuing threads, and the
-    // barriers each group needs are tested (without blocking) in the middle of the group
-    // before it.  Per KV tile j: S_t(j+1) = Q_t K_{j+1}^T into the other S buffer, then
-    // O_t += P_t(j) V_j once the softmax warps of tile t have written P_t(j).  Both threads
-    // release every KV tile (after it has landed), used or not, so the shared empty barriers
-    // count two arrivals per phase.
+    // ======================= MMA issue: warp MMA_WARP + t for query tile t; the whole warp runs
+    // the loop and its waits, one elected lane issues each MMA and commit.
+    // tcgen05.mma issue runs nearly in step with execution, so whatever the issuing warp does
+    // between MMAs (waits, fences, commits) idles the tensor core unless another warp has MMAs
+    // queued: the two query tiles therefore have their own issuing warps, and the barriers each
+    // group needs are tested (without blocking) in the middle of the group before it.  Per KV
+    // tile j: S_t(j+1) = Q_t K_{j+1}^T into the other S buffer, then O_t += P_t(j) V_j once the
+    // softmax warps of tile t have written P_t(j).  Both warps release every KV tile (after it
+    // has landed), used or not, so the shared empty barriers count two arrivals per phase.
     const int t = warp - C::MMA_WARP;
     // descriptor halves of query slot 0, K stage 0 (K-major) and V stage 0 (MN-major)
     const uint64_t qd0 = tc::smem_desc_swz(sbase + C::Q_OFF, 16, C::ATOM, C::SW_MODE);
@@ -670,118 +701,104 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
     int gs = 0;       // KV tiles of tile t so far (S buffer / phase counter)
     int n_used = 0;   // items so far that had tile t (o_done / o_free phases)
     int u0 = 0;       // query tiles of the items before this one
-    int uw = 0;       // query tiles waited for so far (every thread waits for all, in order)
-    bool ok = true;
+    int uw = 0;       // query tiles waited for so far (every warp waits for all, in order)
+    bool ok = true;   // warp-uniform
     PrefillItem it;
     for (int n_item = 0; ok; ++n_item) {
       if (!get_item(n_item, it)) break;
-      if (lane == 0) {
-        const int nk =
-            (t < it.nq) ? (min(it.cb + min(it.q_len, it.first0 + (t + 1) * C::BQ), it.kvn) + C::BN - 1) / C::BN : 0;
-        const int n = it.n_tiles;
-        const uint32_t q_lo = (uint32_t)qd0 + (uint32_t)((((u0 + t) % C::Q_SLOTS) * C::Q_BYTES) >> 4);
-        // blocking only if not pre-tested ready; gives up (and stops this thread's issue) on a
-        // timeout or once another warp has given up
-        auto wait_one = [&](uint32_t bar, uint32_t parity, bool ready) {
-          if (ok && (*err != 0 || (!ready && !tc::mbar_wait(bar, parity, p.wait_limit)))) {
-            *err = 1;
-            ok = false;
-          }
-          tc::fence_after_sync();
-        };
-        auto stage = [&](int j) { return (g_base + j) % C::STAGES; };
-        auto kv_par = [&](int j) { return (uint32_t)(((g_base + j) / C::STAGES) & 1); };
-        auto sbuf = [&](int j) { return (gs + j) & 1; };
-        auto s_par = [&](int j) { return (uint32_t)(((gs + j) >> 1) & 1); };
-        // issue S_t(j); while it runs, test barrier `nb` (parity `np`); returns that test.
-        // Descriptors are formed before the first MMA so the MMAs issue back to back.
-        auto issue_s = [&](int j, uint32_t nb, uint32_t np) -> bool {
-          if (!ok) return false;  // a wait gave up: issue nothing more
-          const uint32_t sd = od + D + sbuf(j) * C::BN;
-          const uint32_t klo = k_lo + (uint32_t)((stage(j) * C::KV_BYTES) >> 4);
-          uint32_t al[D / 16], bl[D / 16];
+      const int nk =
+          (t < it.nq) ? (min(it.cb + min(it.q_len, it.first0 + (t + 1) * C::BQ), it.kvn) + C::BN - 1) / C::BN : 0;
+      const int n = it.n_tiles;
+      const uint32_t q_lo = (uint32_t)qd0 + (uint32_t)((((u0 + t) % C::Q_SLOTS) * C::Q_BYTES) >> 4);
+      // blocking only if not pre-tested ready; gives up (and stops this warp's issue) on a
+      // timeout or once another warp has given up; the whole warp agrees
+      auto wait_one = [&](uint32_t bar, uint32_t parity, bool ready) {
+        if (ok) {
+          const bool good = *err == 0 && (ready || tc::mbar_wait(bar, parity, p.wait_limit));
+          ok = __all_sync(kFullMask, good);
+          if (!ok) *err = 1;
+        }
+        tc::fence_after_sync();
+      };
+      auto stage = [&](int j) { return (g_base + j) % C::STAGES; };
+      auto kv_par = [&](int j) { return (uint32_t)(((g_base + j) / C::STAGES) & 1); };
+      auto sbuf = [&](int j) { return (gs + j) & 1; };
+      auto s_par = [&](int j) { return (uint32_t)(((gs + j) >> 1) & 1); };
+      // issue S_t(j); while it runs, test barrier `nb` (parity `np`); returns that test (agreed
+      // by the warp).
+      auto issue_s = [&](int j, uint32_t nb, uint32_t np) -> bool {
+        if (!ok) return false;  // a wait gave up: issue nothing more
+        const uint32_t sd = od + D + sbuf(j) * C::BN;
+        const uint32_t klo = k_lo + (uint32_t)((stage(j) * C::KV_BYTES) >> 4);
+        bool r = false;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            al[kk] = q_lo + (uint32_t)(((kk / C::KPB) * (C::M * C::SW_BYTES) + (kk % C::KPB) * 32) >> 4);
-            bl[kk] = klo + (uint32_t)(((kk / C::KPB) * (C::BN * C::SW_BYTES) + (kk % C::KPB) * 32) >> 4);
-          }
-          keep_regs(al);
-          keep_regs(bl);
-          bool r = false;
+        for (int kk = 0; kk < D / 16; ++kk) {
+          mma_ss_e(sd, q_lo + (uint32_t)(((kk / C::KPB) * (C::M * C::SW_BYTES) + (kk % C::KPB) * 32) >> 4), q_hi,
+                   klo + (uint32_t)(((kk / C::KPB) * (C::BN * C::SW_BYTES) + (kk % C::KPB) * 32) >> 4), k_hi,
+                   C::IDESC_S, kk > 0 ? 1u : 0u);
+          if (kk == D / 32) r = nb != 0u && tc::mbar_test(nb, np);
+        }
+        mma_commit_e(s_full(t, sbuf(j)));
+        return __all_sync(kFullMask, r);
+      };
+      auto issue_pv = [&](int j, uint32_t nb, uint32_t np) -> bool {
+        if (!ok) return false;  // a wait gave up: issue nothing more
+        const uint32_t pa = od + D + sbuf(j) * C::BN;  // P (fp16 pairs) in columns [0, 32)
+        const uint32_t vlo = v_lo + (uint32_t)((stage(j) * C::KV_BYTES) >> 4);
+        const uint32_t acc0 = j > 0 ? 1u : 0u;
+        bool r = false;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            mma_ss_h(sd, al[kk], q_hi, bl[kk], k_hi, C::IDESC_S, kk > 0 ? 1u : 0u);
-            if (kk == D / 32) r = nb != 0u && tc::mbar_test(nb, np);
-          }
-          tc::mma_commit(s_full(t, sbuf(j)));
-          return r;
-        };
-        auto issue_pv = [&](int j, uint32_t nb, uint32_t np) -> bool {
-          if (!ok) return false;  // a wait gave up: issue nothing more
-          const uint32_t pa = od + D + sbuf(j) * C::BN;  // P (fp16 pairs) in columns [0, 32)
-          const uint32_t vlo = v_lo + (uint32_t)((stage(j) * C::KV_BYTES) >> 4);
-          uint32_t bl[C::BN / 16];
-#pragma unroll
-          for (int kk = 0; kk < C::BN / 16; ++kk) bl[kk] = vlo + (uint32_t)((kk * 16 * C::SW_BYTES) >> 4);
-          keep_regs(bl);
-          const uint32_t acc0 = j > 0 ? 1u : 0u;
-          bool r = false;
-#pragma unroll
-          for (int kk = 0; kk < C::BN / 16; ++kk) {
-            mma_ts_h(od, pa + kk * 8, bl[kk], v_hi, C::IDESC_PV, kk > 0 ? 1u : acc0);
-            if (kk == 1) r = nb != 0u && tc::mbar_test(nb, np);
-          }
-          tc::mma_commit(kv_empty(stage(j)));  // the stage may be refilled once P V_j is done
-          if (j == nk - 1) tc::mma_commit(o_done(t));
-          return r;
-        };
+        for (int kk = 0; kk < C::BN / 16; ++kk) {
+          mma_ts_e(od, pa + kk * 8, vlo + (uint32_t)((kk * 16 * C::SW_BYTES) >> 4), v_hi, C::IDESC_PV,
+                   kk > 0 ? 1u : acc0);
+          if (kk == 1) r = nb != 0u && tc::mbar_test(nb, np);
+        }
+        mma_commit_e(kv_empty(stage(j)));  // the stage may be refilled once P V_j is done
+        if (j == nk - 1) mma_commit_e(o_done(t));
+        return __all_sync(kFullMask, r);
+      };
 
-        // the query tiles are waited for in order, this thread's own and the other's, up to
-        // its own (so no wait is ever more than one phase of a slot away); a tile seen is
-        // released at once: the tensor core's reads of it are covered by its epilogue's
-        // o_done wait
-        for (; ok && uw < u0 + min(t + 1, it.nq); ++uw) {
-          wait_one(q_full(uw), q_par(uw), false);
-          if (ok) tc::mbar_arrive(q_free(uw));  // (a tile not seen landing is never released)
-        }
-        bool ready = false;  // pre-test result for the next wait
-        if (nk > 0) {
-          wait_one(kv_full(stage(0)), kv_par(0), false);
-          ready = issue_s(0, nk > 1 ? kv_full(stage(1)) : 0u, kv_par(1));
-        }
-        for (int j = 0; ok && j < n; ++j) {
-          if (j < nk) {
-            if (j + 1 < nk) {  // S of KV tile j + 1 into the other buffer
-              wait_one(kv_full(stage(j + 1)), kv_par(j + 1), ready);
-              ready = issue_s(j + 1, p_full(t, sbuf(j)), s_par(j));
-            }
-            // O_t += P_t(j) V_j (the item's first P V overwrites O once the epilogue of the
-            // item before has read it)
-            if (j == 0 && n_used > 0) wait_one(o_free(t), (uint32_t)((n_used - 1) & 1), false);
-            wait_one(v_full(stage(j)), kv_par(j), false);
-            wait_one(p_full(t, sbuf(j)), s_par(j), ready);
-            ready = issue_pv(j, j + 2 < nk ? kv_full(stage(j + 2)) : 0u, kv_par(j + 2));
-          } else {
-            // a KV tile this query tile does not need is still released by this thread, but
-            // only once it has landed: otherwise the release could run ahead and count toward
-            // an earlier phase of the stage's empty barrier
-            wait_one(kv_full(stage(j)), kv_par(j), false);
-            if (ok) tc::mma_commit(kv_empty(stage(j)));
-          }
-        }
-        gs += nk;
-        if (nk > 0) ++n_used;
+      // the query tiles are waited for in order, this warp's own and the other's, up to its
+      // own (so no wait is ever more than one phase of a slot away); a tile seen is released
+      // at once: the tensor core's reads of it are covered by its epilogue's o_done wait
+      for (; ok && uw < u0 + min(t + 1, it.nq); ++uw) {
+        wait_one(q_full(uw), q_par(uw), false);
+        if (ok && lane == 0) tc::mbar_arrive(q_free(uw));  // (a tile not seen landing is never released)
       }
-      ok = __shfl_sync(kFullMask, ok ? 1 : 0, 0) != 0;
+      bool ready = false;  // pre-test result for the next wait
+      if (nk > 0) {
+        wait_one(kv_full(stage(0)), kv_par(0), false);
+        ready = issue_s(0, nk > 1 ? kv_full(stage(1)) : 0u, kv_par(1));
+      }
+      for (int j = 0; ok && j < n; ++j) {
+        if (j < nk) {
+          if (j + 1 < nk) {  // S of KV tile j + 1 into the other buffer
+            wait_one(kv_full(stage(j + 1)), kv_par(j + 1), ready);
+            ready = issue_s(j + 1, p_full(t, sbuf(j)), s_par(j));
+          }
+          // O_t += P_t(j) V_j (the item's first P V overwrites O once the epilogue of the
+          // item before has read it)
+          if (j == 0 && n_used > 0) wait_one(o_free(t), (uint32_t)((n_used - 1) & 1), false);
+          wait_one(v_full(stage(j)), kv_par(j), false);
+          wait_one(p_full(t, sbuf(j)), s_par(j), ready);
+          ready = issue_pv(j, j + 2 < nk ? kv_full(stage(j + 2)) : 0u, kv_par(j + 2));
+        } else {
+          // a KV tile this query tile does not need is still released by this warp, but only
+          // once it has landed: otherwise the release could run ahead and count toward an
+          // earlier phase of the stage's empty barrier
+          wait_one(kv_full(stage(j)), kv_par(j), false);
+          if (ok) mma_commit_e(kv_empty(stage(j)));
+        }
+      }
+      gs += nk;
+      if (nk > 0) ++n_used;
       g_base += it.n_tiles;
       u0 += it.nq;
     }
-    if (lane == 0) {
-      // every MMA this thread issued has completed before the CTA may release tensor memory
-      // (MMAs always complete, so this wait takes the default limit whatever the caller's)
-      tc::mma_commit(fin);
-      if (!tc::mbar_wait(fin, 0, tc::kWaitLimit)) *err = 1;
-    }
+    // every MMA this warp issued has completed before the CTA may release tensor memory
+    // (MMAs always complete, so this wait takes the default limit whatever the caller's)
+    mma_commit_e(fin);
+    if (!__all_sync(kFullMask, tc::mbar_wait(fin, 0, tc::kWaitLimit))) *err = 1;
     __syncwarp();
   } else {
     // ======================= softmax: warp group t = warp / 4; thread owns row tid % 128
