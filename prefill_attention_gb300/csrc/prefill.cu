@@ -923,21 +923,33 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
           const float neg_m = (m_run == -CUDART_INF_F) ? 0.f : C::kPOffset - m_run;
           const uint64_t sc2 = pk2(scale, scale), nm2 = pk2(neg_m, neg_m);
           uint64_t lsum2 = pk2(0.f, 0.f);
+          if (has_mask || masked) {  // a tile with hidden keys: their p is forced to 0
 #pragma unroll
-          for (int e = 0; e < C::BN / 2; ++e) {
-            const int c0 = 2 * e;
-            float x0, x1;
-            upk2(fma2(pk2(s[c0], s[c0 + 1]), sc2, nm2), x0, x1);
-            float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-            if (has_mask) {
-              p0 = ((vb >> c0) & 1ull) ? p0 : 0.f;
-              p1 = ((vb >> (c0 + 1)) & 1ull) ? p1 : 0.f;
-            } else if (masked) {
-              p0 = (j0 + c0 <= limit) ? p0 : 0.f;
-              p1 = (j0 + c0 + 1 <= limit) ? p1 : 0.f;
+            for (int e = 0; e < C::BN / 2; ++e) {
+              const int c0 = 2 * e;
+              float x0, x1;
+              upk2(fma2(pk2(s[c0], s[c0 + 1]), sc2, nm2), x0, x1);
+              float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+              if (has_mask) {
+                p0 = ((vb >> c0) & 1ull) ? p0 : 0.f;
+                p1 = ((vb >> (c0 + 1)) & 1ull) ? p1 : 0.f;
+              } else {
+                p0 = (j0 + c0 <= limit) ? p0 : 0.f;
+                p1 = (j0 + c0 + 1 <= limit) ? p1 : 0.f;
+              }
+              lsum2 = add2(lsum2, pk2(p0, p1));
+              ph[e] = float2_to_f16x2_rn(p0, p1);
             }
-            lsum2 = add2(lsum2, pk2(p0, p1));
-            ph[e] = float2_to_f16x2_rn(p0, p1);
+          } else {  // every key of the tile is visible to every row
+#pragma unroll
+            for (int e = 0; e < C::BN / 2; ++e) {
+              const int c0 = 2 * e;
+              float x0, x1;
+              upk2(fma2(pk2(s[c0], s[c0 + 1]), sc2, nm2), x0, x1);
+              const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+              lsum2 = add2(lsum2, pk2(p0, p1));
+              ph[e] = float2_to_f16x2_rn(p0, p1);
+            }
           }
           float ls0, ls1;
           upk2(lsum2, ls0, ls1);
