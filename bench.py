@@ -17,7 +17,10 @@ Also reported in the same line:
                     on its stream: algorithmic K+V bytes per launch / mean duration.
   * prefill      -- the ragged prefill entry point on the 16-request extend workload,
                     FLOP/s against the measured dense bf16 tensor-core peak (rotating
-                    query / pool / output copies, so each call is cold in L2).
+                    query / pool / output copies, so each call is cold in L2), with the
+                    batch's host work plan attached (made once outside the timed region, as a
+                    serving step makes it once for all layers); us_per_call_unplanned is the
+                    same call without a plan (the kernel orders the work itself).
   * decode_workloads -- the other decode workloads (B=4 d=64 tiny, B=8 long context, B=256
                     large batch): us per call, K+V GB/s and the fraction of the copy peak.
   * masked       -- the explicit-mask entry points on the same workloads: prefill with a 3-D
@@ -532,14 +535,27 @@ def main():
                          wp.max_seq_len, total_q=wp.total_q, max_q_len=wp.max_q_len)
     pouts = [torch.empty_like(pq) for _ in range(n_pcp)]
     pout = pouts[0]
+    # the host work plan of this batch, made once outside the timed region (a serving step makes
+    # it once per batch and every layer's call reuses it); the call without it is timed as well
+    pplan = pa.make_prefill_plan(wp.qo_indptr, wp.seq_lens, pdims)
+    udims = pdims
+    pdims = pa.attach_prefill_plan(pa.make_dims(wp.batch, wp.num_qo_heads, wp.num_kv_heads, wp.head_dim,
+                                                wp.num_slots, wp.r2t_stride, wp.max_seq_len, total_q=wp.total_q,
+                                                max_q_len=wp.max_q_len), pplan)
 
-    def prefill(i):
-        q_, k_, v_ = pcopies[i % n_pcp]
-        pa.astr_attn_prefill_ragged(q_, pqo, k_, v_, pr, ps_, pki, pouts[i % n_pcp], pdims, wp.sm_scale, stream=sh)
+    def prefill_with(dims_):
+        def run(i):
+            q_, k_, v_ = pcopies[i % n_pcp]
+            pa.astr_attn_prefill_ragged(q_, pqo, k_, v_, pr, ps_, pki, pouts[i % n_pcp], dims_, wp.sm_scale,
+                                        stream=sh)
+        return run
 
+    prefill, prefill_unplanned = prefill_with(pdims), prefill_with(udims)
     timed(prefill, 6)
+    timed(prefill_unplanned, 6)
     n_pf = max(21, min(args.steps // 10, 399))
     t_pf = statistics.median(timed(prefill, n_pf) / n_pf for _ in range(3))
+    t_pfu = statistics.median(timed(prefill_unplanned, n_pf) / n_pf for _ in range(3))
     flops = prefill_flops(wp)
     pf_tflops = flops / t_pf / 1e12
     pf_copy_mb = (wp.q.nbytes * 2 + wp.k_pool.nbytes * 2) / 1e6
@@ -678,6 +694,10 @@ def main():
                      "frac": round(split_gbs / peaks["hbm_gbs"], 4), "us_per_launch": round(t_split * 1e6, 3),
                      "traffic": traffic},
         "prefill": {"workload": wp.name, "seed": wp.seed, "us_per_call": round(t_pf * 1e6, 3),
+                    "plan": "host work plan of the batch (made once, outside the timed region)"
+                    if pplan is not None else "none applies",
+                    "us_per_call_unplanned": round(t_pfu * 1e6, 3),
+                    "frac_unplanned": round(flops / t_pfu / 1e12 / peaks["bf16_tflops"], 4),
                     "flops_per_call": flops,
                     "l2": f"rotating {n_pcp} query/pool/output copies ({n_pcp * pf_copy_mb:.0f} MB)",
                     "roofline": {"bound": "tensor", "achieved": round(pf_tflops, 2), "peak": peaks["bf16_tflops"],

@@ -86,6 +86,8 @@ typedef enum astr_status {
 #define ASTR_KSTATUS_SMEM 4       /* the shared-memory window was not 1024-byte aligned: no work done */
 #define ASTR_KSTATUS_RANGE 8      /* prefill: an output row came out non-finite -- P V runs in fp16, so a
                                      V element beyond 65504 (or a non-finite input) makes it so */
+#define ASTR_KSTATUS_PLAN 16      /* prefill: dims->prefill_plan does not match the call and was not used
+                                     (the kernel ordered the work itself; the results are valid) */
 
 /* Shapes and capacities; host struct read during the call only.  Zero-initialise it: the
  * trailing fields then take their defaults. */
@@ -105,6 +107,10 @@ typedef struct astr_attn_dims {
                             into it (NULL = not reported); owned by the caller */
   uint32_t wait_limit;   /* polls per pipeline wait before a kernel gives up (the first poll does not
                             block, later ones may suspend the thread briefly); 0 = default (2^20) */
+  const int32_t* prefill_plan;  /* prefill: optional DEVICE copy of a work plan written by
+                                   astr_attn_prefill_plan for this call (NULL = the kernel orders the
+                                   work itself); ignored by decode; owned by the caller */
+  int64_t prefill_plan_words;   /* int32 words readable at prefill_plan (the plan's words_needed) */
 } astr_attn_dims;
 
 /*
@@ -176,6 +182,32 @@ int astr_attn_decode_split(const uint16_t* q, const uint16_t* k_pool, const uint
  */
 int astr_attn_decode_combine(const float* o_part, const float* ml_part, const int32_t* seq_lens,
                              const int32_t* kv_indptr, uint16_t* out, const astr_attn_dims* dims, void* stream);
+
+/*
+ * Work plan for the prefill calls (optional: it orders the work and changes no result; not a
+ * step of the pages' method).  Without a plan, every CTA of a prefill launch first derives the
+ * work order from qo_indptr and seq_lens in shared memory (a few microseconds of every call).
+ * A plan is made once on the host, from host copies of the same two arrays, and serves every
+ * call of the batch (one per layer): it holds each CTA's work items (KV head x pair of query
+ * tiles), dealt longest-estimated-first to the least-loaded CTA.  The kernel checks the plan
+ * against the call -- batch, num_kv_heads, group size, grid, causal flag and a checksum of
+ * qo_indptr and seq_lens -- and ignores one that does not match (ASTR_KSTATUS_PLAN).
+ *   qo_indptr_host [batch + 1], seq_lens_host [batch]: HOST int32 copies of the call's arrays.
+ *   dims: the call's dims (batch, heads, head_dim, total_q and max_q_len as the call passes them).
+ *   causal: 1 for astr_attn_prefill_ragged / _contiguous / _strided without a mask, else the
+ *     mask's causal flag.
+ *   num_ctas: CTAs the call launches on; 0 = the SM count of `device` (what the call uses).
+ *   plan: HOST buffer of plan_words int32 words to write (the caller copies it to the device and
+ *     sets dims->prefill_plan and dims->prefill_plan_words); NULL = only report the size.
+ *   *words_needed: the plan's size in int32 words.
+ * Returns OK; INVALID_ARG (a null pointer, bad dims, a negative q_len or seq_len, q_len above
+ * seq_len for a causal call, plan_words below words_needed); UNSUPPORTED (head_dim / group size
+ * as for the prefill calls, more than 1024 requests, or more than 128 items on one CTA: the
+ * kernel then deals the items in their natural order and no plan applies); DEVICE.
+ */
+int astr_attn_prefill_plan(const int32_t* qo_indptr_host, const int32_t* seq_lens_host, const astr_attn_dims* dims,
+                           int32_t causal, int32_t num_ctas, int device, int32_t* plan, size_t plan_words,
+                           size_t* words_needed);
 
 /*
  * Ragged packed prefill/extend over the same pool (P1, batched-SDPA commit; P3,

@@ -26,6 +26,7 @@ __all__ = [
     "ASTR_OK", "ASTR_ERR_INVALID_ARG", "ASTR_ERR_UNSUPPORTED", "ASTR_ERR_MISALIGNED",
     "ASTR_ERR_WORKSPACE_TOO_SMALL", "ASTR_ERR_LAUNCH_FAILED", "ASTR_ERR_DEVICE", "EXPORTED_SYMBOLS",
     "ASTR_KSTATUS_TIMEOUT", "ASTR_KSTATUS_BAD_INPUT", "ASTR_KSTATUS_SMEM", "ASTR_KSTATUS_RANGE",
+    "ASTR_KSTATUS_PLAN", "astr_attn_prefill_plan", "make_prefill_plan", "attach_prefill_plan",
 ]
 
 ASTR_OK = 0
@@ -41,6 +42,7 @@ ASTR_KSTATUS_TIMEOUT = 1
 ASTR_KSTATUS_BAD_INPUT = 2
 ASTR_KSTATUS_SMEM = 4
 ASTR_KSTATUS_RANGE = 8
+ASTR_KSTATUS_PLAN = 16
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libastr_attn.so")
@@ -52,6 +54,7 @@ EXPORTED_SYMBOLS = [
     "astr_attn_decode_split", "astr_attn_paged_decode_noalloc", "astr_attn_kv_append",
     "astr_attn_paged_decode_masked", "astr_attn_prefill_ragged_masked", "astr_attn_decode_contiguous",
     "astr_attn_prefill_contiguous", "astr_attn_decode_strided", "astr_attn_prefill_strided",
+    "astr_attn_prefill_plan",
 ]
 
 
@@ -69,6 +72,7 @@ class Dims(ctypes.Structure):
         ("max_seq_len", ctypes.c_int32), ("total_q", ctypes.c_int32), ("max_q_len", ctypes.c_int32),
         ("max_splits", ctypes.c_int32), ("num_splits", ctypes.c_int32),
         ("status", ctypes.c_void_p), ("wait_limit", ctypes.c_uint32),
+        ("prefill_plan", ctypes.c_void_p), ("prefill_plan_words", ctypes.c_int64),
     ]
 
 
@@ -157,6 +161,8 @@ def load():
     QL = ctypes.POINTER(QoLayout)
     lib.astr_attn_decode_strided.argtypes = [P, P, P, P, LY, QL, P, P, M, P, P, P, D, F, P]
     lib.astr_attn_prefill_strided.argtypes = [P, P, P, P, P, LY, QL, P, P, M, P, D, F, P]
+    SZ = ctypes.c_size_t
+    lib.astr_attn_prefill_plan.argtypes = [P, P, D, I32, I32, I32, P, SZ, ctypes.POINTER(SZ)]
     lib.astr_attn_status_string.argtypes = [I32]
     lib.astr_attn_status_string.restype = ctypes.c_char_p
     lib.astr_attn_version.argtypes = []
@@ -164,7 +170,7 @@ def load():
               "astr_attn_decode_split", "astr_attn_decode_combine", "astr_attn_prefill_ragged", "astr_attn_version",
               "astr_attn_paged_decode_noalloc", "astr_attn_kv_append", "astr_attn_paged_decode_masked",
               "astr_attn_prefill_ragged_masked", "astr_attn_decode_contiguous", "astr_attn_prefill_contiguous",
-              "astr_attn_decode_strided", "astr_attn_prefill_strided"):
+              "astr_attn_decode_strided", "astr_attn_prefill_strided", "astr_attn_prefill_plan"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -268,6 +274,51 @@ def astr_attn_prefill_ragged(q, qo_indptr, k_pool, v_pool, req_to_token, seq_len
                                          _ptr(seq_lens), _ptr(kv_indptr), _ptr(out), ctypes.byref(dims),
                                          float(sm_scale), _stream(stream))
     return _check(st, "astr_attn_prefill_ragged", check)
+
+
+def astr_attn_prefill_plan(qo_indptr_host, seq_lens_host, dims: Dims, causal: bool = True, num_ctas: int = 0,
+                           device: int = 0, check: bool = True):
+    """Host work plan for the prefill calls of one batch (``astr_attn_prefill_plan``): returns the
+    plan as a numpy int32 array, or None when no plan applies (UNSUPPORTED).  ``qo_indptr_host``
+    and ``seq_lens_host`` are host arrays (numpy, lists or CPU tensors) equal to the call's."""
+    import numpy as np
+    qo = np.ascontiguousarray(np.asarray(qo_indptr_host, dtype=np.int32))
+    sl = np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32))
+    if qo.shape != (dims.batch + 1,) or sl.shape != (dims.batch,):
+        raise ValueError("qo_indptr_host must hold batch + 1 entries and seq_lens_host batch entries")
+    lib = load()
+    need = ctypes.c_size_t(0)
+    args = (qo.ctypes.data, sl.ctypes.data, ctypes.byref(dims), int(bool(causal)), int(num_ctas), int(device))
+    st = lib.astr_attn_prefill_plan(*args, None, 0, ctypes.byref(need))
+    if st == ASTR_ERR_UNSUPPORTED:
+        return None
+    _check(st, "astr_attn_prefill_plan", check)
+    if st != ASTR_OK:
+        return None
+    plan = np.zeros(max(int(need.value), 1), np.int32)
+    st = lib.astr_attn_prefill_plan(*args, plan.ctypes.data, plan.size, ctypes.byref(need))
+    _check(st, "astr_attn_prefill_plan", check)
+    return plan if st == ASTR_OK else None
+
+
+def make_prefill_plan(qo_indptr_host, seq_lens_host, dims: Dims, causal: bool = True, device=None):
+    """The plan of ``astr_attn_prefill_plan`` copied to the current CUDA device (an int32 tensor),
+    or None when no plan applies; ``attach_prefill_plan`` points a Dims at it."""
+    import torch
+    dev = torch.cuda.current_device() if device is None else int(device)
+    plan = astr_attn_prefill_plan(qo_indptr_host, seq_lens_host, dims, causal=causal, device=dev)
+    if plan is None:
+        return None
+    return torch.from_numpy(plan).to(torch.device("cuda", dev))
+
+
+def attach_prefill_plan(dims: Dims, plan) -> Dims:
+    """Point ``dims`` at a device plan tensor (or detach it with None); returns dims."""
+    if plan is None:
+        dims.prefill_plan, dims.prefill_plan_words = None, 0
+    else:
+        dims.prefill_plan, dims.prefill_plan_words = int(plan.data_ptr()), int(plan.numel())
+    return dims
 
 
 def astr_attn_kv_append(k_new, v_new, qo_indptr, req_to_token, seq_lens, k_pool, v_pool, dims: Dims, stream=None,

@@ -1,9 +1,13 @@
 // api.cu -- the C ABI declared in include/astr_attn.h: argument checks, split planning
 // and kernel launches on the caller's stream.  No allocation, no synchronisation, no
 // device-memory reads on the host, so every entry point can be captured in a CUDA graph.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <queue>
+#include <utility>
+#include <vector>
 
 #include <cuda_runtime.h>
 
@@ -106,6 +110,21 @@ int current_device(int* dev) {
   return ASTR_OK;
 }
 
+// Prefill launch size: pairs of query tiles per KV head (an upper bound from host-known
+// values) and the persistent grid, min(items, SMs).  Shared by the call and the planner so a
+// plan is made for exactly the grid the call launches.
+int64_t prefill_q_tiles(const astr_attn_dims* d) {
+  const int G = d->num_qo_heads / d->num_kv_heads;
+  const int bq = astr::prefill_rows_per_cta() / G;  // query positions per pair
+  const int64_t by_total = ((int64_t)d->total_q + bq - 1) / bq + d->batch;
+  const int64_t by_max = (int64_t)d->batch * (((int64_t)d->max_q_len + bq - 1) / bq);
+  return by_total < by_max ? by_total : by_max;
+}
+int prefill_grid(const astr_attn_dims* d, int sms) {
+  const int64_t items = prefill_q_tiles(d) * d->num_kv_heads;
+  return (int)(items < sms ? items : sms);
+}
+
 }  // namespace
 
 extern "C" {
@@ -123,7 +142,7 @@ const char* astr_attn_status_string(int status) {
   }
 }
 
-int astr_attn_version(void) { return 20000; }
+int astr_attn_version(void) { return 20100; }
 
 int astr_attn_decode_workspace_bytes(const astr_attn_dims* d, size_t* o_bytes, size_t* ml_bytes) {
   if (d == nullptr || o_bytes == nullptr || ml_bytes == nullptr) return ASTR_ERR_INVALID_ARG;
@@ -388,15 +407,21 @@ static int prefill_impl(const uint16_t* q, const int32_t* qo_indptr, const uint1
   p.head_dim = d->head_dim;
   p.num_slots = d->num_slots;
   p.total_q = d->total_q;
-  const int bq = astr::prefill_rows_per_cta() / G;  // query positions per CTA
-  const int64_t by_total = ((int64_t)d->total_q + bq - 1) / bq + d->batch;
-  const int64_t by_max = (int64_t)d->batch * (((int64_t)d->max_q_len + bq - 1) / bq);
-  const int64_t tiles = by_total < by_max ? by_total : by_max;
+  const int64_t tiles = prefill_q_tiles(d);
   if (tiles > 0x7fffffffLL) return ASTR_ERR_INVALID_ARG;
   p.num_q_tiles = (int)tiles;
   int sms = 0;
   if ((st = sm_count(dev, &sms)) != ASTR_OK) return st;
   p.num_ctas = sms;
+  // a plan is read only if it holds a row for every CTA of this launch
+  if (d->prefill_plan != nullptr) {
+    if (!aligned(d->prefill_plan, 4)) return ASTR_ERR_MISALIGNED;
+    const int64_t need = astr::kPlanHeader + (int64_t)prefill_grid(d, sms) * astr::kPlanRow;
+    if (d->prefill_plan_words >= need)
+      p.plan = d->prefill_plan;
+    else
+      p.plan_rejected = 1;
+  }
   p.scale_log2 = sm_scale * 1.4426950408889634f;
   p.causal = (mask == nullptr) ? 1 : mask->causal;
   if (mask != nullptr && mask->mask != nullptr) {
@@ -449,6 +474,91 @@ int astr_attn_prefill_strided(const uint16_t* q, const int32_t* qo_indptr, const
                               void* stream) {
   return prefill_impl(q, qo_indptr, k, v, kv_layout != nullptr ? nullptr : req_to_token, seq_lens, kv_indptr, mask,
                       kv_layout, qo_layout, out, d, sm_scale, stream);
+}
+
+// Host work plan.  Items (request b, pair pr, KV head) carry the cost estimate the kernel's own
+// order uses, 53 n_tiles + 13 units + 260 (about 10 ns each: a KV tile streamed, a (query tile,
+// KV tile) MMA unit, and an item's fill, drain and epilogue; fitted to measured per-CTA busy
+// times); longest first, each to the least-loaded CTA (ties: lowest CTA index), items of a CTA
+// in the order dealt.
+int astr_attn_prefill_plan(const int32_t* qo_indptr_host, const int32_t* seq_lens_host, const astr_attn_dims* d,
+                           int32_t causal, int32_t num_ctas, int device, int32_t* plan, size_t plan_words,
+                           size_t* words_needed) {
+  if (qo_indptr_host == nullptr || seq_lens_host == nullptr || words_needed == nullptr) return ASTR_ERR_INVALID_ARG;
+  int st = check_common(d);
+  if (st != ASTR_OK) return st;
+  if (d->total_q < 0 || d->max_q_len < 0 || num_ctas < 0) return ASTR_ERR_INVALID_ARG;
+  const int G = d->num_qo_heads / d->num_kv_heads;
+  if (!astr::prefill_supported(d->head_dim, G)) return ASTR_ERR_UNSUPPORTED;
+  if (d->batch > 1024 || d->num_kv_heads >= 32768) return ASTR_ERR_UNSUPPORTED;  // the kernel's shared tables
+  const int B = d->batch, H = d->num_kv_heads;
+  const int bq2 = astr::prefill_rows_per_cta() / G, bq = bq2 / 2, bn = 64;
+  for (int b = 0; b < B; ++b) {
+    const int64_t ql = (int64_t)qo_indptr_host[b + 1] - qo_indptr_host[b];
+    if (ql < 0 || seq_lens_host[b] < 0 || (causal && ql > seq_lens_host[b])) return ASTR_ERR_INVALID_ARG;
+  }
+  int sms = num_ctas;
+  if (sms == 0 && (st = sm_count(device, &sms)) != ASTR_OK) return st;
+  const int grid = prefill_grid(d, sms);
+  struct Item {
+    int64_t cost;
+    int b, pair, kvh;
+  };
+  std::vector<Item> items;
+  for (int b = 0; b < B; ++b) {
+    const int q_len = qo_indptr_host[b + 1] - qo_indptr_host[b], kvn = seq_lens_host[b];
+    const int cb = causal ? kvn - q_len : kvn - 1;
+    const int pairs = (q_len + bq2 - 1) / bq2;
+    if (pairs > 65535) return ASTR_ERR_UNSUPPORTED;
+    for (int pr = 0; pr < pairs; ++pr) {
+      const int first0 = pr * bq2;
+      const int nq = std::min(2, (q_len - first0 + bq - 1) / bq);
+      const int last = std::min(q_len, first0 + nq * bq) - 1;
+      const int64_t n_tiles = (std::min<int64_t>((int64_t)cb + last + 1, kvn) + bn - 1) / bn;
+      int64_t units = 0;
+      for (int t = 0; t < nq; ++t)
+        units += (std::min<int64_t>((int64_t)cb + std::min(q_len, first0 + (t + 1) * bq), kvn) + bn - 1) / bn;
+      const int64_t cost = 53 * n_tiles + 13 * units + 260;
+      for (int h = 0; h < H; ++h) items.push_back({cost, b, pr, h});
+    }
+  }
+  std::vector<int> order(items.size());
+  for (size_t i = 0; i < order.size(); ++i) order[i] = (int)i;
+  std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return items[x].cost > items[y].cost; });
+  std::vector<std::vector<int>> rows(grid > 0 ? grid : 0);
+  if (grid > 0) {
+    using Load = std::pair<int64_t, int>;  // (estimated load, CTA): the smallest first
+    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+    for (int c = 0; c < grid; ++c) heap.push({0, c});
+    for (const int i : order) {
+      const Load l = heap.top();
+      heap.pop();
+      rows[l.second].push_back(i);
+      if (rows[l.second].size() > (size_t)astr::kPlanMaxItems) return ASTR_ERR_UNSUPPORTED;
+      heap.push({l.first + items[i].cost, l.second});
+    }
+  }
+  const size_t words = (size_t)astr::kPlanHeader + (size_t)(grid > 0 ? grid : 0) * astr::kPlanRow;
+  *words_needed = words;
+  if (plan == nullptr) return ASTR_OK;
+  if (plan_words < words) return ASTR_ERR_INVALID_ARG;
+  uint32_t h = 0;
+  for (int i = 0; i <= B; ++i) h += astr::plan_mix((uint32_t)i, (uint32_t)qo_indptr_host[i]);
+  for (int i = 0; i < B; ++i) h += astr::plan_mix(astr::kPlanSeqTag + (uint32_t)i, (uint32_t)seq_lens_host[i]);
+  const int32_t header[astr::kPlanHeader] = {astr::kPlanMagic, astr::kPlanVersion, B, H, bq2, grid, (int32_t)h,
+                                             causal ? 1 : 0};
+  std::copy(header, header + astr::kPlanHeader, plan);
+  for (int c = 0; c < grid; ++c) {
+    int32_t* row = plan + astr::kPlanHeader + (size_t)c * astr::kPlanRow;
+    std::fill(row, row + astr::kPlanRow, 0);
+    row[0] = (int32_t)rows[c].size();
+    for (size_t k = 0; k < rows[c].size(); ++k) {
+      const Item& it = items[rows[c][k]];
+      row[1 + 2 * k] = it.b;
+      row[2 + 2 * k] = (int32_t)(((uint32_t)it.pair << 16) | (uint32_t)it.kvh);
+    }
+  }
+  return ASTR_OK;
 }
 
 int astr_attn_kv_append(const uint16_t* k_new, const uint16_t* v_new, const int32_t* qo_indptr,

@@ -17,7 +17,29 @@ constexpr int kMaxDevices = 64;
 cudaError_t set_smem_limit_once(const void* func, int bytes, std::atomic<bool> (&done)[kMaxDevices]);
 
 // Status-word bits (the ASTR_KSTATUS_* values of the C header).
-constexpr int kStatusTimeout = 1, kStatusBadInput = 2, kStatusSmem = 4, kStatusRange = 8;
+constexpr int kStatusTimeout = 1, kStatusBadInput = 2, kStatusSmem = 4, kStatusRange = 8, kStatusPlan = 16;
+
+// Prefill work plan (int32 words): a header, then one row per CTA of the launch -- the item
+// count and up to kPlanMaxItems items, each (request, pair << 16 | KV head).
+constexpr int kPlanMagic = 0x41535450;  // "ASTP"
+constexpr int kPlanVersion = 1;
+constexpr int kPlanHeader = 8;          // magic, version, batch, Hkv, pair height, grid, checksum, causal
+constexpr int kPlanMaxItems = 128;
+constexpr int kPlanRow = 1 + 2 * kPlanMaxItems;
+
+// Checksum of a call's qo_indptr [batch + 1] and seq_lens [batch], the same on the host and in
+// the kernel: a sum of per-element mixes (an integer hash of the index and the value), so
+// threads can add their shares in any order.
+__host__ __device__ inline uint32_t plan_mix(uint32_t i, uint32_t v) {
+  uint32_t h = v * 0x9E3779B1u + i * 0x85EBCA77u + 0x165667B1u;
+  h ^= h >> 15;
+  h *= 0x2C1B3C6Du;
+  h ^= h >> 12;
+  h *= 0x297A2D39u;
+  h ^= h >> 15;
+  return h;
+}
+constexpr uint32_t kPlanSeqTag = 0x40000000u;  // index offset of the seq_lens elements
 
 // Decode split kernel: a CTA runs this many independent warp pairs, one key chunk each.
 constexpr int kDecodeChunksPerCta = 4;
@@ -101,6 +123,8 @@ struct PrefillParams {
   // b * q_batch + i * q_token + h * q_head (padded, q_rows positions per request).  Same for out.
   int64_t q_batch, q_token, q_head, o_batch, o_token, o_head;
   int q_rows;
+  const int32_t* plan;           // work plan (kPlan* layout) the host found large enough, or null
+  int plan_rejected;             // 1: the call had a plan too small for its grid (reported, not read)
 };
 
 // KV append: one launch, one warp per new token.

@@ -87,13 +87,17 @@ struct PrefillCfg {
   // [NQ][2]; o_done, o_free [NQ]; fin; v_full [STAGES].  Then the error flag and TMEM address.
   static constexpr int NBAR = 2 * STAGES + 3 * Q_SLOTS + 6 * NQ + 1 + STAGES;  // + v_full [STAGES]
   static constexpr int LIST_OFF = (BAR_OFF + NBAR * 8 + 8 + 15) & ~15;
-  // this CTA's items in order, as (request, pair within the request, KV head)
+  // this CTA's items in order, five words each: request | KV head << 16, the request's first
+  // query row, query count and key count, the pair's first request-local query position
   static constexpr int MAX_CTA_ITEMS = 128;
-  static constexpr int SMEM_BYTES = LIST_OFF + MAX_CTA_ITEMS * 12;
-  // prologue scratch in the K/V ring: per-request pair offsets, bucket counts, keys, order
+  static constexpr int LIST_WORDS = 5;
+  static constexpr int SMEM_BYTES = LIST_OFF + MAX_CTA_ITEMS * LIST_WORDS * 4;
+  // prologue scratch in the query and K/V rings: copies of qo_indptr and seq_lens, per-request
+  // pair offsets, bucket counts, keys, order, the request of each pair
   static constexpr int MAX_SORT_REQS = 1024;
-  static constexpr int MAX_SORT_PAIRS = 8192;
+  static constexpr int MAX_SORT_PAIRS = D >= 64 ? 8192 : 4096;  // (the rings are smaller for D = 32)
   static constexpr int SORT_BUCKETS = 1024;              // sort key range (estimated cost, clamped)
+  static constexpr int RANK_PAIRS = 256;                 // up to this many pairs: rank count, not counting sort
   static constexpr uint32_t TMEM_TILE = 256;           // tile t: O at 256 t, S buffers at 256 t + D + {0, BN}
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr int KV_IT = BN * CPR / 32;          // cp.async per producer lane per K (or V) tile
@@ -108,8 +112,18 @@ struct PrefillCfg {
   static_assert((Q_OFF | K_OFF | V_OFF | Q_BYTES | KV_BYTES) % 1024 == 0, "swizzle atoms must be 1024-byte aligned");
   static_assert(D + 2 * BN <= (int)TMEM_TILE, "tensor-memory budget per tile");
   static_assert(KV_IT * 32 == BN * CPR && (D == 32 || D % 64 == 0), "whole warp iterations, whole column blocks");
-  static_assert((MAX_SORT_REQS + 1 + SORT_BUCKETS) * 4 + MAX_SORT_PAIRS * 4 <= Q_SLOTS * Q_BYTES + 2 * STAGES * KV_BYTES,
+  // scratch offsets in int32 words from the query ring's start (16-byte aligned arrays)
+  static constexpr int SCR_RS = MAX_SORT_REQS + 4;                 // seq_lens copy (qo_indptr copy at 0)
+  static constexpr int SCR_PST = SCR_RS + MAX_SORT_REQS;           // pair offsets per request
+  static constexpr int SCR_CNT = SCR_PST + MAX_SORT_REQS + 4;      // bucket counts / rank words
+  static constexpr int SCR_KEY = SCR_CNT + SORT_BUCKETS;           // keys, order, pair -> request (uint16 each)
+  static constexpr int SCR_PLAN = SCR_KEY + 3 * MAX_SORT_PAIRS / 2;  // plan header + this CTA's row, 2 words
+  static constexpr int SCR_END = SCR_PLAN + kPlanHeader + kPlanRow + 2;
+  static_assert(MAX_SORT_REQS % 4 == 0 && MAX_SORT_PAIRS % 8 == 0 && SCR_END * 4 <= Q_SLOTS * Q_BYTES + 2 * STAGES * KV_BYTES,
                 "prologue scratch");
+  static_assert(MAX_CTA_ITEMS == kPlanMaxItems, "a plan row fits the per-CTA list");
+  static_assert(MAX_SORT_REQS <= 65536, "request index and KV head share a list word");
+  static_assert(RANK_PAIRS <= SORT_BUCKETS && SORT_BUCKETS * MAX_SORT_PAIRS < (1 << 30), "rank words in the count array");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
@@ -250,19 +264,28 @@ struct PrefillItem {
   int b, kvh, q0, q_len, cb, kvn, first0, nq, n_tiles;
 };
 
-// Fills the item's fields once its request b and pair pr are known.
+// Fills the item's fields from its request's first query row q0, query count q_len and key
+// count kvn, and the pair's first request-local query position first0.
 template <int BQ2, int BQ, int BN>
-__device__ __forceinline__ void fill_item(const PrefillParams& p, int b, int pr, int kvh, PrefillItem& it) {
+__device__ __forceinline__ void fill_item_vals(const PrefillParams& p, int b, int kvh, int q0, int q_len, int kvn,
+                                               int first0, PrefillItem& it) {
   it.b = b;
   it.kvh = kvh;
-  it.q0 = __ldg(p.qo_indptr + b);
-  it.q_len = __ldg(p.qo_indptr + b + 1) - it.q0;
-  it.kvn = __ldg(p.seq_lens + b);
-  it.cb = p.causal ? it.kvn - it.q_len : it.kvn - 1;
-  it.first0 = pr * BQ2;
-  it.nq = min(BQ2 / BQ, (it.q_len - it.first0 + BQ - 1) / BQ);
-  const int last = min(it.q_len, it.first0 + it.nq * BQ) - 1;
-  it.n_tiles = (min(it.cb + last + 1, it.kvn) + BN - 1) / BN;
+  it.q0 = q0;
+  it.q_len = q_len;
+  it.kvn = kvn;
+  it.cb = p.causal ? kvn - q_len : kvn - 1;
+  it.first0 = first0;
+  it.nq = min(BQ2 / BQ, (q_len - first0 + BQ - 1) / BQ);
+  const int last = min(q_len, first0 + it.nq * BQ) - 1;
+  it.n_tiles = (min(it.cb + last + 1, kvn) + BN - 1) / BN;
+}
+
+// The same, reading the request's row range and key count from the call's arrays.
+template <int BQ2, int BQ, int BN>
+__device__ __forceinline__ void fill_item(const PrefillParams& p, int b, int pr, int kvh, PrefillItem& it) {
+  const int q0 = __ldg(p.qo_indptr + b);
+  fill_item_vals<BQ2, BQ, BN>(p, b, kvh, q0, __ldg(p.qo_indptr + b + 1) - q0, __ldg(p.seq_lens + b), pr * BQ2, it);
 }
 
 // Decodes item w of the natural order by a warp-parallel prefix scan of the per-request pair
@@ -294,16 +317,6 @@ __device__ __forceinline__ bool scan_item(const PrefillParams& p, int w, int lan
   return false;
 }
 
-// Largest b with pst[b] <= x (pst ascending, pst[0] = 0).
-__device__ __forceinline__ int upper_index(const int* pst, int n, int x) {
-  int l = 0, h = n - 1;
-  while (l < h) {
-    const int m = (l + h + 1) >> 1;
-    if (pst[m] <= x) l = m; else h = m - 1;
-  }
-  return l;
-}
-
 template <int D, int G, bool MASK, bool CONTIG>
 __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(const PrefillParams p,
                                                                                 const __grid_constant__ CUtensorMap q_map,
@@ -316,6 +329,22 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
   if ((sbase & 1023u) != 0) {  // swizzle atoms need a 1024-byte aligned window: report, do nothing
     if (tid == 0 && p.status != nullptr) atomicOr(p.status, kStatusSmem);
     return;
+  }
+
+  // The request tables go to shared memory first (scratch in the query and K/V rings, unused
+  // until the work order is known): their one global round trip overlaps the set-up below.
+  // A work plan's header and this CTA's row load in the same round trip (the host passes a plan
+  // only when it holds a row for every CTA of the launch).
+  int* rq = reinterpret_cast<int*>(smem + C::Q_OFF);  // qo_indptr[0 .. B]
+  int* rs = rq + C::SCR_RS;                          // seq_lens[0 .. B - 1]
+  int* pl = rq + C::SCR_PLAN;                        // plan header, row, then two words of results
+  const bool tables = p.batch <= C::MAX_SORT_REQS;
+  if (tables && warp > 0) {  // (warp 0 sets up barriers and tensor memory meanwhile)
+    for (int i = tid - 32; i <= p.batch; i += C::THREADS - 32) rq[i] = __ldg(p.qo_indptr + i);
+    for (int i = tid - 32; i < p.batch; i += C::THREADS - 32) rs[i] = __ldg(p.seq_lens + i);
+    if (p.plan != nullptr)
+      for (int i = tid - 32; i < kPlanHeader + kPlanRow; i += C::THREADS - 32)
+        pl[i] = __ldg(p.plan + (i < kPlanHeader ? i : kPlanHeader + (int64_t)blockIdx.x * kPlanRow + (i - kPlanHeader)));
   }
 
   const uint32_t bars = sbase + C::BAR_OFF;
@@ -361,6 +390,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
     tc::mbar_init(fin, C::NQ);
     for (int s = 0; s < C::STAGES; ++s) tc::mbar_init(v_full(s), 32);
     *err = 0;
+    pl[kPlanHeader + kPlanRow] = 0;  // checksum of the request tables (plan check)
     tc::fence_mbarrier_init();
   }
   if (warp == 0) tc::tmem_alloc<C::TMEM_COLS>(slot);
@@ -371,59 +401,136 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
 
   // ---- work order, computed identically by every CTA (no cross-CTA communication): items
   // sorted by estimated time (descending; ties by index) and dealt out in snake order (CTA c
-  // takes sorted positions c, 2G-1-c, 2G+c, ... for G CTAs).  The estimate, in half KV tiles,
-  // weighs the KV tiles an item streams (the S -> softmax -> P V chain of each query tile
-  // sets the pace per KV tile), its (query tile, KV tile) MMA units and a fixed per-item cost
-  // (pipeline fill and drain, epilogue): 2 n_tiles + units / 4 + 9, less 3 for a single query
-  // tile, coefficients fitted to measured per-CTA end times.  The KV heads of one query-tile pair
+  // takes sorted positions c, 2G-1-c, 2G+c, ... for G CTAs).  The estimate, in about 10 ns
+  // steps, weighs the KV tiles an item streams (the S -> softmax -> P V chain of each query
+  // tile sets the pace per KV tile), its (query tile, KV tile) MMA units and a fixed per-item
+  // cost (pipeline fill and drain, epilogue): 53 n_tiles + 13 units + 260, coefficients fitted
+  // to measured per-CTA busy times (sorted in steps of 16).  The KV heads of one query-tile pair
   // cost the same and have consecutive indices, so the pairs are sorted and then expanded.
-  // Each CTA keeps only its own list; problems too large for it use the natural order.
+  // Each CTA keeps only its own list; problems too large for it use the natural order.  Every
+  // step is a short dependent chain on shared memory, so the steps are kept few: a pair -> request
+  // map instead of searches, and for up to RANK_PAIRS pairs a rank count (each thread counts the
+  // pairs that sort before its own, one compare per pair) instead of the counting sort.
   int* list = reinterpret_cast<int*>(smem + C::LIST_OFF);
-  int* pst = reinterpret_cast<int*>(smem + C::Q_OFF);  // scratch: the query and K/V rings are not in use yet
-  int* cnt = pst + C::MAX_SORT_REQS + 1;
-  uint16_t* key = reinterpret_cast<uint16_t*>(cnt + C::SORT_BUCKETS);
+  int* pst = rq + C::SCR_PST;
+  int* cnt = rq + C::SCR_CNT;  // bucket counts; (key, index) words of the rank count
+  uint16_t* key = reinterpret_cast<uint16_t*>(rq + C::SCR_KEY);
   uint16_t* order = key + C::MAX_SORT_PAIRS;
+  uint16_t* pmap = order + C::MAX_SORT_PAIRS;  // request of each pair
   const int H = p.num_kv_heads;
   int per_cta = 0;
-  bool sorted = p.batch <= C::MAX_SORT_REQS;
-  if (sorted) {
+  bool sorted = tables && H < 32768;
+  // A plan is used when its header and the checksum of the request tables match the call (every
+  // CTA sees the same tables and header, so all CTAs take the same decision).
+  bool planned = false;
+  if (sorted && p.plan != nullptr) {
+    uint32_t h = 0;
+    for (int i = tid; i <= p.batch; i += C::THREADS) h += plan_mix((uint32_t)i, (uint32_t)rq[i]);
+    for (int i = tid; i < p.batch; i += C::THREADS) h += plan_mix(kPlanSeqTag + (uint32_t)i, (uint32_t)rs[i]);
+    h = __reduce_add_sync(kFullMask, h);
+    if (lane == 0) atomicAdd(reinterpret_cast<unsigned*>(pl + kPlanHeader + kPlanRow), h);
+    __syncthreads();
+    planned = pl[0] == kPlanMagic && pl[1] == kPlanVersion && pl[2] == p.batch && pl[3] == H && pl[4] == BQ2 &&
+              pl[5] == (int)gridDim.x && pl[6] == pl[kPlanHeader + kPlanRow] && pl[7] == p.causal;
+  }
+  if (blockIdx.x == 0 && tid == 0 && p.status != nullptr && (p.plan_rejected || (p.plan != nullptr && !planned)))
+    atomicOr(p.status, kStatusPlan);
+  if (planned) {
+    // this CTA's items, in plan order; an entry that names no item of the call is dropped and
+    // reported (the plan's checksum matched, so only a damaged plan buffer has one)
+    if (warp == 0) {
+      const int n = min(max(pl[kPlanHeader], 0), C::MAX_CTA_ITEMS);
+      int kept = 0;
+      bool bad = pl[kPlanHeader] != n;
+      for (int base = 0; base < n; base += 32) {
+        const int k = base + lane;
+        int b = -1, kvh = 0, pair = 0;
+        bool valid = false;
+        if (k < n) {
+          b = pl[kPlanHeader + 1 + 2 * k];
+          const int pk = pl[kPlanHeader + 2 + 2 * k];
+          kvh = pk & 0xffff;
+          pair = (int)((uint32_t)pk >> 16);
+          valid = b >= 0 && b < p.batch && kvh < H && pair < (rq[b + 1] - rq[b] + BQ2 - 1) / BQ2;
+          bad |= !valid;
+        }
+        const unsigned vm = __ballot_sync(kFullMask, valid);
+        if (valid) {
+          int* e = list + C::LIST_WORDS * (kept + __popc(vm & ((1u << lane) - 1u)));
+          e[0] = b | (kvh << 16);
+          e[1] = rq[b];
+          e[2] = rq[b + 1] - rq[b];
+          e[3] = rs[b];
+          e[4] = pair * BQ2;
+        }
+        kept += __popc(vm);
+      }
+      if (lane == 0) pl[kPlanHeader + kPlanRow + 1] = kept;
+      if (__any_sync(kFullMask, bad) && lane == 0 && p.status != nullptr) atomicOr(p.status, kStatusBadInput);
+    }
+    __syncthreads();
+    per_cta = pl[kPlanHeader + kPlanRow + 1];
+  } else if (sorted) {
     if (warp == 0) {  // pst[b] = first pair index of request b, pst[B] = number of pairs
       int acc = 0;
       for (int base = 0; base < p.batch; base += 32) {
         const int bb = base + lane;
         int np = 0;
-        if (bb < p.batch) np = (__ldg(p.qo_indptr + bb + 1) - __ldg(p.qo_indptr + bb) + BQ2 - 1) / BQ2;
+        if (bb < p.batch) np = (rq[bb + 1] - rq[bb] + BQ2 - 1) / BQ2;
         int inc = np;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const int y = __shfl_up_sync(kFullMask, inc, o);
           if (lane >= o) inc += y;
         }
-        if (bb < p.batch) pst[bb] = acc + inc - np;
+        const int first = acc + inc - np;
+        if (bb < p.batch) {
+          pst[bb] = first;
+          for (int w = first; w < min(first + np, C::MAX_SORT_PAIRS); ++w) pmap[w] = (uint16_t)bb;
+        }
         acc += __shfl_sync(kFullMask, inc, 31);
       }
       if (lane == 0) pst[p.batch] = acc;
     }
     __syncthreads();
     const int n_pairs = pst[p.batch];
-    per_cta = (int)(((int64_t)n_pairs * H + gridDim.x - 1) / gridDim.x);
-    sorted = n_pairs <= C::MAX_SORT_PAIRS && per_cta <= C::MAX_CTA_ITEMS;
+    sorted = n_pairs <= C::MAX_SORT_PAIRS;
+    per_cta = sorted ? (int)(((unsigned)(n_pairs * H) + gridDim.x - 1) / gridDim.x) : 0;
+    sorted = sorted && per_cta <= C::MAX_CTA_ITEMS;
   }
-  if (sorted) {
+  if (sorted && !planned) {
     const int n_pairs = pst[p.batch];
+    const bool rank = n_pairs <= C::RANK_PAIRS;
     for (int w = tid; w < n_pairs; w += C::THREADS) {
-      const int b = upper_index(pst, p.batch, w);
+      const int b = pmap[w];
       PrefillItem it;
-      fill_item<BQ2, C::BQ, C::BN>(p, b, w - pst[b], 0, it);
+      fill_item_vals<BQ2, C::BQ, C::BN>(p, b, 0, rq[b], rq[b + 1] - rq[b], rs[b], (w - pst[b]) * BQ2, it);
       int units = 0;
       for (int t = 0; t < it.nq; ++t)
         units += (min(it.cb + min(it.q_len, it.first0 + (t + 1) * C::BQ), it.kvn) + C::BN - 1) / C::BN;
-      const int c = 2 * it.n_tiles + (units + 2) / 4 + 9 - (it.nq == 1 ? 3 : 0);
-      key[w] = (uint16_t)(C::SORT_BUCKETS - 1 - min(max(c, 0), C::SORT_BUCKETS - 1));  // ascending key = descending cost
+      const int c = (53 * it.n_tiles + 13 * units + 260) >> 4;  // cost estimate in ~0.16 us steps
+      const int k = C::SORT_BUCKETS - 1 - min(max(c, 0), C::SORT_BUCKETS - 1);  // ascending key = descending cost
+      if (rank)
+        cnt[w] = k * C::MAX_SORT_PAIRS + w;  // (key, index): distinct, ordered like the stable sort
+      else
+        key[w] = (uint16_t)k;
     }
-    for (int i = tid; i < C::SORT_BUCKETS; i += C::THREADS) cnt[i] = 0;
+    if (!rank)
+      for (int i = tid; i < C::SORT_BUCKETS; i += C::THREADS) cnt[i] = 0;
     __syncthreads();
-    if (warp == 0) {  // stable counting sort of the pairs, one warp, chunks of 32 in index order
+    if (rank) {
+      for (int w = tid; w < n_pairs; w += C::THREADS) {
+        const int mine = cnt[w];
+        int r = 0;
+        int j = 0;
+        for (; j + 4 <= n_pairs; j += 4) {
+          const int4 v = *reinterpret_cast<const int4*>(cnt + j);
+          r += (v.x < mine) + (v.y < mine) + (v.z < mine) + (v.w < mine);
+        }
+        for (; j < n_pairs; ++j) r += cnt[j] < mine;
+        order[r] = (uint16_t)w;
+      }
+    } else if (warp == 0) {  // stable counting sort of the pairs, one warp, chunks of 32 in index order
       for (int base = 0; base < n_pairs; base += 32) {
         const int w = base + lane;
         const int k = (w < n_pairs) ? key[w] : -1;
@@ -462,16 +569,18 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
       }
     }
     __syncthreads();
-    for (int k = tid; k < per_cta; k += C::THREADS) {  // this CTA's sorted positions
+    for (int k = tid; k < per_cta; k += C::THREADS) {  // this CTA's sorted positions, fields resolved
       const int c = blockIdx.x, nc = gridDim.x;
       const int pos = k * nc + ((k & 1) ? nc - 1 - c : c);
-      int* e = list + 3 * k;
+      int* e = list + C::LIST_WORDS * k;
       if (pos < n_pairs * H) {
         const int pair = order[pos / H];
-        const int b = upper_index(pst, p.batch, pair);
-        e[0] = b;
-        e[1] = pair - pst[b];
-        e[2] = pos % H;
+        const int b = pmap[pair];
+        e[0] = b | ((pos % H) << 16);
+        e[1] = rq[b];
+        e[2] = rq[b + 1] - rq[b];
+        e[3] = rs[b];
+        e[4] = (pair - pst[b]) * BQ2;
       } else {
         e[0] = -1;
       }
@@ -482,9 +591,9 @@ __global__ void __launch_bounds__(PrefillCfg<D, G>::THREADS, 1) prefill_kernel(c
   auto get_item = [&](int k, PrefillItem& it) -> bool {
     if (sorted) {
       if (k >= per_cta) return false;
-      const int* e = list + 3 * k;
+      const int* e = list + C::LIST_WORDS * k;
       if (e[0] < 0) return false;
-      fill_item<BQ2, C::BQ, C::BN>(p, e[0], e[1], e[2], it);
+      fill_item_vals<BQ2, C::BQ, C::BN>(p, e[0] & 0xffff, e[0] >> 16, e[1], e[2], e[3], e[4], it);
       return true;
     }
     const int c = blockIdx.x, nc = gridDim.x;
