@@ -20,7 +20,8 @@ Also reported in the same line:
                     query / pool / output copies, so each call is cold in L2), with the
                     batch's host work plan attached (made once outside the timed region, as a
                     serving step makes it once for all layers); us_per_call_unplanned is the
-                    same call without a plan (the kernel orders the work itself).
+                    same call without a plan (the kernel orders the work itself),
+                    us_per_call_graph the planned calls replayed from a CUDA graph.
   * decode_workloads -- the other decode workloads (B=4 d=64 tiny, B=8 long context, B=256
                     large batch): us per call, K+V GB/s and the fraction of the copy peak.
   * masked       -- the explicit-mask entry points on the same workloads: prefill with a 3-D
@@ -556,6 +557,27 @@ def main():
     n_pf = max(21, min(args.steps // 10, 399))
     t_pf = statistics.median(timed(prefill, n_pf) / n_pf for _ in range(3))
     t_pfu = statistics.median(timed(prefill_unplanned, n_pf) / n_pf for _ in range(3))
+    # the planned calls replayed from a CUDA graph (a fixed batch's calls are capturable: the
+    # plan and every argument stay the same), which removes the per-launch gap of the stream
+    try:
+        gp = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gp, stream=stream):
+            for i in range(30):
+                prefill(i)
+        gp.replay()
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(SPIN_CYCLES)
+            ev0.record(stream)
+            for _ in range(5):
+                gp.replay()
+            ev1.record(stream)
+        ev1.synchronize()
+        t_pfg = ev0.elapsed_time(ev1) * 1e-3 / 150
+        del gp
+    except Exception as e:  # noqa: BLE001 (reported in the line)
+        t_pfg = f"capture failed: {e}"
     flops = prefill_flops(wp)
     pf_tflops = flops / t_pf / 1e12
     pf_copy_mb = (wp.q.nbytes * 2 + wp.k_pool.nbytes * 2) / 1e6
@@ -697,6 +719,7 @@ def main():
                     "plan": "host work plan of the batch (made once, outside the timed region)"
                     if pplan is not None else "none applies",
                     "us_per_call_unplanned": round(t_pfu * 1e6, 3),
+                    "us_per_call_graph": round(t_pfg * 1e6, 3) if isinstance(t_pfg, float) else t_pfg,
                     "frac_unplanned": round(flops / t_pfu / 1e12 / peaks["bf16_tflops"], 4),
                     "flops_per_call": flops,
                     "l2": f"rotating {n_pcp} query/pool/output copies ({n_pcp * pf_copy_mb:.0f} MB)",
