@@ -14,7 +14,9 @@
 //     KV head).  A 128-row MMA tile packs BQ = 128/G query positions x the G query heads
 //     that share the KV head (row r = position r / G, head r % G), so each gathered K/V tile
 //     feeds 2 x 128 rows.  Every CTA computes the same cost-sorted order of the items in its
-//     prologue and takes its share in snake order.
+//     prologue and takes its share in snake order -- or, when the call carries a work plan
+//     made on the host for exactly its batch (checked against a checksum of qo_indptr and
+//     seq_lens), reads its own item list from the plan instead.
 //   * Warp roles (15 warps): 0-7 softmax and epilogue, four per query tile, thread = row =
 //     TMEM lane; 8-9 issue the MMAs, one thread per query tile; 10-13 gather K/V, one warp
 //     per ring stage; 14 loads the query tiles by TMA (a box of BQ positions x G heads x one
