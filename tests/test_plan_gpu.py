@@ -135,3 +135,52 @@ def test_damaged_plan_row_is_reported():
     st = _status()
     _run(w, t, pa.attach_prefill_plan(dims, torch.from_numpy(plan).cuda()), st)
     assert int(st.item()) == pa.ASTR_KSTATUS_BAD_INPUT
+
+
+def test_planned_strided_padded_query_and_output():
+    """A plan serves the strided entry point too: padded "bhld" query and "blhd" output."""
+    w = workload.make_prefill(6, 32, 8, 128, (1, 130), (0, 400), seed=67, name="plan-strided")
+    t = upload(w)
+    B, H, d, L = w.batch, w.num_qo_heads, w.head_dim, w.max_q_len
+    q = torch.zeros(B, H, L, d, dtype=torch.bfloat16, device="cuda")
+    qv = q.transpose(1, 2)
+    for b in range(B):
+        q0, q1 = int(w.qo_indptr[b]), int(w.qo_indptr[b + 1])
+        qv[b, :q1 - q0].copy_(t["q"][q0:q1])
+    def run(dims):
+        o = torch.full((B, L, H, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+        pa.astr_attn_prefill_strided(qv, t["qo"], t["k"], t["v"], t["r2t"], t["seq"], t["kvi"], o, dims, w.sm_scale,
+                                     qo_layout=pa.make_qo_layout(qv, o, padded=True))
+        torch.cuda.synchronize()
+        return o
+
+    ref = run(prefill_dims(w))
+    dims = prefill_dims(w)
+    st = _status()
+    dims.status = int(st.data_ptr())
+    got = run(pa.attach_prefill_plan(dims, pa.make_prefill_plan(w.qo_indptr, w.seq_lens, dims)))
+    assert int(st.item()) == 0
+    assert np.array_equal(_bits(got), _bits(ref))
+
+
+def test_planned_call_in_a_cuda_graph():
+    """The plan and every argument stay fixed for a batch, so planned calls capture and replay."""
+    w = workload.config(5)
+    t = upload(w)
+    dims = prefill_dims(w)
+    plan = pa.make_prefill_plan(w.qo_indptr, w.seq_lens, dims)
+    pa.attach_prefill_plan(dims, plan)
+    out = torch.empty_like(t["q"])
+    args = (t["q"], t["qo"], t["k"], t["v"], t["r2t"], t["seq"], t["kvi"], out, dims, w.sm_scale)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        pa.astr_attn_prefill_ragged(*args, stream=s)
+    torch.cuda.synchronize()
+    eager = out.clone()
+    out.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        pa.astr_attn_prefill_ragged(*args, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
