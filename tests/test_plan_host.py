@@ -151,3 +151,36 @@ def test_plan_errors():
     assert pa.astr_attn_prefill_plan(qo3, sl3, _dims(qo3, sl3, 32, 32, 64), num_ctas=40) is None
     with pytest.raises(ValueError):
         pa.astr_attn_prefill_plan(qo[:-1], sl, dims, num_ctas=152)
+
+
+def test_plan_edge_shapes():
+    """Requests with no query rows contribute no items; one KV head; a grid larger than the
+    items (one item per CTA at most); every row is listed longest first."""
+    qo = np.array([0, 0, 5, 5, 300, 300], np.int32)      # requests 0, 2 and 4 have q_len 0
+    sl = np.array([7, 40, 9, 1000, 300], np.int32)
+    for Hq, Hkv in ((8, 1), (16, 16)):
+        dims = _dims(qo, sl, Hq, Hkv)
+        plan = pa.astr_attn_prefill_plan(qo, sl, dims, num_ctas=4096)
+        G = Hq // Hkv
+        items = _items(qo, sl, G, Hkv)
+        grid = _grid(dims, 4096)
+        assert int(plan[5]) == grid
+        rows = _rows(plan, grid)
+        dealt = [it for r in rows for it in r]
+        assert sorted(dealt) == sorted(items)
+        assert all(b in (1, 3) for b, _, _ in dealt), "only requests with query rows"
+        assert max(len(r) for r in rows) <= 1 or grid < len(items)
+
+
+def test_plan_without_causal_offset_allows_more_queries_than_keys():
+    """With the causal rule off (explicit-mask calls), q_len may exceed seq_len; every key is
+    visible to every row, so an item's KV tiles cover the whole key range."""
+    qo = np.array([0, 100, 164], np.int32)
+    sl = np.array([30, 64], np.int32)
+    dims = _dims(qo, sl, 32, 8, max_q_len=100)
+    with pytest.raises(pa.AstrAttnError):
+        pa.astr_attn_prefill_plan(qo, sl, dims, causal=True, num_ctas=152)
+    plan = pa.astr_attn_prefill_plan(qo, sl, dims, causal=False, num_ctas=152)
+    items = _items(qo, sl, 4, 8, causal=False)
+    rows = _rows(plan, _grid(dims, 152))
+    assert sorted(it for r in rows for it in r) == sorted(items)
