@@ -14,7 +14,10 @@ line reports the median region and the spread of all of them.
 
 Also reported in the same line:
   * roofline     -- the split kernel alone (the dominant kernel), timed with CUDA events
-                    on its stream: algorithmic K+V bytes per launch / mean duration.
+                    on its stream: algorithmic K+V bytes per launch / mean duration;
+                    stable_indices: the same, and the call, with ASTR_DIMS_STABLE_INDICES
+                    (chunks planned before the dependency wait; valid here: the index arrays
+                    are never written between calls).
   * prefill      -- the ragged prefill entry point on the 16-request extend workload,
                     FLOP/s against the measured dense bf16 tensor-core peak (rotating
                     query / pool / output copies, so each call is cold in L2), with the
@@ -408,6 +411,24 @@ def main():
     timed(split_only, 20)
     t_split = timed(split_only, n_split) / n_split
     split_gbs = nbytes["kv"] / t_split / 1e9
+    # the same with ASTR_DIMS_STABLE_INDICES (the index arrays are never written here, so the
+    # split step may plan its chunks before waiting for the preceding kernel), and the call
+    sdims = pa.make_dims(w.batch, w.num_qo_heads, w.num_kv_heads, w.head_dim, w.num_slots, w.r2t_stride,
+                         w.max_seq_len, max_splits=MAX_SPLITS, num_splits=args.num_splits,
+                         flags=pa.ASTR_DIMS_STABLE_INDICES)
+
+    def split_stable(i):
+        k, v = pools[i % n_copies]
+        pa.astr_attn_decode_split(q, k, v, r2t, seq, kvi, o_part, ml_part, sdims, w.sm_scale, stream=sh)
+
+    def decode_stable(i):
+        k, v = pools[i % n_copies]
+        pa.astr_attn_paged_decode(q, k, v, r2t, seq, kvi, o_part, ml_part, out, sdims, w.sm_scale, stream=sh)
+
+    timed(split_stable, 20)
+    t_split_s = timed(split_stable, n_split) / n_split
+    timed(decode_stable, 20)
+    t_call_s = timed(decode_stable, n_split) / n_split
 
     # ---------------- CUDA-graph replay (launch overhead amortised)
     graph_us = None
@@ -714,6 +735,9 @@ def main():
         "roofline": {"bound": "hbm", "kernel": "decode_split_kernel<128,4>", "achieved": round(split_gbs, 2),
                      "peak": peaks["hbm_gbs"], "peak_source": f"hbm_gbs ({peaks_src})", "unit": "GB/s",
                      "frac": round(split_gbs / peaks["hbm_gbs"], 4), "us_per_launch": round(t_split * 1e6, 3),
+                     "stable_indices": {"us_per_launch": round(t_split_s * 1e6, 3),
+                                        "frac": round(nbytes["kv"] / t_split_s / 1e9 / peaks["hbm_gbs"], 4),
+                                        "us_per_call": round(t_call_s * 1e6, 3)},
                      "traffic": traffic},
         "prefill": {"workload": wp.name, "seed": wp.seed, "us_per_call": round(t_pf * 1e6, 3),
                     "plan": "host work plan of the batch (made once, outside the timed region)"

@@ -111,7 +111,16 @@ typedef struct astr_attn_dims {
                                    astr_attn_prefill_plan for this call (NULL = the kernel orders the
                                    work itself); ignored by decode; owned by the caller */
   int64_t prefill_plan_words;   /* int32 words readable at prefill_plan (the plan's words_needed) */
+  uint32_t flags;               /* ASTR_DIMS_* bits below; 0 = none */
 } astr_attn_dims;
+
+/* dims->flags.  STABLE_INDICES: req_to_token, seq_lens and kv_indptr were written before the
+ * kernel that precedes this call in its stream (true for every layer of a decode step once the
+ * step's tables are in place).  The decode split step then plans its chunks from them before it
+ * waits for that kernel (a programmatic dependent launch), so the planning overlaps the
+ * preceding kernel instead of following it; K, V and q are still read only after the wait.
+ * Wrong results if the preceding kernel does write one of the three arrays. */
+#define ASTR_DIMS_STABLE_INDICES 1u
 
 /*
  * Decode split schedule (P3, shared-helpers commit: the split count is chosen per call;

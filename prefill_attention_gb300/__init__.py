@@ -27,6 +27,7 @@ __all__ = [
     "ASTR_ERR_WORKSPACE_TOO_SMALL", "ASTR_ERR_LAUNCH_FAILED", "ASTR_ERR_DEVICE", "EXPORTED_SYMBOLS",
     "ASTR_KSTATUS_TIMEOUT", "ASTR_KSTATUS_BAD_INPUT", "ASTR_KSTATUS_SMEM", "ASTR_KSTATUS_RANGE",
     "ASTR_KSTATUS_PLAN", "astr_attn_prefill_plan", "make_prefill_plan", "attach_prefill_plan",
+    "ASTR_DIMS_STABLE_INDICES",
 ]
 
 ASTR_OK = 0
@@ -43,6 +44,9 @@ ASTR_KSTATUS_BAD_INPUT = 2
 ASTR_KSTATUS_SMEM = 4
 ASTR_KSTATUS_RANGE = 8
 ASTR_KSTATUS_PLAN = 16
+
+# dims.flags
+ASTR_DIMS_STABLE_INDICES = 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libastr_attn.so")
@@ -73,6 +77,7 @@ class Dims(ctypes.Structure):
         ("max_splits", ctypes.c_int32), ("num_splits", ctypes.c_int32),
         ("status", ctypes.c_void_p), ("wait_limit", ctypes.c_uint32),
         ("prefill_plan", ctypes.c_void_p), ("prefill_plan_words", ctypes.c_int64),
+        ("flags", ctypes.c_uint32),
     ]
 
 
@@ -177,12 +182,15 @@ def load():
 
 
 def make_dims(batch, num_qo_heads, num_kv_heads, head_dim, num_slots, r2t_stride, max_seq_len, total_q=0,
-              max_q_len=0, max_splits=1, num_splits=0, status=None, wait_limit=0) -> Dims:
+              max_q_len=0, max_splits=1, num_splits=0, status=None, wait_limit=0, flags=0) -> Dims:
     """``status``: optional device int32 tensor (or pointer) the kernels OR their ASTR_KSTATUS_*
-    bits into; ``wait_limit``: polls per pipeline wait before a kernel gives up (0 = default)."""
-    return Dims(int(batch), int(num_qo_heads), int(num_kv_heads), int(head_dim), int(num_slots), int(r2t_stride),
-                int(max_seq_len), int(total_q), int(max_q_len), int(max_splits), int(num_splits), _ptr(status),
-                int(wait_limit))
+    bits into; ``wait_limit``: polls per pipeline wait before a kernel gives up (0 = default);
+    ``flags``: ASTR_DIMS_* bits (see include/astr_attn.h)."""
+    d = Dims(int(batch), int(num_qo_heads), int(num_kv_heads), int(head_dim), int(num_slots), int(r2t_stride),
+             int(max_seq_len), int(total_q), int(max_q_len), int(max_splits), int(num_splits), _ptr(status),
+             int(wait_limit))
+    d.flags = int(flags)
+    return d
 
 
 def _ptr(t) -> Optional[int]:

@@ -76,6 +76,7 @@ int check_common(const astr_attn_dims* d) {
   if (d->batch > 0 && d->max_seq_len > 0 && d->num_slots < 1) return ASTR_ERR_INVALID_ARG;
   if (d->num_kv_heads > 65535 || d->batch > 65535) return ASTR_ERR_INVALID_ARG;  // grid y / z limits
   if (d->status != nullptr && !aligned(d->status, 4)) return ASTR_ERR_MISALIGNED;
+  if ((d->flags & ~ASTR_DIMS_STABLE_INDICES) != 0) return ASTR_ERR_INVALID_ARG;  // an undefined flag bit
   return ASTR_OK;
 }
 
@@ -189,6 +190,7 @@ static int decode_prepare(const astr_attn_dims* d, float sm_scale, astr::DecodeP
   p->scale_log2 = sm_scale * 1.4426950408889634f;
   p->status = d->status;
   p->wait_limit = wait_limit_of(d);
+  p->early_index = (d->flags & ASTR_DIMS_STABLE_INDICES) ? 1 : 0;
   if (p->num_splits > 0x7fffffff / 2) return ASTR_ERR_INVALID_ARG;
   return ASTR_OK;
 }

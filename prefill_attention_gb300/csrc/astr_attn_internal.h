@@ -74,6 +74,8 @@ struct DecodeParams {
   int combine_all;               // combine even single-chunk requests (partials supplied by the caller)
   int indptr_before_wait;        // combine: kv_indptr may be read before the dependency wait (the
                                  // previous kernel is this call's split kernel, which does not write it)
+  int early_index;               // split: plan the chunks before the dependency wait (the caller's
+                                 // index arrays are not written by the preceding kernel)
   int32_t* status;               // optional status word (kStatus* bits, OR-ed in); may be null
   uint32_t wait_limit;           // polls per pipeline wait before giving up
 };

@@ -422,22 +422,29 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(
     warm_first_slots<D, G, C::BK, 1, CONTIG>(p, strides_of(arg), blockIdx.x * C::NPAIR + pair, kvh, C::STAGES, lane);
   else if (is_producer && B <= 256)
     warm_first_slots<D, G, C::BK, 8, CONTIG>(p, strides_of(arg), blockIdx.x * C::NPAIR + pair, kvh, C::STAGES, lane);
+  // ---- this pair's chunk (chunk index vc of the KV head): batch slots [ls, hs), and the
+  // request that holds slot ls.  Planned after the dependency wait below, or before it when
+  // the caller declares the index arrays untouched by the preceding kernel (they are then
+  // final already, and the planning overlaps that kernel).
+  const int vc = blockIdx.x * C::NPAIR + pair;
+  int S_tot = 0, CS = 1, ls = 0, hs = 0;
+  SlotBracket first{0, 0, 0, 0};
+  auto plan_chunk = [&]() {
+    S_tot = slot_totals(ind, B, 0, lane).x;
+    CS = decode_chunk_slots(S_tot, p.num_splits, p.min_chunk, p.part_pitch);
+    ls = (vc < p.num_splits) ? (int)min((int64_t)vc * CS, (int64_t)S_tot) : S_tot;
+    hs = min(ls + CS, S_tot);
+    if (ls < hs) first = locate_slot(ind, B, ls, lane);
+  };
+  if (p.early_index) plan_chunk();
   // Launched as a programmatic dependent of the previous kernel in the stream: the set-up
   // above overlapped its tail; from here on its writes are visible and its reads are done,
-  // so nothing read before this point is used.  (A no-op for an ordinary launch.)
+  // so nothing read before this point is used (but the index arrays under early_index).
+  // (A no-op for an ordinary launch.)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // let the combine kernel's CTAs launch now; they wait for this grid's memory to be visible
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-
-  // ---- this pair's chunk (chunk index vc of the KV head): batch slots [ls, hs), and the
-  // request that holds slot ls
-  const int vc = blockIdx.x * C::NPAIR + pair;
-  const int S_tot = slot_totals(ind, B, 0, lane).x;
-  const int CS = decode_chunk_slots(S_tot, p.num_splits, p.min_chunk, p.part_pitch);
-  const int ls = (vc < p.num_splits) ? (int)min((int64_t)vc * CS, (int64_t)S_tot) : S_tot;
-  const int hs = min(ls + CS, S_tot);
-  SlotBracket first{0, 0, 0, 0};
-  if (ls < hs) first = locate_slot(ind, B, ls, lane);
+  if (!p.early_index) plan_chunk();
 
   if (ls < hs && smem_ok && is_producer) {
     // ======================= producer warp: gathers the chunk's K / V rows slot by slot

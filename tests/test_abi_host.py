@@ -107,6 +107,7 @@ def test_int_arrays_need_only_4_byte_alignment(lib):
     (dict(max_splits=0), pa.ASTR_ERR_INVALID_ARG),
     (dict(num_splits=-1), pa.ASTR_ERR_INVALID_ARG),
     (dict(num_slots=0), pa.ASTR_ERR_INVALID_ARG),
+    (dict(flags=2), pa.ASTR_ERR_INVALID_ARG),                             # an undefined flag bit
 ])
 def test_decode_bad_dims(lib, kw, status):
     assert _dec(_dims(**kw)) == status
