@@ -271,6 +271,35 @@ struct TileIter {
 // requests, one coalesced load and one broadcast per round, all rounds issued together (R is
 // picked from the batch size: the unrolled rounds cost latency even when idle); batches of
 // more than 256 requests skip the warm-up.
+// Prefetch hints into L2 for the K/V rows of the first n_slots slots of a chunk that starts at
+// batch slot ls inside request b (first slot spb, keys [ib, ib1) of the flat key range).
+template <int D, int G, int BK, bool CONTIG>
+__device__ __forceinline__ void warm_slots_from(const DecodeParams& p, const KvStrides& ks, int b, int spb, int ib,
+                                                int ib1, int ls, int kvh, int n_slots, int lane) {
+  const int k0 = (ls - spb) * BK;  // the chunk's first key within request b
+  const size_t head_stride = (size_t)p.num_kv_heads * D;
+  for (int k = lane; k < n_slots * BK; k += 32) {
+    const int key = k0 + k;
+    size_t row;
+    if constexpr (CONTIG) {
+      if (key < 0 || key >= ib1 - ib || key >= ks.max_len) continue;
+      row = (size_t)b * ks.batch + (size_t)key * ks.token + (size_t)kvh * ks.head;
+    } else {
+      if (key < 0 || key >= ib1 - ib || (int64_t)key >= p.r2t_stride) continue;
+      const int id = ldcg_i32(p.req_to_token + (int64_t)b * p.r2t_stride + key);
+      if ((uint64_t)(uint32_t)id >= (uint64_t)p.num_slots) continue;  // negative ids wrap past num_slots
+      row = (size_t)id * head_stride + (size_t)kvh * D;
+    }
+    const uint16_t* kr = p.k_pool + row;
+    const uint16_t* vr = p.v_pool + row;
+#pragma unroll
+    for (int off = 0; off < D; off += 64) {  // 128-byte lines
+      prefetch_l2(kr + off);
+      prefetch_l2(vr + off);
+    }
+  }
+}
+
 template <int D, int G, int BK, int R, bool CONTIG>
 __device__ __forceinline__ void warm_first_slots(const DecodeParams& p, const KvStrides& ks, int vc, int kvh,
                                                  int n_slots, int lane) {
@@ -323,28 +352,7 @@ __device__ __forceinline__ void warm_first_slots(const DecodeParams& p, const Kv
     }
   }
   if (b < 0 || b >= B) return;
-  const int k0 = (ls - spb) * BK;  // the chunk's first key within request b
-  const size_t head_stride = (size_t)p.num_kv_heads * D;
-  for (int k = lane; k < n_slots * BK; k += 32) {
-    const int key = k0 + k;
-    size_t row;
-    if constexpr (CONTIG) {
-      if (key < 0 || key >= ib1 - ib || key >= ks.max_len) continue;
-      row = (size_t)b * ks.batch + (size_t)key * ks.token + (size_t)kvh * ks.head;
-    } else {
-      if (key < 0 || key >= ib1 - ib || (int64_t)key >= p.r2t_stride) continue;
-      const int id = ldcg_i32(p.req_to_token + (int64_t)b * p.r2t_stride + key);
-      if ((uint64_t)(uint32_t)id >= (uint64_t)p.num_slots) continue;  // negative ids wrap past num_slots
-      row = (size_t)id * head_stride + (size_t)kvh * D;
-    }
-    const uint16_t* kr = p.k_pool + row;
-    const uint16_t* vr = p.v_pool + row;
-#pragma unroll
-    for (int off = 0; off < D; off += 64) {  // 128-byte lines
-      prefetch_l2(kr + off);
-      prefetch_l2(vr + off);
-    }
-  }
+  warm_slots_from<D, G, BK, CONTIG>(p, ks, b, spb, ib, ib1, ls, kvh, n_slots, lane);
 }
 
 // Bounded wait, agreed by the whole warp, that gives up (and raises the pair's error flag) on
@@ -416,12 +424,6 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(
     sts128_zero(sbase + slot * C::SLOT + 2 * C::KV_BYTES + c * 16);
   }
   __syncthreads();
-  // Before the wait: warm L2 with this pair's first ring slots (prefetch hints only, from
-  // tables read through L2 that may still be changing; see warm_first_slots).
-  if (is_producer && B <= 32)
-    warm_first_slots<D, G, C::BK, 1, CONTIG>(p, strides_of(arg), blockIdx.x * C::NPAIR + pair, kvh, C::STAGES, lane);
-  else if (is_producer && B <= 256)
-    warm_first_slots<D, G, C::BK, 8, CONTIG>(p, strides_of(arg), blockIdx.x * C::NPAIR + pair, kvh, C::STAGES, lane);
   // ---- this pair's chunk (chunk index vc of the KV head): batch slots [ls, hs), and the
   // request that holds slot ls.  Planned after the dependency wait below, or before it when
   // the caller declares the index arrays untouched by the preceding kernel (they are then
@@ -436,7 +438,19 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1) decode_split_kernel(
     hs = min(ls + CS, S_tot);
     if (ls < hs) first = locate_slot(ind, B, ls, lane);
   };
-  if (p.early_index) plan_chunk();
+  if (p.early_index) {
+    // the index arrays are final: plan now and warm L2 with the chunk's first slots from the plan
+    plan_chunk();
+    if (is_producer && ls < hs && B <= 256)
+      warm_slots_from<D, G, C::BK, CONTIG>(p, strides_of(arg), first.b, first.spb, first.ind_b, first.ind_b1, ls, kvh,
+                                           C::STAGES, lane);
+  } else if (is_producer && B <= 32) {
+    // before the wait: warm L2 with this pair's first ring slots (prefetch hints only, from
+    // tables read through L2 that may still be changing; see warm_first_slots)
+    warm_first_slots<D, G, C::BK, 1, CONTIG>(p, strides_of(arg), vc, kvh, C::STAGES, lane);
+  } else if (is_producer && B <= 256) {
+    warm_first_slots<D, G, C::BK, 8, CONTIG>(p, strides_of(arg), vc, kvh, C::STAGES, lane);
+  }
   // Launched as a programmatic dependent of the previous kernel in the stream: the set-up
   // above overlapped its tail; from here on its writes are visible and its reads are done,
   // so nothing read before this point is used (but the index arrays under early_index).
