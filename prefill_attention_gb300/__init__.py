@@ -290,8 +290,13 @@ def astr_attn_prefill_plan(qo_indptr_host, seq_lens_host, dims: Dims, causal: bo
     plan as a numpy int32 array, or None when no plan applies (UNSUPPORTED).  ``qo_indptr_host``
     and ``seq_lens_host`` are host arrays (numpy, lists or CPU tensors) equal to the call's."""
     import numpy as np
-    qo = np.ascontiguousarray(np.asarray(qo_indptr_host, dtype=np.int32))
-    sl = np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32))
+
+    def host(a):
+        if hasattr(a, "detach"):  # a torch tensor (on any device): its values on the host
+            a = a.detach().cpu().numpy()
+        return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+    qo, sl = host(qo_indptr_host), host(seq_lens_host)
     if qo.shape != (dims.batch + 1,) or sl.shape != (dims.batch,):
         raise ValueError("qo_indptr_host must hold batch + 1 entries and seq_lens_host batch entries")
     lib = load()
@@ -324,8 +329,11 @@ def attach_prefill_plan(dims: Dims, plan) -> Dims:
     """Point ``dims`` at a device plan tensor (or detach it with None); returns dims."""
     if plan is None:
         dims.prefill_plan, dims.prefill_plan_words = None, 0
-    else:
-        dims.prefill_plan, dims.prefill_plan_words = int(plan.data_ptr()), int(plan.numel())
+        return dims
+    import torch
+    if not (isinstance(plan, torch.Tensor) and plan.is_cuda and plan.dtype == torch.int32 and plan.is_contiguous()):
+        raise ValueError("a prefill plan is a contiguous int32 CUDA tensor (see make_prefill_plan)")
+    dims.prefill_plan, dims.prefill_plan_words = int(plan.data_ptr()), int(plan.numel())
     return dims
 
 

@@ -184,3 +184,16 @@ def test_plan_without_causal_offset_allows_more_queries_than_keys():
     items = _items(qo, sl, 4, 8, causal=False)
     rows = _rows(plan, _grid(dims, 152))
     assert sorted(it for r in rows for it in r) == sorted(items)
+
+
+def test_plan_accepts_host_tensors_and_attach_checks_its_argument():
+    torch = pytest.importorskip("torch")
+    w = workload.config(5)
+    qo, sl = w.qo_indptr.astype(np.int32), w.seq_lens.astype(np.int32)
+    dims = _dims(qo, sl, w.num_qo_heads, w.num_kv_heads)
+    a = pa.astr_attn_prefill_plan(qo, sl, dims, num_ctas=152)
+    b = pa.astr_attn_prefill_plan(torch.from_numpy(qo), torch.from_numpy(sl).long(), dims, num_ctas=152)
+    assert np.array_equal(a, b)
+    with pytest.raises(ValueError):
+        pa.attach_prefill_plan(dims, torch.from_numpy(a))  # a host tensor is not a device plan
+    assert pa.attach_prefill_plan(dims, None).prefill_plan is None
